@@ -1,0 +1,234 @@
+/*
+ * tq.h — C ABI of the TurboQuant KV-cache library for GB300 (sm_103a).
+ *
+ * Keys are coded with the TurboQuant product quantiser and values with the MSE-only
+ * quantiser; decode attention reads the packed codes directly.  Sources, by page:
+ *
+ *   [QJL]  "TurboQuant QJL投影深度剖析：揭秘注意力分数背后的无偏内积估计器原理"
+ *          (bjdmk.com.cn): §二 the three-stage compression pipeline, §四 the QJL sign
+ *          sketch and its constant √(π/2)/d, §五 the combined unbiased estimator and the
+ *          packed (indices, sign bytes, ‖r‖, ‖x‖) record, §六 the read path (forward-rotated
+ *          and pre-sketched query, fused online-softmax decode attention), per-layer seeds.
+ *   [MLX]  the MLX-port article (cf-1.com): "背景" K = full TurboQuant, V = MSE-only;
+ *          "对称 vs 非对称" the asymmetric K = FP16 / V = turbo mode; quick start
+ *          (`key_bits=0`, `min_compress_tokens`).
+ *
+ * Conventions shared by every call
+ *   - head_dim d must be 128 (TQ_HEAD_DIM); anything else returns TQ_ERR_UNSUPPORTED.
+ *   - Pointers named "device" must be device (or managed) memory on the current device;
+ *     pointers named "host" are host memory.  The library never frees caller memory and
+ *     keeps no pointer to it after a call returns.
+ *   - Every device call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Arguments are validated on the host before any launch; a failed
+ *     validation returns an error code and launches nothing.  Launch failures return
+ *     TQ_ERR_CUDA.  Conditions only visible on the device (a position or length beyond the
+ *     capacity) make the kernel skip the offending tokens and raise a bit in a per-device
+ *     status word that tq_device_status() reads.
+ *   - Hot calls (quantise, scores, decode) allocate nothing: decode attention takes a
+ *     caller-owned workspace sized by tq_decode_workspace_bytes().
+ *
+ * Packed code layout (one KV head, one token, d = 128)
+ *   A 16-byte plane holds one bit per coordinate: coordinate j is bit (j % 8) of byte j / 8.
+ *   - Product code of a key, b total bits (b ≥ 2): (b−1) index planes (plane p = bit p of
+ *     each coordinate's Lloyd-Max index), one sign plane (bit = 1 iff (S r)_j ≥ 0),
+ *     ‖x‖ (float) and ‖r‖ (float).  [QJL] §二 step 3 ("d/8 bytes"), §五.
+ *   - MSE code of a value, B bits: B index planes, except B = 4 which is nibble-packed
+ *     (byte k = idx(2k) | idx(2k+1) << 4, 64 bytes), and ‖x‖ (float).
+ *   Cache arrays are plane-major per (batch, head) so that a run of tokens of one plane is
+ *   contiguous:
+ *     prod idx  : uint8 [batch][heads][b−1][capacity][16]
+ *     prod sgn  : uint8 [batch][heads][capacity][16]
+ *     prod xnorm, rnorm : float [batch][heads][capacity]
+ *     mse idx   : uint8 [batch][heads][B][capacity][16]   (B ≤ 3)
+ *                 uint8 [batch][heads][capacity][64]      (B = 4)
+ *     mse xnorm : float [batch][heads][capacity]
+ *   capacity must be a positive multiple of 64 and every array 16-byte aligned.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_HEAD_DIM 128
+#define TQ_MAX_GROUP 8          /* maximum query heads per KV head (GQA group) */
+#define TQ_CAPACITY_ALIGN 64
+
+/* A cudaStream_t without requiring the CUDA headers. */
+typedef struct CUstream_st* tq_stream_t;
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment */
+  TQ_ERR_UNSUPPORTED = 2,   /* valid but not built: d != 128, bit width, dtype, group > 8 */
+  TQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  TQ_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up */
+  TQ_ERR_DEVICE_STATUS = 5  /* the device status word reports skipped tokens */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
+typedef enum { TQ_PROD = 0, TQ_MSE = 1 } tq_kind;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tq_status_string(tq_status s);
+
+/* ------------------------------------------------------------------ host-side constants */
+
+/* Lloyd-Max codebook for one coordinate of a uniform point on the unit sphere S^{d−1},
+ * density ∝ (1 − t²)^((d−3)/2) on [−1, 1] ([QJL] §二 step 2: continuous 1-D k-means for
+ * the rotated-coordinate law).  Writes 2^index_bits centroids, ascending, unit-sphere
+ * scale, to `centroids` (host, caller-owned).  Decision boundaries are the midpoints.
+ * index_bits in 1..4.  Pure host code; needs no GPU. */
+tq_status tq_lloyd_max_codebook(int d, int index_bits, double* centroids);
+
+/* Random rotation from a Gaussian matrix ([QJL] §二 step 1: rotation by QR): Π = Q of
+ * G = Q R with diag(R) > 0.  `g` and `pi` are host, row-major d×d, caller-owned;
+ * y = Π x.  Pure host code; needs no GPU. */
+tq_status tq_rotation_from_gaussian(int d, const double* g, double* pi);
+
+/* ------------------------------------------------------------------ codec */
+
+typedef struct tq_codec tq_codec;
+
+/* Creates an immutable codec on the current device.
+ *   kind = TQ_PROD: keys; `bits` = total bits per coordinate b in 2..5 (b−1 index bits plus
+ *          one QJL sign bit, [QJL] §二 "(b−1) + 1"); needs `s`.
+ *   kind = TQ_MSE : values; `bits` = index bits B in 1..4; `s` may be NULL.
+ *   pi        : host, d×d row-major rotation Π (float64), copied.
+ *   s         : host, d×d row-major Gaussian sketch S (float64), copied; m = d rows.
+ *   centroids : host, the 2^(index bits) ascending Lloyd-Max levels (float64), copied.
+ * The codec owns device copies of Π, Πᵀ, Sᵀ and M = S Πᵀ (float32) and is safe to use
+ * from several streams at once.  Allocates device memory (not a hot call). */
+tq_status tq_codec_create(int d, tq_kind kind, int bits, const double* pi, const double* s,
+                          const double* centroids, tq_codec** out);
+
+/* Frees a codec (NULL is a no-op).  The caller must ensure no work using it is pending. */
+tq_status tq_codec_destroy(tq_codec* codec);
+
+/* ------------------------------------------------------------------ caches */
+
+typedef struct {
+  uint8_t* idx;    /* device, [batch][heads][b−1][capacity][16] */
+  uint8_t* sgn;    /* device, [batch][heads][capacity][16] */
+  float* xnorm;    /* device, [batch][heads][capacity] */
+  float* rnorm;    /* device, [batch][heads][capacity] */
+} tq_prod_cache;
+
+typedef struct {
+  uint8_t* idx;    /* device, planes [batch][heads][B][capacity][16] or nibbles [..][capacity][64] */
+  float* xnorm;    /* device, [batch][heads][capacity] */
+} tq_mse_cache;
+
+/* Bytes of packed codes per token per head (norms included): prod b bits → (b−1)·16+16+8;
+ * MSE B bits → B·16+4.  Returns 0 for unsupported widths. */
+size_t tq_code_bytes(tq_kind kind, int bits);
+
+/* ------------------------------------------------------------------ quantisation */
+
+/* Quantises keys x with the product quantiser and writes the codes into `cache`
+ * ([QJL] §二 steps 1–3, §五 quantize()).
+ *   x        : device, elements of `x_dtype` (F32/F16/BF16); vector (b, h, t) starts at
+ *              x + b*stride_b + h*stride_h + t*stride_t (strides in elements, ≥ 0) and its
+ *              d = 128 coordinates are contiguous.
+ *   batch, heads, tokens : x holds tokens t < tokens for every (b, h).
+ *   pos      : device int32[batch] or NULL (= 0): cache position of token 0 of batch b.
+ *   count    : device int32[batch] or NULL (= tokens): tokens of batch b to write (≤ tokens).
+ *   cache, capacity : destination cache of shape [batch][heads][capacity]; tokens landing
+ *              at or beyond `capacity` are skipped and flagged in the device status word.
+ * Appending one decode token per sequence is tokens = 1 with pos = current lengths. */
+tq_status tq_quantize_prod(const tq_codec* kc, const void* x, tq_dtype x_dtype, int32_t batch,
+                           int32_t heads, int32_t tokens, int64_t stride_b, int64_t stride_h,
+                           int64_t stride_t, const int32_t* pos, const int32_t* count,
+                           tq_prod_cache cache, int32_t capacity, tq_stream_t stream);
+
+/* Same for values with the MSE-only quantiser (Algorithm 1: rotation + Lloyd-Max index +
+ * ‖x‖), [MLX] "背景". */
+tq_status tq_quantize_mse(const tq_codec* vc, const void* x, tq_dtype x_dtype, int32_t batch,
+                          int32_t heads, int32_t tokens, int64_t stride_b, int64_t stride_h,
+                          int64_t stride_t, const int32_t* pos, const int32_t* count,
+                          tq_mse_cache cache, int32_t capacity, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ scores */
+
+/* Raw estimator ⟨q, k⟩ ≈ ‖x‖·⟨Π q, c[idx]⟩ + ‖r‖·√(π/2)/d·⟨S q, 2·sign − 1⟩ for every
+ * query and key, without 1/√d ([QJL] §五 estimator, §六 "attention_score" path).
+ *   q      : device float32, nq rows with row stride q_stride (elements).
+ *   keys   : a prod cache with batch = heads = 1 and the given capacity; keys t < n.
+ *   scores : device float32 [nq][scores_stride], row i column t = score(q_i, k_t). */
+tq_status tq_prod_scores(const tq_codec* kc, const float* q, int32_t nq, int64_t q_stride,
+                         tq_prod_cache keys, int32_t capacity, int32_t n, float* scores,
+                         int64_t scores_stride, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ decode attention */
+
+typedef struct {
+  int32_t batch;          /* B */
+  int32_t q_heads;        /* Hq */
+  int32_t kv_heads;       /* Hkv; Hq % Hkv == 0 and Hq / Hkv ≤ TQ_MAX_GROUP */
+  int32_t head_dim;       /* must be 128 */
+  int32_t capacity;       /* cache capacity per (b, kv head), multiple of 64 */
+  int32_t max_seq_len;    /* upper bound of seq_lens[b] (≤ capacity); sizes the grid */
+  int32_t tail_capacity;  /* asymmetric call: FP16 tail capacity per (b, kv head); else 0 */
+  float softmax_scale;    /* ≤ 0 selects 1/√head_dim */
+  tq_dtype q_dtype;       /* F32, F16 or BF16 */
+  tq_dtype out_dtype;     /* F32, F16 or BF16 */
+} tq_attn_desc;
+
+/* Workspace bytes needed by tq_decode_attention / tq_decode_attention_asym for `desc`
+ * (0 if desc is invalid).  Depends on the device's SM count (current device). */
+size_t tq_decode_workspace_bytes(const tq_attn_desc* desc);
+
+/* One decode step of attention on the compressed cache ([QJL] §六: forward-rotated and
+ * pre-sketched query, scores on the packed bits, one online softmax; values accumulated
+ * in the rotated domain and rotated back once).  Query head h reads KV head h / G.
+ *   q        : device [batch][q_heads][128] of desc->q_dtype.
+ *   k, v     : caches of shape [batch][kv_heads][capacity] coded by kc (prod) and vc (MSE).
+ *   seq_lens : device int32[batch]; tokens t < seq_lens[b] are attended (clamped to
+ *              capacity, flagged if larger).  A zero length gives a zero output row.
+ *   out      : device [batch][q_heads][128] of desc->out_dtype.
+ *   workspace: device, ≥ tq_decode_workspace_bytes(desc) bytes, 256-byte aligned; its
+ *              contents on entry are ignored.  Calls that share a workspace must be
+ *              serialised on one stream. */
+tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
+                              const void* q, tq_prod_cache k, tq_mse_cache v,
+                              const int32_t* seq_lens, void* out, void* workspace,
+                              size_t workspace_bytes, tq_stream_t stream);
+
+/* Asymmetric mode ([MLX] "对称 vs 非对称": K = FP16, V = turbo): keys stay FP16, values
+ * are MSE-coded, and the most recent tokens sit uncompressed in an FP16 tail that joins
+ * the same softmax.
+ *   k_f16    : device fp16 [batch][kv_heads][capacity][128], keys of the compressed segment.
+ *   v        : MSE cache [batch][kv_heads][capacity], values of the compressed segment.
+ *   seq_lens : device int32[batch], length of the compressed segment.
+ *   k_tail, v_tail : device fp16 [batch][kv_heads][tail_capacity][128].
+ *   tail_lens: device int32[batch] (≤ tail_capacity).
+ *   Other arguments as tq_decode_attention. */
+tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc, const void* q,
+                                   const uint16_t* k_f16, tq_mse_cache v,
+                                   const int32_t* seq_lens, const uint16_t* k_tail,
+                                   const uint16_t* v_tail, const int32_t* tail_lens, void* out,
+                                   void* workspace, size_t workspace_bytes, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Bits of the per-device status word (see tq_device_status). */
+#define TQ_FLAG_POS_OVERFLOW 0x1u   /* a quantised token landed at or beyond capacity */
+#define TQ_FLAG_LEN_OVERFLOW 0x2u   /* a seq_len or tail_len exceeded its capacity */
+#define TQ_FLAG_TIMEOUT      0x4u   /* a bounded device-side wait gave up */
+
+/* Synchronises the current device, returns the status word in *flags (host) and clears
+ * it.  Returns TQ_ERR_DEVICE_STATUS if any bit was set, TQ_OK otherwise. */
+tq_status tq_device_status(uint32_t* flags);
+
+/* Library version string. */
+const char* tq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,240 @@
+"""PyTorch-facing convenience layer over the C ABI.
+
+PyTorch only owns memory and streams here: caches and workspaces are torch tensors whose
+addresses are handed to libtq.so; every step of quantisation and attention runs in the
+library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _binding as B
+
+HEAD_DIM = B.TQ_HEAD_DIM
+
+_DT = {torch.float32: B.TQ_F32, torch.float16: B.TQ_F16, torch.bfloat16: B.TQ_BF16}
+
+
+def tq_dtype(dt: torch.dtype) -> int:
+    if dt not in _DT:
+        raise TypeError(f"unsupported dtype {dt}")
+    return _DT[dt]
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------------------ host constants
+
+def lloyd_max_codebook(index_bits: int, d: int = HEAD_DIM) -> np.ndarray:
+    """Ascending Lloyd-Max levels for the sphere-coordinate law (library host code)."""
+    out = np.zeros(1 << index_bits, dtype=np.float64)
+    B.check(B.tq_lloyd_max_codebook(d, index_bits, out.ctypes.data), "tq_lloyd_max_codebook")
+    return out
+
+
+def rotation_from_gaussian(g: np.ndarray) -> np.ndarray:
+    """Π = sign-fixed Q of G = QR (library host code)."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    d = g.shape[0]
+    out = np.zeros((d, d), dtype=np.float64)
+    B.check(B.tq_rotation_from_gaussian(d, g.ctypes.data, out.ctypes.data),
+            "tq_rotation_from_gaussian")
+    return out
+
+
+def layer_constants(layer: int = 0, d: int = HEAD_DIM):
+    """(Π, S) of a layer from the per-layer Gaussians (seeds 42 + 7ℓ and 43 + 7ℓ)."""
+    from .synth import gaussian_matrix, layer_seeds
+    sp, ss = layer_seeds(layer)
+    return rotation_from_gaussian(gaussian_matrix(sp, d)), gaussian_matrix(ss, d)
+
+
+# ------------------------------------------------------------------ codec
+
+class Codec:
+    """Owns a tq_codec (device copies of Π, Πᵀ, Sᵀ, M and the codebook)."""
+
+    def __init__(self, kind: int, bits: int, pi: np.ndarray, s: Optional[np.ndarray] = None,
+                 centroids: Optional[np.ndarray] = None):
+        self.kind = kind
+        self.bits = bits
+        self.index_bits = bits - 1 if kind == B.TQ_PROD else bits
+        if centroids is None:
+            centroids = lloyd_max_codebook(self.index_bits)
+        self.pi = np.ascontiguousarray(pi, dtype=np.float64)
+        self.s = None if s is None else np.ascontiguousarray(s, dtype=np.float64)
+        self.centroids = np.ascontiguousarray(centroids, dtype=np.float64)
+        h = ctypes.c_void_p()
+        B.check(B.tq_codec_create(HEAD_DIM, kind, bits, self.pi.ctypes.data,
+                                  0 if self.s is None else self.s.ctypes.data,
+                                  self.centroids.ctypes.data, h), "tq_codec_create")
+        self.handle = h
+
+    @classmethod
+    def prod(cls, bits: int, layer: int = 0) -> "Codec":
+        pi, s = layer_constants(layer)
+        return cls(B.TQ_PROD, bits, pi, s)
+
+    @classmethod
+    def mse(cls, bits: int, layer: int = 0) -> "Codec":
+        pi, _ = layer_constants(layer)
+        return cls(B.TQ_MSE, bits, pi)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            B.tq_codec_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------ caches
+
+def _cap(capacity: int) -> int:
+    a = B.TQ_CAPACITY_ALIGN
+    return (capacity + a - 1) // a * a
+
+
+@dataclasses.dataclass
+class ProdCache:
+    """Packed key cache [batch][heads][capacity] (layout of include/tq.h)."""
+    idx: torch.Tensor      # uint8 [B, H, b-1, cap, 16]
+    sgn: torch.Tensor      # uint8 [B, H, cap, 16]
+    xnorm: torch.Tensor    # float32 [B, H, cap]
+    rnorm: torch.Tensor    # float32 [B, H, cap]
+
+    @classmethod
+    def empty(cls, batch, heads, capacity, bits, device="cuda"):
+        cap = _cap(capacity)
+        return cls(torch.zeros(batch, heads, bits - 1, cap, 16, dtype=torch.uint8, device=device),
+                   torch.zeros(batch, heads, cap, 16, dtype=torch.uint8, device=device),
+                   torch.zeros(batch, heads, cap, dtype=torch.float32, device=device),
+                   torch.zeros(batch, heads, cap, dtype=torch.float32, device=device))
+
+    @property
+    def capacity(self):
+        return self.sgn.shape[2]
+
+    def c(self):
+        return B.tq_prod_cache(self.idx.data_ptr(), self.sgn.data_ptr(), self.xnorm.data_ptr(),
+                               self.rnorm.data_ptr())
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.idx, self.sgn, self.xnorm, self.rnorm))
+
+
+@dataclasses.dataclass
+class MSECache:
+    """Packed value cache [batch][heads][capacity]: bit planes, or nibbles for 4 bits."""
+    idx: torch.Tensor      # uint8 [B, H, bits, cap, 16] or [B, H, cap, 64]
+    xnorm: torch.Tensor    # float32 [B, H, cap]
+    bits: int
+
+    @classmethod
+    def empty(cls, batch, heads, capacity, bits, device="cuda"):
+        cap = _cap(capacity)
+        if bits == 4:
+            idx = torch.zeros(batch, heads, cap, 64, dtype=torch.uint8, device=device)
+        else:
+            idx = torch.zeros(batch, heads, bits, cap, 16, dtype=torch.uint8, device=device)
+        return cls(idx, torch.zeros(batch, heads, cap, dtype=torch.float32, device=device), bits)
+
+    @property
+    def capacity(self):
+        return self.xnorm.shape[2]
+
+    def c(self):
+        return B.tq_mse_cache(self.idx.data_ptr(), self.xnorm.data_ptr())
+
+    def nbytes(self):
+        return self.idx.numel() + self.xnorm.numel() * 4
+
+
+# ------------------------------------------------------------------ calls
+
+def _x_args(x: torch.Tensor):
+    if x.dim() != 4 or x.shape[-1] != HEAD_DIM or x.stride(-1) != 1:
+        raise ValueError("x must be [batch, heads, tokens, 128] with contiguous last dim")
+    bsz, h, t, _ = x.shape
+    return bsz, h, t, x.stride(0), x.stride(1), x.stride(2)
+
+
+def quantize_prod(codec: Codec, x: torch.Tensor, cache: ProdCache, pos=None, count=None,
+                  stream=None):
+    bsz, h, t, sb, sh, st = _x_args(x)
+    B.check(B.tq_quantize_prod(codec.handle, x, tq_dtype(x.dtype), bsz, h, t, sb, sh, st, pos,
+                               count, cache.c(), cache.capacity, _stream(stream)),
+            "tq_quantize_prod")
+
+
+def quantize_mse(codec: Codec, x: torch.Tensor, cache: MSECache, pos=None, count=None,
+                 stream=None):
+    bsz, h, t, sb, sh, st = _x_args(x)
+    B.check(B.tq_quantize_mse(codec.handle, x, tq_dtype(x.dtype), bsz, h, t, sb, sh, st, pos,
+                              count, cache.c(), cache.capacity, _stream(stream)),
+            "tq_quantize_mse")
+
+
+def prod_scores(codec: Codec, q: torch.Tensor, keys: ProdCache, n: int, out=None, stream=None):
+    """[nq, n] raw estimator scores of fp32 queries q [nq, 128] against keys[0, 0, :n]."""
+    q = q.contiguous()
+    if out is None:
+        out = torch.empty(q.shape[0], n, dtype=torch.float32, device=q.device)
+    B.check(B.tq_prod_scores(codec.handle, q, q.shape[0], q.stride(0), keys.c(), keys.capacity,
+                             n, out, out.stride(0), _stream(stream)), "tq_prod_scores")
+    return out
+
+
+class DecodePlan:
+    """A decode-attention configuration with its workspace (allocated once, reused)."""
+
+    def __init__(self, batch, q_heads, kv_heads, capacity, max_seq_len, q_dtype=torch.bfloat16,
+                 out_dtype=torch.float32, tail_capacity=0, softmax_scale=None, device="cuda"):
+        self.desc = B.tq_attn_desc(batch, q_heads, kv_heads, HEAD_DIM, _cap(capacity),
+                                   max_seq_len, tail_capacity,
+                                   softmax_scale if softmax_scale else 0.0,
+                                   tq_dtype(q_dtype), tq_dtype(out_dtype))
+        nbytes = B.tq_decode_workspace_bytes(self.desc)
+        if nbytes == 0:
+            raise ValueError("invalid decode-attention configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.out_dtype = out_dtype
+        self.shape = (batch, q_heads, HEAD_DIM)
+
+    def new_out(self, device="cuda"):
+        return torch.empty(self.shape, dtype=self.out_dtype, device=device)
+
+    def run(self, kc: Codec, vc: Codec, q, k: ProdCache, v: MSECache, seq_lens, out, stream=None):
+        B.check(B.tq_decode_attention(self.desc, kc.handle, vc.handle, q, k.c(), v.c(), seq_lens,
+                                      out, self.workspace, self.workspace.numel(),
+                                      _stream(stream)), "tq_decode_attention")
+        return out
+
+    def run_asym(self, vc: Codec, q, k_f16, v: MSECache, seq_lens, k_tail, v_tail, tail_lens,
+                 out, stream=None):
+        B.check(B.tq_decode_attention_asym(self.desc, vc.handle, q, k_f16, v.c(), seq_lens,
+                                           k_tail, v_tail, tail_lens, out, self.workspace,
+                                           self.workspace.numel(), _stream(stream)),
+                "tq_decode_attention_asym")
+        return out
+
+
+def device_status():
+    """(status, flags) of the device status word (synchronises the device)."""
+    return B.tq_device_status()

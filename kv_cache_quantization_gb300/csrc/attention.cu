@@ -1,0 +1,430 @@
+// Decode attention on the compressed cache (QJL deep-dive §五–§六) and the asymmetric
+// K = FP16 / V = MSE mode (MLX-port article, "对称 vs 非对称").
+//
+// Three launches per call, all on the caller's stream:
+//   1. query prep   — q_rot = Π q and q_sk = S q for every query head ("forward-rotate and
+//                     pre-sketch the query once").  Symmetric mode only.
+//   2. split decode — grid (context split, KV head, batch); every CTA serves the whole GQA
+//                     group of its KV head, scores its tokens straight from the packed bits,
+//                     runs a local softmax and accumulates Σ p·‖v‖·c[idx] in the rotated
+//                     domain (FP16-tail splits of the asymmetric mode accumulate plain
+//                     values instead); it writes (m, l, acc[128]) per query head.
+//   3. merge        — log-sum-exp combination of the splits, one rotation back Πᵀ·acc,
+//                     division by the softmax denominator, cast to the output dtype.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "tq_internal.h"
+
+TQ_DEFINE_FLAGS(tq_take_flags_attention)
+
+namespace {
+
+constexpr int kSplit = 256;          // tokens per split
+constexpr int kThreads = 128;
+constexpr int kRec = 2 + TQ_D;       // partial record: m, l, acc[128]
+constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
+
+struct Plan {
+  int G, nsplit_main, nsplit_tail, nsplit;
+  size_t q_off, part_off, bytes;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
+  if (!d) return TQ_ERR_INVALID_ARG;
+  if (d->head_dim != TQ_HEAD_DIM) return TQ_ERR_UNSUPPORTED;
+  if (d->batch < 0 || d->q_heads <= 0 || d->kv_heads <= 0) return TQ_ERR_INVALID_ARG;
+  if (d->q_heads % d->kv_heads) return TQ_ERR_INVALID_ARG;
+  if (d->q_heads / d->kv_heads > TQ_MAX_GROUP) return TQ_ERR_UNSUPPORTED;
+  if (d->capacity <= 0 || d->capacity % TQ_CAPACITY_ALIGN) return TQ_ERR_INVALID_ARG;
+  if (d->max_seq_len < 0 || d->max_seq_len > d->capacity) return TQ_ERR_INVALID_ARG;
+  if (d->tail_capacity < 0 || (!asym && d->tail_capacity != 0)) return TQ_ERR_INVALID_ARG;
+  for (tq_dtype t : {d->q_dtype, d->out_dtype})
+    if (t != TQ_F32 && t != TQ_F16 && t != TQ_BF16) return TQ_ERR_UNSUPPORTED;
+  p->G = d->q_heads / d->kv_heads;
+  p->nsplit_main = d->max_seq_len > 0 ? (d->max_seq_len + kSplit - 1) / kSplit : 1;
+  p->nsplit_tail = asym ? (d->tail_capacity + kSplit - 1) / kSplit : 0;
+  p->nsplit = p->nsplit_main + p->nsplit_tail;
+  const size_t qf = (size_t)d->batch * d->q_heads * 2 * TQ_D;
+  const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
+  p->q_off = 0;
+  p->part_off = ((qf * sizeof(float)) + 255) / 256 * 256;
+  p->bytes = p->part_off + pf * sizeof(float);
+  return TQ_OK;
+}
+
+__device__ __forceinline__ float load_elem(const void* base, int dtype, long long i) {
+  if (dtype == TQ_F32) return static_cast<const float*>(base)[i];
+  const uint16_t u = static_cast<const uint16_t*>(base)[i];
+  if (dtype == TQ_BF16) return __uint_as_float((uint32_t)u << 16);
+  return __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ void store_elem(void* base, int dtype, long long i, float v) {
+  if (dtype == TQ_F32) static_cast<float*>(base)[i] = v;
+  else if (dtype == TQ_BF16) static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else static_cast<__half*>(base)[i] = __float2half_rn(v);
+}
+
+// ---------------------------------------------------------------- 1. query prep
+__global__ void __launch_bounds__(kThreads) query_prep_kernel(const void* q, int q_dtype,
+                                                              const float* piT, const float* sT,
+                                                              float* qv) {
+  __shared__ float qf[TQ_D];
+  const int row = blockIdx.x;  // b * Hq + h
+  const int j = threadIdx.x;
+  qf[j] = load_elem(q, q_dtype, (long long)row * TQ_D + j);
+  __syncthreads();
+  float r = 0.f, s = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < TQ_D; ++k) {
+    r = fmaf(__ldg(&piT[k * TQ_D + j]), qf[k], r);
+    s = fmaf(__ldg(&sT[k * TQ_D + j]), qf[k], s);
+  }
+  qv[(size_t)row * 2 * TQ_D + j] = r;
+  qv[(size_t)row * 2 * TQ_D + TQ_D + j] = s;
+}
+
+struct DecodeArgs {
+  int B, Hq, Hkv, G, cap, tail_cap;
+  int nsplit_main, nsplit;
+  float scale;
+  // symmetric
+  const float* qv;
+  const uint8_t* kidx;
+  const uint8_t* ksgn;
+  const float* kxn;
+  const float* krn;
+  int kbits;                 // key index bits
+  tq_levels kl;
+  // asymmetric
+  const void* q;
+  int q_dtype;
+  const __half* kf16;
+  const __half* ktail;
+  const __half* vtail;
+  const int* tail_lens;
+  // values
+  const uint8_t* vidx;
+  const float* vxn;
+  int vbits;
+  tq_levels vl;
+  const int* seq_lens;
+  float* part;
+};
+
+__device__ __forceinline__ int value_index(const DecodeArgs& a, long long bh, int t, int j) {
+  if (a.vbits == 4) {
+    const uint8_t byte = a.vidx[((long long)bh * a.cap + t) * 64 + (j >> 1)];
+    return (byte >> ((j & 1) * 4)) & 15;
+  }
+  int q = 0;
+  for (int p = 0; p < a.vbits; ++p) {
+    const uint8_t byte = a.vidx[(((long long)bh * a.vbits + p) * a.cap + t) * 16 + (j >> 3)];
+    q |= ((byte >> (j & 7)) & 1) << p;
+  }
+  return q;
+}
+
+// Online-softmax pieces shared by both modes: scores in sc[g][tt] → probabilities, then the
+// value accumulation of thread j and the partial record.
+__device__ void softmax_and_values(const DecodeArgs& a, float (*sc)[kSplit], int n_tok, int start,
+                                   bool plain_values, long long bh, int split, float* s_m,
+                                   float* s_l) {
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  for (int g = warp; g < a.G; g += kThreads / 32) {
+    float m = -INFINITY;
+    for (int tt = lane; tt < n_tok; tt += 32) m = fmaxf(m, sc[g][tt]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float l = 0.f;
+    for (int tt = lane; tt < n_tok; tt += 32) {
+      const float p = n_tok > 0 ? expf(sc[g][tt] - m) : 0.f;
+      sc[g][tt] = p;
+      l += p;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) {
+      s_m[g] = m;
+      s_l[g] = l;
+    }
+  }
+  __syncthreads();
+  const int j = tid;
+  float acc[TQ_MAX_GROUP];
+#pragma unroll
+  for (int g = 0; g < TQ_MAX_GROUP; ++g) acc[g] = 0.f;
+  for (int tt = 0; tt < n_tok; ++tt) {
+    const int t = start + tt;
+    float val;
+    if (plain_values) {
+      val = __half2float(a.vtail[((long long)bh * a.tail_cap + t) * TQ_D + j]);
+    } else {
+      val = a.vxn[(long long)bh * a.cap + t] * a.vl.c[value_index(a, bh, t, j)];
+    }
+#pragma unroll
+    for (int g = 0; g < TQ_MAX_GROUP; ++g)
+      if (g < a.G) acc[g] = fmaf(sc[g][tt], val, acc[g]);
+  }
+  float* rec = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
+  for (int g = 0; g < a.G; ++g) {
+    if (j == 0) {
+      rec[g * kRec + 0] = s_m[g];
+      rec[g * kRec + 1] = s_l[g];
+    }
+    rec[g * kRec + 2 + j] = acc[g];
+  }
+}
+
+// ---------------------------------------------------------------- 2a. symmetric split decode
+__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
+  __shared__ float qr[TQ_MAX_GROUP][TQ_D];
+  __shared__ float qs[TQ_MAX_GROUP][TQ_D];
+  __shared__ float sc[TQ_MAX_GROUP][kSplit];
+  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int tid = threadIdx.x;
+  int len = a.seq_lens[b];
+  if (len > a.cap) {
+    if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
+    len = a.cap;
+  }
+  const int start = split * kSplit;
+  const int n_tok = max(0, min(start + kSplit, len) - start);
+  for (int g = 0; g < a.G; ++g) {
+    const long long row = (long long)b * a.Hq + kvh * a.G + g;
+    qr[g][tid] = a.qv[row * 2 * TQ_D + tid];
+    qs[g][tid] = a.qv[row * 2 * TQ_D + TQ_D + tid];
+  }
+  __syncthreads();
+  const float qjl = kQjlNum / TQ_D;
+  for (int tt = tid; tt < n_tok; tt += kThreads) {
+    const int t = start + tt;
+    uint4 planes[4];
+    for (int p = 0; p < a.kbits; ++p)
+      planes[p] = *reinterpret_cast<const uint4*>(a.kidx + ((bh * a.kbits + p) * a.cap + t) * 16);
+    const uint4 sg = *reinterpret_cast<const uint4*>(a.ksgn + (bh * a.cap + t) * 16);
+    const float xn = a.kxn[bh * a.cap + t], rn = a.krn[bh * a.cap + t];
+    float mse[TQ_MAX_GROUP], qj[TQ_MAX_GROUP];
+#pragma unroll
+    for (int g = 0; g < TQ_MAX_GROUP; ++g) mse[g] = qj[g] = 0.f;
+    for (int w = 0; w < 4; ++w) {
+      uint32_t pw[4];
+      for (int p = 0; p < 4; ++p) {
+        const uint4 u = planes[p];
+        pw[p] = w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w;
+      }
+      const uint32_t sw = w == 0 ? sg.x : w == 1 ? sg.y : w == 2 ? sg.z : sg.w;
+      for (int bit = 0; bit < 32; ++bit) {
+        const int j = w * 32 + bit;
+        int q = 0;
+        for (int p = 0; p < a.kbits; ++p) q |= ((pw[p] >> bit) & 1) << p;
+        const float c = a.kl.c[q];
+        const float s = ((sw >> bit) & 1) ? 1.f : -1.f;
+#pragma unroll
+        for (int g = 0; g < TQ_MAX_GROUP; ++g) {
+          if (g < a.G) {
+            mse[g] = fmaf(qr[g][j], c, mse[g]);
+            qj[g] = fmaf(qs[g][j], s, qj[g]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < TQ_MAX_GROUP; ++g)
+      if (g < a.G) sc[g][tt] = a.scale * (xn * mse[g] + rn * qjl * qj[g]);
+  }
+  __syncthreads();
+  softmax_and_values(a, sc, n_tok, start, false, bh, split, s_m, s_l);
+}
+
+// ---------------------------------------------------------------- 2b. asymmetric split decode
+__global__ void __launch_bounds__(kThreads) decode_asym_kernel(DecodeArgs a) {
+  __shared__ float qf[TQ_MAX_GROUP][TQ_D];
+  __shared__ float sc[TQ_MAX_GROUP][kSplit];
+  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int tid = threadIdx.x;
+  const bool tail = split >= a.nsplit_main;
+  int len = tail ? a.tail_lens[b] : a.seq_lens[b];
+  const int cap = tail ? a.tail_cap : a.cap;
+  if (len > cap) {
+    if (tid == 0 && (split == 0 || split == a.nsplit_main) && kvh == 0)
+      atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
+    len = cap;
+  }
+  const int start = (tail ? split - a.nsplit_main : split) * kSplit;
+  const int n_tok = max(0, min(start + kSplit, len) - start);
+  for (int g = 0; g < a.G; ++g)
+    qf[g][tid] = load_elem(a.q, a.q_dtype, ((long long)b * a.Hq + kvh * a.G + g) * TQ_D + tid);
+  __syncthreads();
+  const __half* K = tail ? a.ktail : a.kf16;
+  for (int tt = tid; tt < n_tok; tt += kThreads) {
+    const int t = start + tt;
+    const uint4* row = reinterpret_cast<const uint4*>(K + ((long long)bh * cap + t) * TQ_D);
+    float dot[TQ_MAX_GROUP];
+#pragma unroll
+    for (int g = 0; g < TQ_MAX_GROUP; ++g) dot[g] = 0.f;
+    for (int c = 0; c < TQ_D / 8; ++c) {
+      const uint4 u = row[c];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        const int j = c * 8 + 2 * e;
+#pragma unroll
+        for (int g = 0; g < TQ_MAX_GROUP; ++g)
+          if (g < a.G) dot[g] = fmaf(qf[g][j], f.x, fmaf(qf[g][j + 1], f.y, dot[g]));
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < TQ_MAX_GROUP; ++g)
+      if (g < a.G) sc[g][tt] = a.scale * dot[g];
+  }
+  __syncthreads();
+  softmax_and_values(a, sc, n_tok, start, tail, bh, split, s_m, s_l);
+}
+
+// ---------------------------------------------------------------- 3. merge
+__global__ void __launch_bounds__(kThreads) merge_kernel(const float* part, int Hq, int Hkv, int G,
+                                                         int nsplit_main, int nsplit,
+                                                         const float* pi, void* out, int out_dtype) {
+  __shared__ float accR[TQ_D];
+  const int row = blockIdx.x;  // b * Hq + h
+  const int b = row / Hq, h = row % Hq;
+  const int kvh = h / G, g = h % G;
+  const long long bh = (long long)b * Hkv + kvh;
+  const int j = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part[((bh * nsplit + s) * G + g) * kRec]);
+  float L = 0.f, aR = 0.f, aP = 0.f;
+  if (M > -INFINITY) {
+    for (int s = 0; s < nsplit; ++s) {
+      const float* rec = part + ((bh * nsplit + s) * G + g) * kRec;
+      const float l = rec[1];
+      if (!(l > 0.f)) continue;
+      const float w = expf(rec[0] - M);
+      L += w * l;
+      if (s < nsplit_main) aR += w * rec[2 + j];
+      else aP += w * rec[2 + j];
+    }
+  }
+  accR[j] = aR;
+  __syncthreads();
+  float o = 0.f;
+  if (L > 0.f) {
+    float r = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < TQ_D; ++k) r = fmaf(__ldg(&pi[k * TQ_D + j]), accR[k], r);
+    o = (r + aP) / L;
+  }
+  store_elem(out, out_dtype, (long long)row * TQ_D + j, o);
+}
+
+tq_status check_prod_cache(const tq_prod_cache& k) {
+  if (!k.idx || !k.sgn || !k.xnorm || !k.rnorm) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(k.idx) || !aligned16(k.sgn) || !aligned16(k.xnorm) || !aligned16(k.rnorm))
+    return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+
+tq_status check_mse_cache(const tq_mse_cache& v) {
+  if (!v.idx || !v.xnorm) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(v.idx) || !aligned16(v.xnorm)) return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tq_decode_workspace_bytes(const tq_attn_desc* desc) {
+  Plan p;
+  if (!desc) return 0;
+  if (plan(desc, desc->tail_capacity > 0, &p) != TQ_OK) return 0;
+  return p.bytes;
+}
+
+extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc,
+                                         const tq_codec* vc, const void* q, tq_prod_cache k,
+                                         tq_mse_cache v, const int32_t* seq_lens, void* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         tq_stream_t stream_) {
+  Plan p;
+  tq_status st = plan(desc, false, &p);
+  if (st != TQ_OK) return st;
+  if ((st = tq_check_codec(kc, TQ_PROD)) != TQ_OK) return st;
+  if ((st = tq_check_codec(vc, TQ_MSE)) != TQ_OK) return st;
+  if ((st = check_prod_cache(k)) != TQ_OK) return st;
+  if ((st = check_mse_cache(v)) != TQ_OK) return st;
+  if (!q || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < p.bytes)
+    return TQ_ERR_INVALID_ARG;
+  if (desc->batch == 0) return TQ_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  DecodeArgs a{};
+  a.B = desc->batch; a.Hq = desc->q_heads; a.Hkv = desc->kv_heads; a.G = p.G;
+  a.cap = desc->capacity; a.tail_cap = 0;
+  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit;
+  a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)TQ_D);
+  a.qv = reinterpret_cast<const float*>(ws + p.q_off);
+  a.kidx = k.idx; a.ksgn = k.sgn; a.kxn = k.xnorm; a.krn = k.rnorm;
+  a.kbits = kc->ibits; a.kl = tq_make_levels(kc);
+  a.vidx = v.idx; a.vxn = v.xnorm; a.vbits = vc->ibits; a.vl = tq_make_levels(vc);
+  a.seq_lens = seq_lens;
+  a.part = reinterpret_cast<float*>(ws + p.part_off);
+  const int rows = desc->batch * desc->q_heads;
+  query_prep_kernel<<<rows, kThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
+                                                   reinterpret_cast<float*>(ws + p.q_off));
+  decode_kernel<<<dim3(p.nsplit_main, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+  merge_kernel<<<rows, kThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
+                                              vc->d_pi, out, desc->out_dtype);
+  return tq_cuda_status(cudaGetLastError());
+}
+
+extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,
+                                              const void* q, const uint16_t* k_f16,
+                                              tq_mse_cache v, const int32_t* seq_lens,
+                                              const uint16_t* k_tail, const uint16_t* v_tail,
+                                              const int32_t* tail_lens, void* out,
+                                              void* workspace, size_t workspace_bytes,
+                                              tq_stream_t stream_) {
+  Plan p;
+  tq_status st = plan(desc, true, &p);
+  if (st != TQ_OK) return st;
+  if ((st = tq_check_codec(vc, TQ_MSE)) != TQ_OK) return st;
+  if ((st = check_mse_cache(v)) != TQ_OK) return st;
+  if (!q || !k_f16 || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
+  if (desc->tail_capacity > 0 && (!k_tail || !v_tail || !tail_lens)) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(k_f16) || (k_tail && !aligned16(k_tail)) || (v_tail && !aligned16(v_tail)))
+    return TQ_ERR_INVALID_ARG;
+  if (desc->tail_capacity % 8) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < p.bytes)
+    return TQ_ERR_INVALID_ARG;
+  if (desc->batch == 0) return TQ_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  DecodeArgs a{};
+  a.B = desc->batch; a.Hq = desc->q_heads; a.Hkv = desc->kv_heads; a.G = p.G;
+  a.cap = desc->capacity; a.tail_cap = desc->tail_capacity;
+  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit;
+  a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)TQ_D);
+  a.q = q; a.q_dtype = desc->q_dtype;
+  a.kf16 = reinterpret_cast<const __half*>(k_f16);
+  a.ktail = reinterpret_cast<const __half*>(k_tail);
+  a.vtail = reinterpret_cast<const __half*>(v_tail);
+  a.tail_lens = tail_lens;
+  a.vidx = v.idx; a.vxn = v.xnorm; a.vbits = vc->ibits; a.vl = tq_make_levels(vc);
+  a.seq_lens = seq_lens;
+  a.part = reinterpret_cast<float*>(ws + p.part_off);
+  const int rows = desc->batch * desc->q_heads;
+  decode_asym_kernel<<<dim3(p.nsplit, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+  merge_kernel<<<rows, kThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
+                                              vc->d_pi, out, desc->out_dtype);
+  return tq_cuda_status(cudaGetLastError());
+}

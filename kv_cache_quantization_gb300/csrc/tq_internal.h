@@ -1,0 +1,59 @@
+// Internal definitions shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tq.h"
+
+#define TQ_D 128
+
+// Codec: immutable after creation.  Small constants travel to kernels by value.
+struct tq_codec {
+  int d;
+  tq_kind kind;
+  int bits;        // total bits (prod) or index bits (mse)
+  int ibits;       // index bits
+  int levels;      // 2^ibits
+  int device;
+  float* d_pi;     // Π   row-major [d][d]
+  float* d_piT;    // Πᵀ  row-major [d][d]  (PT[k][j] = Π[j][k])
+  float* d_sT;     // Sᵀ  row-major [d][d]  (prod only)
+  float* d_mT;     // Mᵀ  row-major [d][d], M = S Πᵀ (prod only)
+  float centroids[16];
+  float boundaries[16];
+};
+
+// Constants passed by value to kernels.
+struct tq_levels {
+  float c[16];
+  float b[16];
+  int levels;
+};
+
+// Device status words.  Kernels are compiled without relocatable device code, so every
+// translation unit that raises flags owns its word and a host function that reads and
+// clears it (on the current device); tq_device_status() ORs them together.
+#ifdef __CUDACC__
+#define TQ_DEFINE_FLAGS(reader)                                               \
+  static __device__ unsigned int g_tq_flags = 0;                              \
+  unsigned int reader() {                                                     \
+    unsigned int v = 0, z = 0;                                                \
+    if (cudaMemcpyFromSymbol(&v, g_tq_flags, sizeof(v)) != cudaSuccess) return ~0u; \
+    if (cudaMemcpyToSymbol(g_tq_flags, &z, sizeof(z)) != cudaSuccess) return ~0u;   \
+    return v;                                                                 \
+  }
+#endif
+unsigned int tq_take_flags_quantize();
+unsigned int tq_take_flags_attention();
+
+static inline tq_status tq_cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// Host helpers implemented in host.cpp
+tq_status tq_check_codec(const tq_codec* c, tq_kind kind);
+int tq_num_sms();
+
+// Launch helpers implemented in the .cu files
+tq_levels tq_make_levels(const tq_codec* c);

@@ -1,0 +1,134 @@
+"""Helpers for comparing the CUDA library with the CPU oracle.
+
+Codes: indices and sign bits must be bit-identical to the oracle's, except at coordinates
+whose rotated value lies within 1e-6 of a decision boundary (either neighbouring cell is a
+valid output there).  For every vector with such coordinates the oracle enumerates all
+valid index choices and their second-stage codes; the GPU's code must equal one of them.
+Sign bits are compared for the matching choice, except where |(S r)_j|/‖x‖ < 1e-6·√d.
+Attention is then compared against the oracle evaluated on the matching (oracle-computed)
+codes, so both sides attend the same code choice.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+import oracle.turboquant as o
+from kv_cache_quantization_gb300.synth import gaussian_matrix, layer_seeds
+
+D = 128
+MAX_AMBIGUOUS = 6
+
+
+def oracle_constants(layer=0):
+    sp, ss = layer_seeds(layer)
+    return o.rotation_from_gaussian(gaussian_matrix(sp)), gaussian_matrix(ss)
+
+
+def oracle_codebook(index_bits):
+    return o.lloyd_max_codebook(D, index_bits)[0]
+
+
+class CodeStats:
+    def __init__(self):
+        self.coords = 0
+        self.idx_excluded = 0
+        self.idx_flipped = 0
+        self.sign_excluded = 0
+        self.vectors_dropped = 0
+
+    def __repr__(self):
+        return (f"coords={self.coords} idx_excluded={self.idx_excluded} "
+                f"idx_flipped={self.idx_flipped} sign_excluded={self.sign_excluded} "
+                f"vectors_dropped={self.vectors_dropped}")
+
+
+def _variants(idx_row, excl_row, alt_row):
+    """All index rows obtained by choosing either cell at each ambiguous coordinate."""
+    pos = np.nonzero(excl_row)[0]
+    for choice in itertools.product((False, True), repeat=len(pos)):
+        v = idx_row.copy()
+        for p, use_alt in zip(pos, choice):
+            if use_alt:
+                v[p] = alt_row[p]
+        yield v
+
+
+def match_prod_codes(x, gpu_idx, gpu_sign, gpu_xn, gpu_rn, pi, s, c, stats: CodeStats):
+    """x: float64 [n, d]; gpu_idx: int [n, d]; gpu_sign: uint8 [n, d].  Checks the GPU codes
+    against the oracle and returns the oracle codes (dict) for the GPU's valid choice."""
+    k = o.quantize_prod(x, pi, s, c)
+    excl, alt = o.boundary_exclusion(k["y"], c)
+    stats.coords += x.size
+    stats.idx_excluded += int(excl.sum())
+    diff = gpu_idx != k["idx"]
+    bad = diff & ~excl
+    assert not bad.any(), f"{int(bad.sum())} index codes differ away from any boundary"
+    idx = k["idx"].copy()
+    sign = k["sign"].copy()
+    gamma = k["gamma"].copy()
+    z = k["z"].copy()
+    drop = np.zeros(len(x), dtype=bool)
+    for v in np.nonzero(diff.any(axis=1))[0]:
+        stats.idx_flipped += int(diff[v].sum())
+        if excl[v].sum() > MAX_AMBIGUOUS:
+            drop[v] = True
+            continue
+        found = False
+        for cand in _variants(k["idx"][v], excl[v], alt[v]):
+            if np.array_equal(cand, gpu_idx[v]):
+                sg, gm, zz = o.prod_residual(x[v:v + 1], k["n"][v:v + 1], cand[None], pi, s, c)
+                idx[v], sign[v], gamma[v], z[v] = cand, sg[0], gm[0], zz[0]
+                found = True
+                break
+        assert found, f"vector {v}: GPU index choice is not a valid alternative"
+    stats.vectors_dropped += int(drop.sum())
+    sx = o.sign_exclusion(z, k["n"], D)
+    sx[drop] = True
+    stats.sign_excluded += int(sx.sum())
+    sbad = (gpu_sign.astype(bool) != sign) & ~sx
+    assert not sbad.any(), f"{int(sbad.sum())} sign bits differ (vectors {np.nonzero(sbad.any(1))[0][:8]})"
+    np.testing.assert_allclose(gpu_xn, k["n"], rtol=2e-6, atol=1e-30)
+    ok = ~drop
+    np.testing.assert_allclose(gpu_rn[ok], gamma[ok], rtol=2e-5, atol=2e-6 * (k["n"][ok].max() if ok.any() else 1))
+    return {"idx": idx, "sign": sign, "n": k["n"], "gamma": gamma, "drop": drop}
+
+
+def match_mse_codes(x, gpu_idx, gpu_xn, pi, c, stats: CodeStats):
+    idx, n, y = o.quantize_mse(x, pi, c)
+    excl, alt = o.boundary_exclusion(y, c)
+    stats.coords += x.size
+    stats.idx_excluded += int(excl.sum())
+    diff = gpu_idx != idx
+    assert not (diff & ~excl).any(), f"{int((diff & ~excl).sum())} MSE codes differ"
+    assert np.all(gpu_idx[diff] == alt[diff]), "GPU MSE code is not a valid alternative"
+    stats.idx_flipped += int(diff.sum())
+    np.testing.assert_allclose(gpu_xn, n, rtol=2e-6, atol=1e-30)
+    # where the GPU took the other valid cell, use the oracle's alternative for that cell
+    return {"idx": np.where(diff, alt, idx), "n": n}
+
+
+# ---------------------------------------------------------------- unpacking GPU caches
+
+def unpack_prod(cache, b, h, n, ibits):
+    """GPU prod cache (torch tensors) of (b, h), tokens < n -> numpy codes."""
+    planes = cache.idx[b, h, :, :n].permute(1, 0, 2).cpu().numpy()   # [n, ibits, 16]
+    idx = o.unpack_index_planes(planes, D)
+    sign = o.unpack_bits(cache.sgn[b, h, :n].cpu().numpy(), D)
+    return idx, sign, cache.xnorm[b, h, :n].double().cpu().numpy(), cache.rnorm[b, h, :n].double().cpu().numpy()
+
+
+def unpack_mse(cache, b, h, n, bits):
+    if bits == 4:
+        idx = o.unpack_nibbles(cache.idx[b, h, :n].cpu().numpy(), D)
+    else:
+        idx = o.unpack_index_planes(cache.idx[b, h, :, :n].permute(1, 0, 2).cpu().numpy(), D)
+    return idx, cache.xnorm[b, h, :n].double().cpu().numpy()
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))

@@ -1,0 +1,304 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+Tolerances: index and sign codes bit-exact outside the boundary exclusions (see parity.py);
+scores within 1e-4·‖q‖‖k‖; attention outputs within relative L2 1e-3 (fp32 out) or 1e-2
+(bf16/fp16 out).  Excluded coordinates must stay below 1e-4 of all coordinates.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.turboquant as o
+from kv_cache_quantization_gb300 import _binding as B
+from kv_cache_quantization_gb300 import api, synth
+from parity import (CodeStats, match_mse_codes, match_prod_codes, oracle_codebook,
+                    oracle_constants, rel_l2, unpack_mse, unpack_prod)
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def rand_x(shape, seed, dtype, lognormal=True, device="cuda"):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(*shape, generator=g, device=device)
+    if lognormal:
+        sc = torch.exp(0.5 * torch.randn(shape[-1], generator=g, device=device))
+        x = x * sc
+    return x.to(dtype)
+
+
+def out_tol(dt):
+    return 1e-3 if dt == torch.float32 else 1e-2
+
+
+def check_flags_clear():
+    st, flags = api.device_status()
+    assert st == B.TQ_OK and flags == 0, f"device status flags {flags:#x}"
+
+
+# ------------------------------------------------------------------ quantisation
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_quantize_prod_codes(bits, dtype):
+    bsz, h, t = 2, 3, 333
+    x = rand_x((bsz, h, t, D), 100 + bits, dtype)
+    x[0, 1, 5] = 0          # zero vector
+    x[1, 2, 7] *= 1e-3      # tiny vector
+    kc = api.Codec.prod(bits)
+    cache = api.ProdCache.empty(bsz, h, t, bits)
+    api.quantize_prod(kc, x, cache)
+    check_flags_clear()
+    pi, s = oracle_constants()
+    c = oracle_codebook(bits - 1)
+    stats = CodeStats()
+    for b in range(bsz):
+        for hh in range(h):
+            gi, gs, gx, gr = unpack_prod(cache, b, hh, t, bits - 1)
+            match_prod_codes(x[b, hh].double().cpu().numpy(), gi, gs, gx, gr, pi, s, c, stats)
+    assert stats.idx_excluded + stats.sign_excluded < 1e-4 * stats.coords * 2 + 2, stats
+    # zero vector: all signs one, norms zero
+    assert cache.sgn[0, 1, 5].cpu().numpy().tolist() == [255] * 16
+    assert cache.xnorm[0, 1, 5].item() == 0 and cache.rnorm[0, 1, 5].item() == 0
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_mse_codes(bits, dtype):
+    bsz, h, t = 2, 2, 517
+    x = rand_x((bsz, h, t, D), 200 + bits, dtype)
+    vc = api.Codec.mse(bits)
+    cache = api.MSECache.empty(bsz, h, t, bits)
+    api.quantize_mse(vc, x, cache)
+    check_flags_clear()
+    pi, _ = oracle_constants()
+    c = oracle_codebook(bits)
+    stats = CodeStats()
+    for b in range(bsz):
+        for hh in range(h):
+            gi, gx = unpack_mse(cache, b, hh, t, bits)
+            match_mse_codes(x[b, hh].double().cpu().numpy(), gi, gx, pi, c, stats)
+    assert stats.idx_excluded < 1e-4 * stats.coords + 2, stats
+
+
+def test_quantize_positions_and_counts():
+    """Appends land at pos[b] + t for t < count[b]; other slots stay untouched."""
+    bsz, h, t, cap = 3, 2, 5, 128
+    x = rand_x((bsz, h, t, D), 7, torch.bfloat16)
+    kc = api.Codec.prod(3)
+    cache = api.ProdCache.empty(bsz, h, cap, 3)
+    cache.xnorm.fill_(-1)
+    pos = torch.tensor([0, 10, 120], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([5, 2, 0], dtype=torch.int32, device="cuda")
+    api.quantize_prod(kc, x, cache, pos=pos, count=cnt)
+    check_flags_clear()
+    xn = cache.xnorm.cpu()
+    ref = x.float().norm(dim=-1).cpu()
+    assert torch.allclose(xn[0, :, :5], ref[0], rtol=1e-6)
+    assert torch.allclose(xn[1, :, 10:12], ref[1, :, :2], rtol=1e-6)
+    assert (xn[0, :, 5:] == -1).all() and (xn[1, :, :10] == -1).all() and (xn[1, :, 12:] == -1).all()
+    assert (xn[2] == -1).all()
+
+
+def test_quantize_overflow_flag():
+    """A token past the capacity is skipped and raises TQ_FLAG_POS_OVERFLOW."""
+    x = rand_x((1, 1, 4, D), 8, torch.bfloat16)
+    kc = api.Codec.prod(3)
+    cache = api.ProdCache.empty(1, 1, 64, 3)
+    pos = torch.tensor([62], dtype=torch.int32, device="cuda")
+    api.quantize_prod(kc, x, cache, pos=pos)
+    st, flags = api.device_status()
+    assert st == B.TQ_ERR_DEVICE_STATUS and flags & B.TQ_FLAG_POS_OVERFLOW
+    assert cache.xnorm[0, 0, 62].item() > 0 and cache.xnorm[0, 0, 63].item() > 0
+    check_flags_clear()
+
+
+# ------------------------------------------------------------------ scores (1024 keys x 64 queries)
+
+def test_scores_fp32_1k():
+    w = synth.SCORES_1K
+    k, _ = synth.make_kv(w, device="cuda")
+    q = synth.make_queries(w, device="cuda")[0, 0]                  # [64, 128] fp32
+    kc = api.Codec.prod(w.k_bits)
+    cache = api.ProdCache.empty(1, 1, w.context, w.k_bits)
+    api.quantize_prod(kc, k, cache)
+    scores = api.prod_scores(kc, q, cache, w.context).double().cpu().numpy()
+    check_flags_clear()
+    pi, s = oracle_constants()
+    c = oracle_codebook(w.k_bits - 1)
+    stats = CodeStats()
+    x = k[0, 0].double().cpu().numpy()
+    gi, gs, gx, gr = unpack_prod(cache, 0, 0, w.context, w.k_bits - 1)
+    codes = match_prod_codes(x, gi, gs, gx, gr, pi, s, c, stats)
+    qn = q.double().cpu().numpy()
+    ref = o.prod_scores(qn, codes["idx"], codes["sign"], codes["n"], codes["gamma"], pi, s, c)
+    bound = 1e-4 * np.linalg.norm(qn, axis=1)[:, None] * codes["n"][None, :]
+    err = np.abs(scores - ref)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
+    assert stats.idx_excluded < 1e-4 * stats.coords + 2
+
+
+# ------------------------------------------------------------------ decode attention
+
+def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sample=None,
+               q_dtype=None, zero_tokens=()):
+    cap = max(64, (max(lens) + 63) // 64 * 64)
+    k = rand_x((batch, hkv, cap, D), seed, in_dtype)
+    v = rand_x((batch, hkv, cap, D), seed + 1, in_dtype)
+    for (b, h, t) in zero_tokens:
+        k[b, h, t] = 0
+        v[b, h, t] = 0
+    q = rand_x((batch, hq, D), seed + 2, q_dtype or in_dtype)
+    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits)
+    kcache = api.ProdCache.empty(batch, hkv, cap, kbits)
+    vcache = api.MSECache.empty(batch, hkv, cap, vbits)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    api.quantize_prod(kc, k, kcache, count=lens_t)
+    api.quantize_mse(vc, v, vcache, count=lens_t)
+    plan = api.DecodePlan(batch, hq, hkv, cap, max(lens), q.dtype, out_dtype)
+    out = plan.new_out()
+    plan.run(kc, vc, q, kcache, vcache, lens_t, out)
+    got = out.double().cpu().numpy()
+    check_flags_clear()
+    pi, s = oracle_constants()
+    ck, cv = oracle_codebook(kbits - 1), oracle_codebook(vbits)
+    g = hq // hkv
+    stats = CodeStats()
+    worst = 0.0
+    pairs = sample or [(b, h) for b in range(batch) for h in range(hkv)]
+    for b, h in pairs:
+        n = lens[b]
+        qq = q[b, h * g:(h + 1) * g].double().cpu().numpy()[None]
+        if n == 0:
+            assert np.all(got[b, h * g:(h + 1) * g] == 0)
+            continue
+        gi, gs, gx, gr = unpack_prod(kcache, b, h, n, kbits - 1)
+        kcodes = match_prod_codes(k[b, h, :n].double().cpu().numpy(), gi, gs, gx, gr, pi, s, ck, stats)
+        assert not kcodes["drop"].any()
+        vi, vx = unpack_mse(vcache, b, h, n, vbits)
+        vcodes = match_mse_codes(v[b, h, :n].double().cpu().numpy(), vi, vx, pi, cv, stats)
+        kd = {key: kcodes[key][None, None] for key in ("idx", "sign", "n", "gamma")}
+        vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
+        ref = o.decode_attention(qq, kd, vd, [n], pi, s, ck, cv)[0]
+        err = rel_l2(got[b, h * g:(h + 1) * g], ref)
+        worst = max(worst, err)
+        assert err < out_tol(out_dtype), f"(b={b}, kv head={h}) rel L2 {err:.3g}"
+    assert stats.idx_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
+    return worst
+
+
+@pytest.mark.parametrize("kbits,vbits", [(3, 4), (3, 2), (4, 4), (2, 1), (5, 3)])
+def test_decode_small(kbits, vbits):
+    run_decode(2, 8, 2, [300, 1000], kbits, vbits, torch.bfloat16, torch.float32, 300 + kbits)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_decode_out_dtypes(out_dtype):
+    run_decode(1, 7, 1, [777], 3, 4, torch.bfloat16, out_dtype, 400, q_dtype=torch.float32)
+
+
+def test_decode_edge_lengths():
+    """Empty, single-token, exactly-one-split and capacity-filling sequences, a zero vector,
+    and plain multi-head attention (G = 1)."""
+    run_decode(5, 4, 4, [0, 1, 256, 257, 1024], 3, 4, torch.bfloat16, torch.float32, 500,
+               zero_tokens=[(1, 0, 0), (4, 3, 100)])
+
+
+def test_decode_group_of_eight():
+    run_decode(1, 16, 2, [640], 3, 4, torch.float16, torch.float32, 600)
+
+
+def test_decode_qwen7b_32k():
+    """One decode step, B=1, 28/4 heads, 32768 tokens, K 3-bit prod, V 4-bit MSE, bf16."""
+    w = synth.DECODE_32K
+    kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
+    k, v = synth.make_kv(w, device="cuda")
+    q = synth.make_queries(w, device="cuda")[:, :, 0]
+    lens = synth.seq_lengths(w)
+    kcache = api.ProdCache.empty(w.batch, w.kv_heads, w.context, w.k_bits)
+    vcache = api.MSECache.empty(w.batch, w.kv_heads, w.context, w.v_bits)
+    api.quantize_prod(kc, k, kcache)
+    api.quantize_mse(vc, v, vcache)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, w.context, q.dtype, w.out_dtype)
+    out = plan.run(kc, vc, q, kcache, vcache, lens_t, plan.new_out()).double().cpu().numpy()
+    check_flags_clear()
+    pi, s = oracle_constants()
+    ck, cv = oracle_codebook(w.k_bits - 1), oracle_codebook(w.v_bits)
+    g = w.group
+    stats = CodeStats()
+    for h in range(w.kv_heads):
+        n = int(lens[0])
+        gi, gs, gx, gr = unpack_prod(kcache, 0, h, n, w.k_bits - 1)
+        kcodes = match_prod_codes(k[0, h, :n].double().cpu().numpy(), gi, gs, gx, gr, pi, s, ck, stats)
+        vi, vx = unpack_mse(vcache, 0, h, n, w.v_bits)
+        vcodes = match_mse_codes(v[0, h, :n].double().cpu().numpy(), vi, vx, pi, cv, stats)
+        kd = {key: kcodes[key][None, None] for key in ("idx", "sign", "n", "gamma")}
+        vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
+        ref = o.decode_attention(q[0:1, h * g:(h + 1) * g].double().cpu().numpy(), kd, vd, [n],
+                                 pi, s, ck, cv)[0]
+        err = rel_l2(out[0, h * g:(h + 1) * g], ref)
+        assert err < 1e-3, f"kv head {h}: rel L2 {err:.3g}"
+    assert stats.idx_excluded + stats.sign_excluded < 1e-4 * stats.coords * 2, stats
+
+
+# ------------------------------------------------------------------ asymmetric mode
+
+def run_asym(batch, hq, hkv, lens, tlens, vbits, out_dtype, seed, tail_cap=256, sample=None):
+    cap = max(64, (max(lens) + 63) // 64 * 64)
+    k = rand_x((batch, hkv, cap, D), seed, torch.bfloat16).to(torch.float16)
+    v = rand_x((batch, hkv, cap, D), seed + 1, torch.bfloat16)
+    kt = rand_x((batch, hkv, tail_cap, D), seed + 2, torch.bfloat16).to(torch.float16)
+    vt = rand_x((batch, hkv, tail_cap, D), seed + 3, torch.bfloat16).to(torch.float16)
+    q = rand_x((batch, hq, D), seed + 4, torch.bfloat16)
+    vc = api.Codec.mse(vbits)
+    vcache = api.MSECache.empty(batch, hkv, cap, vbits)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    tl_t = torch.tensor(tlens, dtype=torch.int32, device="cuda")
+    api.quantize_mse(vc, v, vcache, count=lens_t)
+    plan = api.DecodePlan(batch, hq, hkv, cap, max(lens), q.dtype, out_dtype, tail_capacity=tail_cap)
+    out = plan.run_asym(vc, q, k, vcache, lens_t, kt, vt, tl_t, plan.new_out())
+    got = out.double().cpu().numpy()
+    check_flags_clear()
+    pi, _ = oracle_constants()
+    cv = oracle_codebook(vbits)
+    g = hq // hkv
+    stats = CodeStats()
+    for b, h in (sample or [(b, h) for b in range(batch) for h in range(hkv)]):
+        n, tl = lens[b], tlens[b]
+        vi, vx = unpack_mse(vcache, b, h, n, vbits)
+        vcodes = match_mse_codes(v[b, h, :n].double().cpu().numpy(), vi, vx, pi, cv, stats)
+        vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
+        ref = o.decode_attention_asym(q[b:b + 1, h * g:(h + 1) * g].double().cpu().numpy(),
+                                      k[b:b + 1, h:h + 1, :n].double().cpu().numpy(), vd, [n],
+                                      kt[b:b + 1, h:h + 1].double().cpu().numpy(),
+                                      vt[b:b + 1, h:h + 1].double().cpu().numpy(), [tl], pi, cv)[0]
+        if n + tl == 0:
+            assert np.all(got[b, h * g:(h + 1) * g] == 0)
+            continue
+        err = rel_l2(got[b, h * g:(h + 1) * g], ref)
+        assert err < out_tol(out_dtype), f"(b={b}, kv head={h}) rel L2 {err:.3g}"
+
+
+def test_asym_small():
+    run_asym(3, 8, 2, [100, 0, 700], [255, 17, 0], 4, torch.float32, 700)
+
+
+def test_asym_b8_8k():
+    """B=8, 28/4 heads, 7937 FP16-key / 4-bit-value tokens + 255 FP16 tail tokens, bf16 out."""
+    w = synth.ASYM_8K
+    lens = [int(x) for x in synth.seq_lengths(w)]
+    run_asym(w.batch, w.q_heads, w.kv_heads, lens, [w.tail] * w.batch, w.v_bits, w.out_dtype, 800,
+             sample=[(0, 0), (3, 1), (7, 3)])
