@@ -1,0 +1,412 @@
+"""Benchmark: one decode step of compressed-KV attention (quantise the new token's K and V
+into the packed cache, then decode attention over the whole packed context), on the
+Qwen2.5-7B-shaped GQA layer: batch 1, 28 query / 4 KV heads, head_dim 128, 32768 tokens,
+K 3-bit product code, V 4-bit MSE code, bf16 inputs.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
+Metric: KV tokens/s = (tokens attended per sequence, summed over the batch) / step time.
+Multi-GPU (torchrun): every rank runs its own independent batch (weak scaling, no
+data-path collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode attention: KV tokens/s and % of GB300 HBM roofline"
+UNIT = "KV tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks sampling
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ our implementation
+
+def run_ours(args):
+    import torch
+
+    from kv_cache_quantization_gb300 import api, synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.WORKLOADS[args.workload]
+    ctx = w.context
+    n_pre = ctx - 1                              # cached tokens before this step
+    kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
+
+    # Prefill compaction: quantise the cached tokens once (not part of the timed step).
+    k, v = synth.make_kv(w, device=dev)
+    base_k = api.ProdCache.empty(w.batch, w.kv_heads, ctx, w.k_bits, device=dev)
+    base_v = api.MSECache.empty(w.batch, w.kv_heads, ctx, w.v_bits, device=dev)
+    pre = torch.full((w.batch,), n_pre, dtype=torch.int32, device=dev)
+    api.quantize_prod(kc, k, base_k, count=pre)
+    api.quantize_mse(vc, v, base_v, count=pre)
+    torch.cuda.synchronize()
+    # compaction throughput (full cache, K and V), reported as an extra
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    api.quantize_prod(kc, k, base_k, count=pre)
+    api.quantize_mse(vc, v, base_v, count=pre)
+    ev1.record()
+    torch.cuda.synchronize()
+    compaction_ms = ev0.elapsed_time(ev1)
+    del k, v
+
+    # Rotate several cache copies so that each timed step reads from HBM, not L2.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = base_k.nbytes() + base_v.nbytes()
+    copies = max(3, math.ceil(3 * l2 / per_copy))
+    kcs = [base_k] + [api.ProdCache(*(t.clone() for t in (base_k.idx, base_k.sgn, base_k.xnorm,
+                                                          base_k.rnorm))) for _ in range(copies - 1)]
+    vcs = [base_v] + [api.MSECache(base_v.idx.clone(), base_v.xnorm.clone(), w.v_bits)
+                      for _ in range(copies - 1)]
+    steps_q = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
+    steps_kv = [synth.make_new_tokens(w, device=dev, step=i) for i in range(4)]
+    pos = torch.full((w.batch,), n_pre, dtype=torch.int32, device=dev)
+    lens = torch.full((w.batch,), ctx, dtype=torch.int32, device=dev)
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, ctx, ctx, w.in_dtype, w.out_dtype,
+                          device=dev)
+    out = plan.new_out(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, kv_new=None, q=None):
+        kn, vn = kv_new if kv_new is not None else steps_kv[i % 4]
+        c = i % copies
+        api.quantize_prod(kc, kn, kcs[c], pos=pos, stream=stream)
+        api.quantize_mse(vc, vn, vcs[c], pos=pos, stream=stream)
+        plan.run(kc, vc, steps_q[i % 4] if q is None else q, kcs[c], vcs[c], lens, out,
+                 stream=stream)
+
+    launches_per_step = 2 + 3   # quantise K, quantise V, query prep, split decode, merge
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        barrier(ws)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            kn, vn = steps_kv[i % 4]
+            c = i % copies
+            api.quantize_prod(kc, kn, kcs[c], pos=pos, stream=stream)
+            api.quantize_mse(vc, vn, vcs[c], pos=pos, stream=stream)
+            mids[i].record(stream)
+            plan.run(kc, vc, steps_q[i % 4], kcs[c], vcs[c], lens, out, stream=stream)
+            ends[i].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    total_ms = t_all0.elapsed_time(t_all1)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dec_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    ms_per_step = max_over_ranks(total_ms / args.steps, ws, dev)
+    dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), ws, dev)
+
+    tokens_per_step = w.batch * ctx
+    value = tokens_per_step * ws / (ms_per_step * 1e-3)
+    # algorithmic bytes of one decode-attention call: packed K and V codes of every cached
+    # token and head, the query and the output
+    from kv_cache_quantization_gb300 import _binding as Bn
+    code_bytes = (Bn.tq_code_bytes(Bn.TQ_PROD, w.k_bits) + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
+    dec_bytes = (w.batch * w.kv_heads * ctx * code_bytes
+                 + w.batch * w.q_heads * 128 * (2 + torch.finfo(w.out_dtype).bits // 8))
+    peak, peak_kind = read_peaks()
+    achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get(args.workload)
+        except Exception:
+            traffic = None
+
+    # ---------------- end to end through the public API with host buffers
+    q_host = [steps_q[i].cpu().pin_memory() for i in range(4)]
+    kv_host = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in steps_kv]
+    q_dev = torch.empty_like(steps_q[0])
+    k_dev = torch.empty_like(steps_kv[0][0])
+    v_dev = torch.empty_like(steps_kv[0][1])
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = q_dev.numel() * q_dev.element_size() + 2 * k_dev.numel() * k_dev.element_size()
+    d2h = out.numel() * out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0.record(stream)
+    for i in range(args.steps):
+        q_dev.copy_(q_host[i % 4], non_blocking=True)
+        k_dev.copy_(kv_host[i % 4][0], non_blocking=True)
+        v_dev.copy_(kv_host[i % 4][1], non_blocking=True)
+        step(i, (k_dev, v_dev), q_dev)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in / fp32 accumulate on packed K3/V4 codes",
+        "data": "synthetic (seeded N(0,1) x lognormal(0,0.5) per channel)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
+                   "kv_heads": w.kv_heads, "head_dim": 128, "context": ctx,
+                   "k_bits": w.k_bits, "v_bits": w.v_bits,
+                   "parallelism": f"replicas x{ws} (independent batches)",
+                   "l2": f"{copies} rotating cache copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
+                   "step": "quantise new K,V token + decode attention over all tokens"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "tq_decode_attention (query prep + split decode + merge)",
+                     "algorithmic_bytes": dec_bytes, "ms": dec_mean,
+                     "peak_source": peak_kind},
+        "e2e": {"value": tokens_per_step * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "compaction": {"tokens": w.batch * w.kv_heads * n_pre, "ms": compaction_ms,
+                       "vectors_per_s": 2 * w.batch * w.kv_heads * n_pre / (compaction_ms * 1e-3)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ the CPU oracle
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle (as it stands): one KV head's GQA
+    group over a prefix of the context.  One repetition quantises the sample's K and V and
+    runs decode attention over it."""
+
+    def __init__(self, w, sample_tokens=4096):
+        import oracle.turboquant as o
+        from kv_cache_quantization_gb300 import synth
+        from kv_cache_quantization_gb300.synth import gaussian_matrix, layer_seeds
+
+        self.o = o
+        self.w = w
+        self.n = min(w.context, sample_tokens)
+        k, v = synth.make_kv(w, device="cpu", tokens=self.n)
+        q = synth.make_queries(w, device="cpu")[:, :, 0]
+        sp, ss = layer_seeds(w.layer)
+        self.pi, self.s = o.rotation_from_gaussian(gaussian_matrix(sp)), gaussian_matrix(ss)
+        self.ck = o.lloyd_max_codebook(128, w.k_bits - 1)[0]
+        self.cv = o.lloyd_max_codebook(128, w.v_bits)[0]
+        self.kx = k[0, 0].double().numpy()
+        self.vx = v[0, 0].double().numpy()
+        self.q = q[0:1, :w.group].double().numpy()
+
+    def rep(self):
+        o = self.o
+        kq = o.quantize_prod(self.kx, self.pi, self.s, self.ck)
+        vi, vn, _ = o.quantize_mse(self.vx, self.pi, self.cv)
+        o.decode_attention(self.q, {k: kq[k][None, None] for k in ("idx", "sign", "n", "gamma")},
+                           {"idx": vi[None, None], "n": vn[None, None]}, [self.n], self.pi,
+                           self.s, self.ck, self.cv)
+
+    def tokens_per_s(self, seconds_per_rep):
+        """KV tokens/s of a whole step equivalent: one of kv_heads heads per repetition."""
+        return self.n / (seconds_per_rep * self.w.kv_heads)
+
+    def describe(self, reps, el):
+        return (f"1 of {self.w.kv_heads} KV heads (its {self.w.group} query heads), {self.n} of "
+                f"{self.w.context} tokens; quantise K/V + attention; {reps} reps in {el:.1f} s")
+
+
+def oracle_baseline(w, budget_s=15.0):
+    """cpu_baseline object: the oracle timed on its bounded sample for about budget_s."""
+    smp = OracleSample(w)
+    smp.rep()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        smp.rep()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s:
+            break
+    return {"value": smp.tokens_per_s(el / reps), "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle", "sample": smp.describe(reps, el)}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, W warm-up and K timed steps,
+    each step one repetition of the bounded sample.  Only rank 0 runs."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from kv_cache_quantization_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    # size the sample so that the whole run stays within a few minutes
+    smp = OracleSample(w, sample_tokens=1024 if args.steps + args.warmup > 60 else 4096)
+    for _ in range(args.warmup):
+        smp.rep()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        smp.rep()
+    el = time.perf_counter() - t0
+    value = smp.tokens_per_s(el / args.steps)
+    ms = w.batch * w.context / value * 1e3
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                         "sample": smp.describe(args.steps, el)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_gqa28x4_ctx32768_k3v4")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -61,8 +61,9 @@ def match_prod_codes(x, gpu_idx, gpu_sign, gpu_xn, gpu_rn, pi, s, c, stats: Code
     against the oracle and returns the oracle codes (dict) for the GPU's valid choice."""
     k = o.quantize_prod(x, pi, s, c)
     excl, alt = o.boundary_exclusion(k["y"], c)
-    stats.coords += x.size
-    stats.idx_excluded += int(excl.sum())
+    nz = k["n"] > 0          # a zero vector sits on the middle boundary by definition
+    stats.coords += int(nz.sum()) * x.shape[-1]
+    stats.idx_excluded += int(excl[nz].sum())
     diff = gpu_idx != k["idx"]
     bad = diff & ~excl
     assert not bad.any(), f"{int(bad.sum())} index codes differ away from any boundary"
@@ -87,7 +88,7 @@ def match_prod_codes(x, gpu_idx, gpu_sign, gpu_xn, gpu_rn, pi, s, c, stats: Code
     stats.vectors_dropped += int(drop.sum())
     sx = o.sign_exclusion(z, k["n"], D)
     sx[drop] = True
-    stats.sign_excluded += int(sx.sum())
+    stats.sign_excluded += int(sx[nz].sum())
     sbad = (gpu_sign.astype(bool) != sign) & ~sx
     assert not sbad.any(), f"{int(sbad.sum())} sign bits differ (vectors {np.nonzero(sbad.any(1))[0][:8]})"
     np.testing.assert_allclose(gpu_xn, k["n"], rtol=2e-6, atol=1e-30)
@@ -99,8 +100,9 @@ def match_prod_codes(x, gpu_idx, gpu_sign, gpu_xn, gpu_rn, pi, s, c, stats: Code
 def match_mse_codes(x, gpu_idx, gpu_xn, pi, c, stats: CodeStats):
     idx, n, y = o.quantize_mse(x, pi, c)
     excl, alt = o.boundary_exclusion(y, c)
-    stats.coords += x.size
-    stats.idx_excluded += int(excl.sum())
+    nz = n > 0
+    stats.coords += int(nz.sum()) * x.shape[-1]
+    stats.idx_excluded += int(excl[nz].sum())
     diff = gpu_idx != idx
     assert not (diff & ~excl).any(), f"{int((diff & ~excl).sum())} MSE codes differ"
     assert np.all(gpu_idx[diff] == alt[diff]), "GPU MSE code is not a valid alternative"

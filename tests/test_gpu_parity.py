@@ -68,7 +68,8 @@ def test_quantize_prod_codes(bits, dtype):
         for hh in range(h):
             gi, gs, gx, gr = unpack_prod(cache, b, hh, t, bits - 1)
             match_prod_codes(x[b, hh].double().cpu().numpy(), gi, gs, gx, gr, pi, s, c, stats)
-    assert stats.idx_excluded + stats.sign_excluded < 1e-4 * stats.coords * 2 + 2, stats
+    assert stats.idx_excluded < 1e-4 * stats.coords + 3, stats
+    assert stats.sign_excluded < 1e-4 * stats.coords + 3, stats
     # zero vector: all signs one, norms zero
     assert cache.sgn[0, 1, 5].cpu().numpy().tolist() == [255] * 16
     assert cache.xnorm[0, 1, 5].item() == 0 and cache.rnorm[0, 1, 5].item() == 0
@@ -196,6 +197,7 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
         worst = max(worst, err)
         assert err < out_tol(out_dtype), f"(b={b}, kv head={h}) rel L2 {err:.3g}"
     assert stats.idx_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
+    assert stats.sign_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
     return worst
 
 
@@ -251,7 +253,9 @@ def test_decode_qwen7b_32k():
                                  pi, s, ck, cv)[0]
         err = rel_l2(out[0, h * g:(h + 1) * g], ref)
         assert err < 1e-3, f"kv head {h}: rel L2 {err:.3g}"
-    assert stats.idx_excluded + stats.sign_excluded < 1e-4 * stats.coords * 2, stats
+    assert stats.idx_excluded < 1e-4 * stats.coords, stats
+    assert stats.sign_excluded < 1e-4 * stats.coords, stats
+    print(f"qwen7b 32k code stats: {stats}")
 
 
 # ------------------------------------------------------------------ asymmetric mode
