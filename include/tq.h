@@ -67,7 +67,8 @@ typedef enum {
   TQ_ERR_UNSUPPORTED = 2,   /* valid but not built: d != 128, bit width, dtype, group > 8 */
   TQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   TQ_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up */
-  TQ_ERR_DEVICE_STATUS = 5  /* the device status word reports skipped tokens */
+  TQ_ERR_DEVICE_STATUS = 5, /* the device status word reports skipped tokens */
+  TQ_ERR_SCRATCH_LIMIT = 6  /* the call needs more scratch than the library's static array */
 } tq_status;
 
 typedef enum { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
@@ -212,6 +213,33 @@ tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,
                                    const int32_t* seq_lens, const uint16_t* k_tail,
                                    const uint16_t* v_tail, const int32_t* tail_lens, void* out,
                                    void* workspace, size_t workspace_bytes, tq_stream_t stream);
+
+/* Decode attention for callers that cannot allocate device memory (no counterpart on the
+ * pages: this is a deployment variant of tq_decode_attention, computing exactly the same
+ * result).  Callers such as an inference runtime's plugin whose enqueue call may not
+ * allocate, a process whose device memory is owned by another framework's pool, or a
+ * latency-critical loop that must not enter the allocator (cudaMalloc/cudaFree may
+ * synchronise the device) cannot provide the workspace that tq_decode_attention takes.
+ * This entry point uses instead a static device array inside the library, of
+ * tq_decode_noalloc_scratch_bytes() bytes (8 MiB), which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing.
+ *   Arguments: as tq_decode_attention, without the workspace.
+ *   Returns TQ_ERR_SCRATCH_LIMIT, launching nothing, when tq_decode_workspace_bytes(desc)
+ *   exceeds the static size (e.g. very long contexts or large batches: use the workspace
+ *   entry point there).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current, so make the first call on each device before capturing any
+ *   stream.  All calls on a device share the one array: calls that may overlap on the GPU
+ *   (different streams without ordering between them) race and must not be issued; calls
+ *   ordered on one stream are safe.  The array keeps the previous call's data; nothing in it
+ *   needs to start at zero. */
+tq_status tq_decode_attention_noalloc(const tq_attn_desc* desc, const tq_codec* kc,
+                                      const tq_codec* vc, const void* q, tq_prod_cache k,
+                                      tq_mse_cache v, const int32_t* seq_lens, void* out,
+                                      tq_stream_t stream);
+
+/* Size in bytes of the static scratch array used by tq_decode_attention_noalloc. */
+size_t tq_decode_noalloc_scratch_bytes(void);
 
 /* ------------------------------------------------------------------ diagnostics */
 

@@ -12,7 +12,8 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "lib", "libtq.so")
 
-TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_TIMEOUT, TQ_ERR_DEVICE_STATUS = range(6)
+(TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_TIMEOUT, TQ_ERR_DEVICE_STATUS,
+ TQ_ERR_SCRATCH_LIMIT) = range(7)
 TQ_F32, TQ_F16, TQ_BF16 = 0, 1, 2
 TQ_PROD, TQ_MSE = 0, 1
 TQ_HEAD_DIM = 128
@@ -63,6 +64,9 @@ SIGNATURES = {
     "tq_decode_attention_asym": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp,
                                                 tq_mse_cache, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 ctypes.c_size_t, _vp]),
+    "tq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp,
+                                                   tq_prod_cache, tq_mse_cache, _vp, _vp, _vp]),
+    "tq_decode_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "tq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -174,6 +178,16 @@ def tq_decode_attention_asym(desc: tq_attn_desc, vc, q, k_f16, v: tq_mse_cache, 
                                            ptr(seq_lens), ptr(k_tail), ptr(v_tail),
                                            ptr(tail_lens), ptr(out), ptr(workspace),
                                            workspace_bytes, ptr(stream))
+
+
+def tq_decode_attention_noalloc(desc: tq_attn_desc, kc, vc, q, k: tq_prod_cache,
+                                v: tq_mse_cache, seq_lens, out, stream) -> int:
+    return load().tq_decode_attention_noalloc(ctypes.byref(desc), kc, vc, ptr(q), k, v,
+                                              ptr(seq_lens), ptr(out), ptr(stream))
+
+
+def tq_decode_noalloc_scratch_bytes() -> int:
+    return load().tq_decode_noalloc_scratch_bytes()
 
 
 def tq_device_status():

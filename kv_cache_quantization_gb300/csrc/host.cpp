@@ -15,6 +15,7 @@ extern "C" const char* tq_status_string(tq_status s) {
     case TQ_ERR_CUDA: return "TQ_ERR_CUDA";
     case TQ_ERR_TIMEOUT: return "TQ_ERR_TIMEOUT";
     case TQ_ERR_DEVICE_STATUS: return "TQ_ERR_DEVICE_STATUS";
+    case TQ_ERR_SCRATCH_LIMIT: return "TQ_ERR_SCRATCH_LIMIT";
   }
   return "TQ_UNKNOWN_STATUS";
 }

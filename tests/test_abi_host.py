@@ -47,7 +47,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert B.tq_status_string(s).startswith("TQ_")
     assert "sm_103a" in B.tq_version()
 
