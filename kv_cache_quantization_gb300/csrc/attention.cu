@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "decode_mma.h"
 #include "tq_internal.h"
 
 TQ_DEFINE_FLAGS(tq_take_flags_attention)
@@ -27,12 +28,19 @@ constexpr int kRec = 2 + TQ_D;       // partial record: m, l, acc[128]
 constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
 
 struct Plan {
-  int G, nsplit_main, nsplit_tail, nsplit;
+  int G, nsplit_main, nsplit_tail, nsplit, split_len;
   size_t q_off, part_off, bytes;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int sm_count() {
+  const int n = tq_num_sms();
+  return n > 0 ? n : 148;
+}
+
+// Context split: one CTA per (batch, KV head, split); about one CTA per SM for the longest
+// sequence, splits a multiple of 128 tokens (the tensor-core kernel's chunk).
 tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   if (!d) return TQ_ERR_INVALID_ARG;
   if (d->head_dim != TQ_HEAD_DIM) return TQ_ERR_UNSUPPORTED;
@@ -45,7 +53,13 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   for (tq_dtype t : {d->q_dtype, d->out_dtype})
     if (t != TQ_F32 && t != TQ_F16 && t != TQ_BF16) return TQ_ERR_UNSUPPORTED;
   p->G = d->q_heads / d->kv_heads;
-  p->nsplit_main = d->max_seq_len > 0 ? (d->max_seq_len + kSplit - 1) / kSplit : 1;
+  const long long units = (long long)(d->batch > 0 ? d->batch : 1) * d->kv_heads;
+  const long long want = (sm_count() + units - 1) / units;          // splits per sequence
+  long long sl = (d->max_seq_len + want - 1) / (want > 0 ? want : 1);
+  sl = (sl + 127) / 128 * 128;
+  if (sl < 128) sl = 128;
+  p->split_len = (int)sl;
+  p->nsplit_main = d->max_seq_len > 0 ? (int)((d->max_seq_len + sl - 1) / sl) : 1;
   p->nsplit_tail = asym ? (d->tail_capacity + kSplit - 1) / kSplit : 0;
   p->nsplit = p->nsplit_main + p->nsplit_tail;
   const size_t qf = (size_t)d->batch * d->q_heads * 2 * TQ_D;
@@ -70,27 +84,36 @@ __device__ __forceinline__ void store_elem(void* base, int dtype, long long i, f
 }
 
 // ---------------------------------------------------------------- 1. query prep
-__global__ void __launch_bounds__(kThreads) query_prep_kernel(const void* q, int q_dtype,
-                                                              const float* piT, const float* sT,
-                                                              float* qv) {
+// One CTA of 512 threads per query row: both 128×128 products split four ways over k.
+constexpr int kPrepThreads = 512;
+__global__ void __launch_bounds__(kPrepThreads) query_prep_kernel(const void* q, int q_dtype,
+                                                                  const float* piT, const float* sT,
+                                                                  float* qv) {
   __shared__ float qf[TQ_D];
+  __shared__ float part[2][4][TQ_D];
   const int row = blockIdx.x;  // b * Hq + h
-  const int j = threadIdx.x;
-  qf[j] = load_elem(q, q_dtype, (long long)row * TQ_D + j);
+  const int tid = threadIdx.x, j = tid & 127, kq = tid >> 7;
+  if (tid < TQ_D) qf[tid] = load_elem(q, q_dtype, (long long)row * TQ_D + tid);
   __syncthreads();
   float r = 0.f, s = 0.f;
 #pragma unroll 8
-  for (int k = 0; k < TQ_D; ++k) {
+  for (int k = 32 * kq; k < 32 * kq + 32; ++k) {
     r = fmaf(__ldg(&piT[k * TQ_D + j]), qf[k], r);
     s = fmaf(__ldg(&sT[k * TQ_D + j]), qf[k], s);
   }
-  qv[(size_t)row * 2 * TQ_D + j] = r;
-  qv[(size_t)row * 2 * TQ_D + TQ_D + j] = s;
+  part[0][kq][j] = r;
+  part[1][kq][j] = s;
+  __syncthreads();
+  if (tid < 2 * TQ_D) {
+    const int w = tid >> 7;
+    qv[(size_t)row * 2 * TQ_D + w * TQ_D + j] =
+        (part[w][0][j] + part[w][1][j]) + (part[w][2][j] + part[w][3][j]);
+  }
 }
 
 struct DecodeArgs {
   int B, Hq, Hkv, G, cap, tail_cap;
-  int nsplit_main, nsplit;
+  int nsplit_main, nsplit, split_len;
   float scale;
   // symmetric
   const float* qv;
@@ -129,35 +152,45 @@ __device__ __forceinline__ int value_index(const DecodeArgs& a, long long bh, in
   return q;
 }
 
-// Online-softmax pieces shared by both modes: scores in sc[g][tt] → probabilities, then the
-// value accumulation of thread j and the partial record.
-__device__ void softmax_and_values(const DecodeArgs& a, float (*sc)[kSplit], int n_tok, int start,
-                                   bool plain_values, long long bh, int split, float* s_m,
-                                   float* s_l) {
+// Running softmax state of one CTA (one KV head's query group over one split): m and l per
+// head in shared memory, acc[g] of coordinate j = threadIdx.x in registers.
+struct RunState {
+  float acc[TQ_MAX_GROUP];
+};
+
+// Folds one sub-chunk of scores sc[g][0..n_tok) into the running state: new maxima rescale
+// l and acc, probabilities replace the scores, values are accumulated.
+__device__ void fold_chunk(const DecodeArgs& a, float (*sc)[kSplit], int n_tok, int start,
+                           bool plain_values, long long bh, float* s_m, float* s_l, float* s_corr,
+                           RunState& rs) {
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   for (int g = warp; g < a.G; g += kThreads / 32) {
     float m = -INFINITY;
     for (int tt = lane; tt < n_tok; tt += 32) m = fmaxf(m, sc[g][tt]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float m_old = s_m[g];
+    const float m_new = fmaxf(m_old, m);
     float l = 0.f;
     for (int tt = lane; tt < n_tok; tt += 32) {
-      const float p = n_tok > 0 ? expf(sc[g][tt] - m) : 0.f;
+      const float p = expf(sc[g][tt] - m_new);
       sc[g][tt] = p;
       l += p;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
     if (lane == 0) {
-      s_m[g] = m;
-      s_l[g] = l;
+      const float corr = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+      s_corr[g] = corr;
+      s_m[g] = m_new;
+      s_l[g] = s_l[g] * corr + l;
     }
   }
   __syncthreads();
   const int j = tid;
-  float acc[TQ_MAX_GROUP];
 #pragma unroll
-  for (int g = 0; g < TQ_MAX_GROUP; ++g) acc[g] = 0.f;
+  for (int g = 0; g < TQ_MAX_GROUP; ++g)
+    if (g < a.G) rs.acc[g] *= s_corr[g];
   for (int tt = 0; tt < n_tok; ++tt) {
     const int t = start + tt;
     float val;
@@ -168,24 +201,31 @@ __device__ void softmax_and_values(const DecodeArgs& a, float (*sc)[kSplit], int
     }
 #pragma unroll
     for (int g = 0; g < TQ_MAX_GROUP; ++g)
-      if (g < a.G) acc[g] = fmaf(sc[g][tt], val, acc[g]);
+      if (g < a.G) rs.acc[g] = fmaf(sc[g][tt], val, rs.acc[g]);
   }
+  __syncthreads();   // sc is rewritten by the next sub-chunk
+}
+
+__device__ void write_record(const DecodeArgs& a, long long bh, int split, const float* s_m,
+                             const float* s_l, const RunState& rs) {
+  const int j = threadIdx.x;
   float* rec = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
   for (int g = 0; g < a.G; ++g) {
     if (j == 0) {
       rec[g * kRec + 0] = s_m[g];
       rec[g * kRec + 1] = s_l[g];
     }
-    rec[g * kRec + 2 + j] = acc[g];
+    rec[g * kRec + 2 + j] = rs.acc[g];
   }
 }
 
 // ---------------------------------------------------------------- 2a. symmetric split decode
+// CUDA-core path, used for key codes with 4 index bits (the tensor-core kernel covers 1–3).
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
   __shared__ float qr[TQ_MAX_GROUP][TQ_D];
   __shared__ float qs[TQ_MAX_GROUP][TQ_D];
   __shared__ float sc[TQ_MAX_GROUP][kSplit];
-  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP];
+  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP], s_corr[TQ_MAX_GROUP];
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x;
@@ -194,60 +234,70 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
     len = a.cap;
   }
-  const int start = split * kSplit;
-  const int n_tok = max(0, min(start + kSplit, len) - start);
   for (int g = 0; g < a.G; ++g) {
     const long long row = (long long)b * a.Hq + kvh * a.G + g;
     qr[g][tid] = a.qv[row * 2 * TQ_D + tid];
     qs[g][tid] = a.qv[row * 2 * TQ_D + TQ_D + tid];
   }
+  if (tid < TQ_MAX_GROUP) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.f;
+  }
+  RunState rs;
+#pragma unroll
+  for (int g = 0; g < TQ_MAX_GROUP; ++g) rs.acc[g] = 0.f;
   __syncthreads();
   const float qjl = kQjlNum / TQ_D;
-  for (int tt = tid; tt < n_tok; tt += kThreads) {
-    const int t = start + tt;
-    uint4 planes[4];
-    for (int p = 0; p < a.kbits; ++p)
-      planes[p] = *reinterpret_cast<const uint4*>(a.kidx + ((bh * a.kbits + p) * a.cap + t) * 16);
-    const uint4 sg = *reinterpret_cast<const uint4*>(a.ksgn + (bh * a.cap + t) * 16);
-    const float xn = a.kxn[bh * a.cap + t], rn = a.krn[bh * a.cap + t];
-    float mse[TQ_MAX_GROUP], qj[TQ_MAX_GROUP];
+  const int s_begin = split * a.split_len, s_end = min(s_begin + a.split_len, len);
+  for (int start = s_begin; start < s_end; start += kSplit) {
+    const int n_tok = min(kSplit, s_end - start);
+    for (int tt = tid; tt < n_tok; tt += kThreads) {
+      const int t = start + tt;
+      uint4 planes[4];
+      for (int p = 0; p < a.kbits; ++p)
+        planes[p] = *reinterpret_cast<const uint4*>(a.kidx + ((bh * a.kbits + p) * a.cap + t) * 16);
+      const uint4 sg = *reinterpret_cast<const uint4*>(a.ksgn + (bh * a.cap + t) * 16);
+      const float xn = a.kxn[bh * a.cap + t], rn = a.krn[bh * a.cap + t];
+      float mse[TQ_MAX_GROUP], qj[TQ_MAX_GROUP];
 #pragma unroll
-    for (int g = 0; g < TQ_MAX_GROUP; ++g) mse[g] = qj[g] = 0.f;
-    for (int w = 0; w < 4; ++w) {
-      uint32_t pw[4];
-      for (int p = 0; p < 4; ++p) {
-        const uint4 u = planes[p];
-        pw[p] = w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w;
-      }
-      const uint32_t sw = w == 0 ? sg.x : w == 1 ? sg.y : w == 2 ? sg.z : sg.w;
-      for (int bit = 0; bit < 32; ++bit) {
-        const int j = w * 32 + bit;
-        int q = 0;
-        for (int p = 0; p < a.kbits; ++p) q |= ((pw[p] >> bit) & 1) << p;
-        const float c = a.kl.c[q];
-        const float s = ((sw >> bit) & 1) ? 1.f : -1.f;
+      for (int g = 0; g < TQ_MAX_GROUP; ++g) mse[g] = qj[g] = 0.f;
+      for (int w = 0; w < 4; ++w) {
+        uint32_t pw[4];
+        for (int p = 0; p < 4; ++p) {
+          const uint4 u = planes[p];
+          pw[p] = w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w;
+        }
+        const uint32_t sw = w == 0 ? sg.x : w == 1 ? sg.y : w == 2 ? sg.z : sg.w;
+        for (int bit = 0; bit < 32; ++bit) {
+          const int j = w * 32 + bit;
+          int q = 0;
+          for (int p = 0; p < a.kbits; ++p) q |= ((pw[p] >> bit) & 1) << p;
+          const float c = a.kl.c[q];
+          const float s = ((sw >> bit) & 1) ? 1.f : -1.f;
 #pragma unroll
-        for (int g = 0; g < TQ_MAX_GROUP; ++g) {
-          if (g < a.G) {
-            mse[g] = fmaf(qr[g][j], c, mse[g]);
-            qj[g] = fmaf(qs[g][j], s, qj[g]);
+          for (int g = 0; g < TQ_MAX_GROUP; ++g) {
+            if (g < a.G) {
+              mse[g] = fmaf(qr[g][j], c, mse[g]);
+              qj[g] = fmaf(qs[g][j], s, qj[g]);
+            }
           }
         }
       }
-    }
 #pragma unroll
-    for (int g = 0; g < TQ_MAX_GROUP; ++g)
-      if (g < a.G) sc[g][tt] = a.scale * (xn * mse[g] + rn * qjl * qj[g]);
+      for (int g = 0; g < TQ_MAX_GROUP; ++g)
+        if (g < a.G) sc[g][tt] = a.scale * (xn * mse[g] + rn * qjl * qj[g]);
+    }
+    __syncthreads();
+    fold_chunk(a, sc, n_tok, start, false, bh, s_m, s_l, s_corr, rs);
   }
-  __syncthreads();
-  softmax_and_values(a, sc, n_tok, start, false, bh, split, s_m, s_l);
+  write_record(a, bh, split, s_m, s_l, rs);
 }
 
 // ---------------------------------------------------------------- 2b. asymmetric split decode
 __global__ void __launch_bounds__(kThreads) decode_asym_kernel(DecodeArgs a) {
   __shared__ float qf[TQ_MAX_GROUP][TQ_D];
   __shared__ float sc[TQ_MAX_GROUP][kSplit];
-  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP];
+  __shared__ float s_m[TQ_MAX_GROUP], s_l[TQ_MAX_GROUP], s_corr[TQ_MAX_GROUP];
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x;
@@ -259,72 +309,108 @@ __global__ void __launch_bounds__(kThreads) decode_asym_kernel(DecodeArgs a) {
       atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
     len = cap;
   }
-  const int start = (tail ? split - a.nsplit_main : split) * kSplit;
-  const int n_tok = max(0, min(start + kSplit, len) - start);
+  const int span = tail ? kSplit : a.split_len;
+  const int s_begin = (tail ? split - a.nsplit_main : split) * span;
+  const int s_end = min(s_begin + span, len);
   for (int g = 0; g < a.G; ++g)
     qf[g][tid] = load_elem(a.q, a.q_dtype, ((long long)b * a.Hq + kvh * a.G + g) * TQ_D + tid);
+  if (tid < TQ_MAX_GROUP) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.f;
+  }
+  RunState rs;
+#pragma unroll
+  for (int g = 0; g < TQ_MAX_GROUP; ++g) rs.acc[g] = 0.f;
   __syncthreads();
   const __half* K = tail ? a.ktail : a.kf16;
-  for (int tt = tid; tt < n_tok; tt += kThreads) {
-    const int t = start + tt;
-    const uint4* row = reinterpret_cast<const uint4*>(K + ((long long)bh * cap + t) * TQ_D);
-    float dot[TQ_MAX_GROUP];
+  for (int start = s_begin; start < s_end; start += kSplit) {
+    const int n_tok = min(kSplit, s_end - start);
+    for (int tt = tid; tt < n_tok; tt += kThreads) {
+      const int t = start + tt;
+      const uint4* row = reinterpret_cast<const uint4*>(K + ((long long)bh * cap + t) * TQ_D);
+      float dot[TQ_MAX_GROUP];
 #pragma unroll
-    for (int g = 0; g < TQ_MAX_GROUP; ++g) dot[g] = 0.f;
-    for (int c = 0; c < TQ_D / 8; ++c) {
-      const uint4 u = row[c];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      for (int g = 0; g < TQ_MAX_GROUP; ++g) dot[g] = 0.f;
+      for (int c = 0; c < TQ_D / 8; ++c) {
+        const uint4 u = row[c];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-        const int j = c * 8 + 2 * e;
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          const int j = c * 8 + 2 * e;
 #pragma unroll
-        for (int g = 0; g < TQ_MAX_GROUP; ++g)
-          if (g < a.G) dot[g] = fmaf(qf[g][j], f.x, fmaf(qf[g][j + 1], f.y, dot[g]));
+          for (int g = 0; g < TQ_MAX_GROUP; ++g)
+            if (g < a.G) dot[g] = fmaf(qf[g][j], f.x, fmaf(qf[g][j + 1], f.y, dot[g]));
+        }
       }
-    }
 #pragma unroll
-    for (int g = 0; g < TQ_MAX_GROUP; ++g)
-      if (g < a.G) sc[g][tt] = a.scale * dot[g];
+      for (int g = 0; g < TQ_MAX_GROUP; ++g)
+        if (g < a.G) sc[g][tt] = a.scale * dot[g];
+    }
+    __syncthreads();
+    fold_chunk(a, sc, n_tok, start, tail, bh, s_m, s_l, s_corr, rs);
   }
-  __syncthreads();
-  softmax_and_values(a, sc, n_tok, start, tail, bh, split, s_m, s_l);
+  write_record(a, bh, split, s_m, s_l, rs);
 }
 
 // ---------------------------------------------------------------- 3. merge
-__global__ void __launch_bounds__(kThreads) merge_kernel(const float* part, int Hq, int Hkv, int G,
-                                                         int nsplit_main, int nsplit,
-                                                         const float* pi, void* out, int out_dtype) {
-  __shared__ float accR[TQ_D];
+// One CTA of 512 threads per (batch, query head): the splits are combined four ways in
+// parallel (log-sum-exp weights), then out = Πᵀ·acc / L with the product split over k.
+constexpr int kMergeThreads = 512;
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* part, int Hq, int Hkv,
+                                                              int G, int nsplit_main, int nsplit,
+                                                              const float* pi, void* out,
+                                                              int out_dtype) {
+  __shared__ float accR[4][TQ_D], accP[4][TQ_D], accs[TQ_D], prod[4][TQ_D];
+  __shared__ float s_M, s_L[4];
   const int row = blockIdx.x;  // b * Hq + h
   const int b = row / Hq, h = row % Hq;
   const int kvh = h / G, g = h % G;
   const long long bh = (long long)b * Hkv + kvh;
-  const int j = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part[((bh * nsplit + s) * G + g) * kRec]);
+  const int tid = threadIdx.x, j = tid & 127, q = tid >> 7;
+  const float* recs = part + (bh * nsplit * G + g) * kRec;   // split s at recs + s*G*kRec
+  if (tid < 32) {
+    float M = -INFINITY;
+    for (int sp = tid; sp < nsplit; sp += 32) M = fmaxf(M, recs[(long long)sp * G * kRec]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (tid == 0) s_M = M;
+  }
+  __syncthreads();
+  const float M = s_M;
   float L = 0.f, aR = 0.f, aP = 0.f;
   if (M > -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float* rec = part + ((bh * nsplit + s) * G + g) * kRec;
+    for (int sp = q; sp < nsplit; sp += 4) {
+      const float* rec = recs + (long long)sp * G * kRec;
       const float l = rec[1];
       if (!(l > 0.f)) continue;
       const float w = expf(rec[0] - M);
       L += w * l;
-      if (s < nsplit_main) aR += w * rec[2 + j];
+      if (sp < nsplit_main) aR += w * rec[2 + j];
       else aP += w * rec[2 + j];
     }
   }
-  accR[j] = aR;
+  accR[q][j] = aR;
+  accP[q][j] = aP;
+  if (j == 0) s_L[q] = L;
   __syncthreads();
-  float o = 0.f;
-  if (L > 0.f) {
-    float r = 0.f;
+  if (tid < TQ_D) accs[j] = (accR[0][j] + accR[1][j]) + (accR[2][j] + accR[3][j]);
+  __syncthreads();
+  float r = 0.f;
 #pragma unroll 8
-    for (int k = 0; k < TQ_D; ++k) r = fmaf(__ldg(&pi[k * TQ_D + j]), accR[k], r);
-    o = (r + aP) / L;
+  for (int k = 32 * q; k < 32 * q + 32; ++k) r = fmaf(__ldg(&pi[k * TQ_D + j]), accs[k], r);
+  prod[q][j] = r;
+  __syncthreads();
+  if (tid < TQ_D) {
+    const float Lt = (s_L[0] + s_L[1]) + (s_L[2] + s_L[3]);
+    float o = 0.f;
+    if (Lt > 0.f) {
+      const float rot = (prod[0][j] + prod[1][j]) + (prod[2][j] + prod[3][j]);
+      const float pl = (accP[0][j] + accP[1][j]) + (accP[2][j] + accP[3][j]);
+      o = (rot + pl) / Lt;
+    }
+    store_elem(out, out_dtype, (long long)row * TQ_D + j, o);
   }
-  store_elem(out, out_dtype, (long long)row * TQ_D + j, o);
 }
 
 tq_status check_prod_cache(const tq_prod_cache& k) {
@@ -370,7 +456,7 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   DecodeArgs a{};
   a.B = desc->batch; a.Hq = desc->q_heads; a.Hkv = desc->kv_heads; a.G = p.G;
   a.cap = desc->capacity; a.tail_cap = 0;
-  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit;
+  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit; a.split_len = p.split_len;
   a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)TQ_D);
   a.qv = reinterpret_cast<const float*>(ws + p.q_off);
   a.kidx = k.idx; a.ksgn = k.sgn; a.kxn = k.xnorm; a.krn = k.rnorm;
@@ -379,10 +465,29 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   a.seq_lens = seq_lens;
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
-  query_prep_kernel<<<rows, kThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
+  query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
                                                    reinterpret_cast<float*>(ws + p.q_off));
-  decode_kernel<<<dim3(p.nsplit_main, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
-  merge_kernel<<<rows, kThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
+  if (tq_mma_supported(kc->ibits, vc->ibits, p.G)) {
+    tq_mma_launch m{};
+    m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap;
+    m.nsplit = p.nsplit; m.split_len = p.split_len;
+    m.scale_log2 = a.scale * 1.4426950408889634f;
+    m.qv = a.qv;
+    m.kidx = k.idx; m.ksgn = k.sgn; m.kxn = k.xnorm; m.krn = k.rnorm;
+    m.kbits = kc->ibits; m.kd = tq_decompose_levels(kc);
+    m.vidx = v.idx; m.vxn = v.xnorm; m.vbits = vc->ibits;
+    if (vc->ibits < 4) m.vd = tq_decompose_levels(vc);
+    for (int i = 0; i < 16; ++i) m.vc[i] = vc->centroids[i];
+    m.vc_scale = vc->ibits == 4 ? vc->lut_scale : 1.f;
+    m.vc_unscale = 1.f / m.vc_scale;
+    m.seq_lens = seq_lens;
+    m.part = a.part;
+    st = tq_launch_decode_mma(m, stream);
+    if (st != TQ_OK) return st;
+  } else {
+    decode_kernel<<<dim3(p.nsplit_main, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+  }
+  merge_kernel<<<rows, kMergeThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
                                               vc->d_pi, out, desc->out_dtype);
   return tq_cuda_status(cudaGetLastError());
 }
@@ -412,7 +517,7 @@ extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq
   DecodeArgs a{};
   a.B = desc->batch; a.Hq = desc->q_heads; a.Hkv = desc->kv_heads; a.G = p.G;
   a.cap = desc->capacity; a.tail_cap = desc->tail_capacity;
-  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit;
+  a.nsplit_main = p.nsplit_main; a.nsplit = p.nsplit; a.split_len = p.split_len;
   a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)TQ_D);
   a.q = q; a.q_dtype = desc->q_dtype;
   a.kf16 = reinterpret_cast<const __half*>(k_f16);
@@ -424,7 +529,7 @@ extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
   decode_asym_kernel<<<dim3(p.nsplit, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
-  merge_kernel<<<rows, kThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
+  merge_kernel<<<rows, kMergeThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
                                               vc->d_pi, out, desc->out_dtype);
   return tq_cuda_status(cudaGetLastError());
 }

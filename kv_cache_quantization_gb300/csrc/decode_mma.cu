@@ -1,0 +1,744 @@
+// Split-context decode attention on packed codes with tensor-core contractions.
+//
+// The estimator of the QJL deep-dive (§五, §六) for key t and query head h is
+//   s = ‖x_t‖·⟨Π q_h, c[idx_t]⟩ + ‖r_t‖·√(π/2)/d·⟨S q_h, 2·sign_t − 1⟩,
+// and the value side accumulates Σ_t p_t·‖v_t‖·c_v[idx_t] in the rotated domain.  Both
+// are contractions between a bit-structured operand and a small dense one, so the CTA
+// runs them as mma.sync m16n8k16 (fp16 in, fp32 accumulate):
+//
+//  * key scores: A = 16 tokens × 16 coordinates taken straight from the packed bit
+//    planes, B = 16 coordinates × 8 query columns (the GQA group, or 4 heads × hi/lo
+//    halves of the query when G ≤ 4).  A bit becomes an fp16 operand with a single AND:
+//    masking bit p (p = 10..14) of a 32-bit word yields an fp16 pair whose halves are 0 or
+//    the power of two 2^e(p); the query carries 2^-e(p), so products are exact.  The
+//    Lloyd-Max levels are expanded into odd Walsh monomials (XORs of bit planes) so that
+//    every plane is a 0/1 matrix; coefficients live in the query operand.
+//  * values: A = 16 coordinates × 16 tokens (4-bit codes through a shared-memory table of
+//    level pairs; 1–3-bit codes as planes, transposed on load by ldmatrix.trans),
+//    B = softmax weights × ‖v‖ transposed from the score accumulators with movmatrix.
+//
+// Packed K/V chunks stream through a 4-stage shared-memory ring filled by bulk-copy (TMA)
+// engines and mbarriers; a dedicated producer warp issues the copies, eight consumer warps
+// each own 16 tokens of a 128-token chunk and keep an online softmax; the CTA combines its
+// warps and writes one (m, l, acc[128]) record per query head for the LSE merge.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "decode_mma.h"
+
+TQ_DEFINE_FLAGS(tq_take_flags_decode_mma)
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kChunk = 16 * kConsumerWarps;   // tokens per stage
+constexpr int kStages = 4;
+constexpr int kRec = 2 + TQ_D;
+constexpr unsigned kSpinLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false after kSpinLimit polls (the caller raises TQ_FLAG_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  for (unsigned i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// ---------------------------------------------------------------- warp-level matrix ops
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                    uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- bit-pair expansion
+// Pair e (0..15) of a 32-bit word holds bit lo(e) in its low fp16 half and bit lo(e)+16 in
+// its high half, each as 0 or 2^exp(e):
+//   e = 0..4  : bits 10+e,  26+e   (mask at 10+e)
+//   e = 5..9  : bits e,     16+e   (word << 5,  mask at e+5)
+//   e = 10..14: bits e-10,  e+6    (word << 10, mask at e)
+//   e = 15    : bits 15,    31     (word >> 1,  mask at 14)
+// An fp16 with only bit 10/11/12/13/14 set equals 2^-14 / 2^-13 / 2^-11 / 2^-7 / 2^1.
+__host__ __device__ constexpr int pair_lo(int e) {
+  return e < 5 ? 10 + e : e < 10 ? e : e < 15 ? e - 10 : 15;
+}
+__host__ __device__ constexpr int pair_pos(int e) { return e < 15 ? 10 + e % 5 : 14; }
+__host__ __device__ constexpr int pos_exp(int pos) {
+  return pos == 10 ? -14 : pos == 11 ? -13 : pos == 12 ? -11 : pos == 13 ? -7 : 1;
+}
+
+template <int E>
+__device__ __forceinline__ uint32_t pair_of(uint32_t w, uint32_t w5, uint32_t w10, uint32_t w1) {
+  constexpr int pos = pair_pos(E);
+  constexpr uint32_t mask = (1u << pos) | (1u << (pos + 16));
+  return (E < 5 ? w : E < 10 ? w5 : E < 15 ? w10 : w1) & mask;
+}
+
+struct Expanded {
+  uint32_t p[16];
+};
+__device__ __forceinline__ Expanded expand(uint32_t w) {
+  Expanded x;
+  const uint32_t w5 = w << 5, w10 = w << 10, w1 = w >> 1;
+  x.p[0] = pair_of<0>(w, w5, w10, w1);
+  x.p[1] = pair_of<1>(w, w5, w10, w1);
+  x.p[2] = pair_of<2>(w, w5, w10, w1);
+  x.p[3] = pair_of<3>(w, w5, w10, w1);
+  x.p[4] = pair_of<4>(w, w5, w10, w1);
+  x.p[5] = pair_of<5>(w, w5, w10, w1);
+  x.p[6] = pair_of<6>(w, w5, w10, w1);
+  x.p[7] = pair_of<7>(w, w5, w10, w1);
+  x.p[8] = pair_of<8>(w, w5, w10, w1);
+  x.p[9] = pair_of<9>(w, w5, w10, w1);
+  x.p[10] = pair_of<10>(w, w5, w10, w1);
+  x.p[11] = pair_of<11>(w, w5, w10, w1);
+  x.p[12] = pair_of<12>(w, w5, w10, w1);
+  x.p[13] = pair_of<13>(w, w5, w10, w1);
+  x.p[14] = pair_of<14>(w, w5, w10, w1);
+  x.p[15] = pair_of<15>(w, w5, w10, w1);
+  return x;
+}
+
+// Virtual planes of a KB-bit index: the odd subsets of its bit positions, as bit masks.
+__host__ __device__ constexpr int num_vplanes(int kb) { return kb == 1 ? 1 : kb == 2 ? 2 : 4; }
+__host__ __device__ constexpr int vplane_mask(int kb, int v) {
+  return kb == 1 ? 1 : kb == 2 ? (v == 0 ? 1 : 2) : (v == 0 ? 1 : v == 1 ? 2 : v == 2 ? 4 : 7);
+}
+
+template <int KB>
+__device__ __forceinline__ uint32_t vplane_word(const uint32_t* w, int v) {
+  const int m = vplane_mask(KB, v);
+  uint32_t x = 0;
+#pragma unroll
+  for (int i = 0; i < KB; ++i)
+    if (m & (1 << i)) x ^= w[i];
+  return x;
+}
+
+// ---------------------------------------------------------------- shared-memory layout
+template <int KB, int VB>
+struct Layout {
+  static constexpr int kplanes = 0;
+  static constexpr int ksgn = kplanes + KB * kChunk * 16;
+  static constexpr int kxn = ksgn + kChunk * 16;
+  static constexpr int krn = kxn + kChunk * 4;
+  static constexpr int vcodes = krn + kChunk * 4;
+  static constexpr int vcode_bytes = VB == 4 ? kChunk * 64 : VB * kChunk * 16;
+  static constexpr int vxn = vcodes + vcode_bytes;
+  static constexpr int stage = vxn + kChunk * 4;            // bytes per stage
+  static constexpr int ring = kStages * stage;
+  static constexpr int lut = ring;                           // VB == 4: 256 × 32 words
+  static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
+  static constexpr int q = lut + lut_bytes;                  // q_rot, q_sk [2][8][128] f32
+  static constexpr int total = q + 2 * 8 * TQ_D * 4;
+  // the CTA combine reuses everything above (ring, table and query buffer are dead by
+  // then): per warp m, l, Σw [3][8] and acc [8][128]
+  static constexpr int comb_acc = 0;
+  static constexpr int comb_stats = kConsumerWarps * 8 * TQ_D * 4;
+  static_assert(comb_stats + kConsumerWarps * 3 * 8 * 4 <= total, "combine buffer");
+};
+
+// ---------------------------------------------------------------- the kernel
+template <int KB, int VB, bool HILO>
+__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_launch a) {
+  using L = Layout<KB, VB>;
+  constexpr int NKV = num_vplanes(KB);                      // key virtual planes
+  constexpr int NVV = VB == 4 ? 0 : num_vplanes(VB);
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ float s_hd[8][6];   // per query column: A, Cm, B, Cq (score constants)
+  __shared__ int s_timeout;
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int len = a.seq_lens[b];
+  if (len > a.cap) {
+    if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
+    len = a.cap;
+  }
+  const int t_begin = split * a.split_len;
+  const int t_end = min(t_begin + a.split_len, len);
+  const int nchunks = t_end > t_begin ? (t_end - t_begin + kChunk - 1) / kChunk : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    s_timeout = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer warp
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kStages;
+        if (c >= kStages && !mbar_wait(&empty_bar[st], ((c / kStages) - 1) & 1)) {
+          atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+          s_timeout = 1;
+          break;
+        }
+        const int t0 = t_begin + c * kChunk;
+        const int n = min(kChunk, a.cap - t0);   // multiple of 64 (capacity is)
+        unsigned char* base = smem + st * L::stage;
+        const unsigned bytes = (unsigned)n * (KB * 16 + 16 + 4 + 4 + (VB == 4 ? 64 : VB * 16) + 4);
+        mbar_expect_tx(&full_bar[st], bytes);
+        for (int p = 0; p < KB; ++p)
+          bulk_g2s(base + L::kplanes + p * kChunk * 16,
+                   a.kidx + ((bh * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+        bulk_g2s(base + L::ksgn, a.ksgn + (bh * a.cap + t0) * 16, n * 16, &full_bar[st]);
+        bulk_g2s(base + L::kxn, a.kxn + bh * a.cap + t0, n * 4, &full_bar[st]);
+        bulk_g2s(base + L::krn, a.krn + bh * a.cap + t0, n * 4, &full_bar[st]);
+        if (VB == 4) {
+          bulk_g2s(base + L::vcodes, a.vidx + (bh * a.cap + t0) * 64, n * 64, &full_bar[st]);
+        } else {
+          for (int p = 0; p < VB; ++p)
+            bulk_g2s(base + L::vcodes + p * kChunk * 16,
+                     a.vidx + ((bh * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+        }
+        bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
+      }
+      // do not leave while copies may still be landing in this CTA's shared memory
+      for (int c = nchunks - kStages > 0 ? nchunks - kStages : 0; c < nchunks; ++c)
+        if (!mbar_wait(&full_bar[c % kStages], (c / kStages) & 1)) {
+          atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+          break;
+        }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer prologue
+  float* qs = reinterpret_cast<float*>(smem + L::q);   // [2][8][128]
+  const int g = lane >> 2, c = lane & 3;
+  for (int i = tid; i < 2 * 8 * TQ_D; i += kConsumerWarps * 32) {
+    const int which = i / (8 * TQ_D), h = (i / TQ_D) % 8, j = i % TQ_D;
+    const int head = HILO ? (h >> 1) : h;            // query column → head of the group
+    float v = 0.f;
+    if (head < a.G) v = a.qv[((long long)b * a.Hq + kvh * a.G + head) * 2 * TQ_D + which * TQ_D + j];
+    qs[i] = v;
+  }
+  if (VB == 4) {
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L::lut);
+    for (int i = tid; i < 256 * 32; i += kConsumerWarps * 32) {
+      const int key = i >> 5;
+      lut[i] = pack_half2(a.vc_scale * a.vc[key & 15], a.vc_scale * a.vc[key >> 4]);
+    }
+  }
+  consumer_sync();
+  // per query column: max |q| (normalises the fp16 operand) and the constant terms
+  {
+    const int col = warp;  // 8 consumer warps, one column each
+    float mr = 0.f, ms = 0.f, sr = 0.f, ss = 0.f;
+    for (int j = lane; j < TQ_D; j += 32) {
+      mr = fmaxf(mr, fabsf(qs[col * TQ_D + j]));
+      ms = fmaxf(ms, fabsf(qs[(8 + col) * TQ_D + j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+      ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+    }
+    const float ir = mr > 0.f ? 1.f / mr : 0.f, is = ms > 0.f ? 1.f / ms : 0.f;
+    for (int j = lane; j < TQ_D; j += 32) {
+      sr += qs[col * TQ_D + j] * ir;
+      ss += qs[(8 + col) * TQ_D + j] * is;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sr += __shfl_xor_sync(0xffffffffu, sr, o);
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    }
+    if (lane == 0) {
+      s_hd[col][0] = mr * a.scale_log2;                              // A
+      s_hd[col][1] = a.kd.cst * sr;                                  // Cm
+      s_hd[col][2] = ms * a.scale_log2 * (1.2533141373155003f / TQ_D);  // B
+      s_hd[col][3] = ss;                                             // Cq
+      s_hd[col][4] = ir;
+      s_hd[col][5] = is;
+    }
+  }
+  consumer_sync();
+  // query operands of this thread: column g, coordinates of word c.  bq = rounded query
+  // (with G ≤ 4, odd columns carry the rounding residue of the even column's head); with
+  // G > 4 the residue of the MSE planes goes to a second 8-column tile, bql.
+  uint32_t bq[NKV + 1][8][2];
+  uint32_t bql[HILO ? 1 : NKV][8][2];
+  {
+    const int col = g;
+    // HILO: even column = rounded query, odd column = its rounding residue (same head)
+    const int qcol = HILO ? (col & ~1) : col;
+    const float ir = s_hd[qcol][4], is = s_hd[qcol][5];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int e = 2 * s + half;
+        const int j0 = 32 * c + pair_lo(e), j1 = j0 + 16;
+        const float sc = exp2f((float)-pos_exp(pair_pos(e)));
+#pragma unroll
+        for (int v = 0; v <= NKV; ++v) {
+          const bool sign_plane = v == NKV;
+          const float coef = sign_plane ? 2.f : a.kd.coef[v];
+          const float* src = qs + (sign_plane ? 8 + qcol : qcol) * TQ_D;
+          const float nrm = sign_plane ? is : ir;
+          float x0 = src[j0] * nrm * coef * sc, x1 = src[j1] * nrm * coef * sc;
+          const float r0 = x0 - __half2float(__float2half_rn(x0));
+          const float r1 = x1 - __half2float(__float2half_rn(x1));
+          if (HILO && (col & 1)) {
+            x0 = r0;
+            x1 = r1;
+          }
+          bq[v][s][half] = pack_half2(x0, x1);
+          if (!HILO && v < NKV) bql[v][s][half] = pack_half2(r0, r1);
+        }
+      }
+    }
+  }
+  // score constants of this thread's columns (2c, 2c+1)
+  float hA[2], hCm[2], hB[2], hCq[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int col = HILO ? 2 * c : 2 * c + k;
+    hA[k] = s_hd[col][0];
+    hCm[k] = s_hd[col][1];
+    hB[k] = s_hd[col][2];
+    hCq[k] = s_hd[col][3];
+  }
+
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, lw_run[2] = {0.f, 0.f};
+  const uint32_t* lut_lane = reinterpret_cast<const uint32_t*>(smem + L::lut) + lane;
+  bool timed_out = false;
+
+  // ------------------------------------------------------------ main loop
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int st = ch % kStages;
+    if (!mbar_wait(&full_bar[st], (ch / kStages) & 1)) {
+      atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      timed_out = true;
+      break;
+    }
+    const unsigned char* base = smem + st * L::stage;
+    const int tok0 = 16 * warp;                          // this warp's tokens in the chunk
+    const int t_abs = t_begin + ch * kChunk + tok0;      // absolute index of token 0
+
+    // ---- key scores: D[token][column]
+    float dm[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
+    float dml[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      uint32_t pw[3][2], sw[2];
+      const int r = lane & 7, m8 = (lane >> 3) & 1;
+      if (KB >= 2) {
+        // matrices: plane0 rows 0-7, plane0 rows 8-15, plane1 rows 0-7, plane1 rows 8-15
+        const int p = lane >> 4;
+        ldsm_x4(smem_u32(base + L::kplanes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
+                pw[0][0], pw[0][1], pw[1][0], pw[1][1]);
+      }
+      if (KB == 1 || KB == 3) {
+        const int p = KB - 1;
+        ldsm_x2(smem_u32(base + L::kplanes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
+                pw[p][0], pw[p][1]);
+      }
+      ldsm_x2(smem_u32(base + L::ksgn + (tok0 + r + 8 * m8) * 16), sw[0], sw[1]);
+#pragma unroll
+      for (int v = 0; v <= NKV; ++v) {
+        uint32_t x0, x1;
+        if (v < NKV) {
+          const uint32_t w0[3] = {pw[0][0], pw[1][0], pw[2][0]};
+          const uint32_t w1[3] = {pw[0][1], pw[1][1], pw[2][1]};
+          x0 = vplane_word<KB>(w0, v);
+          x1 = vplane_word<KB>(w1, v);
+        } else {
+          x0 = sw[0];
+          x1 = sw[1];
+        }
+        const Expanded e0 = expand(x0), e1 = expand(x1);
+        float* d = v < NKV ? dm : dq;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          mma(d, e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bq[v][s][0], bq[v][s][1]);
+          if (!HILO && v < NKV)
+            mma(dml, e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bql[v][s][0],
+                bql[v][s][1]);
+        }
+      }
+      if (!HILO) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dm[i] += dml[i];
+      }
+    }
+    // ---- scores → base-2 logits; rows: token g (k = 0) and g + 8 (k = 1)
+    const float* kxn = reinterpret_cast<const float*>(base + L::kxn);
+    const float* krn = reinterpret_cast<const float*>(base + L::krn);
+    const float* vxn = reinterpret_cast<const float*>(base + L::vxn);
+    float lg[2][2];   // [row][column pair]
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int tl = tok0 + g + 8 * k;
+      const bool valid = t_abs + g + 8 * k < t_end;
+      const float xn = kxn[tl], rn = krn[tl];
+      if (HILO) {
+        const float m = dm[2 * k] + dm[2 * k + 1], q = dq[2 * k] + dq[2 * k + 1];
+        const float s = xn * hA[0] * (m - hCm[0]) + rn * hB[0] * (q - hCq[0]);
+        lg[k][0] = lg[k][1] = valid ? s : -INFINITY;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float s = xn * hA[h] * (dm[2 * k + h] - hCm[h]) + rn * hB[h] * (dq[2 * k + h] - hCq[h]);
+          lg[k][h] = valid ? s : -INFINITY;
+        }
+      }
+    }
+    // ---- online softmax (per column pair), max over the 16 rows held by lanes g = 0..7
+    float mt[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float m = fmaxf(lg[0][h], lg[1][h]);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      mt[h] = fmaxf(m_run[h], m);
+    }
+    if (__any_sync(0xffffffffu, mt[0] > m_run[0] || mt[1] > m_run[1])) {
+      float corr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        corr[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - mt[h]);
+        l_run[h] *= corr[h];
+        lw_run[h] *= corr[h];
+        m_run[h] = mt[h];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i][0] *= corr[0];
+        acc[i][1] *= corr[1];
+        acc[i][2] *= corr[0];
+        acc[i][3] *= corr[1];
+      }
+    }
+    float w[2][2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      // tokens past the sequence (or past the capacity in a short last chunk) may hold
+      // stale bytes: their weight is exactly zero, never 0 × (stale norm)
+      const bool valid = t_abs + g + 8 * k < t_end;
+      const float vn = vxn[tok0 + g + 8 * k];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float p = valid ? exp2f(lg[k][h] - m_run[h]) : 0.f;
+        l_run[h] += p;
+        w[k][h] = valid ? p * vn : 0.f;
+        lw_run[h] += w[k][h];
+      }
+    }
+    // ---- value accumulation: acc[coord][column] += Σ_t A[coord][t] · B[t][column]
+    if constexpr (VB == 4) {
+      uint32_t bw0, bw1;
+      if (HILO) {
+        const float h0 = __half2float(__float2half_rn(w[0][0]));
+        const float h1 = __half2float(__float2half_rn(w[1][0]));
+        bw0 = movm_t(pack_half2(h0, w[0][0] - h0));
+        bw1 = movm_t(pack_half2(h1, w[1][0] - h1));
+      } else {
+        bw0 = movm_t(pack_half2(w[0][0], w[0][1]));
+        bw1 = movm_t(pack_half2(w[1][0], w[1][1]));
+      }
+      // 8 code bytes (coordinates 16g..16g+15) of tokens 2c, 2c+1, 2c+8, 2c+9
+      const unsigned char* vb = base + L::vcodes + (tok0 + 2 * c) * 64 + 8 * g;
+      const uint2 u0 = *reinterpret_cast<const uint2*>(vb);
+      const uint2 u1 = *reinterpret_cast<const uint2*>(vb + 64);
+      const uint2 u2 = *reinterpret_cast<const uint2*>(vb + 8 * 64);
+      const uint2 u3 = *reinterpret_cast<const uint2*>(vb + 9 * 64);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t A = half ? u0.y : u0.x, Bw = half ? u1.y : u1.x;
+        const uint32_t C = half ? u2.y : u2.x, D = half ? u3.y : u3.x;
+        // key byte i: low nibble = code of the first token, high nibble = second token
+        const uint32_t klo01 = (A & 0x0f0f0f0fu) | ((Bw << 4) & 0xf0f0f0f0u);
+        const uint32_t khi01 = ((A >> 4) & 0x0f0f0f0fu) | (Bw & 0xf0f0f0f0u);
+        const uint32_t klo23 = (C & 0x0f0f0f0fu) | ((D << 4) & 0xf0f0f0f0u);
+        const uint32_t khi23 = ((C >> 4) & 0x0f0f0f0fu) | (D & 0xf0f0f0f0u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t a0 = lut_lane[((klo01 >> (8 * i)) & 0xffu) << 5];
+          const uint32_t a1 = lut_lane[((khi01 >> (8 * i)) & 0xffu) << 5];
+          const uint32_t a2 = lut_lane[((klo23 >> (8 * i)) & 0xffu) << 5];
+          const uint32_t a3 = lut_lane[((khi23 >> (8 * i)) & 0xffu) << 5];
+          mma(acc[4 * half + i], a0, a1, a2, a3, bw0, bw1);
+        }
+      }
+    } else {
+      // planes transposed on load: pair word = {chunk g of token 2c, chunk g of token 2c+1}
+      uint32_t mw[3][2];
+      {
+        const int r = lane & 7, m8 = (lane >> 3) & 1;
+#pragma unroll
+        for (int p = 0; p < VB; ++p)
+          ldsm_x2_t(smem_u32(base + L::vcodes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
+                    mw[p][0], mw[p][1]);
+      }
+#pragma unroll
+      for (int v = 0; v < NVV; ++v) {
+        const float coef = a.vd.coef[v];
+        uint32_t bw0, bw1;
+        if (HILO) {
+          const float x0 = coef * w[0][0], x1 = coef * w[1][0];
+          const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
+          bw0 = movm_t(pack_half2(h0, x0 - h0));
+          bw1 = movm_t(pack_half2(h1, x1 - h1));
+        } else {
+          bw0 = movm_t(pack_half2(coef * w[0][0], coef * w[0][1]));
+          bw1 = movm_t(pack_half2(coef * w[1][0], coef * w[1][1]));
+        }
+        const uint32_t w0[3] = {mw[0][0], mw[1][0], mw[2][0]};
+        const uint32_t w1[3] = {mw[0][1], mw[1][1], mw[2][1]};
+        const Expanded e0 = expand(vplane_word<VB < 4 ? VB : 1>(w0, v));
+        const Expanded e1 = expand(vplane_word<VB < 4 ? VB : 1>(w1, v));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          mma(acc[i], e0.p[2 * i], e0.p[2 * i + 1], e1.p[2 * i], e1.p[2 * i + 1], bw0, bw1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[st]);
+  }
+
+  // ------------------------------------------------------------ CTA combine
+  // l and Σw over the 16 rows of each column (lanes sharing c)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], o);
+      lw_run[h] += __shfl_xor_sync(0xffffffffu, lw_run[h], o);
+    }
+  }
+  consumer_sync();   // every warp is done with the ring: reuse it
+  float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);           // [warp][col][128]
+  float* cst = reinterpret_cast<float*>(smem + L::comb_stats);          // [warp][3][8]
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int row = k < 2 ? g : g + 8;
+      const int col = 2 * c + (k & 1);
+      int coord;
+      float v = acc[i][k];
+      if (VB == 4) {
+        coord = 16 * g + 2 * i + (row >= 8 ? 1 : 0);
+        v *= a.vc_unscale;
+      } else {
+        const int e = 2 * i + (row >= 8 ? 1 : 0);
+        coord = 16 * g + pair_lo(e);
+        v *= exp2f((float)-pos_exp(pair_pos(e)));
+      }
+      cacc[(warp * 8 + col) * TQ_D + coord] = v;
+    }
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int col = 2 * c + k;
+      cst[(warp * 3 + 0) * 8 + col] = m_run[k];
+      cst[(warp * 3 + 1) * 8 + col] = l_run[k];
+      cst[(warp * 3 + 2) * 8 + col] = lw_run[k];
+    }
+  }
+  consumer_sync();
+  float* rec_base = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
+  for (int i = tid; i < a.G * TQ_D; i += kConsumerWarps * 32) {
+    const int head = i / TQ_D, j = i % TQ_D;
+    const int col = HILO ? 2 * head : head;
+    float M = -INFINITY;
+    for (int wp = 0; wp < kConsumerWarps; ++wp) M = fmaxf(M, cst[(wp * 3) * 8 + col]);
+    float Lsum = 0.f, lw = 0.f, acc_j = 0.f;
+    if (M > -INFINITY) {
+      for (int wp = 0; wp < kConsumerWarps; ++wp) {
+        const float mw_ = cst[(wp * 3) * 8 + col];
+        if (mw_ == -INFINITY) continue;
+        const float f = exp2f(mw_ - M);
+        Lsum += f * cst[(wp * 3 + 1) * 8 + col];
+        lw += f * cst[(wp * 3 + 2) * 8 + col];
+        float av = cacc[(wp * 8 + col) * TQ_D + j];
+        if (HILO) av += cacc[(wp * 8 + col + 1) * TQ_D + j];
+        acc_j += f * av;
+      }
+      if (VB != 4) acc_j -= a.vd.cst * lw;
+    }
+    float* rec = rec_base + head * kRec;
+    if (j == 0) {
+      // natural-log maximum (the merge combines with expf)
+      rec[0] = M == -INFINITY ? -INFINITY : M * 0.69314718055994531f;
+      rec[1] = Lsum;
+    }
+    rec[2 + j] = acc_j;
+  }
+  (void)timed_out;
+}
+
+template <int KB, int VB, bool HILO>
+tq_status launch_one(const tq_mma_launch& a, cudaStream_t stream) {
+  constexpr int smem = Layout<KB, VB>::total;
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(decode_mma_kernel<KB, VB, HILO>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    configured[dev] = true;
+  }
+  dim3 grid(a.nsplit, a.Hkv, a.B);
+  decode_mma_kernel<KB, VB, HILO><<<grid, kThreads, smem, stream>>>(a);
+  return tq_cuda_status(cudaGetLastError());
+}
+
+template <int KB, int VB>
+tq_status launch_kv(const tq_mma_launch& a, cudaStream_t stream) {
+  return a.G <= 4 ? launch_one<KB, VB, true>(a, stream) : launch_one<KB, VB, false>(a, stream);
+}
+
+template <int KB>
+tq_status launch_k(const tq_mma_launch& a, cudaStream_t stream) {
+  switch (a.vbits) {
+    case 1: return launch_kv<KB, 1>(a, stream);
+    case 2: return launch_kv<KB, 2>(a, stream);
+    case 3: return launch_kv<KB, 3>(a, stream);
+    case 4: return launch_kv<KB, 4>(a, stream);
+  }
+  return TQ_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+bool tq_mma_supported(int kbits, int vbits, int G) {
+  return kbits >= 1 && kbits <= 3 && vbits >= 1 && vbits <= 4 && G >= 1 && G <= 8;
+}
+
+tq_plane_decomp tq_decompose_levels(const tq_codec* c) {
+  // Walsh–Hadamard coefficients of the levels over the ±1 bit variables.
+  tq_plane_decomp d{};
+  const int B = c->ibits, L = c->levels;
+  static const int masks[3][4] = {{1, 0, 0, 0}, {1, 2, 0, 0}, {1, 2, 4, 7}};
+  const int nv = B == 1 ? 1 : B == 2 ? 2 : 4;
+  d.n = nv;
+  double cst = 0;
+  for (int v = 0; v < nv; ++v) {
+    const int m = masks[B - 1][v];
+    double a = 0;
+    for (int idx = 0; idx < L; ++idx) {
+      int prod = 1;
+      for (int i = 0; i < B; ++i)
+        if (m & (1 << i)) prod *= ((idx >> i) & 1) ? 1 : -1;
+      a += (double)c->centroids_d[idx] * prod;
+    }
+    a /= L;
+    d.coef[v] = (float)(2 * a);
+    cst += a;
+  }
+  d.cst = (float)cst;
+  return d;
+}
+
+tq_status tq_launch_decode_mma(const tq_mma_launch& a, cudaStream_t stream) {
+  if (!tq_mma_supported(a.kbits, a.vbits, a.G)) return TQ_ERR_UNSUPPORTED;
+  switch (a.kbits) {
+    case 1: return launch_k<1>(a, stream);
+    case 2: return launch_k<2>(a, stream);
+    case 3: return launch_k<3>(a, stream);
+  }
+  return TQ_ERR_UNSUPPORTED;
+}
+
+float tq_fp16_friendly_scale(const float* levels, int n) {
+  // An exhaustive search over σ = 1 + k/2^16: the table is then exact to a few 1e-5 instead
+  // of the 2.4e-4 of plain fp16 rounding.
+  float best = 1.f;
+  double best_err = 1e30;
+  for (int k = 0; k < (1 << 16); ++k) {
+    const float sg = 1.f + (float)k / 65536.f;
+    double worst = 0;
+    for (int i = 0; i < n; ++i) {
+      const float x = sg * levels[i];
+      if (x == 0.f) continue;
+      const float r = __half2float(__float2half_rn(x));
+      worst = fmax(worst, fabs((double)r - x) / fabs((double)x));
+      if (worst >= best_err) break;
+    }
+    if (worst < best_err) {
+      best_err = worst;
+      best = sg;
+    }
+  }
+  return best;
+}

@@ -1,0 +1,43 @@
+// Launch interface of the tensor-core split-decode kernel (decode_mma.cu), used by
+// attention.cu.  Internal to the library.
+#pragma once
+
+#include "tq_internal.h"
+
+// A codebook written as a sum over "virtual bit planes": with s_i = 2·bit_i − 1 the
+// antisymmetric Lloyd-Max levels expand into odd Walsh monomials,
+//   c(idx) = Σ_S a_S Π_{i∈S} s_i = Σ_S (2 a_S)·X_S − Σ_S a_S,
+// where X_S is the XOR of the index bits in S (|S| odd).  coef[v] = 2 a_S, cst = Σ a_S.
+struct tq_plane_decomp {
+  int n;             // number of virtual planes
+  float coef[4];
+  float cst;
+};
+
+struct tq_mma_launch {
+  int B, Hq, Hkv, G, cap, nsplit, split_len;
+  float scale_log2;            // softmax scale × log2(e)
+  const float* qv;             // [B][Hq][2][128]: Π q then S q (fp32), from the query prep
+  const uint8_t* kidx;
+  const uint8_t* ksgn;
+  const float* kxn;
+  const float* krn;
+  int kbits;                   // key index bits (1..3)
+  tq_plane_decomp kd;
+  const uint8_t* vidx;
+  const float* vxn;
+  int vbits;                   // value bits (1..4)
+  tq_plane_decomp vd;          // value decomposition (vbits ≤ 3)
+  float vc[16];                // value levels (vbits == 4: pair lookup table)
+  float vc_scale, vc_unscale;  // table levels are vc·vc_scale (chosen to round well to fp16)
+  const int* seq_lens;
+  float* part;                 // [B][Hkv][nsplit][G][130]
+};
+
+// True when the tensor-core kernel handles this configuration.
+bool tq_mma_supported(int kbits, int vbits, int G);
+// Odd-Walsh decomposition of a codec's levels (index bits ≤ 3).
+tq_plane_decomp tq_decompose_levels(const tq_codec* c);
+tq_status tq_launch_decode_mma(const tq_mma_launch& a, cudaStream_t stream);
+// Scale σ in [1, 2) for which σ·levels are closest to fp16 numbers (worst relative error).
+float tq_fp16_friendly_scale(const float* levels, int n);

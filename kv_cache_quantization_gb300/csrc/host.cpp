@@ -235,9 +235,11 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
   }
   for (int i = 0; i < 16; ++i) {
     c->centroids[i] = i < L ? (float)centroids[i] : 0.f;
+    c->centroids_d[i] = i < L ? centroids[i] : 0.0;
     c->boundaries[i] = i < L - 1 ? (float)(0.5 * (centroids[i] + centroids[i + 1])) : 0.f;
   }
 
+  c->lut_scale = tq_fp16_friendly_scale(c->centroids, L);
   const size_t n = (size_t)d * d;
   std::vector<float> h_pi(n), h_piT(n), h_sT(n), h_mT(n);
   for (int i = 0; i < d; ++i)

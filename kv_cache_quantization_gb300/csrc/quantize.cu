@@ -246,6 +246,101 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   }
 }
 
+// Few vectors (a decode step appends one token per sequence and head): one CTA of 512
+// threads per vector.  Each 128×128 product is split four ways over k, so every thread
+// issues 32 independent coalesced loads of Πᵀ (or Mᵀ) from L2 instead of a 128-long chain;
+// codes are assembled with warp ballots.
+constexpr int kSmallThreads = 512;
+
+__device__ __forceinline__ float small_matvec(const float* __restrict__ T, const float* v,
+                                              float* part, int tid) {
+  const int j = tid & 127, q = tid >> 7;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int k = 32 * q; k < 32 * q + 32; ++k) acc = fmaf(__ldg(&T[k * TQ_D + j]), v[k], acc);
+  part[q * TQ_D + j] = acc;
+  __syncthreads();
+  float r = 0.f;
+  if (tid < TQ_D) r = (part[j] + part[TQ_D + j]) + (part[2 * TQ_D + j] + part[3 * TQ_D + j]);
+  __syncthreads();
+  return r;
+}
+
+template <bool kProd>
+__global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs a) {
+  __shared__ float xs[TQ_D], rho[TQ_D], part[4 * TQ_D];
+  __shared__ float red[4];
+  const int tid = threadIdx.x;
+  const long long i = blockIdx.x;
+  const int t = (int)(i % a.tokens);
+  const int bh = (int)(i / a.tokens);
+  const int b = bh / a.heads, h = bh % a.heads;
+  const int cnt = a.count ? a.count[b] : a.tokens;
+  if (t >= cnt) return;
+  const int dst = (a.pos ? a.pos[b] : 0) + t;
+  if (dst < 0 || dst >= a.capacity) {
+    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
+    return;
+  }
+  const long long slot = (long long)bh * a.capacity + dst;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < 16) {
+    float vals[8];
+    load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xs[tid * 8 + e] = vals[e];
+  }
+  __syncthreads();
+  float x2 = 0.f;
+  if (tid < TQ_D) x2 = xs[tid] * xs[tid];
+  if (warp < 4) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x2 += __shfl_xor_sync(0xffffffffu, x2, o);
+    if (lane == 0) red[warp] = x2;
+  }
+  __syncthreads();
+  const float n = sqrtf((red[0] + red[1]) + (red[2] + red[3]));
+  const float acc = small_matvec(a.piT, xs, part, tid);
+  int q = 0;
+  float r = 0.f;
+  if (tid < TQ_D) {
+    const float y = n > 0.f ? acc / n : 0.f;
+    for (int bnd = 0; bnd < a.lv.levels - 1; ++bnd) q += (a.lv.b[bnd] <= y) ? 1 : 0;
+    r = y - a.lv.c[q];
+    rho[tid] = r;
+  }
+  // index codes: warp w < 4 owns coordinates 32w..32w+31
+  if (warp < 4) {
+    if (a.nibbles) {
+      // byte k = idx(2k) | idx(2k+1) << 4: lane pairs combine through a shuffle
+      const int other = __shfl_xor_sync(0xffffffffu, q, 1);
+      if ((lane & 1) == 0) a.idx[slot * 64 + (tid >> 1)] = (uint8_t)(q | (other << 4));
+    } else {
+      for (int p = 0; p < a.ibits; ++p) {
+        const unsigned word = __ballot_sync(0xffffffffu, (q >> p) & 1);
+        if (lane == 0)
+          reinterpret_cast<uint32_t*>(a.idx + (((long long)bh * a.ibits + p) * a.capacity + dst) * 16)[warp] = word;
+      }
+    }
+    if (tid == 0) a.xnorm[slot] = n;
+  }
+  if constexpr (kProd) {
+    float r2 = r * r;
+    if (warp < 4) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, o);
+    }
+    __syncthreads();   // rho complete; red reused
+    if (warp < 4 && lane == 0) red[warp] = r2;
+    const float z = small_matvec(a.mT, rho, part, tid);   // contains __syncthreads
+    if (warp < 4) {
+      const unsigned word = n > 0.f ? __ballot_sync(0xffffffffu, z >= 0.f) : 0xffffffffu;
+      if (lane == 0) reinterpret_cast<uint32_t*>(a.sgn + slot * 16)[warp] = word;
+      if (tid == 0) a.rnorm[slot] = n * sqrtf((red[0] + red[1]) + (red[2] + red[3]));
+    }
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 tq_status check_x(const void* x, tq_dtype dt, int batch, int heads, int tokens, long long sb,
@@ -263,17 +358,23 @@ template <bool kProd>
 tq_status launch(const QuantArgs& a, cudaStream_t stream) {
   const long long total = (long long)a.batch * a.heads * a.tokens;
   if (total == 0) return TQ_OK;
+  const int sms = tq_num_sms();
+  if (total <= 2LL * (sms > 0 ? sms : 148)) {
+    quantize_small_kernel<kProd><<<(unsigned)total, kSmallThreads, 0, stream>>>(a);
+    return tq_cuda_status(cudaGetLastError());
+  }
   const size_t smem = (size_t)(kProd ? 2 : 1) * TQ_D * TQ_D * sizeof(float) +
                       (size_t)kTile * kXStride * sizeof(float);
-  static bool configured[2] = {false, false};
-  if (!configured[kProd]) {
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
+  if (!configured[dev]) {
     if (cudaFuncSetAttribute(quantize_kernel<kProd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    configured[kProd] = true;
+    configured[dev] = true;
   }
   const long long ntiles = (total + kTile - 1) / kTile;
-  const int sms = tq_num_sms();
   const long long per_sm = kProd ? 1 : 2;
   const int grid = (int)(ntiles < sms * per_sm ? ntiles : sms * per_sm);
   quantize_kernel<kProd><<<grid, kThreads, smem, stream>>>(a);
@@ -328,7 +429,8 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   if (!flags) return TQ_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int a = tq_take_flags_quantize(), b = tq_take_flags_attention();
-  if (a == ~0u || b == ~0u) return TQ_ERR_CUDA;
-  *flags = a | b;
+  const unsigned int c = tq_take_flags_decode_mma();
+  if (a == ~0u || b == ~0u || c == ~0u) return TQ_ERR_CUDA;
+  *flags = a | b | c;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

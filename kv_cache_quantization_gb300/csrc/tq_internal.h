@@ -22,6 +22,8 @@ struct tq_codec {
   float* d_mT;     // Mᵀ  row-major [d][d], M = S Πᵀ (prod only)
   float centroids[16];
   float boundaries[16];
+  double centroids_d[16];
+  float lut_scale;   // fp16-friendly scale of the levels (decode pair table)
 };
 
 // Constants passed by value to kernels.
@@ -46,6 +48,7 @@ struct tq_levels {
 #endif
 unsigned int tq_take_flags_quantize();
 unsigned int tq_take_flags_attention();
+unsigned int tq_take_flags_decode_mma();
 
 static inline tq_status tq_cuda_status(cudaError_t e) {
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -57,3 +60,4 @@ int tq_num_sms();
 
 // Launch helpers implemented in the .cu files
 tq_levels tq_make_levels(const tq_codec* c);
+float tq_fp16_friendly_scale(const float* levels, int n);

@@ -94,6 +94,39 @@ def test_quantize_mse_codes(bits, dtype):
     assert stats.idx_excluded < 1e-4 * stats.coords + 2, stats
 
 
+@pytest.mark.parametrize("kind,bits", [("prod", 2), ("prod", 3), ("prod", 4), ("prod", 5),
+                                       ("mse", 2), ("mse", 3), ("mse", 4)])
+def test_quantize_append_path_codes(kind, bits):
+    """Few vectors (one new token per sequence and head) take the one-CTA-per-vector path."""
+    bsz, h, t, cap = 5, 4, 2, 64
+    x = rand_x((bsz, h, t, D), 900 + bits, torch.bfloat16)
+    x[1, 2, 0] = 0
+    pos = torch.tensor([0, 7, 30, 62, 1], dtype=torch.int32, device="cuda")
+    pi, s = oracle_constants()
+    stats = CodeStats()
+    if kind == "prod":
+        codec = api.Codec.prod(bits)
+        cache = api.ProdCache.empty(bsz, h, cap, bits)
+        api.quantize_prod(codec, x, cache, pos=pos)
+        c = oracle_codebook(bits - 1)
+    else:
+        codec = api.Codec.mse(bits)
+        cache = api.MSECache.empty(bsz, h, cap, bits)
+        api.quantize_mse(codec, x, cache, pos=pos)
+        c = oracle_codebook(bits)
+    check_flags_clear()
+    for b in range(bsz):
+        p0 = int(pos[b])
+        for hh in range(h):
+            xs = x[b, hh].double().cpu().numpy()
+            if kind == "prod":
+                gi, gs, gx, gr = unpack_prod(cache, b, hh, p0 + t, bits - 1)
+                match_prod_codes(xs, gi[p0:], gs[p0:], gx[p0:], gr[p0:], pi, s, c, stats)
+            else:
+                gi, gx = unpack_mse(cache, b, hh, p0 + t, bits)
+                match_mse_codes(xs, gi[p0:], gx[p0:], pi, c, stats)
+
+
 def test_quantize_positions_and_counts():
     """Appends land at pos[b] + t for t < count[b]; other slots stay untouched."""
     bsz, h, t, cap = 3, 2, 5, 128
@@ -201,9 +234,13 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
     return worst
 
 
-@pytest.mark.parametrize("kbits,vbits", [(3, 4), (3, 2), (4, 4), (2, 1), (5, 3)])
-def test_decode_small(kbits, vbits):
-    run_decode(2, 8, 2, [300, 1000], kbits, vbits, torch.bfloat16, torch.float32, 300 + kbits)
+@pytest.mark.parametrize("kbits,vbits,hq", [
+    (3, 4, 8), (3, 2, 8), (4, 4, 8), (2, 1, 8), (5, 3, 8),      # G = 4 (query hi/lo columns)
+    (4, 4, 14), (3, 3, 14), (2, 2, 12), (5, 4, 14),             # G = 7, 7, 6 (one column per head)
+    (4, 1, 6), (2, 3, 4)])                                      # G = 3, 2
+def test_decode_small(kbits, vbits, hq):
+    run_decode(2, hq, 2, [300, 1000], kbits, vbits, torch.bfloat16, torch.float32,
+               300 + 10 * kbits + vbits)
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])

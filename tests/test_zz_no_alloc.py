@@ -63,8 +63,8 @@ def test_noalloc_matches_workspace_entry_point():
 
 def test_noalloc_rejects_requests_beyond_the_static_scratch():
     B.load()
-    # a long, wide batch whose partial results exceed the static array
-    desc = B.tq_attn_desc(64, 32, 8, 128, 262144, 262144, 0, 0.0, B.TQ_BF16, B.TQ_F32)
+    # a very large batch: its per-query vectors alone exceed the static array
+    desc = B.tq_attn_desc(2048, 32, 8, 128, 4096, 4096, 0, 0.0, B.TQ_BF16, B.TQ_F32)
     need = B.tq_decode_workspace_bytes(desc)
     assert need > B.tq_decode_noalloc_scratch_bytes()
     st = B.tq_decode_attention_noalloc(desc, None, None, 16, B.tq_prod_cache(16, 16, 16, 16),
