@@ -56,7 +56,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -172,7 +172,7 @@ def run_ours(args):
     out = plan.new_out(dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, kv_new=None, q=None):
+    def step(i, kv_new=None, q=None, stream=stream):
         kn, vn = kv_new if kv_new is not None else steps_kv[i % 4]
         c = i % copies
         api.quantize_prod(kc, kn, kcs[c], pos=pos, stream=stream)
@@ -180,39 +180,56 @@ def run_ours(args):
         plan.run(kc, vc, steps_q[i % 4] if q is None else q, kcs[c], vcs[c], lens, out,
                  stream=stream)
 
-    launches_per_step = 2 + 3   # quantise K, quantise V, query prep, split decode, merge
+    def decode_only(i, stream=stream):
+        c = i % copies
+        plan.run(kc, vc, steps_q[i % 4], kcs[c], vcs[c], lens, out, stream=stream)
+
+    # quantise K, quantise V, query fragments, split decode (its last CTA per head merges)
+    launches_per_step = 4
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+
+    # The timed steps replay CUDA graphs captured from the same library calls, so that the
+    # measurement is the GPU's time and not the Python launch loop's.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            cs = torch.cuda.current_stream(dev)
+            for i in range(args.steps):
+                fn(i, stream=cs)
+        stream.wait_stream(cap)
+        return g
+
+    g_step = capture(step)
+    g_dec = capture(decode_only)
+    g_step.replay()
+    g_dec.replay()
+    torch.cuda.synchronize()
     barrier(ws)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_all0 = torch.cuda.Event(enable_timing=True)
-    t_all1 = torch.cuda.Event(enable_timing=True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(3):                 # untimed replays keep the clock sampler busy
+            g_step.replay()
         torch.cuda.synchronize()
         barrier(ws)
-        t_all0.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            kn, vn = steps_kv[i % 4]
-            c = i % copies
-            api.quantize_prod(kc, kn, kcs[c], pos=pos, stream=stream)
-            api.quantize_mse(vc, vn, vcs[c], pos=pos, stream=stream)
-            mids[i].record(stream)
-            plan.run(kc, vc, steps_q[i % 4], kcs[c], vcs[c], lens, out, stream=stream)
-            ends[i].record(stream)
-        t_all1.record(stream)
+        t0.record(stream)
+        g_step.replay()                    # exactly args.steps steps
+        t1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
-    total_ms = t_all0.elapsed_time(t_all1)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    dec_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+        d0.record(stream)
+        g_dec.replay()                     # the same decode-attention calls alone
+        d1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
     ms_per_step = max_over_ranks(total_ms / args.steps, ws, dev)
-    dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), ws, dev)
+    dec_mean = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws, dev)
 
     tokens_per_step = w.batch * ctx
     value = tokens_per_step * ws / (ms_per_step * 1e-3)
@@ -273,7 +290,8 @@ def run_ours(args):
                    "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "parallelism": f"replicas x{ws} (independent batches)",
                    "l2": f"{copies} rotating cache copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
-                   "step": "quantise new K,V token + decode attention over all tokens"},
+                   "step": "quantise new K,V token + decode attention over all tokens",
+                   "timing": "CUDA-graph replay of the K steps, CUDA events around it"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "tq_decode_attention (query prep + split decode + merge)",

@@ -24,12 +24,12 @@ namespace {
 
 constexpr int kSplit = 256;          // tokens per split
 constexpr int kThreads = 128;
-constexpr int kRec = 2 + TQ_D;       // partial record: m, l, acc[128]
+constexpr int kRec = TQ_REC;        // partial record: m, l, acc[128], padding
 constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
 
 struct Plan {
   int G, nsplit_main, nsplit_tail, nsplit, split_len;
-  size_t q_off, part_off, bytes;
+  size_t q_off, part_off, cnt_off, bytes;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -62,11 +62,16 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   p->nsplit_main = d->max_seq_len > 0 ? (int)((d->max_seq_len + sl - 1) / sl) : 1;
   p->nsplit_tail = asym ? (d->tail_capacity + kSplit - 1) / kSplit : 0;
   p->nsplit = p->nsplit_main + p->nsplit_tail;
-  const size_t qf = (size_t)d->batch * d->q_heads * 2 * TQ_D;
+  // per-query vectors (CUDA-core path) or per-(batch, KV head) query fragments
+  // (tensor-core path), whichever is larger
+  size_t qbytes = (size_t)d->batch * d->q_heads * 2 * TQ_D * sizeof(float);
+  const size_t fbytes = (size_t)d->batch * d->kv_heads * tq_mma_frag_bytes_max();
+  if (fbytes > qbytes) qbytes = fbytes;
   const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
   p->q_off = 0;
-  p->part_off = ((qf * sizeof(float)) + 255) / 256 * 256;
-  p->bytes = p->part_off + pf * sizeof(float);
+  p->part_off = (qbytes + 255) / 256 * 256;
+  p->cnt_off = (p->part_off + pf * sizeof(float) + 255) / 256 * 256;
+  p->bytes = p->cnt_off + (size_t)d->batch * d->kv_heads * sizeof(int);
   return TQ_OK;
 }
 
@@ -85,7 +90,7 @@ __device__ __forceinline__ void store_elem(void* base, int dtype, long long i, f
 
 // ---------------------------------------------------------------- 1. query prep
 // One CTA of 512 threads per query row: both 128×128 products split four ways over k.
-constexpr int kPrepThreads = 512;
+constexpr int kPrepThreads = 512;   // CUDA-core path query prep
 __global__ void __launch_bounds__(kPrepThreads) query_prep_kernel(const void* q, int q_dtype,
                                                                   const float* piT, const float* sT,
                                                                   float* qv) {
@@ -95,11 +100,17 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_kernel(const void* q,
   const int tid = threadIdx.x, j = tid & 127, kq = tid >> 7;
   if (tid < TQ_D) qf[tid] = load_elem(q, q_dtype, (long long)row * TQ_D + tid);
   __syncthreads();
+  float tp[32], ts[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {   // all loads first: one round trip
+    tp[k] = __ldg(&piT[(32 * kq + k) * TQ_D + j]);
+    ts[k] = __ldg(&sT[(32 * kq + k) * TQ_D + j]);
+  }
   float r = 0.f, s = 0.f;
-#pragma unroll 8
-  for (int k = 32 * kq; k < 32 * kq + 32; ++k) {
-    r = fmaf(__ldg(&piT[k * TQ_D + j]), qf[k], r);
-    s = fmaf(__ldg(&sT[k * TQ_D + j]), qf[k], s);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    r = fmaf(tp[k], qf[32 * kq + k], r);
+    s = fmaf(ts[k], qf[32 * kq + k], s);
   }
   part[0][kq][j] = r;
   part[1][kq][j] = s;
@@ -396,9 +407,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* part,
   __syncthreads();
   if (tid < TQ_D) accs[j] = (accR[0][j] + accR[1][j]) + (accR[2][j] + accR[3][j]);
   __syncthreads();
+  float tp[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) tp[k] = __ldg(&pi[(32 * q + k) * TQ_D + j]);
   float r = 0.f;
-#pragma unroll 8
-  for (int k = 32 * q; k < 32 * q + 32; ++k) r = fmaf(__ldg(&pi[k * TQ_D + j]), accs[k], r);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) r = fmaf(tp[k], accs[32 * q + k], r);
   prod[q][j] = r;
   __syncthreads();
   if (tid < TQ_D) {
@@ -465,28 +479,31 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   a.seq_lens = seq_lens;
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
-  query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
-                                                   reinterpret_cast<float*>(ws + p.q_off));
-  if (tq_mma_supported(kc->ibits, vc->ibits, p.G)) {
+  if (tq_mma_supported(kc->ibits, vc->ibits, p.G) && p.nsplit <= 256) {
     tq_mma_launch m{};
     m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap;
     m.nsplit = p.nsplit; m.split_len = p.split_len;
     m.scale_log2 = a.scale * 1.4426950408889634f;
-    m.qv = a.qv;
+    m.q = q; m.q_dtype = desc->q_dtype; m.piT = kc->d_piT; m.sT = kc->d_sT;
+    m.u = kc->d_u; m.w = kc->d_w; m.smax = kc->smax;
+    m.qfrag = ws + p.q_off;
     m.kidx = k.idx; m.ksgn = k.sgn; m.kxn = k.xnorm; m.krn = k.rnorm;
     m.kbits = kc->ibits; m.kd = tq_decompose_levels(kc);
     m.vidx = v.idx; m.vxn = v.xnorm; m.vbits = vc->ibits;
     if (vc->ibits < 4) m.vd = tq_decompose_levels(vc);
-    for (int i = 0; i < 16; ++i) m.vc[i] = vc->centroids[i];
-    m.vc_scale = vc->ibits == 4 ? vc->lut_scale : 1.f;
-    m.vc_unscale = 1.f / m.vc_scale;
+    m.lut = vc->d_lut;
+    m.vc_unscale = vc->ibits == 4 ? 1.f / vc->lut_scale : 1.f;
     m.seq_lens = seq_lens;
     m.part = a.part;
-    st = tq_launch_decode_mma(m, stream);
-    if (st != TQ_OK) return st;
-  } else {
-    decode_kernel<<<dim3(p.nsplit_main, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+    m.counters = reinterpret_cast<int*>(ws + p.cnt_off);
+    m.pi = vc->d_pi;
+    m.out = out;
+    m.out_dtype = desc->out_dtype;
+    return tq_launch_decode_mma(m, stream);   // merges in its last CTA per (b, KV head)
   }
+  query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
+                                                   reinterpret_cast<float*>(ws + p.q_off));
+  decode_kernel<<<dim3(p.nsplit_main, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
   merge_kernel<<<rows, kMergeThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
                                               vc->d_pi, out, desc->out_dtype);
   return tq_cuda_status(cudaGetLastError());

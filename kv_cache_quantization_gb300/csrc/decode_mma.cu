@@ -21,6 +21,7 @@
 // engines and mbarriers; a dedicated producer warp issues the copies, eight consumer warps
 // each own 16 tokens of a 128-token chunk and keep an online softmax; the CTA combines its
 // warps and writes one (m, l, acc[128]) record per query head for the LSE merge.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -31,11 +32,17 @@ TQ_DEFINE_FLAGS(tq_take_flags_decode_mma)
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kChunk = 16 * kConsumerWarps;   // tokens per stage
 constexpr int kStages = 4;
-constexpr int kRec = 2 + TQ_D;
-constexpr unsigned kSpinLimit = 1u << 24;
+constexpr int kRec = TQ_REC;
+constexpr unsigned kSpinLimit = 1u << 20;   // polls; a healthy wait needs a few hundred
+// most splits per (batch, KV head) the last-CTA merge accepts
+constexpr int kMaxSplits = 256;
+// per-warp accumulators in the CTA combine: coordinate j of column col at col·140 + j + j/16,
+// which spreads the 32 lanes of a fragment store over 32 banks
+constexpr int kAccPitch = 140;
+__host__ __device__ constexpr int accidx(int col, int j) { return col * kAccPitch + j + (j >> 4); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -178,6 +185,151 @@ __device__ __forceinline__ uint32_t vplane_word(const uint32_t* w, int v) {
   return x;
 }
 
+// ---------------------------------------------------------------- query fragments
+// The B operands of the key-score MMAs depend only on the lane (g = column, c = word of
+// the planes), not on the warp: they are built once per (batch, KV head) by
+// query_frag_kernel and copied into every CTA.  Word w of lane l sits at [w][32] + l.
+//   w = (v·8 + s)·2 + half           v ≤ NKV (NKV = sign plane): rounded query
+//   w = NWB + (v·8 + s)·2 + half     v < NKV, only when G > 4: the rounding residue
+// followed by 8 columns × {A, Cm, B, Cq} score constants (floats).
+__host__ __device__ constexpr int frag_words(int kb, bool hilo) {
+  return (num_vplanes(kb) + 1) * 16 + (hilo ? 0 : num_vplanes(kb) * 16);
+}
+__host__ __device__ constexpr int frag_bytes(int kb, bool hilo) {
+  return frag_words(kb, hilo) * 128 + 8 * 4 * 4;
+}
+constexpr int kMaxFragBytes = frag_bytes(3, false);
+constexpr int kPrepThreads = 256;
+
+// Grid (4 word slices c, KV heads, batch): the CTA for slice c computes Π q and S q only
+// for coordinates 32c..32c+31 (the plane word c that lanes with lane % 4 == c hold) and
+// writes those lanes' words.  The operand is normalised by ‖q‖ (|(Π q)_j| ≤ ‖q‖) and by
+// smax·‖q‖ for the sketch (|(S q)_j| ≤ ‖S_j‖·‖q‖), and the column sums Σ_j (Π q)_j = (Πᵀ1)·q,
+// Σ_j (S q)_j = (Sᵀ1)·q come straight from q, so no slice needs another slice's results.
+template <int KB, bool HILO>
+__global__ void __launch_bounds__(kPrepThreads) query_frag_kernel(const tq_mma_launch a) {
+  constexpr int NKV = num_vplanes(KB);
+  constexpr int NWB = (NKV + 1) * 16;
+  constexpr int NW = frag_words(KB, HILO);
+  __shared__ float qf[8][TQ_D];
+  __shared__ float part[2][8][8][32];     // [Π|S][k part][head][j in slice]
+  __shared__ float qsl[2][8][33];         // [Π|S][head][j in slice]
+  __shared__ float s_nq[8], s_uq[8], s_wq[8];
+  const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the decode grid may launch now: it streams the cache while this kernel runs and waits
+  // for this grid's completion before it reads the fragments or the counters
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // 1. the group's queries (fp32), zero beyond G
+#pragma unroll
+  for (int r = 0; r < 8 * TQ_D / kPrepThreads; ++r) {
+    const int i = tid + r * kPrepThreads;
+    const int h = i / TQ_D, j = i % TQ_D;
+    float v = 0.f;
+    if (h < a.G) {
+      const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + j;
+      if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[e];
+      else if (a.q_dtype == TQ_BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.q)[e] << 16);
+      else v = __half2float(__ushort_as_half(static_cast<const uint16_t*>(a.q)[e]));
+    }
+    qf[h][j] = v;
+  }
+  // this slice of Πᵀ and Sᵀ: thread (k part, j) loads 16 of each (all loads first)
+  const int jl = tid & 31, kp = tid >> 5;
+  float tp[16], ts[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    tp[k] = __ldg(&a.piT[(16 * kp + k) * TQ_D + 32 * c + jl]);
+    ts[k] = __ldg(&a.sT[(16 * kp + k) * TQ_D + 32 * c + jl]);
+  }
+  const float uk = __ldg(&a.u[lane * 4]), uk1 = __ldg(&a.u[lane * 4 + 1]);
+  const float uk2 = __ldg(&a.u[lane * 4 + 2]), uk3 = __ldg(&a.u[lane * 4 + 3]);
+  const float wk = __ldg(&a.w[lane * 4]), wk1 = __ldg(&a.w[lane * 4 + 1]);
+  const float wk2 = __ldg(&a.w[lane * 4 + 2]), wk3 = __ldg(&a.w[lane * 4 + 3]);
+  __syncthreads();
+  // 2. per head: ‖q‖, (Πᵀ1)·q, (Sᵀ1)·q (warp h)
+  if (warp < a.G) {
+    const float* x = qf[warp] + lane * 4;
+    float n2 = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+    float uq = uk * x[0] + uk1 * x[1] + uk2 * x[2] + uk3 * x[3];
+    float wq = wk * x[0] + wk1 * x[1] + wk2 * x[2] + wk3 * x[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+      uq += __shfl_xor_sync(0xffffffffu, uq, o);
+      wq += __shfl_xor_sync(0xffffffffu, wq, o);
+    }
+    if (lane == 0) {
+      s_nq[warp] = sqrtf(n2);
+      s_uq[warp] = uq;
+      s_wq[warp] = wq;
+    }
+  }
+  // 3. slice products
+  for (int h = 0; h < a.G; ++h) {
+    float r = 0.f, q2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      r = fmaf(tp[k], qf[h][16 * kp + k], r);
+      q2 = fmaf(ts[k], qf[h][16 * kp + k], q2);
+    }
+    part[0][kp][h][jl] = r;
+    part[1][kp][h][jl] = q2;
+  }
+  __syncthreads();
+  for (int i = tid; i < 2 * 8 * 32; i += kPrepThreads) {
+    const int which = i >> 8, h = (i >> 5) & 7, j = i & 31;
+    float v = 0.f;
+    if (h < a.G)
+      for (int k = 0; k < 8; ++k) v += part[which][k][h][j];
+    qsl[which][h][j] = v;
+  }
+  __syncthreads();
+  // 4. fragment words of the 8 lanes (g, c): column g
+  uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.qfrag) +
+                                              bh * (long long)frag_bytes(KB, HILO));
+  for (int i = tid; i < NW * 8; i += kPrepThreads) {
+    const int g = i & 7, w = i >> 3;
+    const bool residue_tile = w >= NWB;
+    const int wv = residue_tile ? w - NWB : w;
+    const int v = wv >> 4, s = (wv >> 1) & 7, half = wv & 1;
+    const int e = 2 * s + half;
+    const int j0 = pair_lo(e), j1 = j0 + 16;          // within the slice
+    const float sc = exp2f((float)-pos_exp(pair_pos(e)));
+    const int head = HILO ? (g >> 1) : g;
+    float x0 = 0.f, x1 = 0.f;
+    if (head < a.G && s_nq[head] > 0.f) {
+      const bool sign_plane = v == NKV;
+      const float coef = sign_plane ? 2.f : a.kd.coef[v];
+      const float nrm = sign_plane ? 1.f / (s_nq[head] * a.smax) : 1.f / s_nq[head];
+      const float* src = qsl[sign_plane ? 1 : 0][head];
+      x0 = src[j0] * nrm * coef * sc;
+      x1 = src[j1] * nrm * coef * sc;
+    }
+    const float r0 = x0 - __half2float(__float2half_rn(x0));
+    const float r1 = x1 - __half2float(__float2half_rn(x1));
+    // G ≤ 4: odd columns carry the rounding residue of the even column's head
+    if (residue_tile || (HILO && (g & 1))) {
+      x0 = r0;
+      x1 = r1;
+    }
+    out[w * 32 + 4 * g + c] = pack_half2(x0, x1);
+  }
+  if (c == 0 && tid < 8) {
+    // score constants of column n: A, Cm, B, Cq
+    const int n = tid, head = HILO ? (n >> 1) : n;
+    float* cst = reinterpret_cast<float*>(out + NW * 32);
+    const float nq = head < a.G ? s_nq[head] : 0.f;
+    const bool ok = nq > 0.f;
+    cst[n * 4 + 0] = nq * a.scale_log2;
+    cst[n * 4 + 1] = ok ? a.kd.cst * s_uq[head] / nq : 0.f;
+    cst[n * 4 + 2] = nq * a.smax * a.scale_log2 * (1.2533141373155003f / TQ_D);
+    cst[n * 4 + 3] = ok ? s_wq[head] / (nq * a.smax) : 0.f;
+  }
+  if (c == 0 && tid == 0) a.counters[bh] = 0;   // the decode kernel's last CTA per (b, KV head) merges
+}
+
 // ---------------------------------------------------------------- shared-memory layout
 template <int KB, int VB>
 struct Layout {
@@ -192,13 +344,13 @@ struct Layout {
   static constexpr int ring = kStages * stage;
   static constexpr int lut = ring;                           // VB == 4: 256 × 32 words
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
-  static constexpr int q = lut + lut_bytes;                  // q_rot, q_sk [2][8][128] f32
-  static constexpr int total = q + 2 * 8 * TQ_D * 4;
+  static constexpr int frag = lut + lut_bytes;               // query fragments + constants
+  static constexpr int total = frag + kMaxFragBytes;
   // the CTA combine reuses everything above (ring, table and query buffer are dead by
   // then): per warp m, l, Σw [3][8] and acc [8][128]
   static constexpr int comb_acc = 0;
-  static constexpr int comb_stats = kConsumerWarps * 8 * TQ_D * 4;
-  static_assert(comb_stats + kConsumerWarps * 3 * 8 * 4 <= total, "combine buffer");
+  static constexpr int comb_stats = kConsumerWarps * 8 * kAccPitch * 4;
+  static_assert(comb_stats + (kConsumerWarps * 3 + kConsumerWarps) * 8 * 4 <= total, "combine buffer");
 };
 
 // ---------------------------------------------------------------- the kernel
@@ -210,8 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ float s_hd[8][6];   // per query column: A, Cm, B, Cq (score constants)
-  __shared__ int s_timeout;
+  __shared__ __align__(8) uint64_t prol_bar;
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
@@ -230,147 +381,86 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
-    s_timeout = 0;
+    mbar_init(&prol_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // ------------------------------------------------------------ producer warp
-  if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c % kStages;
-        if (c >= kStages && !mbar_wait(&empty_bar[st], ((c / kStages) - 1) & 1)) {
-          atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-          s_timeout = 1;
-          break;
-        }
-        const int t0 = t_begin + c * kChunk;
-        const int n = min(kChunk, a.cap - t0);   // multiple of 64 (capacity is)
-        unsigned char* base = smem + st * L::stage;
-        const unsigned bytes = (unsigned)n * (KB * 16 + 16 + 4 + 4 + (VB == 4 ? 64 : VB * 16) + 4);
-        mbar_expect_tx(&full_bar[st], bytes);
-        for (int p = 0; p < KB; ++p)
-          bulk_g2s(base + L::kplanes + p * kChunk * 16,
-                   a.kidx + ((bh * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::ksgn, a.ksgn + (bh * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::kxn, a.kxn + bh * a.cap + t0, n * 4, &full_bar[st]);
-        bulk_g2s(base + L::krn, a.krn + bh * a.cap + t0, n * 4, &full_bar[st]);
-        if (VB == 4) {
-          bulk_g2s(base + L::vcodes, a.vidx + (bh * a.cap + t0) * 64, n * 64, &full_bar[st]);
-        } else {
-          for (int p = 0; p < VB; ++p)
-            bulk_g2s(base + L::vcodes + p * kChunk * 16,
-                     a.vidx + ((bh * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        }
-        bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
-      }
-      // do not leave while copies may still be landing in this CTA's shared memory
-      for (int c = nchunks - kStages > 0 ? nchunks - kStages : 0; c < nchunks; ++c)
-        if (!mbar_wait(&full_bar[c % kStages], (c / kStages) & 1)) {
-          atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-          break;
-        }
+  // ------------------------------------------------------------ copies (thread 0)
+  // Thread 0 keeps kStages − 1 chunks in flight ahead of the one being consumed: it issues
+  // chunk c into stage c % kStages once every warp has released that stage.
+  auto issue = [&](int c) {
+    const int st = c % kStages;
+    const int t0 = t_begin + c * kChunk;
+    const int n = min(kChunk, a.cap - t0);   // multiple of 64 (capacity is)
+    unsigned char* base = smem + st * L::stage;
+    const unsigned bytes = (unsigned)n * (KB * 16 + 16 + 4 + 4 + (VB == 4 ? 64 : VB * 16) + 4);
+    mbar_expect_tx(&full_bar[st], bytes);
+    for (int p = 0; p < KB; ++p)
+      bulk_g2s(base + L::kplanes + p * kChunk * 16, a.kidx + ((bh * KB + p) * a.cap + t0) * 16,
+               n * 16, &full_bar[st]);
+    bulk_g2s(base + L::ksgn, a.ksgn + (bh * a.cap + t0) * 16, n * 16, &full_bar[st]);
+    bulk_g2s(base + L::kxn, a.kxn + bh * a.cap + t0, n * 4, &full_bar[st]);
+    bulk_g2s(base + L::krn, a.krn + bh * a.cap + t0, n * 4, &full_bar[st]);
+    if (VB == 4) {
+      bulk_g2s(base + L::vcodes, a.vidx + (bh * a.cap + t0) * 64, n * 64, &full_bar[st]);
+    } else {
+      for (int p = 0; p < VB; ++p)
+        bulk_g2s(base + L::vcodes + p * kChunk * 16, a.vidx + ((bh * VB + p) * a.cap + t0) * 16,
+                 n * 16, &full_bar[st]);
     }
-    return;
+    bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
+  };
+  int issued = 0;   // chunks issued so far (meaningful in thread 0 only)
+  if (tid == 0) {
+    constexpr unsigned fb = frag_bytes(KB, HILO);
+    mbar_expect_tx(&prol_bar, fb + (VB == 4 ? 256 * 32 * 4 : 0));
+    if (VB == 4) bulk_g2s(smem + L::lut, a.lut, 256 * 32 * 4, &prol_bar);
+    for (; issued < nchunks && issued < kStages; ++issued) issue(issued);
+    // launched as a dependent of the fragment kernel: everything above only reads the
+    // codec and the cache; the fragments are that kernel's output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    bulk_g2s(smem + L::frag, reinterpret_cast<const unsigned char*>(a.qfrag) + bh * (long long)fb,
+             fb, &prol_bar);
   }
 
-  // ------------------------------------------------------------ consumer prologue
-  float* qs = reinterpret_cast<float*>(smem + L::q);   // [2][8][128]
+  // ------------------------------------------------------------ prologue
+  // query fragments (and the value pair table) arrive by bulk copy as well
+  if (tid == 0 && !mbar_wait(&prol_bar, 0)) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+  __syncthreads();
   const int g = lane >> 2, c = lane & 3;
-  for (int i = tid; i < 2 * 8 * TQ_D; i += kConsumerWarps * 32) {
-    const int which = i / (8 * TQ_D), h = (i / TQ_D) % 8, j = i % TQ_D;
-    const int head = HILO ? (h >> 1) : h;            // query column → head of the group
-    float v = 0.f;
-    if (head < a.G) v = a.qv[((long long)b * a.Hq + kvh * a.G + head) * 2 * TQ_D + which * TQ_D + j];
-    qs[i] = v;
-  }
-  if (VB == 4) {
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L::lut);
-    for (int i = tid; i < 256 * 32; i += kConsumerWarps * 32) {
-      const int key = i >> 5;
-      lut[i] = pack_half2(a.vc_scale * a.vc[key & 15], a.vc_scale * a.vc[key >> 4]);
-    }
-  }
-  consumer_sync();
-  // per query column: max |q| (normalises the fp16 operand) and the constant terms
-  {
-    const int col = warp;  // 8 consumer warps, one column each
-    float mr = 0.f, ms = 0.f, sr = 0.f, ss = 0.f;
-    for (int j = lane; j < TQ_D; j += 32) {
-      mr = fmaxf(mr, fabsf(qs[col * TQ_D + j]));
-      ms = fmaxf(ms, fabsf(qs[(8 + col) * TQ_D + j]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-      ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
-    }
-    const float ir = mr > 0.f ? 1.f / mr : 0.f, is = ms > 0.f ? 1.f / ms : 0.f;
-    for (int j = lane; j < TQ_D; j += 32) {
-      sr += qs[col * TQ_D + j] * ir;
-      ss += qs[(8 + col) * TQ_D + j] * is;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sr += __shfl_xor_sync(0xffffffffu, sr, o);
-      ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    }
-    if (lane == 0) {
-      s_hd[col][0] = mr * a.scale_log2;                              // A
-      s_hd[col][1] = a.kd.cst * sr;                                  // Cm
-      s_hd[col][2] = ms * a.scale_log2 * (1.2533141373155003f / TQ_D);  // B
-      s_hd[col][3] = ss;                                             // Cq
-      s_hd[col][4] = ir;
-      s_hd[col][5] = is;
-    }
-  }
-  consumer_sync();
-  // query operands of this thread: column g, coordinates of word c.  bq = rounded query
-  // (with G ≤ 4, odd columns carry the rounding residue of the even column's head); with
-  // G > 4 the residue of the MSE planes goes to a second 8-column tile, bql.
   uint32_t bq[NKV + 1][8][2];
   uint32_t bql[HILO ? 1 : NKV][8][2];
   {
-    const int col = g;
-    // HILO: even column = rounded query, odd column = its rounding residue (same head)
-    const int qcol = HILO ? (col & ~1) : col;
-    const float ir = s_hd[qcol][4], is = s_hd[qcol][5];
+    const uint32_t* fw = reinterpret_cast<const uint32_t*>(smem + L::frag) + lane;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
+    for (int v = 0; v <= NKV; ++v)
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int e = 2 * s + half;
-        const int j0 = 32 * c + pair_lo(e), j1 = j0 + 16;
-        const float sc = exp2f((float)-pos_exp(pair_pos(e)));
+      for (int s = 0; s < 8; ++s)
 #pragma unroll
-        for (int v = 0; v <= NKV; ++v) {
-          const bool sign_plane = v == NKV;
-          const float coef = sign_plane ? 2.f : a.kd.coef[v];
-          const float* src = qs + (sign_plane ? 8 + qcol : qcol) * TQ_D;
-          const float nrm = sign_plane ? is : ir;
-          float x0 = src[j0] * nrm * coef * sc, x1 = src[j1] * nrm * coef * sc;
-          const float r0 = x0 - __half2float(__float2half_rn(x0));
-          const float r1 = x1 - __half2float(__float2half_rn(x1));
-          if (HILO && (col & 1)) {
-            x0 = r0;
-            x1 = r1;
-          }
-          bq[v][s][half] = pack_half2(x0, x1);
-          if (!HILO && v < NKV) bql[v][s][half] = pack_half2(r0, r1);
-        }
-      }
+        for (int half = 0; half < 2; ++half) bq[v][s][half] = fw[((v * 8 + s) * 2 + half) * 32];
+    if (!HILO) {
+#pragma unroll
+      for (int v = 0; v < NKV; ++v)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            bql[v][s][half] = fw[((NKV + 1) * 16 + (v * 8 + s) * 2 + half) * 32];
     }
   }
   // score constants of this thread's columns (2c, 2c+1)
   float hA[2], hCm[2], hB[2], hCq[2];
+  {
+    const float* cst = reinterpret_cast<const float*>(smem + L::frag + frag_words(KB, HILO) * 128);
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int col = HILO ? 2 * c : 2 * c + k;
-    hA[k] = s_hd[col][0];
-    hCm[k] = s_hd[col][1];
-    hB[k] = s_hd[col][2];
-    hCq[k] = s_hd[col][3];
+    for (int k = 0; k < 2; ++k) {
+      const int col = HILO ? 2 * c : 2 * c + k;
+      hA[k] = cst[col * 4 + 0];
+      hCm[k] = cst[col * 4 + 1];
+      hB[k] = cst[col * 4 + 2];
+      hCq[k] = cst[col * 4 + 3];
+    }
   }
 
   float acc[8][4];
@@ -393,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
     const int t_abs = t_begin + ch * kChunk + tok0;      // absolute index of token 0
 
     // ---- key scores: D[token][column]
-    float dm[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
-    float dml[4] = {0.f, 0.f, 0.f, 0.f};
+    // two accumulator sets (even and odd k-steps) halve the dependent MMA chains
+    float dm[2][4] = {}, dq[2][4] = {}, dml[2][4] = {};
     {
       uint32_t pw[3][2], sw[2];
       const int r = lane & 7, m8 = (lane >> 3) & 1;
@@ -423,18 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
           x1 = sw[1];
         }
         const Expanded e0 = expand(x0), e1 = expand(x1);
-        float* d = v < NKV ? dm : dq;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
+          float* d = v < NKV ? dm[s & 1] : dq[s & 1];
           mma(d, e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bq[v][s][0], bq[v][s][1]);
           if (!HILO && v < NKV)
-            mma(dml, e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bql[v][s][0],
+            mma(dml[s & 1], e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bql[v][s][0],
                 bql[v][s][1]);
         }
       }
-      if (!HILO) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dm[i] += dml[i];
+      for (int i = 0; i < 4; ++i) {
+        dm[0][i] += dm[1][i];
+        dq[0][i] += dq[1][i];
+        if (!HILO) dm[0][i] += dml[0][i] + dml[1][i];
       }
     }
     // ---- scores → base-2 logits; rows: token g (k = 0) and g + 8 (k = 1)
@@ -448,13 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
       const bool valid = t_abs + g + 8 * k < t_end;
       const float xn = kxn[tl], rn = krn[tl];
       if (HILO) {
-        const float m = dm[2 * k] + dm[2 * k + 1], q = dq[2 * k] + dq[2 * k + 1];
+        const float m = dm[0][2 * k] + dm[0][2 * k + 1], q = dq[0][2 * k] + dq[0][2 * k + 1];
         const float s = xn * hA[0] * (m - hCm[0]) + rn * hB[0] * (q - hCq[0]);
         lg[k][0] = lg[k][1] = valid ? s : -INFINITY;
       } else {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const float s = xn * hA[h] * (dm[2 * k + h] - hCm[h]) + rn * hB[h] * (dq[2 * k + h] - hCq[h]);
+          const float s = xn * hA[h] * (dm[0][2 * k + h] - hCm[h]) + rn * hB[h] * (dq[0][2 * k + h] - hCq[h]);
           lg[k][h] = valid ? s : -INFINITY;
         }
       }
@@ -571,6 +663,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[st]);
+    if (tid == 0 && ch + kStages < nchunks) {
+      if (!mbar_wait(&empty_bar[st], (ch / kStages) & 1)) {
+        atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+        timed_out = true;
+        break;
+      }
+      issue(ch + kStages);
+      ++issued;
+    }
+  }
+  if (timed_out && tid == 0) {
+    // a stage never filled or was never released: let the copies this thread issued land
+    // before the CTA's shared memory is reused or released (bounded as well)
+    for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
+      mbar_wait(&full_bar[c % kStages], (c / kStages) & 1);
   }
 
   // ------------------------------------------------------------ CTA combine
@@ -584,25 +691,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
     }
   }
   consumer_sync();   // every warp is done with the ring: reuse it
-  float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);           // [warp][col][128]
+  float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);           // [warp][col][140]
   float* cst = reinterpret_cast<float*>(smem + L::comb_stats);          // [warp][3][8]
+  float* fac = cst + kConsumerWarps * 3 * 8;                            // [warp][8]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int row = k < 2 ? g : g + 8;
+      const int hi_row = k >> 1;                  // 0: row g, 1: row g + 8
       const int col = 2 * c + (k & 1);
       int coord;
       float v = acc[i][k];
       if (VB == 4) {
-        coord = 16 * g + 2 * i + (row >= 8 ? 1 : 0);
+        coord = 16 * g + 2 * i + hi_row;
         v *= a.vc_unscale;
       } else {
-        const int e = 2 * i + (row >= 8 ? 1 : 0);
+        const int e = 2 * i + hi_row;
         coord = 16 * g + pair_lo(e);
         v *= exp2f((float)-pos_exp(pair_pos(e)));
       }
-      cacc[(warp * 8 + col) * TQ_D + coord] = v;
+      cacc[accidx(warp * 8 + col, coord)] = v;
     }
   }
   if (g == 0) {
@@ -615,35 +723,135 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
     }
   }
   consumer_sync();
+  // per column: the CTA maximum and each warp's rescaling factor, computed once
+  __shared__ float s_M[8], s_L[8], s_LW[8];
+  if (tid < 8) {
+    const int col = tid;
+    float M = -INFINITY;
+    for (int wp = 0; wp < kConsumerWarps; ++wp) M = fmaxf(M, cst[(wp * 3) * 8 + col]);
+    float Lsum = 0.f, lw = 0.f;
+    for (int wp = 0; wp < kConsumerWarps; ++wp) {
+      const float mw_ = cst[(wp * 3) * 8 + col];
+      const float f = (M == -INFINITY || mw_ == -INFINITY) ? 0.f : exp2f(mw_ - M);
+      fac[wp * 8 + col] = f;
+      Lsum += f * cst[(wp * 3 + 1) * 8 + col];
+      lw += f * cst[(wp * 3 + 2) * 8 + col];
+    }
+    s_M[col] = M;
+    s_L[col] = Lsum;
+    s_LW[col] = lw;
+  }
+  consumer_sync();
   float* rec_base = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
   for (int i = tid; i < a.G * TQ_D; i += kConsumerWarps * 32) {
     const int head = i / TQ_D, j = i % TQ_D;
     const int col = HILO ? 2 * head : head;
-    float M = -INFINITY;
-    for (int wp = 0; wp < kConsumerWarps; ++wp) M = fmaxf(M, cst[(wp * 3) * 8 + col]);
-    float Lsum = 0.f, lw = 0.f, acc_j = 0.f;
-    if (M > -INFINITY) {
-      for (int wp = 0; wp < kConsumerWarps; ++wp) {
-        const float mw_ = cst[(wp * 3) * 8 + col];
-        if (mw_ == -INFINITY) continue;
-        const float f = exp2f(mw_ - M);
-        Lsum += f * cst[(wp * 3 + 1) * 8 + col];
-        lw += f * cst[(wp * 3 + 2) * 8 + col];
-        float av = cacc[(wp * 8 + col) * TQ_D + j];
-        if (HILO) av += cacc[(wp * 8 + col + 1) * TQ_D + j];
-        acc_j += f * av;
-      }
-      if (VB != 4) acc_j -= a.vd.cst * lw;
+    float acc_j = 0.f;
+#pragma unroll
+    for (int wp = 0; wp < kConsumerWarps; ++wp) {
+      float av = cacc[accidx(wp * 8 + col, j)];
+      if (HILO) av += cacc[accidx(wp * 8 + col + 1, j)];
+      acc_j = fmaf(fac[wp * 8 + col], av, acc_j);
     }
+    if (VB != 4) acc_j -= a.vd.cst * s_LW[col];
     float* rec = rec_base + head * kRec;
     if (j == 0) {
       // natural-log maximum (the merge combines with expf)
-      rec[0] = M == -INFINITY ? -INFINITY : M * 0.69314718055994531f;
-      rec[1] = Lsum;
+      rec[0] = s_M[col] == -INFINITY ? -INFINITY : s_M[col] * 0.69314718055994531f;
+      rec[1] = s_L[col];
     }
     rec[2 + j] = acc_j;
   }
-  (void)timed_out;
+  // ------------------------------------------------------------ merge (last CTA)
+  // The CTA that finishes last for its (batch, KV head) combines every split's record with
+  // log-sum-exp weights and rotates the result back: out = Πᵀ·acc / L.
+  __shared__ int s_last;
+  __threadfence();
+  consumer_sync();
+  if (tid == 0) s_last = atomicAdd(&a.counters[bh], 1) == a.nsplit - 1;
+  consumer_sync();
+  if (!s_last) return;
+  __threadfence();
+  // shared memory, all free now: [staged records][split weights][combined acc][products]
+  float* mred = reinterpret_cast<float*>(smem + L::total) - 2 * 8 * TQ_D;   // [2][8][128]
+  float* macc = mred - 8 * TQ_D;                                            // [8][128]
+  float* mw = macc - 8 * kMaxSplits;                                        // [8][kMaxSplits]
+  float* stage = reinterpret_cast<float*>(smem);
+  const int rec_bytes = a.G * kRec * 4;                                     // one split, all heads
+  const int per_batch = (int)(((unsigned char*)mw - smem) / rec_bytes);
+  __shared__ float s_Lt[8];
+  const float* recs = a.part + (bh * a.nsplit) * a.G * kRec;
+  // split weights exp(m_s − M) and the total denominator, one warp per head
+  if (warp < a.G) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int sp = lane; sp < a.nsplit; sp += 32) M = fmaxf(M, __ldcg(&recs[(sp * a.G + h) * kRec]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Lt = 0.f;
+    for (int sp = lane; sp < a.nsplit; sp += 32) {
+      const float m = __ldcg(&recs[(sp * a.G + h) * kRec]);
+      const float l = __ldcg(&recs[(sp * a.G + h) * kRec + 1]);
+      const float wgt = (M == -INFINITY || !(l > 0.f)) ? 0.f : expf(m - M);
+      mw[h * kMaxSplits + sp] = wgt;
+      Lt += wgt * l;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
+    if (lane == 0) s_Lt[h] = Lt;
+  }
+  // Σ_s w_s·acc_s with the records staged through shared memory by bulk copies
+  float accv[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0, batch = 0; s0 < a.nsplit; s0 += per_batch, ++batch) {
+    const int nb = min(per_batch, a.nsplit - s0);
+    consumer_sync();   // weights visible; previous batch consumed
+    if (tid == 0) {
+      mbar_expect_tx(&prol_bar, (unsigned)(nb * rec_bytes));
+      bulk_g2s(stage, recs + (long long)s0 * a.G * kRec, (unsigned)(nb * rec_bytes), &prol_bar);
+    }
+    if (!mbar_wait(&prol_bar, (batch + 1) & 1)) {   // phase 0 was the prologue's copy
+      if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      break;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tid + r * kConsumerWarps * 32;
+      if (i < a.G * TQ_D) {
+        const int h = i / TQ_D, j = i % TQ_D;
+        for (int sp = 0; sp < nb; ++sp)
+          accv[r] = fmaf(mw[h * kMaxSplits + s0 + sp], stage[(sp * a.G + h) * kRec + 2 + j], accv[r]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = tid + r * kConsumerWarps * 32;
+    if (i < a.G * TQ_D) macc[i] = accv[r];
+  }
+  consumer_sync();
+  {
+    // out_j = Σ_k Π[k][j] acc_k, the k range split over the two halves of the CTA
+    const int j = tid & 127, kh = tid >> 7;
+    float t[64];
+#pragma unroll
+    for (int k = 0; k < 64; ++k) t[k] = __ldg(&a.pi[(64 * kh + k) * TQ_D + j]);
+    for (int h = 0; h < a.G; ++h) {
+      float r = 0.f;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) r = fmaf(t[k], macc[h * TQ_D + 64 * kh + k], r);
+      mred[(kh * 8 + h) * TQ_D + j] = r;
+    }
+  }
+  consumer_sync();
+  for (int i = tid; i < a.G * TQ_D; i += kConsumerWarps * 32) {
+    const int h = i / TQ_D, j = i % TQ_D;
+    const float Lt = s_Lt[h];
+    const float o = Lt > 0.f ? (mred[h * TQ_D + j] + mred[(8 + h) * TQ_D + j]) / Lt : 0.f;
+    const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + j;
+    if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = o;
+    else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(o);
+    else static_cast<__half*>(a.out)[e] = __float2half_rn(o);
+  }
 }
 
 template <int KB, int VB, bool HILO>
@@ -658,8 +866,19 @@ tq_status launch_one(const tq_mma_launch& a, cudaStream_t stream) {
       return TQ_ERR_CUDA;
     configured[dev] = true;
   }
-  dim3 grid(a.nsplit, a.Hkv, a.B);
-  decode_mma_kernel<KB, VB, HILO><<<grid, kThreads, smem, stream>>>(a);
+  query_frag_kernel<KB, HILO><<<dim3(4, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nsplit, a.Hkv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_mma_kernel<KB, VB, HILO>, a) != cudaSuccess)
+    return TQ_ERR_CUDA;
   return tq_cuda_status(cudaGetLastError());
 }
 
@@ -742,3 +961,5 @@ float tq_fp16_friendly_scale(const float* levels, int n) {
   }
   return best;
 }
+
+size_t tq_mma_frag_bytes_max() { return (size_t)kMaxFragBytes; }

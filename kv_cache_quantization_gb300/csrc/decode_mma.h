@@ -17,7 +17,14 @@ struct tq_plane_decomp {
 struct tq_mma_launch {
   int B, Hq, Hkv, G, cap, nsplit, split_len;
   float scale_log2;            // softmax scale × log2(e)
-  const float* qv;             // [B][Hq][2][128]: Π q then S q (fp32), from the query prep
+  const void* q;               // [B][Hq][128] queries (q_dtype)
+  int q_dtype;
+  const float* piT;            // Πᵀ, Sᵀ of the key codec
+  const float* sT;
+  const float* u;              // Πᵀ·1 and Sᵀ·1 of the key codec
+  const float* w;
+  float smax;                  // largest row norm of S
+  void* qfrag;                 // workspace: per (b, KV head) query fragments
   const uint8_t* kidx;
   const uint8_t* ksgn;
   const float* kxn;
@@ -28,10 +35,14 @@ struct tq_mma_launch {
   const float* vxn;
   int vbits;                   // value bits (1..4)
   tq_plane_decomp vd;          // value decomposition (vbits ≤ 3)
-  float vc[16];                // value levels (vbits == 4: pair lookup table)
-  float vc_scale, vc_unscale;  // table levels are vc·vc_scale (chosen to round well to fp16)
+  const uint32_t* lut;         // vbits == 4: 256 × 32 pair table of the value codec (device)
+  float vc_unscale;            // 1 / the table's level scale
   const int* seq_lens;
   float* part;                 // [B][Hkv][nsplit][G][130]
+  int* counters;               // [B][Hkv] splits finished (zeroed by the fragment kernel)
+  const float* pi;             // Π of the value codec (row-major): out = Πᵀ·acc / L
+  void* out;                   // [B][Hq][128]
+  int out_dtype;
 };
 
 // True when the tensor-core kernel handles this configuration.
@@ -41,3 +52,5 @@ tq_plane_decomp tq_decompose_levels(const tq_codec* c);
 tq_status tq_launch_decode_mma(const tq_mma_launch& a, cudaStream_t stream);
 // Scale σ in [1, 2) for which σ·levels are closest to fp16 numbers (worst relative error).
 float tq_fp16_friendly_scale(const float* levels, int n);
+// Workspace bytes per (batch, KV head) reserved for the query fragments.
+size_t tq_mma_frag_bytes_max();

@@ -5,6 +5,8 @@
 #include <cstring>
 #include <vector>
 
+#include <cuda_fp16.h>
+
 #include "tq_internal.h"
 
 extern "C" const char* tq_status_string(tq_status s) {
@@ -196,6 +198,9 @@ static void free_codec(tq_codec* c) {
   cudaFree(c->d_piT);
   cudaFree(c->d_sT);
   cudaFree(c->d_mT);
+  cudaFree(c->d_lut);
+  cudaFree(c->d_u);
+  cudaFree(c->d_w);
   std::free(c);
 }
 
@@ -269,6 +274,47 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
     if (e == cudaSuccess) e = cudaMalloc(&c->d_mT, bytes);
     if (e == cudaSuccess) e = cudaMemcpy(c->d_sT, h_sT.data(), bytes, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(c->d_mT, h_mT.data(), bytes, cudaMemcpyHostToDevice);
+  }
+  {
+    // column sums Πᵀ·1 and Sᵀ·1, and the largest row norm of S (query normalisation)
+    std::vector<float> u(d), w(d, 0.f);
+    double smax = 0;
+    for (int k = 0; k < d; ++k) {
+      double su = 0, sw = 0;
+      for (int j = 0; j < d; ++j) {
+        su += pi[(size_t)j * d + k];
+        if (kind == TQ_PROD) sw += s[(size_t)j * d + k];
+      }
+      u[k] = (float)su;
+      w[k] = (float)sw;
+    }
+    if (kind == TQ_PROD)
+      for (int j = 0; j < d; ++j) {
+        double rn = 0;
+        for (int k = 0; k < d; ++k) rn += s[(size_t)j * d + k] * s[(size_t)j * d + k];
+        smax = std::fmax(smax, std::sqrt(rn));
+      }
+    c->smax = (float)(smax * (1.0 + 1e-6));
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_u, d * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_w, d * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemcpy(c->d_u, u.data(), d * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(c->d_w, w.data(), d * sizeof(float), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess && kind == TQ_MSE && ibits == 4) {
+    // decode pair table: key = code of token t | code of token t+1 << 4, entry = the two
+    // (scaled) levels as an fp16 pair, replicated 32× so that every lane has its own bank
+    std::vector<uint32_t> lut(256 * 32);
+    for (int key = 0; key < 256; ++key) {
+      const __half lo = __float2half_rn(c->lut_scale * c->centroids[key & 15]);
+      const __half hi = __float2half_rn(c->lut_scale * c->centroids[key >> 4]);
+      uint16_t ulo, uhi;
+      std::memcpy(&ulo, &lo, 2);
+      std::memcpy(&uhi, &hi, 2);
+      for (int k = 0; k < 32; ++k) lut[key * 32 + k] = (uint32_t)ulo | ((uint32_t)uhi << 16);
+    }
+    e = cudaMalloc(&c->d_lut, lut.size() * 4);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(c->d_lut, lut.data(), lut.size() * 4, cudaMemcpyHostToDevice);
   }
   if (e != cudaSuccess) {
     free_codec(c);

@@ -255,9 +255,12 @@ constexpr int kSmallThreads = 512;
 __device__ __forceinline__ float small_matvec(const float* __restrict__ T, const float* v,
                                               float* part, int tid) {
   const int j = tid & 127, q = tid >> 7;
+  float t[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * q + k) * TQ_D + j]);   // one round trip
   float acc = 0.f;
-#pragma unroll 8
-  for (int k = 32 * q; k < 32 * q + 32; ++k) acc = fmaf(__ldg(&T[k * TQ_D + j]), v[k], acc);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) acc = fmaf(t[k], v[32 * q + k], acc);
   part[q * TQ_D + j] = acc;
   __syncthreads();
   float r = 0.f;

@@ -4,9 +4,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/tq.h"
+#include "tq.h"
 
 #define TQ_D 128
+// partial record of one (split, query head): m, l, acc[128], padded to a 16-byte multiple
+#define TQ_REC 132
 
 // Codec: immutable after creation.  Small constants travel to kernels by value.
 struct tq_codec {
@@ -20,6 +22,10 @@ struct tq_codec {
   float* d_piT;    // Πᵀ  row-major [d][d]  (PT[k][j] = Π[j][k])
   float* d_sT;     // Sᵀ  row-major [d][d]  (prod only)
   float* d_mT;     // Mᵀ  row-major [d][d], M = S Πᵀ (prod only)
+  uint32_t* d_lut; // 4-bit MSE only: pair table [256 keys][32 copies] of fp16 level pairs
+  float* d_u;      // Πᵀ·1 (Σ_j Π[j][k]): Σ_j (Π q)_j = u·q
+  float* d_w;      // Sᵀ·1 (prod only)
+  float smax;      // max_j ‖row j of S‖ (prod only): |(S q)_j| ≤ smax·‖q‖
   float centroids[16];
   float boundaries[16];
   double centroids_d[16];
