@@ -134,14 +134,18 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     w = synth.WORKLOADS[args.workload]
     ctx = w.context
-    n_pre = ctx - 1                              # cached tokens before this step
+    # tokens attended per sequence this step (ragged for the serving workload); the cache
+    # holds lens - 1 of them and the step appends the last one
+    lens_np = synth.seq_lengths(w)
+    lens_np[:] = [min(int(x), ctx) for x in lens_np]
+    n_tok = int(sum(lens_np))
     kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
 
     # Prefill compaction: quantise the cached tokens once (not part of the timed step).
     k, v = synth.make_kv(w, device=dev)
     base_k = api.ProdCache.empty(w.batch, w.kv_heads, ctx, w.k_bits, device=dev)
     base_v = api.MSECache.empty(w.batch, w.kv_heads, ctx, w.v_bits, device=dev)
-    pre = torch.full((w.batch,), n_pre, dtype=torch.int32, device=dev)
+    pre = torch.tensor([int(x) - 1 for x in lens_np], dtype=torch.int32, device=dev)
     api.quantize_prod(kc, k, base_k, count=pre)
     api.quantize_mse(vc, v, base_v, count=pre)
     torch.cuda.synchronize()
@@ -165,9 +169,9 @@ def run_ours(args):
                       for _ in range(copies - 1)]
     steps_q = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
     steps_kv = [synth.make_new_tokens(w, device=dev, step=i) for i in range(4)]
-    pos = torch.full((w.batch,), n_pre, dtype=torch.int32, device=dev)
-    lens = torch.full((w.batch,), ctx, dtype=torch.int32, device=dev)
-    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, ctx, ctx, w.in_dtype, w.out_dtype,
+    pos = pre.clone()
+    lens = torch.tensor([int(x) for x in lens_np], dtype=torch.int32, device=dev)
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, ctx, int(max(lens_np)), w.in_dtype, w.out_dtype,
                           device=dev)
     out = plan.new_out(dev)
     stream = torch.cuda.current_stream(dev)
@@ -231,13 +235,13 @@ def run_ours(args):
     ms_per_step = max_over_ranks(total_ms / args.steps, ws, dev)
     dec_mean = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws, dev)
 
-    tokens_per_step = w.batch * ctx
+    tokens_per_step = n_tok
     value = tokens_per_step * ws / (ms_per_step * 1e-3)
     # algorithmic bytes of one decode-attention call: packed K and V codes of every cached
     # token and head, the query and the output
     from kv_cache_quantization_gb300 import _binding as Bn
     code_bytes = (Bn.tq_code_bytes(Bn.TQ_PROD, w.k_bits) + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
-    dec_bytes = (w.batch * w.kv_heads * ctx * code_bytes
+    dec_bytes = (w.kv_heads * n_tok * code_bytes
                  + w.batch * w.q_heads * 128 * (2 + torch.finfo(w.out_dtype).bits // 8))
     peak, peak_kind = read_peaks()
     achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
@@ -286,7 +290,7 @@ def run_ours(args):
         "dtype": "bf16 in / fp32 accumulate on packed K3/V4 codes",
         "data": "synthetic (seeded N(0,1) x lognormal(0,0.5) per channel)",
         "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
-                   "kv_heads": w.kv_heads, "head_dim": 128, "context": ctx,
+                   "kv_heads": w.kv_heads, "head_dim": 128, "context": ctx, "tokens_attended": n_tok,
                    "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "parallelism": f"replicas x{ws} (independent batches)",
                    "l2": f"{copies} rotating cache copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
@@ -301,8 +305,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
-        "compaction": {"tokens": w.batch * w.kv_heads * n_pre, "ms": compaction_ms,
-                       "vectors_per_s": 2 * w.batch * w.kv_heads * n_pre / (compaction_ms * 1e-3)},
+        "compaction": {"vectors": 2 * w.kv_heads * (n_tok - w.batch), "ms": compaction_ms,
+                       "vectors_per_s": 2 * w.kv_heads * (n_tok - w.batch) / (compaction_ms * 1e-3)},
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)

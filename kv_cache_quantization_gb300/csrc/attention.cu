@@ -29,7 +29,7 @@ constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
 
 struct Plan {
   int G, nsplit_main, nsplit_tail, nsplit, split_len;
-  size_t q_off, part_off, cnt_off, bytes;
+  size_t q_off, part_off, bytes;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -70,8 +70,7 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
   p->q_off = 0;
   p->part_off = (qbytes + 255) / 256 * 256;
-  p->cnt_off = (p->part_off + pf * sizeof(float) + 255) / 256 * 256;
-  p->bytes = p->cnt_off + (size_t)d->batch * d->kv_heads * sizeof(int);
+  p->bytes = p->part_off + pf * sizeof(float);
   return TQ_OK;
 }
 
@@ -495,11 +494,10 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
     m.vc_unscale = vc->ibits == 4 ? 1.f / vc->lut_scale : 1.f;
     m.seq_lens = seq_lens;
     m.part = a.part;
-    m.counters = reinterpret_cast<int*>(ws + p.cnt_off);
     m.pi = vc->d_pi;
     m.out = out;
     m.out_dtype = desc->out_dtype;
-    return tq_launch_decode_mma(m, stream);   // merges in its last CTA per (b, KV head)
+    return tq_launch_decode_mma(m, stream);   // fragments, split decode, merge
   }
   query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
                                                    reinterpret_cast<float*>(ws + p.q_off));

@@ -33,7 +33,8 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = kConsumerWarps * 32;
-constexpr int kChunk = 16 * kConsumerWarps;   // tokens per stage
+constexpr int kTiles = 2;                     // 16-token tiles per warp per chunk
+constexpr int kChunk = 16 * kTiles * kConsumerWarps;   // tokens per stage
 constexpr int kStages = 4;
 constexpr int kRec = TQ_REC;
 constexpr unsigned kSpinLimit = 1u << 20;   // polls; a healthy wait needs a few hundred
@@ -144,29 +145,16 @@ __device__ __forceinline__ uint32_t pair_of(uint32_t w, uint32_t w5, uint32_t w1
   return (E < 5 ? w : E < 10 ? w5 : E < 15 ? w10 : w1) & mask;
 }
 
-struct Expanded {
-  uint32_t p[16];
+// A plane word with the three shifted copies the pair extraction draws from; pair e is then
+// one AND (e is a compile-time constant once the k-step loops are unrolled).
+struct Shifted {
+  uint32_t w, w5, w10, w1;
 };
-__device__ __forceinline__ Expanded expand(uint32_t w) {
-  Expanded x;
-  const uint32_t w5 = w << 5, w10 = w << 10, w1 = w >> 1;
-  x.p[0] = pair_of<0>(w, w5, w10, w1);
-  x.p[1] = pair_of<1>(w, w5, w10, w1);
-  x.p[2] = pair_of<2>(w, w5, w10, w1);
-  x.p[3] = pair_of<3>(w, w5, w10, w1);
-  x.p[4] = pair_of<4>(w, w5, w10, w1);
-  x.p[5] = pair_of<5>(w, w5, w10, w1);
-  x.p[6] = pair_of<6>(w, w5, w10, w1);
-  x.p[7] = pair_of<7>(w, w5, w10, w1);
-  x.p[8] = pair_of<8>(w, w5, w10, w1);
-  x.p[9] = pair_of<9>(w, w5, w10, w1);
-  x.p[10] = pair_of<10>(w, w5, w10, w1);
-  x.p[11] = pair_of<11>(w, w5, w10, w1);
-  x.p[12] = pair_of<12>(w, w5, w10, w1);
-  x.p[13] = pair_of<13>(w, w5, w10, w1);
-  x.p[14] = pair_of<14>(w, w5, w10, w1);
-  x.p[15] = pair_of<15>(w, w5, w10, w1);
-  return x;
+__device__ __forceinline__ Shifted shifted(uint32_t w) { return Shifted{w, w << 5, w << 10, w >> 1}; }
+__device__ __forceinline__ uint32_t pair_at(const Shifted& x, int e) {
+  const int pos = pair_pos(e);
+  const uint32_t mask = (1u << pos) | (1u << (pos + 16));
+  return (e < 5 ? x.w : e < 10 ? x.w5 : e < 15 ? x.w10 : x.w1) & mask;
 }
 
 // Virtual planes of a KB-bit index: the odd subsets of its bit positions, as bit masks.
@@ -219,7 +207,7 @@ __global__ void __launch_bounds__(kPrepThreads) query_frag_kernel(const tq_mma_l
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the decode grid may launch now: it streams the cache while this kernel runs and waits
-  // for this grid's completion before it reads the fragments or the counters
+  // for this grid's completion before it reads the fragments
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // 1. the group's queries (fp32), zero beyond G
 #pragma unroll
@@ -327,7 +315,6 @@ __global__ void __launch_bounds__(kPrepThreads) query_frag_kernel(const tq_mma_l
     cst[n * 4 + 2] = nq * a.smax * a.scale_log2 * (1.2533141373155003f / TQ_D);
     cst[n * 4 + 3] = ok ? s_wq[head] / (nq * a.smax) : 0.f;
   }
-  if (c == 0 && tid == 0) a.counters[bh] = 0;   // the decode kernel's last CTA per (b, KV head) merges
 }
 
 // ---------------------------------------------------------------- shared-memory layout
@@ -479,83 +466,87 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
       break;
     }
     const unsigned char* base = smem + st * L::stage;
-    const int tok0 = 16 * warp;                          // this warp's tokens in the chunk
-    const int t_abs = t_begin + ch * kChunk + tok0;      // absolute index of token 0
-
-    // ---- key scores: D[token][column]
-    // two accumulator sets (even and odd k-steps) halve the dependent MMA chains
-    float dm[2][4] = {}, dq[2][4] = {}, dml[2][4] = {};
-    {
-      uint32_t pw[3][2], sw[2];
-      const int r = lane & 7, m8 = (lane >> 3) & 1;
-      if (KB >= 2) {
-        // matrices: plane0 rows 0-7, plane0 rows 8-15, plane1 rows 0-7, plane1 rows 8-15
-        const int p = lane >> 4;
-        ldsm_x4(smem_u32(base + L::kplanes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
-                pw[0][0], pw[0][1], pw[1][0], pw[1][1]);
-      }
-      if (KB == 1 || KB == 3) {
-        const int p = KB - 1;
-        ldsm_x2(smem_u32(base + L::kplanes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
-                pw[p][0], pw[p][1]);
-      }
-      ldsm_x2(smem_u32(base + L::ksgn + (tok0 + r + 8 * m8) * 16), sw[0], sw[1]);
-#pragma unroll
-      for (int v = 0; v <= NKV; ++v) {
-        uint32_t x0, x1;
-        if (v < NKV) {
-          const uint32_t w0[3] = {pw[0][0], pw[1][0], pw[2][0]};
-          const uint32_t w1[3] = {pw[0][1], pw[1][1], pw[2][1]};
-          x0 = vplane_word<KB>(w0, v);
-          x1 = vplane_word<KB>(w1, v);
-        } else {
-          x0 = sw[0];
-          x1 = sw[1];
-        }
-        const Expanded e0 = expand(x0), e1 = expand(x1);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          float* d = v < NKV ? dm[s & 1] : dq[s & 1];
-          mma(d, e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bq[v][s][0], bq[v][s][1]);
-          if (!HILO && v < NKV)
-            mma(dml[s & 1], e0.p[2 * s], e1.p[2 * s], e0.p[2 * s + 1], e1.p[2 * s + 1], bql[v][s][0],
-                bql[v][s][1]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        dm[0][i] += dm[1][i];
-        dq[0][i] += dq[1][i];
-        if (!HILO) dm[0][i] += dml[0][i] + dml[1][i];
-      }
-    }
-    // ---- scores → base-2 logits; rows: token g (k = 0) and g + 8 (k = 1)
     const float* kxn = reinterpret_cast<const float*>(base + L::kxn);
     const float* krn = reinterpret_cast<const float*>(base + L::krn);
     const float* vxn = reinterpret_cast<const float*>(base + L::vxn);
-    float lg[2][2];   // [row][column pair]
+    const int t_chunk = t_begin + ch * kChunk;           // absolute index of the chunk's token 0
+    const int r8 = lane & 7, m8 = (lane >> 3) & 1;       // ldmatrix row addressing
+
+    // ---- key scores of the warp's two tiles: D[token][column]; one chain per tile
+    float dm[kTiles][4] = {}, dq[kTiles][4] = {}, dml[kTiles][4] = {};
+    {
+      uint32_t pw[kTiles][3][2] = {}, sw[kTiles][2];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int tl = tok0 + g + 8 * k;
-      const bool valid = t_abs + g + 8 * k < t_end;
-      const float xn = kxn[tl], rn = krn[tl];
-      if (HILO) {
-        const float m = dm[0][2 * k] + dm[0][2 * k + 1], q = dq[0][2 * k] + dq[0][2 * k + 1];
-        const float s = xn * hA[0] * (m - hCm[0]) + rn * hB[0] * (q - hCq[0]);
-        lg[k][0] = lg[k][1] = valid ? s : -INFINITY;
-      } else {
+      for (int T = 0; T < kTiles; ++T) {
+        const int row = 32 * warp + 16 * T + r8 + 8 * m8;
+        if (KB >= 2) {
+          // matrices: plane0 rows 0-7, plane0 rows 8-15, plane1 rows 0-7, plane1 rows 8-15
+          const int p = lane >> 4;
+          ldsm_x4(smem_u32(base + L::kplanes + p * kChunk * 16 + row * 16), pw[T][0][0],
+                  pw[T][0][1], pw[T][1][0], pw[T][1][1]);
+        }
+        if (KB == 1 || KB == 3) {
+          const int p = KB - 1;
+          ldsm_x2(smem_u32(base + L::kplanes + p * kChunk * 16 + row * 16), pw[T][p][0], pw[T][p][1]);
+        }
+        ldsm_x2(smem_u32(base + L::ksgn + row * 16), sw[T][0], sw[T][1]);
+      }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float s = xn * hA[h] * (dm[0][2 * k + h] - hCm[h]) + rn * hB[h] * (dq[0][2 * k + h] - hCq[h]);
-          lg[k][h] = valid ? s : -INFINITY;
+      for (int v = 0; v <= NKV; ++v) {
+        Shifted x[kTiles][2];   // [tile][row g / row g + 8]
+#pragma unroll
+        for (int T = 0; T < kTiles; ++T)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const uint32_t words[3] = {pw[T][0][hr], pw[T][1][hr], pw[T][2][hr]};
+            x[T][hr] = shifted(v < NKV ? vplane_word<KB>(words, v) : sw[T][hr]);
+          }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+#pragma unroll
+          for (int T = 0; T < kTiles; ++T) {
+            const uint32_t a0 = pair_at(x[T][0], 2 * s), a1 = pair_at(x[T][1], 2 * s);
+            const uint32_t a2 = pair_at(x[T][0], 2 * s + 1), a3 = pair_at(x[T][1], 2 * s + 1);
+            mma(v < NKV ? dm[T] : dq[T], a0, a1, a2, a3, bq[v][s][0], bq[v][s][1]);
+            if (!HILO && v < NKV) mma(dml[T], a0, a1, a2, a3, bql[v][s][0], bql[v][s][1]);
+          }
+        }
+      }
+      if (!HILO) {
+#pragma unroll
+        for (int T = 0; T < kTiles; ++T)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dm[T][i] += dml[T][i];
+      }
+    }
+    // ---- scores → base-2 logits; rows: token g (k = 0) and g + 8 (k = 1) of each tile
+    float lg[kTiles][2][2];   // [tile][row][column pair]
+#pragma unroll
+    for (int T = 0; T < kTiles; ++T) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int tl = 32 * warp + 16 * T + g + 8 * k;
+        const bool valid = t_chunk + tl < t_end;
+        const float xn = kxn[tl], rn = krn[tl];
+        if (HILO) {
+          const float m = dm[T][2 * k] + dm[T][2 * k + 1], q = dq[T][2 * k] + dq[T][2 * k + 1];
+          const float sc = xn * hA[0] * (m - hCm[0]) + rn * hB[0] * (q - hCq[0]);
+          lg[T][k][0] = lg[T][k][1] = valid ? sc : -INFINITY;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float sc = xn * hA[h] * (dm[T][2 * k + h] - hCm[h]) +
+                             rn * hB[h] * (dq[T][2 * k + h] - hCq[h]);
+            lg[T][k][h] = valid ? sc : -INFINITY;
+          }
         }
       }
     }
-    // ---- online softmax (per column pair), max over the 16 rows held by lanes g = 0..7
+    // ---- online softmax over the warp's 32 tokens (per column pair)
     float mt[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float m = fmaxf(lg[0][h], lg[1][h]);
+      float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
@@ -578,87 +569,93 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
         acc[i][3] *= corr[1];
       }
     }
-    float w[2][2];
+    float w[kTiles][2][2];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      // tokens past the sequence (or past the capacity in a short last chunk) may hold
-      // stale bytes: their weight is exactly zero, never 0 × (stale norm)
-      const bool valid = t_abs + g + 8 * k < t_end;
-      const float vn = vxn[tok0 + g + 8 * k];
+    for (int T = 0; T < kTiles; ++T) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float p = valid ? exp2f(lg[k][h] - m_run[h]) : 0.f;
-        l_run[h] += p;
-        w[k][h] = valid ? p * vn : 0.f;
-        lw_run[h] += w[k][h];
+      for (int k = 0; k < 2; ++k) {
+        // tokens past the sequence (or past the capacity in a short last chunk) may hold
+        // stale bytes: their weight is exactly zero, never 0 × (stale norm)
+        const int tl = 32 * warp + 16 * T + g + 8 * k;
+        const bool valid = t_chunk + tl < t_end;
+        const float vn = vxn[tl];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float pr = valid ? exp2f(lg[T][k][h] - m_run[h]) : 0.f;
+          l_run[h] += pr;
+          w[T][k][h] = valid ? pr * vn : 0.f;
+          lw_run[h] += w[T][k][h];
+        }
       }
     }
     // ---- value accumulation: acc[coord][column] += Σ_t A[coord][t] · B[t][column]
-    if constexpr (VB == 4) {
-      uint32_t bw0, bw1;
-      if (HILO) {
-        const float h0 = __half2float(__float2half_rn(w[0][0]));
-        const float h1 = __half2float(__float2half_rn(w[1][0]));
-        bw0 = movm_t(pack_half2(h0, w[0][0] - h0));
-        bw1 = movm_t(pack_half2(h1, w[1][0] - h1));
-      } else {
-        bw0 = movm_t(pack_half2(w[0][0], w[0][1]));
-        bw1 = movm_t(pack_half2(w[1][0], w[1][1]));
-      }
-      // 8 code bytes (coordinates 16g..16g+15) of tokens 2c, 2c+1, 2c+8, 2c+9
-      const unsigned char* vb = base + L::vcodes + (tok0 + 2 * c) * 64 + 8 * g;
-      const uint2 u0 = *reinterpret_cast<const uint2*>(vb);
-      const uint2 u1 = *reinterpret_cast<const uint2*>(vb + 64);
-      const uint2 u2 = *reinterpret_cast<const uint2*>(vb + 8 * 64);
-      const uint2 u3 = *reinterpret_cast<const uint2*>(vb + 9 * 64);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t A = half ? u0.y : u0.x, Bw = half ? u1.y : u1.x;
-        const uint32_t C = half ? u2.y : u2.x, D = half ? u3.y : u3.x;
-        // key byte i: low nibble = code of the first token, high nibble = second token
-        const uint32_t klo01 = (A & 0x0f0f0f0fu) | ((Bw << 4) & 0xf0f0f0f0u);
-        const uint32_t khi01 = ((A >> 4) & 0x0f0f0f0fu) | (Bw & 0xf0f0f0f0u);
-        const uint32_t klo23 = (C & 0x0f0f0f0fu) | ((D << 4) & 0xf0f0f0f0u);
-        const uint32_t khi23 = ((C >> 4) & 0x0f0f0f0fu) | (D & 0xf0f0f0f0u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t a0 = lut_lane[((klo01 >> (8 * i)) & 0xffu) << 5];
-          const uint32_t a1 = lut_lane[((khi01 >> (8 * i)) & 0xffu) << 5];
-          const uint32_t a2 = lut_lane[((klo23 >> (8 * i)) & 0xffu) << 5];
-          const uint32_t a3 = lut_lane[((khi23 >> (8 * i)) & 0xffu) << 5];
-          mma(acc[4 * half + i], a0, a1, a2, a3, bw0, bw1);
-        }
-      }
-    } else {
-      // planes transposed on load: pair word = {chunk g of token 2c, chunk g of token 2c+1}
-      uint32_t mw[3][2];
-      {
-        const int r = lane & 7, m8 = (lane >> 3) & 1;
-#pragma unroll
-        for (int p = 0; p < VB; ++p)
-          ldsm_x2_t(smem_u32(base + L::vcodes + p * kChunk * 16 + (tok0 + r + 8 * m8) * 16),
-                    mw[p][0], mw[p][1]);
-      }
-#pragma unroll
-      for (int v = 0; v < NVV; ++v) {
-        const float coef = a.vd.coef[v];
+    for (int T = 0; T < kTiles; ++T) {
+      const int trow0 = 32 * warp + 16 * T;              // tile's first token in the chunk
+      if constexpr (VB == 4) {
         uint32_t bw0, bw1;
         if (HILO) {
-          const float x0 = coef * w[0][0], x1 = coef * w[1][0];
-          const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
-          bw0 = movm_t(pack_half2(h0, x0 - h0));
-          bw1 = movm_t(pack_half2(h1, x1 - h1));
+          const float h0 = __half2float(__float2half_rn(w[T][0][0]));
+          const float h1 = __half2float(__float2half_rn(w[T][1][0]));
+          bw0 = movm_t(pack_half2(h0, w[T][0][0] - h0));
+          bw1 = movm_t(pack_half2(h1, w[T][1][0] - h1));
         } else {
-          bw0 = movm_t(pack_half2(coef * w[0][0], coef * w[0][1]));
-          bw1 = movm_t(pack_half2(coef * w[1][0], coef * w[1][1]));
+          bw0 = movm_t(pack_half2(w[T][0][0], w[T][0][1]));
+          bw1 = movm_t(pack_half2(w[T][1][0], w[T][1][1]));
         }
-        const uint32_t w0[3] = {mw[0][0], mw[1][0], mw[2][0]};
-        const uint32_t w1[3] = {mw[0][1], mw[1][1], mw[2][1]};
-        const Expanded e0 = expand(vplane_word<VB < 4 ? VB : 1>(w0, v));
-        const Expanded e1 = expand(vplane_word<VB < 4 ? VB : 1>(w1, v));
+        // 8 code bytes (coordinates 16g..16g+15) of tokens 2c, 2c+1, 2c+8, 2c+9
+        const unsigned char* vb = base + L::vcodes + (trow0 + 2 * c) * 64 + 8 * g;
+        const uint2 u0 = *reinterpret_cast<const uint2*>(vb);
+        const uint2 u1 = *reinterpret_cast<const uint2*>(vb + 64);
+        const uint2 u2 = *reinterpret_cast<const uint2*>(vb + 8 * 64);
+        const uint2 u3 = *reinterpret_cast<const uint2*>(vb + 9 * 64);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          mma(acc[i], e0.p[2 * i], e0.p[2 * i + 1], e1.p[2 * i], e1.p[2 * i + 1], bw0, bw1);
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t A = half ? u0.y : u0.x, Bw = half ? u1.y : u1.x;
+          const uint32_t C = half ? u2.y : u2.x, D = half ? u3.y : u3.x;
+          // key byte i: low nibble = code of the first token, high nibble = second token
+          const uint32_t klo01 = (A & 0x0f0f0f0fu) | ((Bw << 4) & 0xf0f0f0f0u);
+          const uint32_t khi01 = ((A >> 4) & 0x0f0f0f0fu) | (Bw & 0xf0f0f0f0u);
+          const uint32_t klo23 = (C & 0x0f0f0f0fu) | ((D << 4) & 0xf0f0f0f0u);
+          const uint32_t khi23 = ((C >> 4) & 0x0f0f0f0fu) | (D & 0xf0f0f0f0u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t a0 = lut_lane[((klo01 >> (8 * i)) & 0xffu) << 5];
+            const uint32_t a1 = lut_lane[((khi01 >> (8 * i)) & 0xffu) << 5];
+            const uint32_t a2 = lut_lane[((klo23 >> (8 * i)) & 0xffu) << 5];
+            const uint32_t a3 = lut_lane[((khi23 >> (8 * i)) & 0xffu) << 5];
+            mma(acc[4 * half + i], a0, a1, a2, a3, bw0, bw1);
+          }
+        }
+      } else {
+        // planes transposed on load: pair word = {chunk g of token 2c, chunk g of token 2c+1}
+        uint32_t mw[3][2] = {};
+#pragma unroll
+        for (int p = 0; p < VB; ++p)
+          ldsm_x2_t(smem_u32(base + L::vcodes + p * kChunk * 16 + (trow0 + r8 + 8 * m8) * 16),
+                    mw[p][0], mw[p][1]);
+#pragma unroll
+        for (int v = 0; v < NVV; ++v) {
+          const float coef = a.vd.coef[v];
+          uint32_t bw0, bw1;
+          if (HILO) {
+            const float x0 = coef * w[T][0][0], x1 = coef * w[T][1][0];
+            const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
+            bw0 = movm_t(pack_half2(h0, x0 - h0));
+            bw1 = movm_t(pack_half2(h1, x1 - h1));
+          } else {
+            bw0 = movm_t(pack_half2(coef * w[T][0][0], coef * w[T][0][1]));
+            bw1 = movm_t(pack_half2(coef * w[T][1][0], coef * w[T][1][1]));
+          }
+          const uint32_t w0[3] = {mw[0][0], mw[1][0], mw[2][0]};
+          const uint32_t w1[3] = {mw[0][1], mw[1][1], mw[2][1]};
+          const Shifted e0 = shifted(vplane_word<VB < 4 ? VB : 1>(w0, v));
+          const Shifted e1 = shifted(vplane_word<VB < 4 ? VB : 1>(w1, v));
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mma(acc[i], pair_at(e0, 2 * i), pair_at(e0, 2 * i + 1), pair_at(e1, 2 * i),
+                pair_at(e1, 2 * i + 1), bw0, bw1);
+        }
       }
     }
     __syncwarp();
@@ -690,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
       lw_run[h] += __shfl_xor_sync(0xffffffffu, lw_run[h], o);
     }
   }
+  // the merge grid may be scheduled now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   consumer_sync();   // every warp is done with the ring: reuse it
   float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);           // [warp][col][140]
   float* cst = reinterpret_cast<float*>(smem + L::comb_stats);          // [warp][3][8]
@@ -762,92 +761,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const tq_mma_la
     }
     rec[2 + j] = acc_j;
   }
-  // ------------------------------------------------------------ merge (last CTA)
-  // The CTA that finishes last for its (batch, KV head) combines every split's record with
-  // log-sum-exp weights and rotates the result back: out = Πᵀ·acc / L.
-  __shared__ int s_last;
-  __threadfence();
-  consumer_sync();
-  if (tid == 0) s_last = atomicAdd(&a.counters[bh], 1) == a.nsplit - 1;
-  consumer_sync();
-  if (!s_last) return;
-  __threadfence();
-  // shared memory, all free now: [staged records][split weights][combined acc][products]
-  float* mred = reinterpret_cast<float*>(smem + L::total) - 2 * 8 * TQ_D;   // [2][8][128]
-  float* macc = mred - 8 * TQ_D;                                            // [8][128]
-  float* mw = macc - 8 * kMaxSplits;                                        // [8][kMaxSplits]
-  float* stage = reinterpret_cast<float*>(smem);
-  const int rec_bytes = a.G * kRec * 4;                                     // one split, all heads
-  const int per_batch = (int)(((unsigned char*)mw - smem) / rec_bytes);
-  __shared__ float s_Lt[8];
-  const float* recs = a.part + (bh * a.nsplit) * a.G * kRec;
-  // split weights exp(m_s − M) and the total denominator, one warp per head
-  if (warp < a.G) {
-    const int h = warp;
-    float M = -INFINITY;
-    for (int sp = lane; sp < a.nsplit; sp += 32) M = fmaxf(M, __ldcg(&recs[(sp * a.G + h) * kRec]));
+}
+
+// ---------------------------------------------------------------- merge
+// One CTA of 512 threads per (batch, query head), launched as a dependent of the split
+// kernel: Π is prefetched into registers before the dependency wait; the split records are
+// then read with all loads in flight, combined with log-sum-exp weights and rotated back,
+// out = Πᵀ·acc / L.
+constexpr int kMergeThreads = 512;
+__global__ void __launch_bounds__(kMergeThreads) merge_mma_kernel(const tq_mma_launch a) {
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_part[4][TQ_D], s_acc[TQ_D], s_red[32];
+  __shared__ float s_M, s_L;
+  const int row = blockIdx.x;            // b * Hq + h
+  const int b = row / a.Hq, h = row % a.Hq;
+  const int kvh = h / a.G, g = h % a.G;
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int tid = threadIdx.x, j = tid & 127, q = tid >> 7, warp = tid >> 5, lane = tid & 31;
+  float tp[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lt = 0.f;
-    for (int sp = lane; sp < a.nsplit; sp += 32) {
-      const float m = __ldcg(&recs[(sp * a.G + h) * kRec]);
-      const float l = __ldcg(&recs[(sp * a.G + h) * kRec + 1]);
-      const float wgt = (M == -INFINITY || !(l > 0.f)) ? 0.f : expf(m - M);
-      mw[h * kMaxSplits + sp] = wgt;
-      Lt += wgt * l;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
-    if (lane == 0) s_Lt[h] = Lt;
+  for (int k = 0; k < 32; ++k) tp[k] = __ldg(&a.pi[(32 * q + k) * TQ_D + j]);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float* recs = a.part + (bh * a.nsplit * a.G + g) * kRec;   // split s at + s·G·kRec
+  float m = -INFINITY, l = 0.f;
+  if (tid < a.nsplit) {
+    m = __ldcg(&recs[(long long)tid * a.G * kRec]);
+    l = __ldcg(&recs[(long long)tid * a.G * kRec + 1]);
+    if (!(l > 0.f)) m = -INFINITY;
   }
-  // Σ_s w_s·acc_s with the records staged through shared memory by bulk copies
-  float accv[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s0 = 0, batch = 0; s0 < a.nsplit; s0 += per_batch, ++batch) {
-    const int nb = min(per_batch, a.nsplit - s0);
-    consumer_sync();   // weights visible; previous batch consumed
-    if (tid == 0) {
-      mbar_expect_tx(&prol_bar, (unsigned)(nb * rec_bytes));
-      bulk_g2s(stage, recs + (long long)s0 * a.G * kRec, (unsigned)(nb * rec_bytes), &prol_bar);
-    }
-    if (!mbar_wait(&prol_bar, (batch + 1) & 1)) {   // phase 0 was the prologue's copy
-      if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-      break;
-    }
+  // M = max over splits (block reduction)
+  float mx = m;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = tid + r * kConsumerWarps * 32;
-      if (i < a.G * TQ_D) {
-        const int h = i / TQ_D, j = i % TQ_D;
-        for (int sp = 0; sp < nb; ++sp)
-          accv[r] = fmaf(mw[h * kMaxSplits + s0 + sp], stage[(sp * a.G + h) * kRec + 2 + j], accv[r]);
-      }
-    }
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < kMergeThreads / 32 ? s_red[tid] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (tid == 0) s_M = v;
+  }
+  __syncthreads();
+  const float M = s_M;
+  float lw = 0.f;
+  if (tid < a.nsplit) {
+    const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : expf(m - M);
+    s_w[tid] = w;
+    lw = w * l;
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = tid + r * kConsumerWarps * 32;
-    if (i < a.G * TQ_D) macc[i] = accv[r];
+  for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+  __syncthreads();
+  if (lane == 0) s_red[warp] = lw;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < kMergeThreads / 32 ? s_red[tid] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (tid == 0) s_L = v;
   }
-  consumer_sync();
+  // acc_j: splits q, q+4, q+8, ... of thread (q, j), loads issued together
+  float acc = 0.f;
   {
-    // out_j = Σ_k Π[k][j] acc_k, the k range split over the two halves of the CTA
-    const int j = tid & 127, kh = tid >> 7;
-    float t[64];
+    float v[16];
+    const int n = (a.nsplit - q + 3) / 4;
 #pragma unroll
-    for (int k = 0; k < 64; ++k) t[k] = __ldg(&a.pi[(64 * kh + k) * TQ_D + j]);
-    for (int h = 0; h < a.G; ++h) {
-      float r = 0.f;
+    for (int i = 0; i < 16; ++i)
+      v[i] = i < n ? __ldcg(&recs[(long long)(q + 4 * i) * a.G * kRec + 2 + j]) : 0.f;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) r = fmaf(t[k], macc[h * TQ_D + 64 * kh + k], r);
-      mred[(kh * 8 + h) * TQ_D + j] = r;
-    }
+    for (int i = 0; i < 16; ++i)
+      if (i < n) acc = fmaf(s_w[q + 4 * i], v[i], acc);
+    for (int i = 16; i < n; ++i)   // more than 64 splits
+      acc = fmaf(s_w[q + 4 * i], __ldcg(&recs[(long long)(q + 4 * i) * a.G * kRec + 2 + j]), acc);
   }
-  consumer_sync();
-  for (int i = tid; i < a.G * TQ_D; i += kConsumerWarps * 32) {
-    const int h = i / TQ_D, j = i % TQ_D;
-    const float Lt = s_Lt[h];
-    const float o = Lt > 0.f ? (mred[h * TQ_D + j] + mred[(8 + h) * TQ_D + j]) / Lt : 0.f;
-    const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + j;
+  s_part[q][j] = acc;
+  __syncthreads();
+  if (tid < TQ_D) s_acc[tid] = (s_part[0][tid] + s_part[1][tid]) + (s_part[2][tid] + s_part[3][tid]);
+  __syncthreads();
+  float r = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) r = fmaf(tp[k], s_acc[32 * q + k], r);
+  s_part[q][j] = r;
+  __syncthreads();
+  if (tid < TQ_D) {
+    const float L = s_L;
+    const float o = L > 0.f ? ((s_part[0][tid] + s_part[1][tid]) + (s_part[2][tid] + s_part[3][tid])) / L : 0.f;
+    const long long e = (long long)row * TQ_D + tid;
     if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = o;
     else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(o);
     else static_cast<__half*>(a.out)[e] = __float2half_rn(o);
@@ -879,6 +878,11 @@ tq_status launch_one(const tq_mma_launch& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decode_mma_kernel<KB, VB, HILO>, a) != cudaSuccess)
     return TQ_ERR_CUDA;
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3(a.B * a.Hq);
+  mcfg.blockDim = dim3(kMergeThreads);
+  mcfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&mcfg, merge_mma_kernel, a) != cudaSuccess) return TQ_ERR_CUDA;
   return tq_cuda_status(cudaGetLastError());
 }
 

@@ -39,7 +39,6 @@ struct tq_mma_launch {
   float vc_unscale;            // 1 / the table's level scale
   const int* seq_lens;
   float* part;                 // [B][Hkv][nsplit][G][130]
-  int* counters;               // [B][Hkv] splits finished (zeroed by the fragment kernel)
   const float* pi;             // Π of the value codec (row-major): out = Πᵀ·acc / L
   void* out;                   // [B][Hq][128]
   int out_dtype;
