@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libtq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["host.cpp", "quantize.cu", "attention.cu", "scores.cu", "decode_mma.cu",
-           "decode_noalloc.cu"]
+SOURCES = ["host.cpp", "quantize.cu", "quantize_tc.cu", "attention.cu", "scores.cu",
+           "decode_mma.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -201,6 +201,7 @@ static void free_codec(tq_codec* c) {
   cudaFree(c->d_lut);
   cudaFree(c->d_u);
   cudaFree(c->d_w);
+  cudaFree(c->d_img);
   std::free(c);
 }
 
@@ -247,6 +248,7 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
   c->lut_scale = tq_fp16_friendly_scale(c->centroids, L);
   const size_t n = (size_t)d * d;
   std::vector<float> h_pi(n), h_piT(n), h_sT(n), h_mT(n);
+  std::vector<double> h_m(kind == TQ_PROD ? n : 0);
   for (int i = 0; i < d; ++i)
     for (int j = 0; j < d; ++j) {
       h_pi[(size_t)i * d + j] = (float)pi[(size_t)i * d + j];
@@ -261,6 +263,7 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
         double acc = 0;
         for (int k = 0; k < d; ++k) acc += s[(size_t)i * d + k] * pi[(size_t)j * d + k];
         h_mT[(size_t)j * d + i] = (float)acc;
+        h_m[(size_t)i * d + j] = acc;
       }
   }
   cudaError_t e = cudaSuccess;
@@ -274,6 +277,16 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
     if (e == cudaSuccess) e = cudaMalloc(&c->d_mT, bytes);
     if (e == cudaSuccess) e = cudaMemcpy(c->d_sT, h_sT.data(), bytes, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(c->d_mT, h_mT.data(), bytes, cudaMemcpyHostToDevice);
+  }
+  {
+    // tensor-core operand images (64·Π, then 8·M for keys), each as an fp16 hi/lo pair
+    const bool prod = kind == TQ_PROD;
+    const size_t ib = tq_operand_image_bytes(prod);
+    std::vector<uint16_t> img(ib / 2);
+    tq_build_operand_image(pi, false, img.data());
+    if (prod) tq_build_operand_image(h_m.data(), true, img.data() + ib / 4);
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_img, ib);
+    if (e == cudaSuccess) e = cudaMemcpy(c->d_img, img.data(), ib, cudaMemcpyHostToDevice);
   }
   {
     // column sums Πᵀ·1 and Sᵀ·1, and the largest row norm of S (query normalisation)

@@ -357,6 +357,14 @@ tq_status check_x(const void* x, tq_dtype dt, int batch, int heads, int tokens, 
   return TQ_OK;
 }
 
+// Tiles of bf16 / fp16 vectors go to the tensor-core kernel (quantize_tc.cu); fp32 inputs
+// and the few vectors of a decode step stay on the kernels above.
+bool use_tensor_cores(tq_dtype dt, int batch, int heads, int tokens) {
+  const long long total = (long long)batch * heads * tokens;
+  const int sms = tq_num_sms();
+  return tq_quantize_tc_supported(dt) && total > 2LL * (sms > 0 ? sms : 148);
+}
+
 template <bool kProd>
 tq_status launch(const QuantArgs& a, cudaStream_t stream) {
   const long long total = (long long)a.batch * a.heads * a.tokens;
@@ -399,6 +407,10 @@ extern "C" tq_status tq_quantize_prod(const tq_codec* kc, const void* x, tq_dtyp
   if (!aligned16(cache.idx) || !aligned16(cache.sgn) || !aligned16(cache.xnorm) ||
       !aligned16(cache.rnorm))
     return TQ_ERR_INVALID_ARG;
+  if (use_tensor_cores(x_dtype, batch, heads, tokens))
+    return tq_launch_quantize_tc(true, x, x_dtype, batch, heads, tokens, stride_b, stride_h,
+                                 stride_t, pos, count, cache.idx, cache.sgn, cache.xnorm,
+                                 cache.rnorm, capacity, kc, reinterpret_cast<cudaStream_t>(stream));
   QuantArgs a{};
   a.x = x; a.dtype = x_dtype; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = stride_b; a.sh = stride_h; a.st = stride_t; a.pos = pos; a.count = count;
@@ -419,6 +431,10 @@ extern "C" tq_status tq_quantize_mse(const tq_codec* vc, const void* x, tq_dtype
   if (st != TQ_OK) return st;
   if (!cache.idx || !cache.xnorm) return TQ_ERR_INVALID_ARG;
   if (!aligned16(cache.idx) || !aligned16(cache.xnorm)) return TQ_ERR_INVALID_ARG;
+  if (use_tensor_cores(x_dtype, batch, heads, tokens))
+    return tq_launch_quantize_tc(false, x, x_dtype, batch, heads, tokens, stride_b, stride_h,
+                                 stride_t, pos, count, cache.idx, nullptr, cache.xnorm, nullptr,
+                                 capacity, vc, reinterpret_cast<cudaStream_t>(stream));
   QuantArgs a{};
   a.x = x; a.dtype = x_dtype; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = stride_b; a.sh = stride_h; a.st = stride_t; a.pos = pos; a.count = count;
@@ -432,8 +448,8 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   if (!flags) return TQ_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int a = tq_take_flags_quantize(), b = tq_take_flags_attention();
-  const unsigned int c = tq_take_flags_decode_mma();
-  if (a == ~0u || b == ~0u || c == ~0u) return TQ_ERR_CUDA;
-  *flags = a | b | c;
+  const unsigned int c = tq_take_flags_decode_mma(), d = tq_take_flags_quantize_tc();
+  if (a == ~0u || b == ~0u || c == ~0u || d == ~0u) return TQ_ERR_CUDA;
+  *flags = a | b | c | d;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

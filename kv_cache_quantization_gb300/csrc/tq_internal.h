@@ -30,6 +30,7 @@ struct tq_codec {
   float boundaries[16];
   double centroids_d[16];
   float lut_scale;   // fp16-friendly scale of the levels (decode pair table)
+  void* d_img;       // tensor-core operand images: 64·Π as an fp16 pair, then (prod) 8·M
 };
 
 // Constants passed by value to kernels.
@@ -55,6 +56,7 @@ struct tq_levels {
 unsigned int tq_take_flags_quantize();
 unsigned int tq_take_flags_attention();
 unsigned int tq_take_flags_decode_mma();
+unsigned int tq_take_flags_quantize_tc();
 
 static inline tq_status tq_cuda_status(cudaError_t e) {
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -66,4 +68,13 @@ int tq_num_sms();
 
 // Launch helpers implemented in the .cu files
 tq_levels tq_make_levels(const tq_codec* c);
+// Tensor-core quantiser (quantize_tc.cu)
+bool tq_quantize_tc_supported(int dtype);
+tq_status tq_launch_quantize_tc(bool prod, const void* x, int dtype, int batch, int heads,
+                                int tokens, long long sb, long long sh, long long st,
+                                const int* pos, const int* count, uint8_t* idx, uint8_t* sgn,
+                                float* xnorm, float* rnorm, int capacity, const tq_codec* c,
+                                cudaStream_t stream);
+size_t tq_operand_image_bytes(bool prod);
+void tq_build_operand_image(const double* mat, bool sketch, uint16_t* img);
 float tq_fp16_friendly_scale(const float* levels, int n);

@@ -134,3 +134,27 @@ def rel_l2(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def unpack_prod_at(cache, b, h, toks, ibits):
+    """Like unpack_prod, for the listed token slots of (b, h) only."""
+    t = torch_index(toks, cache.idx.device)
+    planes = cache.idx[b, h][:, t].permute(1, 0, 2).cpu().numpy()
+    idx = o.unpack_index_planes(planes, D)
+    sign = o.unpack_bits(cache.sgn[b, h][t].cpu().numpy(), D)
+    return (idx, sign, cache.xnorm[b, h][t].double().cpu().numpy(),
+            cache.rnorm[b, h][t].double().cpu().numpy())
+
+
+def unpack_mse_at(cache, b, h, toks, bits):
+    t = torch_index(toks, cache.idx.device)
+    if bits == 4:
+        idx = o.unpack_nibbles(cache.idx[b, h][t].cpu().numpy(), D)
+    else:
+        idx = o.unpack_index_planes(cache.idx[b, h][:, t].permute(1, 0, 2).cpu().numpy(), D)
+    return idx, cache.xnorm[b, h][t].double().cpu().numpy()
+
+
+def torch_index(toks, device):
+    import torch
+    return torch.as_tensor(np.asarray(toks, dtype=np.int64), device=device)

@@ -76,7 +76,7 @@ def test_quantize_prod_codes(bits, dtype):
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 def test_quantize_mse_codes(bits, dtype):
     bsz, h, t = 2, 2, 517
     x = rand_x((bsz, h, t, D), 200 + bits, dtype)
