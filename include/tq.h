@@ -191,9 +191,12 @@ size_t tq_decode_workspace_bytes(const tq_attn_desc* desc);
  *   seq_lens : device int32[batch]; tokens t < seq_lens[b] are attended (clamped to
  *              capacity, flagged if larger).  A zero length gives a zero output row.
  *   out      : device [batch][q_heads][128] of desc->out_dtype.
- *   workspace: device, ≥ tq_decode_workspace_bytes(desc) bytes, 256-byte aligned; its
- *              contents on entry are ignored.  Calls that share a workspace must be
- *              serialised on one stream. */
+ *   workspace: device, ≥ tq_decode_workspace_bytes(desc) bytes, 256-byte aligned, and
+ *              zero-filled before its first use: the call keeps per-(batch, KV head)
+ *              split tickets in it and leaves them at zero when it completes, so one
+ *              zero fill serves every later call (with any descriptor that fits).  After a
+ *              call whose device status reports TQ_FLAG_TIMEOUT, zero it again.  Calls that
+ *              share a workspace must be serialised on one stream. */
 tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
                               const void* q, tq_prod_cache k, tq_mse_cache v,
                               const int32_t* seq_lens, void* out, void* workspace,

@@ -213,7 +213,9 @@ class DecodePlan:
         nbytes = B.tq_decode_workspace_bytes(self.desc)
         if nbytes == 0:
             raise ValueError("invalid decode-attention configuration")
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        # zero-filled once: the library keeps its split tickets there, and every call
+        # leaves them at zero again
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         self.out_dtype = out_dtype
         self.shape = (batch, q_heads, HEAD_DIM)
 

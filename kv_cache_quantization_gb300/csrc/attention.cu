@@ -29,7 +29,7 @@ constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
 
 struct Plan {
   int G, nsplit_main, nsplit_tail, nsplit, split_len;
-  size_t q_off, part_off, bytes;
+  size_t q_off, part_off, ctr_off, bytes;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -65,12 +65,16 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   // per-query vectors (CUDA-core path) or per-(batch, KV head) query fragments
   // (tensor-core path), whichever is larger
   size_t qbytes = (size_t)d->batch * d->q_heads * 2 * TQ_D * sizeof(float);
-  const size_t fbytes = (size_t)d->batch * d->kv_heads * tq_mma_frag_bytes_max();
+  size_t fbytes = (size_t)d->batch * d->kv_heads * tq_mma_frag_bytes_max();
+  const size_t tbytes = (size_t)d->batch * d->kv_heads * tq_tc_frag_bytes_max();
+  if (tbytes > fbytes) fbytes = tbytes;
   if (fbytes > qbytes) qbytes = fbytes;
   const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
   p->q_off = 0;
   p->part_off = (qbytes + 255) / 256 * 256;
-  p->bytes = p->part_off + pf * sizeof(float);
+  // split tickets of the tensor-core path: one int per (batch, KV head), zero between calls
+  p->ctr_off = (p->part_off + pf * sizeof(float) + 255) / 256 * 256;
+  p->bytes = p->ctr_off + (size_t)d->batch * d->kv_heads * sizeof(int);
   return TQ_OK;
 }
 
@@ -478,7 +482,8 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   a.seq_lens = seq_lens;
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
-  if (tq_mma_supported(kc->ibits, vc->ibits, p.G) && p.nsplit <= 256) {
+  const bool tc = tq_tc_decode_supported(kc->ibits, vc->ibits, p.G, p.nsplit);
+  if (tc || (tq_mma_supported(kc->ibits, vc->ibits, p.G) && p.nsplit <= 256)) {
     tq_mma_launch m{};
     m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap;
     m.nsplit = p.nsplit; m.split_len = p.split_len;
@@ -497,7 +502,10 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
     m.pi = vc->d_pi;
     m.out = out;
     m.out_dtype = desc->out_dtype;
-    return tq_launch_decode_mma(m, stream);   // fragments, split decode, merge
+    m.counters = reinterpret_cast<int*>(ws + p.ctr_off);
+    tq_tc_operand_scales(m.kd, &m.s_idx, &m.s_sgn);
+    if (tc) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
+    return tq_launch_decode_mma(m, stream);          // fragments, split decode, merge
   }
   query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
                                                    reinterpret_cast<float*>(ws + p.q_off));

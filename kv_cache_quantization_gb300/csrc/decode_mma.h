@@ -42,6 +42,8 @@ struct tq_mma_launch {
   const float* pi;             // Π of the value codec (row-major): out = Πᵀ·acc / L
   void* out;                   // [B][Hq][128]
   int out_dtype;
+  int* counters;               // [B][Hkv] split tickets (zero between calls)
+  float s_idx, s_sgn;          // power-of-two scales of the e4m3 query operand
 };
 
 // True when the tensor-core kernel handles this configuration.
@@ -53,3 +55,10 @@ tq_status tq_launch_decode_mma(const tq_mma_launch& a, cudaStream_t stream);
 float tq_fp16_friendly_scale(const float* levels, int n);
 // Workspace bytes per (batch, KV head) reserved for the query fragments.
 size_t tq_mma_frag_bytes_max();
+// Tensor-core (tcgen05) split decode with in-kernel query operand and last-CTA merge.
+bool tq_tc_decode_supported(int kbits, int vbits, int G, int nsplit);
+tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream);
+// Workspace bytes per (batch, KV head) for its query operand images.
+size_t tq_tc_frag_bytes_max();
+// Power-of-two scales of the e4m3 query operand for a key codec's decomposition.
+void tq_tc_operand_scales(const tq_plane_decomp& kd, float* s_idx, float* s_sgn);

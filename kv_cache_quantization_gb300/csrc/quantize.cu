@@ -449,7 +449,8 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int a = tq_take_flags_quantize(), b = tq_take_flags_attention();
   const unsigned int c = tq_take_flags_decode_mma(), d = tq_take_flags_quantize_tc();
-  if (a == ~0u || b == ~0u || c == ~0u || d == ~0u) return TQ_ERR_CUDA;
-  *flags = a | b | c | d;
+  const unsigned int e = tq_take_flags_decode_tc();
+  if (a == ~0u || b == ~0u || c == ~0u || d == ~0u || e == ~0u) return TQ_ERR_CUDA;
+  *flags = a | b | c | d | e;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

@@ -26,6 +26,7 @@
 // plane with one 128-bit store.  One CTA per SM, persistent over tiles.
 #include <cuda_fp16.h>
 
+#include "tc_ptx.h"
 #include "tq_internal.h"
 
 TQ_DEFINE_FLAGS(tq_take_flags_quantize_tc)
@@ -39,7 +40,6 @@ constexpr int kLBO = 128;                      // K-adjacent core matrices
 constexpr int kSBO = 16 * 128;                 // 8-row groups: 16 core matrices along K
 constexpr int kRawPitch = 256;                 // one raw bf16/fp16 vector
 constexpr float kPiScale = 64.f, kMScale = 8.f, kRhoScale = 256.f;
-constexpr unsigned kSpinLimit = 1u << 20;
 
 // shared-memory map (bytes from the dynamic base)
 template <bool kProd>
@@ -84,18 +84,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           s32(bar))
       : "memory");
 }
+// bounded wait (the thread is suspended, not spinning, while the phase is incomplete)
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-  for (unsigned i = 0; i < kSpinLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(s32(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
+  return tq::mbar_wait(bar, parity);
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];

@@ -57,6 +57,7 @@ unsigned int tq_take_flags_quantize();
 unsigned int tq_take_flags_attention();
 unsigned int tq_take_flags_decode_mma();
 unsigned int tq_take_flags_quantize_tc();
+unsigned int tq_take_flags_decode_tc();
 
 static inline tq_status tq_cuda_status(cudaError_t e) {
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
