@@ -54,7 +54,10 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
     if (t != TQ_F32 && t != TQ_F16 && t != TQ_BF16) return TQ_ERR_UNSUPPORTED;
   p->G = d->q_heads / d->kv_heads;
   const long long units = (long long)(d->batch > 0 ? d->batch : 1) * d->kv_heads;
-  const long long want = (sm_count() + units - 1) / units;          // splits per sequence
+  long long want = (sm_count() + units - 1) / units;                // splits per sequence
+  // more units than half the SMs: a wave does not give every unit two splits, and ragged
+  // lengths leave SMs idle; three splits per sequence (several waves) balance better
+  if (units * 2 > sm_count() && want < 3) want = 3;
   long long sl = (d->max_seq_len + want - 1) / (want > 0 ? want : 1);
   sl = (sl + 127) / 128 * 128;
   if (sl < 128) sl = 128;
@@ -500,9 +503,11 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
     m.seq_lens = seq_lens;
     m.part = a.part;
     m.pi = vc->d_pi;
+    m.vpiT = vc->d_piT;
     m.out = out;
     m.out_dtype = desc->out_dtype;
     m.counters = reinterpret_cast<int*>(ws + p.ctr_off);
+    m.max_len = desc->max_seq_len;
     tq_tc_operand_scales(m.kd, &m.s_idx, &m.s_sgn);
     if (tc) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
     return tq_launch_decode_mma(m, stream);          // fragments, split decode, merge

@@ -40,9 +40,11 @@ struct tq_mma_launch {
   const int* seq_lens;
   float* part;                 // [B][Hkv][nsplit][G][130]
   const float* pi;             // Π of the value codec (row-major): out = Πᵀ·acc / L
+  const float* vpiT;           // Πᵀ of the value codec (row-major)
   void* out;                   // [B][Hq][128]
   int out_dtype;
   int* counters;               // [B][Hkv] split tickets (zero between calls)
+  int max_len;                 // longest sequence (tokens) of the call
   float s_idx, s_sgn;          // power-of-two scales of the e4m3 query operand
 };
 

@@ -22,13 +22,15 @@
 // accumulator fragment), keeps an online softmax per column and accumulates values with
 // mma.sync m16n8k16 (4-bit codes through a pair table of fp16 levels, 1–3-bit codes as planes).
 //
-// Data path.  A producer warp streams 128-token stages of packed K/V through an 8-deep
-// shared-memory ring with bulk copies (TMA engine).  The query operand of each (batch, KV
-// head) is built by a small kernel that runs as this kernel's programmatic-launch primary:
-// the split CTAs start streaming the cache at once and wait for that kernel only before
-// their first MMA.  Each CTA writes one (m, l, acc) record per head; the last CTA of a
-// (batch, KV head) to finish (a ticket counter in the workspace) merges the records with
-// log-sum-exp weights and rotates the result back.
+// Data path.  A producer warp streams 256-token stages of packed K/V through a 4-deep
+// shared-memory ring with bulk copies (TMA engine).  The splits of one (batch, KV head) run as
+// thread-block clusters of up to 4 CTAs, which build the query operand together at the start
+// (each computes a quarter of Π q and S q and stores its bytes into every CTA of the cluster
+// through distributed shared memory) while the ring fills.  At the end each CTA sends its
+// (m, l, acc) per head to every CTA of its cluster; every CTA merges the cluster's results and
+// rotates back its quarter of the output coordinates into the cluster's record.  The last CTA
+// of a (batch, KV head) to finish (a ticket counter in the workspace) adds up the records with
+// log-sum-exp weights.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -56,9 +58,9 @@ constexpr int kBImg = kN * 128;               // one plane's query operand (4 KB
 constexpr int kBSbo = 8 * 128;                // 8-row groups of the operand image
 constexpr int kCstBytes = 8 * 4 * 4;          // 8 columns × {A, Cm, B, Cq}
 constexpr int kRec = TQ_REC;
+constexpr int kPrepThreads = 256;
 constexpr int kMaxSplits = 256;
 constexpr int kAccPitch = 140;
-constexpr int kPrepThreads = 256;
 // named barriers
 constexpr int kBarS = 2, kBarAll = 3;
 
@@ -155,8 +157,85 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) 
       : "r"(taddr));
 }
 
+// 2^x by the special-function unit (inputs here are ≤ 8; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
+}
+
+// ---------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+// arrive on the mbarrier at `saddr` in CTA `rank`, ordering this thread's earlier writes
+__device__ __forceinline__ void arrive_remote(uint32_t saddr, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   map_rank(saddr, rank))
+               : "memory");
+}
+// bounded wait with cluster-scope acquire (the phase was completed by arrivals of peers)
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity) {
+  auto try1 = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(s32(bar)), "r"(parity), "r"(10000000u)
+        : "memory");
+    return ok != 0;
+  };
+  if (try1()) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (try1()) return true;
+    if (global_ns() - t0 > 20000000ull) return false;
+  }
+}
+// cluster-wide barrier in two halves: every thread of every CTA arrives once (at kernel
+// start, after its mbarriers are initialised) and waits before its first remote mbarrier
+// access, so the barrier's latency hides behind the work in between
+__device__ __forceinline__ void cluster_arrive_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- query operand kernel
@@ -287,16 +366,18 @@ struct TL {
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
   static constexpr int frag = lut + lut_bytes;               // operand images + constants
   static constexpr int used = frag + frag_block(NP);
-  // the last-CTA merge stages Π (64 KB) and the split records in shared memory, with its
-  // accumulators and weights (12 KB) at the end; make room for 36 split records of 8 heads
-  static constexpr int merge_min = 65536 + 36 * 8 * kRec * 4 + 12288;
-  static constexpr int total = used > merge_min ? used : merge_min;
-  static constexpr int mrg_acc = total - 12288;              // float [8][128]
-  static constexpr int mrg_w = mrg_acc + 4096;               // float [8][kMaxSplits]
-  // after the main loop the ring is reused: softmax-warp accumulators and statistics
+  // the slots for the per-CTA results of the cluster (up to 4 × (16 + 8·128) floats)
+  static constexpr int slots = used;
+  static constexpr int total = slots + 4 * (16 + 8 * 128) * 4;
+  // after the main loop the ring is reused: softmax-warp accumulators and statistics (later
+  // the merged accumulators [8][128]), then rows of Πᵀ (512 bytes each) for the rotation back;
+  // the last CTA's merge keeps its weights [2][8][kMaxSplits] at the start
   static constexpr int comb_acc = 0;
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
-  static_assert(comb_stats + (kSWarps * 4 + 3) * 8 * 4 <= ring, "combine scratch");
+  static constexpr int pi_off = (comb_stats + (kSWarps * 4 + 3 + 4) * 8 * 4 + 127) / 128 * 128;
+  static constexpr int pi_rows = (ring - pi_off) / 512 / 32 * 32;   // rows per chunk
+  static_assert(pi_rows >= 32, "rotation rows");
+  static_assert(2 * 8 * kMaxSplits * 4 <= ring, "merge weights");
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
   static constexpr int d_cols = NP * kN;
@@ -319,14 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   __shared__ __align__(8) uint64_t mma_done[2];
   __shared__ __align__(8) uint64_t d_free[2];
   __shared__ __align__(8) uint64_t a_full[2];
-  __shared__ __align__(8) uint64_t prol_bar;
-  __shared__ __align__(8) uint64_t mrg_bar;
+  __shared__ __align__(8) uint64_t prol_bar;   // query operand (and value pair table) landed
+  __shared__ __align__(8) uint64_t comb_bar;   // every CTA's result is in this CTA's slots
+  __shared__ __align__(8) uint64_t pi_bar;     // rows of Πᵀ landed
+  __shared__ __align__(8) uint64_t rec_bar;    // (leader) every CTA of the cluster wrote its record part
+  __shared__ __align__(8) uint64_t last_bar;   // the leader's verdict (s_last) arrived
+  __shared__ __align__(8) uint64_t mrg_bar;    // a chunk of record slices landed
+  __shared__ float s_hM[8], s_hL[8];
+  __shared__ int s_last;
   __shared__ uint32_t s_tmem;
   __shared__ int s_ticket;
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), C = cluster_ctas();
+  const int cid = split / (int)C, nclus = a.nsplit / (int)C;
   int len = a.seq_lens[b];
   if (len > a.cap) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
@@ -348,14 +437,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       mbar_init(&a_full[i], kEWarps);
     }
     mbar_init(&prol_bar, 1);
+    mbar_init(&comb_bar, C);
+    mbar_init(&pi_bar, 1);
+    mbar_init(&rec_bar, C);
+    mbar_init(&last_bar, 1);
     mbar_init(&mrg_bar, 1);
     mbar_init_fence();
+    s_ticket = -1;
   }
   if (warp == 0) tmem_alloc(&s_tmem, 512);
   tc_before();
   __syncthreads();
   tc_after();
+  // every CTA of the cluster initialises its barriers before any remote access (the wait half
+  // comes just before the first remote store, at the end of the split)
+  if (C > 1) cluster_arrive_all();
   const uint32_t tmem = s_tmem;
+
+  // output coordinates i0..i0+R of this CTA (the rotation back and the final merge), and the
+  // chunks of prow rows of Πᵀ that the rotation back stages in the ring
+  const int R = TQ_D / (int)C, i0 = (int)rank * R;
+  const int prow = R < L::pi_rows ? R : L::pi_rows;
 
   // ============================================================ producer warp
   if (warp == kEWarps + kSWarps + kIWarps) {
@@ -383,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         }
         bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
       };
+      // the ring fills while the query-operand kernel (this grid's programmatic-launch
+      // primary) runs; its output is copied in as soon as that grid has completed
       int c = 0;
       for (; c < nstages && c < kStages; ++c) issue(c);
-      // the operand images are the primary kernel's output
       asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_expect_tx(&prol_bar, frag_block(NP) + L::lut_bytes);
       bulk_g2s(smem + L::frag, static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP),
@@ -404,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         mbar_wait(&full_bar[k % kStages], (k / kStages) & 1);
       mbar_wait(&prol_bar, 0);
     }
+    if (C > 1) cluster_wait_all();
     return;
   }
 
@@ -496,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     const int grp = sw_ >> 2;                             // tiles i ≡ grp (mod 2)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int g = lane >> 2, c = lane & 3;
-    bool okp = ntiles == 0 || mbar_wait(&prol_bar, 0);
+    // the operand constants (and the cluster's stores into this CTA) are complete
+    bool okp = mbar_wait(&prol_bar, 0);
     if (!okp) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
     float hA[2], hCm[2], hB[2], hCq[2];
     {
@@ -575,21 +680,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
             lg[T][k][h] = valid ? sc : -INFINITY;
           }
         }
-      // ---- online softmax over the warp's 32 tokens (per column pair)
-      float mt[2];
+      // ---- online softmax over the warp's 32 tokens (per column pair).  The warp-wide maximum
+      // is needed only when some logit exceeds the running maximum, which after the first tiles
+      // is rare: the common tile skips the shuffles.
+      bool grow = false;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        mt[h] = fmaxf(m_run[h], m);
+        const float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
+        grow |= m > m_run[h];
       }
-      if (__any_sync(0xffffffffu, mt[0] > m_run[0] || mt[1] > m_run[1])) {
-        float corr[2];
+      if (__any_sync(0xffffffffu, grow)) {
+        float mt[2], corr[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          corr[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - mt[h]);
+          float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          mt[h] = fmaxf(m_run[h], m);
+          corr[h] = m_run[h] == -INFINITY ? 0.f : ex2(m_run[h] - mt[h]);
           l_run[h] *= corr[h];
           lw_run[h] *= corr[h];
           m_run[h] = mt[h];
@@ -614,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
           const float vn = vxn[tl];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float pr = valid ? exp2f(lg[T][k][h] - m_run[h]) : 0.f;
+            const float pr = valid ? ex2(lg[T][k][h] - m_run[h]) : 0.f;
             l_run[h] += pr;
             w[T][k][h] = valid ? pr * vn : 0.f;
             lw_run[h] += w[T][k][h];
@@ -705,10 +814,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     }
     named_sync(kBarS, kSWarps * 32);   // every softmax warp is done with the ring: reuse it
     const int stid = tid - kEWarps * 32;
+    // the first chunk of Πᵀ rows is in flight during the combine
+    if (stid == 0) {
+      mbar_expect_tx(&pi_bar, (unsigned)prow * 512u);
+      bulk_g2s(smem + L::pi_off, a.vpiT + (long long)i0 * TQ_D, (unsigned)prow * 512u, &pi_bar);
+    }
     float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);     // [warp][col][140]
     float* cstat = reinterpret_cast<float*>(smem + L::comb_stats);  // [warp][3][8]
     float* fac = cstat + kSWarps * 3 * 8;                           // [warp][8]
-    float* cML = fac + kSWarps * 8;                                 // M, L, LW [3][8]
+    float* cML = fac + kSWarps * 8;                                 // M, L, LW [3][8], then [8][4]
 #pragma unroll
     for (int k8 = 0; k8 < 8; ++k8) {
 #pragma unroll
@@ -755,179 +869,383 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       cML[16 + col] = lw;
     }
     named_sync(kBarS, kSWarps * 32);
-    float* rec_base = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
-    for (int i = stid; i < a.G * TQ_D; i += kSWarps * 32) {
-      const int head = i >> 7, j = i & 127;
+    // ---- this CTA's per-head result (M, L, acc[128]) into slot `rank` of every CTA of the
+    // cluster
+    constexpr int kSlot = 16 + 8 * TQ_D;
+    float* slots = reinterpret_cast<float*>(smem + L::slots);  // [C][M[8], L[8], acc[8][128]]
+    const uint32_t slots_s = s32(slots);
+    if (C > 1) cluster_wait_all();   // every peer's barriers are initialised
+    // item (head, 4 coordinates): the combined values, stored as one 16-byte word per CTA
+    for (int it = stid; it < a.G * (TQ_D / 4); it += kSWarps * 32) {
+      const int head = it >> 5, j0 = 4 * (it & 31);
       const int col = HILO ? 2 * head : head;
-      float acc_j = 0.f;
+      float v4[4];
 #pragma unroll
-      for (int wp = 0; wp < kSWarps; ++wp) {
-        float av = cacc[accidx(wp * 8 + col, j)];
-        if (HILO) av += cacc[accidx(wp * 8 + col + 1, j)];
-        acc_j = fmaf(fac[wp * 8 + col], av, acc_j);
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + e;
+        float acc_j = 0.f;
+#pragma unroll
+        for (int wp = 0; wp < kSWarps; ++wp) {
+          float av = cacc[accidx(wp * 8 + col, j)];
+          if (HILO) av += cacc[accidx(wp * 8 + col + 1, j)];
+          acc_j = fmaf(fac[wp * 8 + col], av, acc_j);
+        }
+        if (VB != 4) acc_j -= a.vd.cst * cML[16 + col];
+        v4[e] = acc_j;
       }
-      if (VB != 4) acc_j -= a.vd.cst * cML[16 + col];
-      float* rec = rec_base + head * kRec;
-      if (j == 0) {
-        rec[0] = cML[col];        // base-2 maximum
-        rec[1] = cML[8 + col];
+      const uint4 u = make_uint4(__float_as_uint(v4[0]), __float_as_uint(v4[1]),
+                                 __float_as_uint(v4[2]), __float_as_uint(v4[3]));
+      const int off = (int)rank * kSlot + 16 + head * TQ_D + j0;
+      for (uint32_t d = 0; d < C; ++d) {
+        if (d == rank) *reinterpret_cast<uint4*>(slots + off) = u;
+        else st_cluster_v4(map_rank(slots_s + 4u * off, d), u);
       }
-      rec[2 + j] = acc_j;
+      if (j0 == 0) {
+        const int o = (int)rank * kSlot + head;
+        for (uint32_t d = 0; d < C; ++d) {
+          if (d == rank) {
+            slots[o] = cML[col];                       // base-2 maximum
+            slots[o + 8] = cML[8 + col];
+          } else {
+            st_cluster_f32(map_rank(slots_s + 4u * o, d), cML[col]);
+            st_cluster_f32(map_rank(slots_s + 4u * (o + 8), d), cML[8 + col]);
+          }
+        }
+      }
     }
-    __threadfence();
+    if (C > 1) fence_cluster();
     named_sync(kBarS, kSWarps * 32);
-    if (stid == 0) s_ticket = atomicAdd(&a.counters[bh], 1);
+    if (stid < (int)C) {
+      if (stid == (int)rank) mbar_arrive(&comb_bar);
+      else arrive_remote(s32(&comb_bar), (uint32_t)stid);
+    }
+    // ---- merge the cluster's C results (every CTA does it; they agree bit for bit): weights
+    // per head first, then 4 coordinates per item
+    bool okc = C == 1 ? mbar_wait(&comb_bar, 0) : mbar_wait_cluster(&comb_bar, 0);
+    if (!okc && stid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    float* cw = cML + 24;                                         // [8][4] slot weights
+    if (stid < a.G) {
+      const int head = stid;
+      float M = -INFINITY;
+      for (uint32_t r = 0; r < C; ++r)
+        if (slots[r * kSlot + 8 + head] > 0.f) M = fmaxf(M, slots[r * kSlot + head]);
+      float Ls = 0.f;
+      for (uint32_t r = 0; r < C; ++r) {
+        const float l = slots[r * kSlot + 8 + head];
+        const float wr = (M == -INFINITY || !(l > 0.f)) ? 0.f : exp2f(slots[r * kSlot + head] - M);
+        cw[head * 4 + r] = wr;
+        Ls = fmaf(wr, l, Ls);
+      }
+      s_hM[head] = M;
+      s_hL[head] = Ls;
+    }
+    named_sync(kBarS, kSWarps * 32);
+    float* mrg = reinterpret_cast<float*>(smem + L::comb_acc);   // [8][128], after cacc is read
+    for (int it = stid; it < a.G * (TQ_D / 4); it += kSWarps * 32) {
+      const int head = it >> 5, j0 = 4 * (it & 31);
+      float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t r = 0; r < C; ++r) {
+        const float wr = cw[head * 4 + r];
+        const float4 v = *reinterpret_cast<const float4*>(slots + r * kSlot + 16 + head * TQ_D + j0);
+        m4.x = fmaf(wr, v.x, m4.x);
+        m4.y = fmaf(wr, v.y, m4.y);
+        m4.z = fmaf(wr, v.z, m4.z);
+        m4.w = fmaf(wr, v.w, m4.w);
+      }
+      *reinterpret_cast<float4*>(mrg + head * TQ_D + j0) = m4;
+    }
   }
 
-  // ============================================================ end of the split; last CTA merges
+  // ============================================================ end of the split
+  // every compute warp: rotate back this CTA's output rows of the merged accumulators into the
+  // cluster's record, then the ticket
   tc_before();
-  fence_async_smem();   // the merge's bulk copies overwrite shared memory written above
   named_sync(kBarAll, kCompute);
   tc_after();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  if (s_ticket != a.nsplit - 1) return;
-  __threadfence();
-  // Stage Π (fp32) and as many split records as fit in shared memory with bulk copies; the
-  // records of one (batch, KV head) are contiguous: [split][head][kRec]
-  float* s_pi = reinterpret_cast<float*>(smem);                       // [128][128]
-  float* s_rec = reinterpret_cast<float*>(smem + 65536);              // up to L::mrg_acc
-  float* s_acc = reinterpret_cast<float*>(smem + L::mrg_acc);         // [8][128]
-  float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);             // [8][kMaxSplits]
-  __shared__ float s_M[8], s_L[8];
-  const long long rec_floats = (long long)a.nsplit * a.G * kRec;
-  const int chunk_splits = (int)((L::mrg_acc - 65536) / (a.G * kRec * 4));
-  const float* recs = a.part + bh * rec_floats;
-  const bool one_chunk = a.nsplit <= chunk_splits;
-  if (tid == 0) {
-    // Π and the first (usually the only) chunk of records, in flight while the weights are
-    // prepared
-    const int ns = min(chunk_splits, a.nsplit);
-    const unsigned bytes = (unsigned)(ns * a.G * kRec * 4);
-    mbar_expect_tx(&mrg_bar, bytes + 65536u);
-    bulk_g2s(s_pi, a.pi, 65536, &mrg_bar);
-    bulk_g2s(s_rec, recs, bytes, &mrg_bar);
+  {
+    const float* mrg = reinterpret_cast<const float*>(smem + L::comb_acc);   // [8][128]
+    float* rec_base = a.part + ((bh * nclus + cid) * a.G) * kRec;
+    const float4* pis = reinterpret_cast<const float4*>(smem + L::pi_off);  // [prow][32]
+    for (int c0 = 0, ph = 0; c0 < R; c0 += prow, ph ^= 1) {
+      if (c0 > 0) {
+        named_sync(kBarAll, kCompute);   // the previous chunk is consumed
+        if (tid == 0) {
+          mbar_expect_tx(&pi_bar, (unsigned)prow * 512u);
+          bulk_g2s(smem + L::pi_off, a.vpiT + (long long)(i0 + c0) * TQ_D, (unsigned)prow * 512u,
+                   &pi_bar);
+        }
+      }
+      const bool okp2 = mbar_wait(&pi_bar, (unsigned)ph);
+      if (!okp2 && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      // task (head, 32-row group) per warp; lane = output row; the j loop starts at a
+      // lane-dependent offset so that the float4 reads of both operands are free of bank
+      // conflicts
+      const int ngrp = prow / 32;
+      for (int task = warp; okp2 && task < a.G * ngrp; task += kCompute / 32) {
+        const int h = task / ngrp, r = (task - h * ngrp) * 32 + lane;
+        const float4* mh = reinterpret_cast<const float4*>(mrg + h * TQ_D);
+        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+          const int jq = (jj + lane) & 31;
+          const float4 pv = pis[r * 32 + jq];
+          const float4 mv = mh[jq];
+          o0 = fmaf(pv.x, mv.x, o0);
+          o1 = fmaf(pv.y, mv.y, o1);
+          o2 = fmaf(pv.z, mv.z, o2);
+          o3 = fmaf(pv.w, mv.w, o3);
+        }
+        rec_base[h * kRec + 4 + i0 + c0 + r] = (o0 + o1) + (o2 + o3);
+      }
+    }
+    if (rank == 0 && tid < a.G) {
+      rec_base[tid * kRec] = s_hM[tid];
+      rec_base[tid * kRec + 1] = s_hL[tid];
+    }
   }
-  // warp h: maximum and weights of head h over the splits, from the staged records when
-  // they all fit, else with plain loads (2 per split)
-  auto weights = [&](const float* src, bool staged) {
+  named_sync(kBarAll, kCompute);
+  if (tid == 0) {
+    // this CTA's part of the record is released at device scope; the leader, once every CTA
+    // of the cluster has reported, takes the cluster's ticket and tells the cluster whether
+    // it was the last one of the (batch, KV head)
+    fence_gpu();
+    if (rank == 0) mbar_arrive(&rec_bar);
+    else arrive_remote(s32(&rec_bar), 0);
+    bool okt = true;
+    if (rank == 0) {
+      okt = C == 1 ? mbar_wait(&rec_bar, 0) : mbar_wait_cluster(&rec_bar, 0);
+      fence_gpu();
+      const int last = atomicAdd(&a.counters[bh], 1) == nclus - 1 ? 1 : 0;
+      for (uint32_t d = 0; d < C; ++d) {
+        if (d == 0) {
+          s_last = last;
+          mbar_arrive(&last_bar);
+        } else {
+          st_cluster_s32(map_rank(s32(&s_last), d), last);
+          arrive_remote(s32(&last_bar), d);
+        }
+      }
+    }
+    okt = (C == 1 ? mbar_wait(&last_bar, 0) : mbar_wait_cluster(&last_bar, 0)) && okt;
+    if (!okt) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    s_ticket = okt ? s_last : 0;
+  }
+  named_sync(kBarAll, kCompute);
+  if (s_ticket != 1) return;
+  // Every record (one per cluster) is rotated back already: out_h = Σ_r w_r·rec_r / Σ_r w_r·L_r
+  // with w_r = 2^(M_r − max M).  CTA `rank` of the last cluster produces output coordinates
+  // i0..i0+R.  Without clusters the records are contiguous and arrive by bulk copy, in chunks
+  // that fit in shared memory; in a cluster each CTA loads its 128-byte slices directly (few
+  // small bulk copies would cost more than they save).  Warp h computes the weights of head h.
+  if (tid == 0) {
+    fence_gpu();
+    fence_proxy_async_global();
+  }
+  named_sync(kBarAll, kCompute);
+  const float* recs = a.part + bh * (long long)nclus * a.G * kRec;
+  float* sa = reinterpret_cast<float*>(smem);                          // C == 1: [chunk][G][kRec]
+  float* s_w = reinterpret_cast<float*>(smem + L::slots);              // [2][8][kMaxSplits]
+  const int chunk = C == 1 ? min(nclus, (int)(L::slots / (a.G * kRec * 4))) : nclus;
+  auto issue_chunk = [&](int r0) {
+    const int n = min(chunk, nclus - r0);
+    const unsigned bytes = (unsigned)(n * a.G * kRec * 4);
+    mbar_expect_tx(&mrg_bar, bytes);
+    bulk_g2s(sa, recs + (long long)r0 * a.G * kRec, bytes, &mrg_bar);
+  };
+  if (C == 1 && tid == 0) issue_chunk(0);
+  constexpr int kPre = 16;
+  float pv[kPre];
+  const bool slice_item = C > 1 && tid < a.G * R;   // R ≤ 64 here: one item per thread
+  const int sh = slice_item ? tid / R : 0, si = slice_item ? tid - sh * R : 0;
+#pragma unroll
+  for (int r = 0; r < kPre; ++r)
+    pv[r] = (slice_item && r < nclus)
+                ? __ldcg(&recs[((long long)r * a.G + sh) * kRec + 4 + i0 + si]) : 0.f;
+  if (warp < a.G) {
     float mx = -INFINITY;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const long long o = ((long long)s * a.G + warp) * kRec;
-      const float m = staged ? src[o] : __ldcg(&src[o]);
-      const float l = staged ? src[o + 1] : __ldcg(&src[o + 1]);
+#pragma unroll 4
+    for (int r = lane; r < nclus; r += 32) {
+      const long long o = ((long long)r * a.G + warp) * kRec;
+      const float m = __ldcg(&recs[o]), l = __ldcg(&recs[o + 1]);
       const float mm = l > 0.f ? m : -INFINITY;
-      s_w[warp * kMaxSplits + s] = mm;
+      s_w[warp * kMaxSplits + r] = mm;
       mx = fmaxf(mx, mm);
+      s_w[(8 + warp) * kMaxSplits + r] = l;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float Ls = 0.f;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const long long o = ((long long)s * a.G + warp) * kRec + 1;
-      const float mm = s_w[warp * kMaxSplits + s];
+    for (int r = lane; r < nclus; r += 32) {
+      const float mm = s_w[warp * kMaxSplits + r];
       const float wgt = (mx == -INFINITY || mm == -INFINITY) ? 0.f : exp2f(mm - mx);
-      s_w[warp * kMaxSplits + s] = wgt;
-      Ls += wgt * (staged ? src[o] : __ldcg(&src[o]));
+      s_w[warp * kMaxSplits + r] = wgt;
+      Ls += wgt * s_w[(8 + warp) * kMaxSplits + r];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (lane == 0) {
-      s_M[warp] = mx;
-      s_L[warp] = Ls;
-    }
-  };
-  if (!one_chunk && warp < a.G) weights(recs, false);
-  float accv[3] = {0.f, 0.f, 0.f};   // thread's (head, j) items: tid, tid + kCompute, ...
-  uint32_t mphase = 0;
-  for (int s0 = 0; s0 < a.nsplit; s0 += chunk_splits) {
-    const int ns = min(chunk_splits, a.nsplit - s0);
-    if (tid == 0 && s0 > 0) {
-      const unsigned bytes = (unsigned)(ns * a.G * kRec * 4);
-      mbar_expect_tx(&mrg_bar, bytes);
-      bulk_g2s(s_rec, recs + (long long)s0 * a.G * kRec, bytes, &mrg_bar);
-    }
-    if (!mbar_wait(&mrg_bar, mphase) && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    mphase ^= 1;
-    if (one_chunk) {
-      if (warp < a.G) weights(s_rec, true);
-    }
-    named_sync(kBarAll, kCompute);   // weights ready and staged records visible
+    if (lane == 0) s_hL[warp] = Ls;
+  }
+  named_sync(kBarAll, kCompute);   // weights ready
+  constexpr int kItems = (8 * TQ_D + kCompute - 1) / kCompute;
+  float x[kItems] = {};
+  if (C > 1) {
+    if (slice_item) {
+      const float* wv = s_w + sh * kMaxSplits;
+      float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-    for (int it = 0; it < 3; ++it) {
-      const int item = tid + it * kCompute;
-      if (item < a.G * TQ_D) {
-        const int head = item >> 7, j = item & 127;
-        const float* wv = s_w + head * kMaxSplits + s0;
-        const float* rv = s_rec + head * kRec + 2 + j;
-        const int step = a.G * kRec;
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-        int sp = 0;
-        for (; sp + 4 <= ns; sp += 4) {
-          x0 = fmaf(wv[sp], rv[sp * step], x0);
-          x1 = fmaf(wv[sp + 1], rv[(sp + 1) * step], x1);
-          x2 = fmaf(wv[sp + 2], rv[(sp + 2) * step], x2);
-          x3 = fmaf(wv[sp + 3], rv[(sp + 3) * step], x3);
+      for (int r = 0; r < kPre; r += 2) {
+        if (r < nclus) x0 = fmaf(wv[r], pv[r], x0);
+        if (r + 1 < nclus) x1 = fmaf(wv[r + 1], pv[r + 1], x1);
+      }
+      for (int r0 = kPre; r0 < nclus; r0 += kPre) {   // beyond the prefetched records
+#pragma unroll
+        for (int r = 0; r < kPre; ++r)
+          pv[r] = r0 + r < nclus ? __ldcg(&recs[((long long)(r0 + r) * a.G + sh) * kRec + 4 + i0 + si]) : 0.f;
+#pragma unroll
+        for (int r = 0; r < kPre; ++r)
+          if (r0 + r < nclus) x0 = fmaf(wv[r0 + r], pv[r], x0);
+      }
+      x[0] = x0 + x1;
+    }
+  } else {
+    uint32_t mphase = 0;
+    for (int r0 = 0; r0 < nclus; r0 += chunk) {
+      const bool okm = mbar_wait(&mrg_bar, mphase);
+      if (!okm && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      mphase ^= 1;
+      const int n = min(chunk, nclus - r0);
+#pragma unroll
+      for (int it = 0; it < kItems; ++it) {
+        const int item = tid + it * kCompute;
+        if (item < a.G * TQ_D) {
+          const int h = item >> 7, i = item & 127;
+          const float* wv = s_w + h * kMaxSplits + r0;
+          const float* av = sa + h * kRec + 4 + i;
+          const int step = a.G * kRec;
+          float x0 = 0.f, x1 = 0.f;
+          int r = 0;
+          for (; r + 2 <= n; r += 2) {
+            x0 = fmaf(wv[r], av[r * step], x0);
+            x1 = fmaf(wv[r + 1], av[(r + 1) * step], x1);
+          }
+          if (r < n) x0 = fmaf(wv[r], av[r * step], x0);
+          x[it] += x0 + x1;
         }
-        for (; sp < ns; ++sp) x0 = fmaf(wv[sp], rv[sp * step], x0);
-        accv[it] += (x0 + x1) + (x2 + x3);
+      }
+      if (r0 + chunk < nclus) {
+        named_sync(kBarAll, kCompute);   // the chunk buffer is consumed
+        if (tid == 0) {
+          fence_async_smem();
+          issue_chunk(r0 + chunk);
+        }
       }
     }
-    named_sync(kBarAll, kCompute);   // the staging buffer is free for the next chunk
   }
 #pragma unroll
-  for (int it = 0; it < 3; ++it) {
-    const int item = tid + it * kCompute;
-    if (item < a.G * TQ_D) s_acc[item] = accv[it];
-  }
-  named_sync(kBarAll, kCompute);
-  // out_h = Πᵀ·acc_h / L_h: thread item (head, i)
-#pragma unroll
-  for (int it = 0; it < 3; ++it) {
-    const int item = tid + it * kCompute;
-    if (item < a.G * TQ_D) {
-      const int head = item >> 7, i = item & 127;
-      float o0 = 0.f, o1 = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < TQ_D; j += 2) {
-        o0 = fmaf(s_pi[j * TQ_D + i], s_acc[head * TQ_D + j], o0);
-        o1 = fmaf(s_pi[(j + 1) * TQ_D + i], s_acc[head * TQ_D + j + 1], o1);
-      }
-      const float Lh = s_L[head];
-      const float v = Lh > 0.f ? (o0 + o1) / Lh : 0.f;
-      const long long e = ((long long)b * a.Hq + kvh * a.G + head) * TQ_D + i;
+  for (int it = 0; it < kItems; ++it) {
+    const int item = C > 1 ? (it == 0 && slice_item ? tid : -1) : tid + it * kCompute;
+    if (item >= 0 && item < a.G * R) {
+      const int h = item / R, i = item - h * R;
+      const float Lh = s_hL[h];
+      const float v = Lh > 0.f ? x[it] / Lh : 0.f;
+      const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + i0 + i;
       if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = v;
       else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(v);
       else static_cast<__half*>(a.out)[e] = __float2half_rn(v);
     }
   }
-  if (tid == 0) a.counters[bh] = 0;   // ready for the next call
+  if (rank == 0 && tid == 0) a.counters[bh] = 0;   // ready for the next call
 }
 
+// Cluster size and split count: as many CTAs as can be co-resident (one per SM), in clusters
+// of 4, 2 or 1 consecutive splits of one (batch, KV head).
 template <int KB, int VB, bool HILO>
-tq_status launch_one(const tq_mma_launch& a, cudaStream_t stream) {
+tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
   constexpr int smem = TL<KB, VB>::total;
+  auto kern = decode_tc_kernel<KB, VB, HILO>;
   static bool configured[64] = {};
+  static int max_ctas[64][3] = {};   // co-resident CTAs with clusters of 1, 2, 4
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(decode_tc_kernel<KB, VB, HILO>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    max_ctas[dev][0] = per_sm * tq_num_sms();
+    for (int k = 1; k < 3; ++k) {
+      const int csz = 1 << k;
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(csz, 1, 1);
+      q.blockDim = dim3(kThreads);
+      q.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = csz;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      q.attrs = at;
+      q.numAttrs = 1;
+      int nclusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &q) != cudaSuccess) nclusters = 0;
+      max_ctas[dev][k] = nclusters * csz;
+    }
+    cudaGetLastError();
     configured[dev] = true;
   }
+  // the choice with the shortest estimated critical path: tiles per CTA plus the end of the
+  // split, which costs about three tiles more without clusters and one and a half more with
+  // clusters of two than with clusters of four (each CTA rotates back a smaller share); on a
+  // tie the larger cluster
+  const int units = a0.B * a0.Hkv;
+  const long long len = a0.max_len > 0 ? a0.max_len : 1;
+  int best_c = 1, best_n = 1;
+  long long best_cost = -1;
+  for (int k = 0; k < 3; ++k) {
+    const int csz = 1 << k;
+    int ns = max_ctas[dev][k] / units;
+    if (ns > a0.nsplit) ns = a0.nsplit;
+    ns -= ns % csz;
+    if (ns < csz) {
+      if (csz > 1) continue;
+      ns = 1;
+    }
+    const long long tiles = ((len + ns - 1) / ns + kTile - 1) / kTile;
+    const long long cost = 2 * tiles + (csz == 1 ? 6 : csz == 2 ? 3 : 0);
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      best_c = csz;
+      best_n = ns;
+    }
+  }
+  if (max_ctas[dev][0] / units < 2 && a0.nsplit > 1) {
+    // fewer SMs than two splits per unit: the plan's splits, in several waves
+    best_c = 1;
+    best_n = a0.nsplit;
+  }
+  tq_mma_launch a = a0;
+  a.nsplit = best_n;
+  long long sl = a.max_len > 0 ? (a.max_len + best_n - 1) / best_n : 1;
+  sl = (sl + kTile - 1) / kTile * kTile;
+  a.split_len = (int)sl;
   query_prep_tc_kernel<KB, HILO><<<dim3(4, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.Hkv, a.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = best_c;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_tc_kernel<KB, VB, HILO>, a) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  cfg.numAttrs = best_c > 1 ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
   return tq_cuda_status(cudaGetLastError());
 }
 
