@@ -15,7 +15,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
-#include "decode_mma.h"
+#include "decode_args.h"
 #include "tq_internal.h"
 
 TQ_DEFINE_FLAGS(tq_take_flags_attention)
@@ -58,6 +58,12 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   // more units than half the SMs: a wave does not give every unit two splits, and ragged
   // lengths leave SMs idle; three splits per sequence (several waves) balance better
   if (units * 2 > sm_count() && want < 3) want = 3;
+  if (asym) {
+    // the tail's CTAs share the wave: splits of the compressed part plus the tail's per unit
+    const long long tail_splits = (d->tail_capacity + kSplit - 1) / kSplit;
+    const long long fit = sm_count() / units - tail_splits;
+    want = fit >= 1 ? fit : 1;
+  }
   long long sl = (d->max_seq_len + want - 1) / (want > 0 ? want : 1);
   sl = (sl + 127) / 128 * 128;
   if (sl < 128) sl = 128;
@@ -68,9 +74,7 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   // per-query vectors (CUDA-core path) or per-(batch, KV head) query fragments
   // (tensor-core path), whichever is larger
   size_t qbytes = (size_t)d->batch * d->q_heads * 2 * TQ_D * sizeof(float);
-  size_t fbytes = (size_t)d->batch * d->kv_heads * tq_mma_frag_bytes_max();
-  const size_t tbytes = (size_t)d->batch * d->kv_heads * tq_tc_frag_bytes_max();
-  if (tbytes > fbytes) fbytes = tbytes;
+  const size_t fbytes = (size_t)d->batch * d->kv_heads * tq_tc_frag_bytes_max();
   if (fbytes > qbytes) qbytes = fbytes;
   const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
   p->q_off = 0;
@@ -486,7 +490,7 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
   const bool tc = tq_tc_decode_supported(kc->ibits, vc->ibits, p.G, p.nsplit);
-  if (tc || (tq_mma_supported(kc->ibits, vc->ibits, p.G) && p.nsplit <= 256)) {
+  if (tc) {
     tq_mma_launch m{};
     m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap;
     m.nsplit = p.nsplit; m.split_len = p.split_len;
@@ -509,8 +513,7 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
     m.counters = reinterpret_cast<int*>(ws + p.ctr_off);
     m.max_len = desc->max_seq_len;
     tq_tc_operand_scales(m.kd, &m.s_idx, &m.s_sgn);
-    if (tc) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
-    return tq_launch_decode_mma(m, stream);          // fragments, split decode, merge
+    return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
   }
   query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
                                                    reinterpret_cast<float*>(ws + p.q_off));
@@ -556,7 +559,25 @@ extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq
   a.seq_lens = seq_lens;
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
-  decode_asym_kernel<<<dim3(p.nsplit, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+  if (tq_asym_tc_supported(vc->ibits, p.G, p.split_len, kSplit)) {
+    tq_asym_launch m{};
+    m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap; m.tail_cap = a.tail_cap;
+    m.nsplit_main = p.nsplit_main; m.nsplit = p.nsplit; m.split_len = p.split_len;
+    m.tail_split = kSplit;
+    m.scale_log2 = a.scale * 1.4426950408889634f;
+    m.q = q; m.q_dtype = desc->q_dtype;
+    m.kf16 = a.kf16; m.ktail = a.ktail; m.vtail = a.vtail; m.tail_lens = tail_lens;
+    m.vidx = v.idx; m.vxn = v.xnorm; m.vbits = vc->ibits;
+    if (vc->ibits < 4) m.vd = tq_decompose_levels(vc);
+    m.lut = vc->d_lut;
+    m.vc_unscale = vc->ibits == 4 ? 1.f / vc->lut_scale : 1.f;
+    m.seq_lens = seq_lens;
+    m.part = a.part;
+    st = tq_launch_decode_asym_tc(m, stream);   // split decode (mma.sync), then the merge
+    if (st != TQ_OK) return st;
+  } else {
+    decode_asym_kernel<<<dim3(p.nsplit, desc->kv_heads, desc->batch), kThreads, 0, stream>>>(a);
+  }
   merge_kernel<<<rows, kMergeThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
                                               vc->d_pi, out, desc->out_dtype);
   return tq_cuda_status(cudaGetLastError());

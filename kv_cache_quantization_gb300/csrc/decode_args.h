@@ -1,6 +1,8 @@
-// Launch interface of the tensor-core split-decode kernel (decode_mma.cu), used by
+// Launch interface of the tensor-core split-decode kernel (decode_tc.cu), used by
 // attention.cu.  Internal to the library.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "tq_internal.h"
 
@@ -24,7 +26,7 @@ struct tq_mma_launch {
   const float* u;              // Πᵀ·1 and Sᵀ·1 of the key codec
   const float* w;
   float smax;                  // largest row norm of S
-  void* qfrag;                 // workspace: per (b, KV head) query fragments
+  void* qfrag;                 // workspace: per (b, KV head) query operand images
   const uint8_t* kidx;
   const uint8_t* ksgn;
   const float* kxn;
@@ -48,15 +50,8 @@ struct tq_mma_launch {
   float s_idx, s_sgn;          // power-of-two scales of the e4m3 query operand
 };
 
-// True when the tensor-core kernel handles this configuration.
-bool tq_mma_supported(int kbits, int vbits, int G);
 // Odd-Walsh decomposition of a codec's levels (index bits ≤ 3).
 tq_plane_decomp tq_decompose_levels(const tq_codec* c);
-tq_status tq_launch_decode_mma(const tq_mma_launch& a, cudaStream_t stream);
-// Scale σ in [1, 2) for which σ·levels are closest to fp16 numbers (worst relative error).
-float tq_fp16_friendly_scale(const float* levels, int n);
-// Workspace bytes per (batch, KV head) reserved for the query fragments.
-size_t tq_mma_frag_bytes_max();
 // Tensor-core (tcgen05) split decode with in-kernel query operand and last-CTA merge.
 bool tq_tc_decode_supported(int kbits, int vbits, int G, int nsplit);
 tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream);
@@ -64,3 +59,29 @@ tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream);
 size_t tq_tc_frag_bytes_max();
 // Power-of-two scales of the e4m3 query operand for a key codec's decomposition.
 void tq_tc_operand_scales(const tq_plane_decomp& kd, float* s_idx, float* s_sgn);
+
+// Launch interface of the asymmetric split-decode kernel (decode_asym.cu): FP16 keys,
+// MSE-coded values and an FP16 tail; one record per (batch, KV head, split) in the layout of
+// the CUDA-core path's merge kernel, which runs after it.
+struct tq_asym_launch {
+  int B, Hq, Hkv, G, cap, tail_cap;
+  int nsplit_main, nsplit, split_len, tail_split;
+  float scale_log2;            // softmax scale × log2(e)
+  const void* q;               // [B][Hq][128] queries (q_dtype)
+  int q_dtype;
+  const __half* kf16;          // [B][Hkv][cap][128]
+  const __half* ktail;         // [B][Hkv][tail_cap][128]
+  const __half* vtail;
+  const int* tail_lens;
+  const uint8_t* vidx;
+  const float* vxn;
+  int vbits;
+  tq_plane_decomp vd;          // value decomposition (vbits ≤ 3)
+  const uint32_t* lut;         // vbits == 4: pair table of the value codec (device)
+  float vc_unscale;            // 1 / the table's level scale
+  const int* seq_lens;
+  float* part;                 // [B][Hkv][nsplit][G][TQ_REC]
+};
+
+bool tq_asym_tc_supported(int vbits, int G, int split_len, int tail_split);
+tq_status tq_launch_decode_asym_tc(const tq_asym_launch& a, cudaStream_t stream);

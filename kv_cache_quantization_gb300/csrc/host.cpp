@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 
 #include "tq_internal.h"
+#include "decode_args.h"
 
 extern "C" const char* tq_status_string(tq_status s) {
   switch (s) {
@@ -345,4 +346,55 @@ extern "C" tq_status tq_codec_destroy(tq_codec* codec) {
   free_codec(codec);
   cudaSetDevice(prev);
   return TQ_OK;
+}
+
+// Odd-Walsh decomposition of a codec's levels (index bits ≤ 3): the coefficients of the
+// levels over the odd monomials of the ±1 bit variables (see decode_args.h).
+tq_plane_decomp tq_decompose_levels(const tq_codec* c) {
+  // Walsh–Hadamard coefficients of the levels over the ±1 bit variables.
+  tq_plane_decomp d{};
+  const int B = c->ibits, L = c->levels;
+  static const int masks[3][4] = {{1, 0, 0, 0}, {1, 2, 0, 0}, {1, 2, 4, 7}};
+  const int nv = B == 1 ? 1 : B == 2 ? 2 : 4;
+  d.n = nv;
+  double cst = 0;
+  for (int v = 0; v < nv; ++v) {
+    const int m = masks[B - 1][v];
+    double a = 0;
+    for (int idx = 0; idx < L; ++idx) {
+      int prod = 1;
+      for (int i = 0; i < B; ++i)
+        if (m & (1 << i)) prod *= ((idx >> i) & 1) ? 1 : -1;
+      a += (double)c->centroids_d[idx] * prod;
+    }
+    a /= L;
+    d.coef[v] = (float)(2 * a);
+    cst += a;
+  }
+  d.cst = (float)cst;
+  return d;
+}
+
+// Scale σ in [1, 2) for which σ·levels are closest to fp16 numbers (worst relative error).
+float tq_fp16_friendly_scale(const float* levels, int n) {
+  // An exhaustive search over σ = 1 + k/2^16: the table is then exact to a few 1e-5 instead
+  // of the 2.4e-4 of plain fp16 rounding.
+  float best = 1.f;
+  double best_err = 1e30;
+  for (int k = 0; k < (1 << 16); ++k) {
+    const float sg = 1.f + (float)k / 65536.f;
+    double worst = 0;
+    for (int i = 0; i < n; ++i) {
+      const float x = sg * levels[i];
+      if (x == 0.f) continue;
+      const float r = __half2float(__float2half_rn(x));
+      worst = fmax(worst, fabs((double)r - x) / fabs((double)x));
+      if (worst >= best_err) break;
+    }
+    if (worst < best_err) {
+      best_err = worst;
+      best = sg;
+    }
+  }
+  return best;
 }

@@ -448,9 +448,9 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   if (!flags) return TQ_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int a = tq_take_flags_quantize(), b = tq_take_flags_attention();
-  const unsigned int c = tq_take_flags_decode_mma(), d = tq_take_flags_quantize_tc();
-  const unsigned int e = tq_take_flags_decode_tc();
-  if (a == ~0u || b == ~0u || c == ~0u || d == ~0u || e == ~0u) return TQ_ERR_CUDA;
-  *flags = a | b | c | d | e;
+  const unsigned int d = tq_take_flags_quantize_tc(), e = tq_take_flags_decode_tc();
+  const unsigned int f = tq_take_flags_decode_asym();
+  if (a == ~0u || b == ~0u || d == ~0u || e == ~0u || f == ~0u) return TQ_ERR_CUDA;
+  *flags = a | b | d | e | f;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

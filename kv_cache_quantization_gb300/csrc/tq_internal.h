@@ -55,9 +55,9 @@ struct tq_levels {
 #endif
 unsigned int tq_take_flags_quantize();
 unsigned int tq_take_flags_attention();
-unsigned int tq_take_flags_decode_mma();
 unsigned int tq_take_flags_quantize_tc();
 unsigned int tq_take_flags_decode_tc();
+unsigned int tq_take_flags_decode_asym();
 
 static inline tq_status tq_cuda_status(cudaError_t e) {
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

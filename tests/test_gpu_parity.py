@@ -337,6 +337,14 @@ def test_asym_small():
     run_asym(3, 8, 2, [100, 0, 700], [255, 17, 0], 4, torch.float32, 700)
 
 
+@pytest.mark.parametrize("vbits,hq,hkv", [(2, 8, 2), (3, 14, 2), (1, 16, 2), (4, 14, 2)])
+def test_asym_value_bits_and_groups(vbits, hq, hkv):
+    """Value codes as planes (1–3 bits) and the pair table (4 bits), G = 4 (fp16 weight pairs)
+    and G = 7, 8 (one column per head); ragged compressed lengths across tile boundaries and
+    tails of 0, 1 and 128 tokens."""
+    run_asym(3, hq, hkv, [383, 129, 1000], [0, 1, 128], vbits, torch.float32, 710 + vbits)
+
+
 def test_asym_b8_8k():
     """B=8, 28/4 heads, 7937 FP16-key / 4-bit-value tokens + 255 FP16 tail tokens, bf16 out."""
     w = synth.ASYM_8K
