@@ -213,6 +213,12 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
   float t[32];
 #pragma unroll
   for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * kq + k) * TQ_D + 32 * s + jl]);
+  float uk[4], wk[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uk[k] = __ldg(&a.u[lane + 32 * k]);
+    wk[k] = __ldg(&a.w[lane + 32 * k]);
+  }
   __syncthreads();
   if (warp < a.G) {
     // ‖q‖, (Πᵀ1)·q and (Sᵀ1)·q of head `warp`
@@ -222,8 +228,8 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
       const int j = lane + 32 * k;
       const float x = qf[warp][j];
       n2 = fmaf(x, x, n2);
-      uq = fmaf(__ldg(&a.u[j]), x, uq);
-      wq = fmaf(__ldg(&a.w[j]), x, wq);
+      uq = fmaf(uk[k], x, uq);
+      wq = fmaf(wk[k], x, wq);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

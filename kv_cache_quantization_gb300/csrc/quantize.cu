@@ -252,12 +252,17 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
 // codes are assembled with warp ballots.
 constexpr int kSmallThreads = 512;
 
-__device__ __forceinline__ float small_matvec(const float* __restrict__ T, const float* v,
-                                              float* part, int tid) {
+// Thread (k quarter q, output j) of the 512 owns T[32q..32q+31][j]: its 32 values are loaded
+// at kernel start, together with every other global input, so that the kernel waits for one
+// round trip only.
+__device__ __forceinline__ void small_load(const float* __restrict__ T, float (&t)[32], int tid) {
   const int j = tid & 127, q = tid >> 7;
-  float t[32];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * q + k) * TQ_D + j]);   // one round trip
+  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * q + k) * TQ_D + j]);
+}
+__device__ __forceinline__ float small_matvec(const float (&t)[32], const float* v, float* part,
+                                              int tid) {
+  const int j = tid & 127, q = tid >> 7;
   float acc = 0.f;
 #pragma unroll
   for (int k = 0; k < 32; ++k) acc = fmaf(t[k], v[32 * q + k], acc);
@@ -278,9 +283,16 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
   const int t = (int)(i % a.tokens);
   const int bh = (int)(i / a.tokens);
   const int b = bh / a.heads, h = bh % a.heads;
+  // every global input first: the vector, Πᵀ and Mᵀ, the count and the position
+  float vals[8];
+  if (tid < 16) load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
+  float tp[32], tm[32];
+  small_load(a.piT, tp, tid);
+  if constexpr (kProd) small_load(a.mT, tm, tid);
   const int cnt = a.count ? a.count[b] : a.tokens;
+  const int pos = a.pos ? a.pos[b] : 0;
   if (t >= cnt) return;
-  const int dst = (a.pos ? a.pos[b] : 0) + t;
+  const int dst = pos + t;
   if (dst < 0 || dst >= a.capacity) {
     if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
     return;
@@ -288,8 +300,6 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
   const long long slot = (long long)bh * a.capacity + dst;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < 16) {
-    float vals[8];
-    load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
 #pragma unroll
     for (int e = 0; e < 8; ++e) xs[tid * 8 + e] = vals[e];
   }
@@ -303,7 +313,7 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
   }
   __syncthreads();
   const float n = sqrtf((red[0] + red[1]) + (red[2] + red[3]));
-  const float acc = small_matvec(a.piT, xs, part, tid);
+  const float acc = small_matvec(tp, xs, part, tid);
   int q = 0;
   float r = 0.f;
   if (tid < TQ_D) {
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
     }
     __syncthreads();   // rho complete; red reused
     if (warp < 4 && lane == 0) red[warp] = r2;
-    const float z = small_matvec(a.mT, rho, part, tid);   // contains __syncthreads
+    const float z = small_matvec(tm, rho, part, tid);   // contains __syncthreads
     if (warp < 4) {
       const unsigned word = n > 0.f ? __ballot_sync(0xffffffffu, z >= 0.f) : 0xffffffffu;
       if (lane == 0) reinterpret_cast<uint32_t*>(a.sgn + slot * 16)[warp] = word;
