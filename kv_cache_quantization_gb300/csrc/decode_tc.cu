@@ -101,6 +101,15 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) 
       : "r"(taddr));
 }
 
+// true in exactly one lane of the (converged) warp
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}\n"
+      : "=r"(p));
+  return p != 0;
+}
+
 __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
 }
@@ -509,31 +518,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   } else if (warp >= kEWarps + kSWarps) {
     // ========================================================== MMA-issue warps
     // Issuer iw owns planes iw, iw + kIWarps, ...: 4 MMAs of K = 32 per plane and tile,
-    // D[i & 1] column block (plane, piece, column).
+    // D[i & 1] column block (plane, piece, column).  The whole warp waits and forms the
+    // (warp-uniform) descriptors; one elected lane issues the MMAs and their commit.
     const int iw = warp - kEWarps - kSWarps;
-    if (lane == 0 && iw < NI && ntiles > 0) {
+    if (iw < NI && ntiles > 0) {
       const uint32_t idesc = idesc_f16(128, kN);   // e4m3 × e4m3 → f32 has the same fields
       const uint32_t frag_s = s32(smem + L::frag);
+      constexpr int kMaxOwn = (NP + kIWarps - 1) / kIWarps;
+      uint64_t bdesc[kMaxOwn][4];
+#pragma unroll
+      for (int o = 0; o < kMaxOwn; ++o)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          bdesc[o][ks] = smem_desc(frag_s + (iw + o * kIWarps) * kBImg + ks * 256, 128, kBSbo);
       bool ok = mbar_wait(&prol_bar, 0);
       for (int i = 0; i < ntiles && ok; ++i) {
         const int ab = L::abufs == 2 ? (i & 1) : 0;
         const int db = i & 1;
         ok = mbar_wait(&a_full[ab], (i / L::abufs) & 1) &&
              (i < 2 || mbar_wait(&d_free[db], ((i - 2) >> 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_after();
-        for (int v = iw; v < NP; v += kIWarps) {
-          const uint32_t d = tmem + L::d_col + db * L::d_cols + v * kN;
+        if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t acol = tmem + ab * L::a_cols + 32 * v + 8 * ks;
-            const uint64_t bd = smem_desc(frag_s + v * kBImg + ks * 256, 128, kBSbo);
-            mma_f8(d, acol, bd, idesc, ks > 0 ? 1u : 0u);
+          for (int o = 0; o < kMaxOwn; ++o) {
+            const int v = iw + o * kIWarps;
+            if (v < NP) {
+              const uint32_t d = tmem + L::d_col + db * L::d_cols + v * kN;
+              const uint32_t a0 = tmem + ab * L::a_cols + 32 * v;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) mma_f8(d, a0 + 8 * ks, bdesc[o][ks], idesc, ks > 0 ? 1u : 0u);
+            }
           }
+          mma_commit(&mma_done[db]);
         }
-        mma_commit(&mma_done[db]);
+        __syncwarp();
       }
-      if (!ok) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      if (!ok && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
     }
     __syncwarp();
   } else {
