@@ -365,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the warp index through a shuffle: the compiler then knows it is warp-uniform and keeps
+  // the TMEM addresses derived from it in uniform registers
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   const uint32_t rank = cluster_rank(), C = cluster_ctas();
   const int cid = split / (int)C, nclus = a.nsplit / (int)C;
   int len = a.seq_lens[b];
