@@ -133,6 +133,8 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = synth.WORKLOADS[args.workload]
+    if w.k_bits == 0:
+        return run_ours_asym(args, w, ws, rank, dev)
     ctx = w.context
     # tokens attended per sequence this step (ragged for the serving workload); the cache
     # holds lens - 1 of them and the step appends the last one
@@ -317,6 +319,132 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ours_asym(args, w, ws, rank, dev):
+    """Asymmetric workload: FP16 keys, 4-bit MSE values and an FP16 tail of 255 tokens per
+    sequence.  The timed step is one decode-attention call over the compressed part and the
+    tail (the tail's FP16 append is a copy, not part of this path)."""
+    import torch
+
+    from kv_cache_quantization_gb300 import api, synth
+
+    lens_np = synth.seq_lengths(w)                       # compressed tokens per sequence
+    tail = w.tail
+    n_tok = int(sum(lens_np)) + w.batch * tail
+    vc = api.Codec.mse(w.v_bits)
+    k, v = synth.make_kv(w, device=dev)
+    lens = torch.tensor([int(x) for x in lens_np], dtype=torch.int32, device=dev)
+    tl = torch.full((w.batch,), tail, dtype=torch.int32, device=dev)
+    tail_cap = 256
+    base_v = api.MSECache.empty(w.batch, w.kv_heads, w.context, w.v_bits, device=dev)
+    api.quantize_mse(vc, v, base_v, count=lens)
+    k16 = k.to(torch.float16)
+    kt = k16[:, :, w.context - tail_cap:].contiguous()
+    vt = v[:, :, w.context - tail_cap:].to(torch.float16).contiguous()
+    del k, v
+    torch.cuda.synchronize()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = k16.numel() * 2 + base_v.nbytes() + kt.numel() * 4
+    copies = max(3, math.ceil(3 * l2 / per_copy))
+    sets = [(k16, base_v, kt, vt)] + [
+        (k16.clone(), api.MSECache(base_v.idx.clone(), base_v.xnorm.clone(), w.v_bits), kt.clone(),
+         vt.clone()) for _ in range(copies - 1)]
+    steps_q = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, int(max(lens_np)), w.in_dtype,
+                          w.out_dtype, device=dev, tail_capacity=tail_cap)
+    out = plan.new_out(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, q=None, stream=stream):
+        kk, vv, ktt, vtt = sets[i % copies]
+        plan.run_asym(vc, steps_q[i % 4] if q is None else q, kk, vv, lens, ktt, vtt, tl, out,
+                      stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cap):
+        cs = torch.cuda.current_stream(dev)
+        for i in range(args.steps):
+            step(i, stream=cs)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms_per_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, ws, dev)
+    value = n_tok * ws / (ms_per_step * 1e-3)
+    from kv_cache_quantization_gb300 import _binding as Bn
+    dec_bytes = (w.kv_heads * (int(sum(lens_np)) * (256 + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
+                               + w.batch * tail * 512)
+                 + w.batch * w.q_heads * 128 * (2 + torch.finfo(w.out_dtype).bits // 8))
+    peak, peak_kind = read_peaks()
+    achieved = dec_bytes / (ms_per_step * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get(args.workload)
+        except Exception:
+            traffic = None
+    # end to end: the query from pinned host memory in, the output back, every step
+    q_host = [steps_q[i].cpu().pin_memory() for i in range(4)]
+    q_dev = torch.empty_like(steps_q[0])
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0.record(stream)
+    for i in range(args.steps):
+        q_dev.copy_(q_host[i % 4], non_blocking=True)
+        step(i, q_dev)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 queries, fp16 keys, 4-bit value codes / fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded N(0,1) x lognormal(0,0.5) per channel)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
+                   "kv_heads": w.kv_heads, "head_dim": 128, "context": w.context,
+                   "tokens_attended": n_tok, "k_bits": 0, "v_bits": w.v_bits, "tail": tail,
+                   "parallelism": f"replicas x{ws} (independent batches)",
+                   "l2": f"{copies} rotating copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
+                   "step": "decode attention over the compressed part and the FP16 tail",
+                   "timing": "CUDA-graph replay of the K steps, CUDA events around it"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "tq_decode_attention_asym (split decode + merge)",
+                     "algorithmic_bytes": dec_bytes, "ms": ms_per_step, "peak_source": peak_kind},
+        "e2e": {"value": n_tok * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": q_dev.numel() * q_dev.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ the CPU oracle
 
 class OracleSample:
@@ -336,14 +464,25 @@ class OracleSample:
         q = synth.make_queries(w, device="cpu")[:, :, 0]
         sp, ss = layer_seeds(w.layer)
         self.pi, self.s = o.rotation_from_gaussian(gaussian_matrix(sp)), gaussian_matrix(ss)
-        self.ck = o.lloyd_max_codebook(128, w.k_bits - 1)[0]
+        self.ck = o.lloyd_max_codebook(128, w.k_bits - 1)[0] if w.k_bits else None
         self.cv = o.lloyd_max_codebook(128, w.v_bits)[0]
         self.kx = k[0, 0].double().numpy()
         self.vx = v[0, 0].double().numpy()
         self.q = q[0:1, :w.group].double().numpy()
+        if not w.k_bits:
+            # asymmetric: FP16 keys, and an FP16 tail of w.tail tokens after the sample
+            kt, vt = synth.make_kv(w, device="cpu", tokens=max(w.tail, 1))
+            self.kx = k[0, 0].to(torch_f16()).double().numpy()
+            self.kt = kt[0:1, 0:1].to(torch_f16()).double().numpy()
+            self.vt = vt[0:1, 0:1].to(torch_f16()).double().numpy()
 
     def rep(self):
         o = self.o
+        if self.ck is None:
+            vi, vn, _ = o.quantize_mse(self.vx, self.pi, self.cv)
+            o.decode_attention_asym(self.q, self.kx[None, None], {"idx": vi[None, None], "n": vn[None, None]},
+                                    [self.n], self.kt, self.vt, [self.w.tail], self.pi, self.cv)
+            return
         kq = o.quantize_prod(self.kx, self.pi, self.s, self.ck)
         vi, vn, _ = o.quantize_mse(self.vx, self.pi, self.cv)
         o.decode_attention(self.q, {k: kq[k][None, None] for k in ("idx", "sign", "n", "gamma")},
@@ -352,11 +491,12 @@ class OracleSample:
 
     def tokens_per_s(self, seconds_per_rep):
         """KV tokens/s of a whole step equivalent: one of kv_heads heads per repetition."""
-        return self.n / (seconds_per_rep * self.w.kv_heads)
+        return (self.n + (0 if self.ck is not None else self.w.tail)) / (seconds_per_rep * self.w.kv_heads)
 
     def describe(self, reps, el):
+        what = "quantise K/V + attention" if self.ck is not None else "quantise V + attention with FP16 keys and tail"
         return (f"1 of {self.w.kv_heads} KV heads (its {self.w.group} query heads), {self.n} of "
-                f"{self.w.context} tokens; quantise K/V + attention; {reps} reps in {el:.1f} s")
+                f"{self.w.context} tokens; {what}; {reps} reps in {el:.1f} s")
 
 
 def oracle_baseline(w, budget_s=15.0):
@@ -372,6 +512,11 @@ def oracle_baseline(w, budget_s=15.0):
             break
     return {"value": smp.tokens_per_s(el / reps), "unit": UNIT, "cores": _blas_threads(),
             "kind": "oracle", "sample": smp.describe(reps, el)}
+
+
+def torch_f16():
+    import torch
+    return torch.float16
 
 
 def _blas_threads():
