@@ -573,6 +573,10 @@ extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq
     m.vc_unscale = vc->ibits == 4 ? 1.f / vc->lut_scale : 1.f;
     m.seq_lens = seq_lens;
     m.part = a.part;
+    const long long units = (long long)desc->batch * desc->kv_heads;
+    if ((st = tq_asym_encode_rows(&m.kmap, k_f16, units * desc->capacity)) != TQ_OK) return st;
+    if ((st = tq_asym_encode_rows(&m.ktmap, k_tail, units * desc->tail_capacity)) != TQ_OK) return st;
+    if ((st = tq_asym_encode_rows(&m.vtmap, v_tail, units * desc->tail_capacity)) != TQ_OK) return st;
     st = tq_launch_decode_asym_tc(m, stream);   // split decode (mma.sync), then the merge
     if (st != TQ_OK) return st;
   } else {

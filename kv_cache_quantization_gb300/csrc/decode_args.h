@@ -2,6 +2,7 @@
 // attention.cu.  Internal to the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "tq_internal.h"
@@ -64,6 +65,9 @@ void tq_tc_operand_scales(const tq_plane_decomp& kd, float* s_idx, float* s_sgn)
 // MSE-coded values and an FP16 tail; one record per (batch, KV head, split) in the layout of
 // the CUDA-core path's merge kernel, which runs after it.
 struct tq_asym_launch {
+  // TMA descriptors (128-byte swizzle, boxes of 64 columns × 128 rows) of the FP16 keys
+  // [B·Hkv·cap][128] and of the tail's keys and values [B·Hkv·tail_cap][128]
+  CUtensorMap kmap, ktmap, vtmap;
   int B, Hq, Hkv, G, cap, tail_cap;
   int nsplit_main, nsplit, split_len, tail_split;
   float scale_log2;            // softmax scale × log2(e)
@@ -84,4 +88,6 @@ struct tq_asym_launch {
 };
 
 bool tq_asym_tc_supported(int vbits, int G, int split_len, int tail_split);
+// TMA descriptor of an FP16 row-major matrix [rows][128] for the asymmetric kernel.
+tq_status tq_asym_encode_rows(CUtensorMap* map, const void* base, long long rows);
 tq_status tq_launch_decode_asym_tc(const tq_asym_launch& a, cudaStream_t stream);

@@ -3,10 +3,10 @@
 // dense models; its quick start's min_compress_tokens tail).
 //
 // One CTA per (batch, KV head, split); splits past the compressed part cover the FP16 tail.
-// A producer warp streams 128-token tiles into a 4-stage ring: the FP16 key rows with 16-byte
-// cp.async copies into an XOR-swizzled layout (16-byte chunk c of token t at chunk c ^ (t & 7),
-// so that ldmatrix reads 8 rows without bank conflicts), the value codes and norms with bulk
-// copies.  Eight softmax warps in two groups of four take alternate tiles; a warp scores its 32
+// A producer warp streams 128-token tiles into a 4-stage ring: the FP16 key rows by TMA tensor
+// copies (two boxes of 64 columns per tile, 128-byte swizzle: 16-byte chunk c of row t at
+// chunk c ^ (t & 7) of its 128-byte row, so that ldmatrix reads 8 rows without bank
+// conflicts), the value codes and norms by bulk copies.  Eight softmax warps in two groups of four take alternate tiles; a warp scores its 32
 // tokens with mma.sync m16n8k16 against the query held as an fp16 pair (value and rounding
 // residue, per-head power-of-two scale), then runs the online softmax and the value products
 // shared with the packed-key kernel.  Tail tiles take FP16 values through ldmatrix.trans.
@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <string.h>
 
 #include "decode_args.h"
 #include "tc_ptx.h"
@@ -46,38 +47,42 @@ __device__ __forceinline__ float load_elem_any(const void* base, int dtype, long
 // 4-bit pair table
 template <int VB>
 struct AL {
-  static constexpr int krows = 0;                                        // 128 × 256 B
+  static constexpr int krows = 0;                      // two 64-column halves of 128 × 128 B
   static constexpr int vcodes = kTile * 256;
   static constexpr int vcode_bytes = VB == 4 ? kTile * 64 : VB * kTile * 16;
   static constexpr int vxn = vcodes + 8192;                              // room for 4-bit codes
-  static constexpr int stage = vxn + kTile * 4;
+  static constexpr int stage = vxn + 1024;             // a multiple of 1024 (swizzle atoms)
   static constexpr int ring = kStages * stage;
   static constexpr int lut = ring;
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
-  static constexpr int total = lut + lut_bytes;
+  static constexpr int total = lut + lut_bytes + 1024;  // + alignment of the base to 1024
+  static_assert(stage % 1024 == 0, "stage alignment");
   // after the main loop the ring holds the softmax warps' accumulators and statistics
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
   static_assert(vcode_bytes <= 8192, "value codes");
   static_assert(comb_stats + (kSWarps * 4 + 3) * 8 * 4 <= ring, "combine scratch");
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
-               : "memory");
+// TMA tensor copy of the box at (column x, row y) into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(s32(bar))
+      : "memory");
 }
-// arrive on `bar` once every cp.async this thread issued so far has landed
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(s32(bar)) : "memory");
-}
-// byte offset of 16-byte chunk `ch` of row `t` in a swizzled 128-row × 256-byte tile
+// byte offset of 16-byte chunk `ch` (0..15) of row `t` in a tile of two swizzled 64-column
+// halves (128 rows × 128 B each)
 __device__ __forceinline__ uint32_t swz(int t, int ch) {
-  return (uint32_t)t * 256u + ((uint32_t)(ch ^ (t & 7)) << 4);
+  return (uint32_t)(ch >> 3) * 16384u + (uint32_t)t * 128u + ((uint32_t)((ch & 7) ^ (t & 7)) << 4);
 }
 
 template <int VB, bool HILO>
-__global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const tq_asym_launch a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const __grid_constant__ tq_asym_launch a) {
   using L = AL<VB>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t lut_bar;
@@ -101,11 +106,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const tq_as
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   // the tail's values are FP16 rows: a tile takes two stages (keys, values)
   const int depth = tail ? kStages / 2 : kStages;
-  const __half* K = tail ? a.ktail : a.kf16;
+  const CUtensorMap* kmap = tail ? &a.ktmap : &a.kmap;
 
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
-      mbar_init(&full_bar[st], 33);   // 32 producer lanes (cp.async) + the bulk-copy arrive
+      mbar_init(&full_bar[st], 1);
       mbar_init(&empty_bar[st], kSWarps / 2);
     }
     mbar_init(&lut_bar, 1);
@@ -128,25 +133,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const tq_as
       }
       const int t0 = t_begin + i * kTile;
       unsigned char* kst = smem + (tail ? 2 * slot : slot) * L::stage;
-      const uint32_t kdst = s32(kst + L::krows);
-      // key rows (and the tail's value rows): 16 chunks per token, two tokens per warp step;
-      // rows past the capacity are zero-filled
-      for (int e = lane; e < kTile * 16; e += 32) {
-        const int t = e >> 4, ch = e & 15;
-        const bool in = t0 + t < cap;
-        const long long row = bh * cap + (in ? t0 + t : cap - 1);
-        cp_async16(kdst + swz(t, ch), K + row * TQ_D + ch * 8, in ? 16u : 0u);
-        if (tail)
-          cp_async16(s32(kst + L::stage) + swz(t, ch), a.vtail + row * TQ_D + ch * 8, in ? 16u : 0u);
-      }
-      cp_async_arrive(&full_bar[slot]);
       if (lane == 0) {
+        // key rows (and the tail's value rows) by TMA; rows past the tensor read as zeros
+        const int y = (int)(bh * cap + t0);
+        unsigned bytes = 2u * 16384u;
         if (tail) {
-          mbar_arrive(&full_bar[slot]);
+          bytes += 2u * 16384u;
         } else {
           const int n = min(kTile, a.cap - t0);   // a multiple of 64 (the capacity is)
-          const unsigned bytes = (unsigned)n * ((VB == 4 ? 64 : VB * 16) + 4);
-          mbar_expect_tx(&full_bar[slot], bytes);
+          bytes += (unsigned)n * ((VB == 4 ? 64 : VB * 16) + 4);
+        }
+        mbar_expect_tx(&full_bar[slot], bytes);
+        tma_rows(s32(kst + L::krows), kmap, 0, y, &full_bar[slot]);
+        tma_rows(s32(kst + L::krows + 16384), kmap, 64, y, &full_bar[slot]);
+        if (tail) {
+          tma_rows(s32(kst + L::stage), &a.vtmap, 0, y, &full_bar[slot]);
+          tma_rows(s32(kst + L::stage + 16384), &a.vtmap, 64, y, &full_bar[slot]);
+        } else {
+          const int n = min(kTile, a.cap - t0);
           if (VB == 4) {
             bulk_g2s(kst + L::vcodes, a.vidx + (bh * a.cap + t0) * 64, n * 64, &full_bar[slot]);
           } else {
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const tq_as
           bulk_g2s(kst + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[slot]);
         }
       }
+      __syncwarp();
     }
     // every copy issued lands before the CTA may finish
     for (int k = i - depth > 0 ? i - depth : 0; k < i; ++k)
@@ -396,6 +401,36 @@ tq_status launch_v(const tq_asym_launch& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+tq_status tq_asym_encode_rows(CUtensorMap* map, const void* base, long long rows) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return TQ_ERR_CUDA;
+    encode = reinterpret_cast<Encode>(fn);
+  }
+  if (rows <= 0 || !base) {   // unused (no tail): never read by the kernel
+    memset(map, 0, sizeof(*map));
+    return TQ_OK;
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)TQ_D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)TQ_D * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TQ_OK : TQ_ERR_CUDA;
+}
 
 bool tq_asym_tc_supported(int vbits, int G, int split_len, int tail_split) {
   return vbits >= 1 && vbits <= 4 && G >= 1 && G <= 8 && split_len % kTile == 0 &&
