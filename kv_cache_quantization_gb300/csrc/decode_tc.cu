@@ -332,7 +332,10 @@ struct TL {
   static_assert(2 * 8 * kMaxSplits * 4 <= ring, "merge weights");
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
-  static constexpr int d_cols = NP * kN;
+  // D: index planes summed in pairs by the MMAs (block j = planes 2j, 2j + 1), then the sign
+  // plane's block
+  static constexpr int d_blocks = (NP - 1 + 1) / 2 + 1;
+  static constexpr int d_cols = d_blocks * kN;
   static constexpr int abufs = (2 * a_cols + 2 * d_cols <= 512) ? 2 : 1;
   static constexpr int d_col = abufs * a_cols;
   static_assert(d_col + 2 * d_cols <= 512, "TMEM columns");
@@ -345,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
   constexpr int NVV = VB == 4 ? 0 : num_vplanes(VB);
-  constexpr int NI = NP < kIWarps ? NP : kIWarps;             // active issuer warps
+  constexpr int NI = L::d_blocks;                              // issuer warps: one per D block
+  static_assert(L::d_blocks <= kIWarps, "issuer warps");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -519,20 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     }
   } else if (warp >= kEWarps + kSWarps) {
     // ========================================================== MMA-issue warps
-    // Issuer iw owns planes iw, iw + kIWarps, ...: 4 MMAs of K = 32 per plane and tile,
-    // D[i & 1] column block (plane, piece, column).  The whole warp waits and forms the
-    // (warp-uniform) descriptors; one elected lane issues the MMAs and their commit.
+    // Issuer iw owns D block iw: index planes 2iw and 2iw + 1 accumulated into one block, or
+    // (last block) the sign plane; 4 MMAs of K = 32 per plane and tile, D[i & 1].  The whole
+    // warp waits and forms the (warp-uniform) descriptors; one elected lane issues the MMAs
+    // and their commit.
     const int iw = warp - kEWarps - kSWarps;
     if (iw < NI && ntiles > 0) {
       const uint32_t idesc = idesc_f16(128, kN);   // e4m3 × e4m3 → f32 has the same fields
       const uint32_t frag_s = s32(smem + L::frag);
-      constexpr int kMaxOwn = (NP + kIWarps - 1) / kIWarps;
-      uint64_t bdesc[kMaxOwn][4];
+      const bool sign_blk = iw == NI - 1;
+      const int v0 = sign_blk ? NKV : 2 * iw;
+      const int nv = sign_blk ? 1 : (2 * iw + 1 < NKV ? 2 : 1);
+      uint64_t bdesc[2][4];
 #pragma unroll
-      for (int o = 0; o < kMaxOwn; ++o)
+      for (int o = 0; o < 2; ++o)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          bdesc[o][ks] = smem_desc(frag_s + (iw + o * kIWarps) * kBImg + ks * 256, 128, kBSbo);
+          bdesc[o][ks] = smem_desc(frag_s + (v0 + (o < nv ? o : 0)) * kBImg + ks * 256, 128, kBSbo);
       bool ok = mbar_wait(&prol_bar, 0);
       for (int i = 0; i < ntiles && ok; ++i) {
         const int ab = L::abufs == 2 ? (i & 1) : 0;
@@ -543,14 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         if (!ok) break;
         tc_after();
         if (elect_one()) {
+          const uint32_t d = tmem + L::d_col + db * L::d_cols + iw * kN;
 #pragma unroll
-          for (int o = 0; o < kMaxOwn; ++o) {
-            const int v = iw + o * kIWarps;
-            if (v < NP) {
-              const uint32_t d = tmem + L::d_col + db * L::d_cols + v * kN;
-              const uint32_t a0 = tmem + ab * L::a_cols + 32 * v;
+          for (int o = 0; o < 2; ++o) {
+            if (o < nv) {
+              const uint32_t a0 = tmem + ab * L::a_cols + 32 * (v0 + o);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) mma_f8(d, a0 + 8 * ks, bdesc[o][ks], idesc, ks > 0 ? 1u : 0u);
+              for (int ks = 0; ks < 4; ++ks)
+                mma_f8(d, a0 + 8 * ks, bdesc[o][ks], idesc, (o > 0 || ks > 0) ? 1u : 0u);
             }
           }
           mma_commit(&mma_done[db]);
@@ -607,17 +614,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         for (int e = 0; e < 4; ++e) dm[T][e] = dq[T][e] = 0.f;
         const uint32_t taddr = tmem + L::d_col + db * L::d_cols + lane_base +
                                ((uint32_t)(16 * T) << 16);
+        // two blocks per load (the 16x256b.x8 shape covers 64 columns) where they pair up;
+        // index blocks add into dm, the last (sign) block is dq
+        constexpr int NB = L::d_blocks;
 #pragma unroll
-        for (int v = 0; v < NP; ++v) {
-          uint32_t r[16];
-          tmem_ld_16x256b_x4(taddr + v * kN, r);
+        for (int j0 = 0; j0 < NB; j0 += 2) {
+          uint32_t r[32];
+          if (j0 + 1 < NB) tmem_ld_16x256b_x8(taddr + j0 * kN, r);
+          else tmem_ld_16x256b_x4(taddr + j0 * kN, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float sum = (__uint_as_float(r[e]) + __uint_as_float(r[4 + e])) +
-                              (__uint_as_float(r[8 + e]) + __uint_as_float(r[12 + e]));
-            if (v < NKV) dm[T][e] += sum;
-            else dq[T][e] = sum;
+          for (int u = 0; u < 2; ++u) {
+            const int j = j0 + u;
+            if (j < NB) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t* rr = r + 16 * u;
+                const float sum = (__uint_as_float(rr[e]) + __uint_as_float(rr[4 + e])) +
+                                  (__uint_as_float(rr[8 + e]) + __uint_as_float(rr[12 + e]));
+                if (j < NB - 1) dm[T][e] += sum;
+                else dq[T][e] = sum;
+              }
+            }
           }
         }
       }
