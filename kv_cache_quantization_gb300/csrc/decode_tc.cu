@@ -1100,9 +1100,16 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
     best_n = a0.nsplit;
   }
   tq_mma_launch a = a0;
-  a.nsplit = best_n;
   long long sl = a.max_len > 0 ? (a.max_len + best_n - 1) / best_n : 1;
   sl = (sl + kTile - 1) / kTile * kTile;
+  // splits rounded to whole tiles may cover the context with fewer of them: launch only those
+  // (whole clusters), which leaves SMs to the query-operand kernel running alongside
+  if (a.max_len > 0) {
+    int used = (int)((a.max_len + sl - 1) / sl);
+    used = (used + best_c - 1) / best_c * best_c;
+    if (used < best_n) best_n = used;
+  }
+  a.nsplit = best_n;
   a.split_len = (int)sl;
   query_prep_tc_kernel<KB, HILO><<<dim3(4, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
   cudaLaunchConfig_t cfg = {};
