@@ -373,7 +373,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   // the TMEM addresses derived from it in uniform registers
   const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   const uint32_t rank = cluster_rank(), C = cluster_ctas();
-  const int cid = split / (int)C, nclus = a.nsplit / (int)C;
   int len = a.seq_lens[b];
   if (len > a.cap) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
@@ -383,6 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   const int t_end = min(t_begin + a.split_len, len);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int nstages = (ntiles + 1) / 2;
+  // Without clusters only the splits that hold tokens take part (ragged batches launch many
+  // empty ones): an empty split leaves at once, and a sequence without tokens gets its zero
+  // output from split 0.
+  const int used = C == 1 ? (len + a.split_len - 1) / a.split_len : a.nsplit;
+  if (C == 1 && ntiles == 0) {
+    if (len == 0 && split == 0)
+      for (int i = tid; i < a.G * TQ_D; i += kThreads) {
+        const long long e = ((long long)b * a.Hq + kvh * a.G) * TQ_D + i;
+        if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = 0.f;
+        else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(0.f);
+        else static_cast<__half*>(a.out)[e] = __float2half_rn(0.f);
+      }
+    return;
+  }
+  const int cid = split / (int)C, nclus = used / (int)C;
 
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -839,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   if (warp == 0) tmem_dealloc(tmem, 512);
   {
     const float* mrg = reinterpret_cast<const float*>(smem + L::comb_acc);   // [8][128]
-    float* rec_base = a.part + ((bh * nclus + cid) * a.G) * kRec;
+    float* rec_base = a.part + ((bh * (a.nsplit / (int)C) + cid) * a.G) * kRec;
     const float4* pis = reinterpret_cast<const float4*>(smem + L::pi_off);  // [prow][32]
     for (int c0 = 0, ph = 0; c0 < R; c0 += prow, ph ^= 1) {
       if (c0 > 0) {
@@ -917,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     fence_proxy_async_global();
   }
   named_sync(kBarAll, kCompute);
-  const float* recs = a.part + bh * (long long)nclus * a.G * kRec;
+  const float* recs = a.part + bh * (long long)(a.nsplit / (int)C) * a.G * kRec;
   float* sa = reinterpret_cast<float*>(smem);                          // C == 1: [chunk][G][kRec]
   float* s_w = reinterpret_cast<float*>(smem + L::slots);              // [2][8][kMaxSplits]
   const int chunk = C == 1 ? min(nclus, (int)(L::slots / (a.G * kRec * 4))) : nclus;

@@ -202,7 +202,7 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
     api.quantize_prod(kc, k, kcache, count=lens_t)
     api.quantize_mse(vc, v, vcache, count=lens_t)
     plan = api.DecodePlan(batch, hq, hkv, cap, max(lens), q.dtype, out_dtype)
-    out = plan.new_out()
+    out = plan.new_out().fill_(float("nan"))   # every output element must be written
     plan.run(kc, vc, q, kcache, vcache, lens_t, out)
     got = out.double().cpu().numpy()
     check_flags_clear()
@@ -253,6 +253,17 @@ def test_decode_edge_lengths():
     and plain multi-head attention (G = 1)."""
     run_decode(5, 4, 4, [0, 1, 256, 257, 1024], 3, 4, torch.bfloat16, torch.float32, 500,
                zero_tokens=[(1, 0, 0), (4, 3, 100)])
+
+
+def test_decode_many_ragged_units():
+    """160 (batch, KV head) units, more than half the SMs: several waves of splits without
+    clusters, where splits without tokens leave at once; empty and one-token sequences."""
+    rng = np.random.default_rng(161)
+    lens = [int(x) for x in rng.integers(0, 900, size=40)]
+    lens[3] = lens[17] = 0
+    lens[5] = 1
+    pairs = [(b, h) for b in (0, 3, 5, 17, 22, 39) for h in range(4)]
+    run_decode(40, 8, 4, lens, 3, 4, torch.bfloat16, torch.float32, 650, sample=pairs)
 
 
 def test_decode_group_of_eight():
