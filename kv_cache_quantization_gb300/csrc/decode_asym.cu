@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const __gri
     } else {
       // FP16 values: A = Vᵀ fragments (coordinates × tokens) by ldmatrix.trans of the rows
       float w[2][2][2];
-      online_softmax(lg, okt, nullptr, acc, m_run, l_run, lw_run, w, lane);
+      online_softmax<HILO ? 1 : 2>(lg, okt, nullptr, acc, m_run, l_run, lw_run, w, lane);
       const uint32_t vbase = s32(kst + L::stage);
 #pragma unroll
       for (int T = 0; T < 2; ++T) {
@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_asym_tc_kernel(const __gri
   }
 
   // ============================================================ combine the softmax warps
+  mirror_stats<HILO ? 1 : 2>(m_run, l_run, lw_run);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
 #pragma unroll

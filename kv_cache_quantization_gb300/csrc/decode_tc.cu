@@ -10,12 +10,15 @@
 // becomes NKV "virtual" 0/1 bit planes (XORs of its index bits); with the sign plane that
 // is NP planes, and each score is a sum over planes of ⟨0/1 bits, query vector⟩.  For a tile
 // of 128 tokens (one token per TMEM lane) the expander warps turn every plane into an e4m3
-// A operand in TMEM: a byte is 0x40 (= 2.0) where the bit is set, else 0, produced four
-// coordinates at a time by one shift and one AND.  The query operand B (shared memory)
-// carries each query value as four e4m3 "pieces" at their true scale (x ≈ p0 + p1 + p2 + p3,
-// about 15 significant bits), one B row per (piece, column), so D column (piece, column)
-// sums to the exact fp32 contraction of that piece and the softmax warps add the four.
-// Each plane is a 128 × 32 × 128 product: 4 MMAs of K = 32, issued by one thread per plane.
+// A operand in TMEM with one AND/OR per four coordinates: bit r of every byte of a plane word
+// becomes the byte a_r + b_r·bit (the bit set into the mantissa, exponent or sign of a constant,
+// see expand_c).  The query operand B (shared memory) carries each query value divided by the
+// b_r of its K position as four e4m3 "pieces" at their true scale (y ≈ p0 + p1 + p2 + p3,
+// about 15 significant bits), one B row per (piece, column), so D column (piece, column) sums
+// to the exact fp32 contraction of that piece plus a known constant (Σ a_r·y), and the softmax
+// warps add the pieces and take the constant off.  Each plane is a 128 × N × 128 product: 4 MMAs
+// of K = 32, issued by one thread per D block (N = 32: 8 head columns, or N = 16 for groups of
+// at most 4 heads, each head's four pieces in two column pairs).
 //
 // Softmax and values.  Two groups of four softmax warps take alternate tiles.  A warp reads
 // its 32 tokens' accumulators with the 16x256b TMEM load (register layout of the mma.sync
@@ -54,10 +57,15 @@ constexpr int kIWarps = 3;                    // issue MMAs (one thread each)
 constexpr int kCompute = (kEWarps + kSWarps + kIWarps) * 32;
 constexpr int kThreads = kCompute + 32;       // + producer warp
 constexpr int kPieces = 4;                    // e4m3 pieces per query value
-constexpr int kN = kPieces * 8;               // MMA N: 4 pieces × 8 columns
-constexpr int kBImg = kN * 128;               // one plane's query operand (4 KB of e4m3)
+// MMA N: 4 pieces × 8 head columns, or (group of at most 4 heads) 4 pieces × 4 heads
+__host__ __device__ constexpr int kNof(bool hilo) { return hilo ? 16 : kPieces * 8; }
+// one plane's query operand (4 KB or 2 KB of e4m3)
+__host__ __device__ constexpr int kBImgOf(bool hilo) { return kNof(hilo) * 128; }
 constexpr int kBSbo = 8 * 128;                // 8-row groups of the operand image
-constexpr int kCstBytes = 8 * 4 * 4;          // 8 columns × {A, Cm, B, Cq}
+// score constants: 8 columns × {A, Cm, B, Cq}, then the operand offsets of the 4 slices
+// ([slice][index planes | sign plane][8 columns], see query_prep_tc_kernel)
+constexpr int kCstFloats = 8 * 4;
+constexpr int kCstBytes = (kCstFloats + 4 * 2 * 8) * 4;
 constexpr int kRec = TQ_REC;
 constexpr int kPrepThreads = 256;
 constexpr int kMaxSplits = 256;
@@ -68,8 +76,29 @@ constexpr int kBarS = 2, kBarAll = 3;
 __host__ __device__ constexpr int accidx(int col, int j) { return col * kAccPitch + j + (j >> 4); }
 
 // Bytes of the operand images per (batch, KV head): NP planes + score constants.
-__host__ __device__ constexpr int frag_block(int np) { return np * kBImg + kCstBytes; }
-constexpr int kMaxFragBlock = frag_block(5);
+__host__ __device__ constexpr int frag_block(int np, bool hilo) {
+  return np * kBImgOf(hilo) + kCstBytes;
+}
+constexpr int kMaxFragBlock = frag_block(5, false);
+
+// The expander turns bit r of every byte of a plane word into one e4m3 byte by a single
+// AND/OR: (word & (0x01 << r)) | C_r per byte.  The byte's value is a_r + b_r·bit: the bit
+// lands in the mantissa (r < 3) or the exponent (3 ≤ r < 7) of the constant C_r, or (r = 7)
+// in its sign.  The query operand at such a K position carries (intended value)/b_r, and the
+// constant part Σ a_r·(operand) is taken off with the score constants.
+__host__ __device__ constexpr uint32_t expand_c(int r) {
+  return r == 0 ? 0x48484848u : r == 1 ? 0x40404040u : r == 2 ? 0x38383838u
+       : r == 3 ? 0x30303030u : r == 4 ? 0x28282828u : r == 5 ? 0x18181818u
+       : r == 6 ? 0u : 0x38383838u;
+}
+// a_r and 1/b_r of the expanded byte a_r + b_r·bit
+__host__ __device__ constexpr float expand_a(int r) {
+  return r == 0 ? 4.f : r == 1 ? 2.f : r == 2 ? 1.f : r == 3 ? 0.5f : r == 4 ? 0.25f
+       : r == 5 ? 0.0625f : r == 6 ? 0.f : 1.f;
+}
+__host__ __device__ constexpr float expand_inv_b(int r) {
+  return r <= 3 ? 2.f : r == 4 ? 4.f / 3.f : r == 5 ? 16.f / 15.f : r == 6 ? 0.5f : -0.5f;
+}
 
 // Operand K position k of plane word i (coordinates 32i..32i+31): column c = k / 4 =
 // 8i + r holds coordinates 32i + 8b + r in its bytes b = 0..3.
@@ -79,6 +108,11 @@ __host__ __device__ constexpr int coord_of_k(int k) {
 // canonical K-major offset of byte (row n < 32, k < 128) in one plane's e4m3 operand
 __host__ __device__ constexpr int bimg_off(int n, int k) {
   return (n >> 3) * kBSbo + (k >> 4) * 128 + (n & 7) * 16 + (k & 15);
+}
+// operand row of piece p of column n: p·8 + n, or (4-head layout) rows 2n, 2n + 1, 8 + 2n,
+// 9 + 2n, so that the accumulator-fragment load gives lane (g, c) the four pieces of head c
+__host__ __device__ constexpr int bimg_row(bool hilo, int p, int n) {
+  return hilo ? (p >> 1) * 8 + 2 * n + (p & 1) : p * 8 + n;
 }
 
 // D (TMEM) (+)= A (TMEM, e4m3) · Bᵀ (shared, e4m3), fp32 accumulation
@@ -99,6 +133,13 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) 
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
 }
 
 // true in exactly one lane of the (converged) warp
@@ -188,9 +229,10 @@ __device__ __forceinline__ void cluster_wait_all() {
 // Grid (4 slices, KV heads, batch).  The CTA for slice s computes (Π q_h)_j and (S q_h)_j
 // for the group's heads h and coordinates j = 32s..32s+31 (plane word s), and writes the
 // operand bytes of K positions 32s..32s+31 of every plane: row (piece p, column n) holds
-// piece p of 0.5·coef_v·(Π q)_j/‖q‖·s_idx (index plane v) or 0.5·2·(S q)_j/(‖q‖·smax)·s_sgn
-// (sign plane), column n = head n (G > 4) or head n/2 (G ≤ 4).  ‖q‖ and the column sums
-// (Πᵀ1)·q, (Sᵀ1)·q come straight from q, so no slice needs another slice's results.
+// piece p of coef_v·(Π q)_j/‖q‖·s_idx (index plane v) or 2·(S q)_j/(‖q‖·smax)·s_sgn (sign
+// plane), divided by the b_r of the K position's expanded A byte; column n = head n.  ‖q‖ and
+// the column sums (Πᵀ1)·q, (Sᵀ1)·q come straight from q, so no slice needs another slice's
+// results; each slice writes its share of the operand offsets Σ a_r·(operand).
 template <int KB, bool HILO>
 __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mma_launch a) {
   constexpr int NKV = num_vplanes(KB);
@@ -267,30 +309,60 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
     qs[wh][h][j] = (part[wh][0][h][j] + part[wh][1][h][j]) + (part[wh][2][h][j] + part[wh][3][h][j]);
   }
   __syncthreads();
-  unsigned char* out = static_cast<unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP);
-  // item (plane v, column n, K position k within the slice): four piece bytes
-  for (int i = tid; i < NP * 8 * 32; i += kPrepThreads) {
-    const int v = i >> 8, n = (i >> 5) & 7, kl = i & 31;
+  constexpr int kBImg = kBImgOf(HILO);
+  unsigned char* out = static_cast<unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO);
+  float* cst = reinterpret_cast<float*>(out + NP * kBImg);
+  {
+    // Warp n: column n (head n); lane: K position 32s + lane; plane after plane.  A set bit
+    // must contribute 2x (x: the half-scaled operand value below), and the expanded A byte at
+    // this K position is a_r + b_r·bit, so the operand is y = 2x/b_r, stored as four e4m3
+    // pieces; the warp adds up a_r·(sum of the pieces) over its K positions: the constant the
+    // MMAs add to the column, which the softmax warps take off.
+    const int n = warp, kl = lane;
     const int k = 32 * s + kl;
     const int jl2 = coord_of_k(k) - 32 * s;
-    const int head = HILO ? n >> 1 : n;
-    float x = 0.f;
-    if (head < a.G && s_nq[head] > 0.f) {
-      const float nq = s_nq[head];
-      x = v < NKV ? 0.5f * a.kd.coef[v] * qs[0][head][jl2] / nq * a.s_idx
-                  : qs[1][head][jl2] / (nq * a.smax) * a.s_sgn;
+    const int r = (k >> 2) & 7;
+    const float ar = expand_a(r), ib = expand_inv_b(r);
+    const bool col_ok = !HILO || n < 4;
+    float off_idx = 0.f, off_sgn = 0.f;
+    for (int v = 0; v < NP && col_ok; ++v) {
+      float x = 0.f;
+      if (n < a.G && s_nq[n] > 0.f) {
+        const float nq = s_nq[n];
+        x = v < NKV ? 0.5f * a.kd.coef[v] * qs[0][n][jl2] / nq * a.s_idx
+                    : qs[1][n][jl2] / (nq * a.smax) * a.s_sgn;
+      }
+      float y = 2.f * x * ib, yhat = 0.f;
+#pragma unroll
+      for (int p = 0; p < kPieces; ++p) {
+        const __nv_fp8_storage_t e = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+        const float pv = e4m3_value(e);
+        y -= pv;
+        yhat += pv;
+        out[v * kBImg + bimg_off(bimg_row(HILO, p, n), k)] = e;
+      }
+      if (v < NKV) off_idx = fmaf(ar, yhat, off_idx);
+      else off_sgn = fmaf(ar, yhat, off_sgn);
     }
 #pragma unroll
-    for (int p = 0; p < kPieces; ++p) {
-      const __nv_fp8_storage_t y = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-      x -= e4m3_value(y);
-      out[v * kBImg + bimg_off(p * 8 + n, k)] = y;
+    for (int o = 16; o > 0; o >>= 1) {
+      off_idx += __shfl_xor_sync(0xffffffffu, off_idx, o);
+      off_sgn += __shfl_xor_sync(0xffffffffu, off_sgn, o);
+    }
+    if (lane == 0 && col_ok) {
+      float* offp = cst + kCstFloats + s * 16;   // [index planes | sign plane][8 columns]
+      const int c0 = HILO ? 2 * n : n;
+      offp[c0] = off_idx;
+      offp[8 + c0] = off_sgn;
+      if (HILO) {
+        offp[c0 + 1] = off_idx;
+        offp[8 + c0 + 1] = off_sgn;
+      }
     }
   }
   if (s == 0 && tid < 8) {
     // score constants of column n: A, Cm, B, Cq (see the softmax warps)
     const int n = tid, head = HILO ? n >> 1 : n;
-    float* cst = reinterpret_cast<float*>(out + NP * kBImg);
     const float nq = head < a.G ? s_nq[head] : 0.f;
     const bool ok = nq > 0.f;
     cst[n * 4 + 0] = nq * a.scale_log2 / a.s_idx;
@@ -301,9 +373,10 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
 }
 
 // ---------------------------------------------------------------- shared memory and TMEM
-template <int KB, int VB>
+template <int KB, int VB, bool HILO>
 struct TL {
   static constexpr int NP = num_vplanes(KB) + 1;             // planes incl. the sign plane
+  static constexpr int kN = kNof(HILO);                      // MMA N (D columns per block)
   // one ring stage (256 tokens)
   static constexpr int kplanes = 0;
   static constexpr int ksgn = kplanes + KB * kStageTok * 16;
@@ -317,7 +390,7 @@ struct TL {
   static constexpr int lut = ring;                           // VB == 4: 256 keys × 32 copies
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
   static constexpr int frag = lut + lut_bytes;               // operand images + constants
-  static constexpr int used = frag + frag_block(NP);
+  static constexpr int used = frag + frag_block(NP, HILO);
   // the slots for the per-CTA results of the cluster (up to 4 × (16 + 8·128) floats)
   static constexpr int slots = used;
   static constexpr int total = slots + 4 * (16 + 8 * 128) * 4;
@@ -344,7 +417,9 @@ struct TL {
 // ---------------------------------------------------------------- the split kernel
 template <int KB, int VB, bool HILO>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_launch a) {
-  using L = TL<KB, VB>;
+  using L = TL<KB, VB, HILO>;
+  constexpr int kN = L::kN;
+  constexpr int kBImg = kBImgOf(HILO);
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
   constexpr int NVV = VB == 4 ? 0 : num_vplanes(VB);
@@ -462,9 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       int c = 0;
       for (; c < nstages && c < kStages; ++c) issue(c);
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      mbar_expect_tx(&prol_bar, frag_block(NP) + L::lut_bytes);
-      bulk_g2s(smem + L::frag, static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP),
-               frag_block(NP), &prol_bar);
+      mbar_expect_tx(&prol_bar, frag_block(NP, HILO) + L::lut_bytes);
+      bulk_g2s(smem + L::frag,
+               static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO),
+               frag_block(NP, HILO), &prol_bar);
       if (VB == 4) bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
       for (; c < nstages; ++c) {
         const int st = c % kStages;
@@ -523,10 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 #pragma unroll
           for (int p = 0; p < KB; ++p) pv[p] = pw[p][w4];
           const uint32_t x = v < NKV ? vplane_word<KB>(pv, v) : sw[w4];
-          // column 8·w4 + r: byte b = bit 8b + r of the word, moved to bit 6 (e4m3 2.0)
+          // column 8·w4 + r: byte b = bit 8b + r of the word as the e4m3 byte a_r + b_r·bit
+          // (one AND/OR per four coordinates)
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
-            col[8 * w4 + r] = (r < 7 ? x << (6 - r) : x >> 1) & 0x40404040u;
+          for (int r = 0; r < 8; ++r) col[8 * w4 + r] = (x & (0x01010101u << r)) | expand_c(r);
         }
         tmem_st_32x32b_x32(abase + 32 * v, col);
       }
@@ -594,13 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     float hA[2], hCm[2], hB[2], hCq[2];
     {
       const float* cst = reinterpret_cast<const float*>(smem + L::frag + NP * kBImg);
+      const float* offp = cst + kCstFloats;   // [slice][index planes | sign plane][column]
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int col = 2 * c + k;
         hA[k] = cst[col * 4 + 0];
-        hCm[k] = cst[col * 4 + 1];
+        hCm[k] = cst[col * 4 + 1] + ((offp[col] + offp[16 + col]) + (offp[32 + col] + offp[48 + col]));
         hB[k] = cst[col * 4 + 2];
-        hCq[k] = cst[col * 4 + 3];
+        hCq[k] = cst[col * 4 + 3] +
+                 ((offp[8 + col] + offp[24 + col]) + (offp[40 + col] + offp[56 + col]));
       }
     }
     float acc[8][4];
@@ -620,7 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         break;
       }
       tc_after();
-      // ---- accumulators → per-fragment sums: dm (index planes), dq (sign plane)
+      // ---- accumulators → per-fragment sums: dm (index planes), dq (sign plane).  A block
+      // is kN columns: 4 pieces × 8 head columns (rows g, g + 8 and columns 2c, 2c + 1 in
+      // registers e = 2·row + h), or 4 pieces × 4 heads (head c's pieces in columns 2c, 2c + 1
+      // of the block's two repetitions; sums in e = 0 and 2).
+      constexpr int NH = HILO ? 1 : 2;
+      constexpr int NB = L::d_blocks;
+      constexpr int RPB = kN / 8;              // 16x256b repetitions per block
+      constexpr int NREP = NB * RPB;
       float dm[2][4], dq[2][4];
 #pragma unroll
       for (int T = 0; T < 2; ++T) {
@@ -628,26 +713,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         for (int e = 0; e < 4; ++e) dm[T][e] = dq[T][e] = 0.f;
         const uint32_t taddr = tmem + L::d_col + db * L::d_cols + lane_base +
                                ((uint32_t)(16 * T) << 16);
-        // two blocks per load (the 16x256b.x8 shape covers 64 columns) where they pair up;
-        // index blocks add into dm, the last (sign) block is dq
-        constexpr int NB = L::d_blocks;
 #pragma unroll
-        for (int j0 = 0; j0 < NB; j0 += 2) {
+        for (int r0 = 0; r0 < NREP; r0 += 8) {
           uint32_t r[32];
-          if (j0 + 1 < NB) tmem_ld_16x256b_x8(taddr + j0 * kN, r);
-          else tmem_ld_16x256b_x4(taddr + j0 * kN, r);
+          const int nr = NREP - r0 < 8 ? NREP - r0 : 8;
+          if (nr == 8) {
+            tmem_ld_16x256b_x8(taddr + 8 * r0, r);
+          } else {
+            if (nr >= 4) tmem_ld_16x256b_x4(taddr + 8 * r0, r);
+            if (nr == 2 || nr == 6) tmem_ld_16x256b_x2(taddr + 8 * (r0 + nr - 2), r + 4 * (nr - 2));
+          }
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = j0 + u;
-            if (j < NB) {
+          for (int u = 0; u < 8; ++u) {
+            if (u < nr) {
+              const int R = r0 + u, j = R / RPB;
+              float* tgt = j < NB - 1 ? dm[T] : dq[T];
+              const uint32_t* rr = r + 4 * u;
+              if (HILO) {
+                tgt[0] += __uint_as_float(rr[0]) + __uint_as_float(rr[1]);
+                tgt[2] += __uint_as_float(rr[2]) + __uint_as_float(rr[3]);
+              } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint32_t* rr = r + 16 * u;
-                const float sum = (__uint_as_float(rr[e]) + __uint_as_float(rr[4 + e])) +
-                                  (__uint_as_float(rr[8 + e]) + __uint_as_float(rr[12 + e]));
-                if (j < NB - 1) dm[T][e] += sum;
-                else dq[T][e] = sum;
+                for (int e = 0; e < 4; ++e) tgt[e] += __uint_as_float(rr[e]);
               }
             }
           }
@@ -672,11 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
           const bool valid = t_tile + tl < t_end;
           const float xn = kxn[tl], rn = krn[tl];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < NH; ++h) {
             const float sc = xn * hA[h] * (dm[T][2 * k + h] - hCm[h]) +
                              rn * hB[h] * (dq[T][2 * k + h] - hCq[h]);
             lg[T][k][h] = valid ? sc : -INFINITY;
           }
+          if (NH == 1) lg[T][k][1] = lg[T][k][0];
         }
       bool okt[2][2];
 #pragma unroll
@@ -692,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     }
 
     // ---------------------------------------------------------- combine the softmax warps
+    mirror_stats<HILO ? 1 : 2>(m_run, l_run, lw_run);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -1050,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 // of 4, 2 or 1 consecutive splits of one (batch, KV head).
 template <int KB, int VB, bool HILO>
 tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
-  constexpr int smem = TL<KB, VB>::total;
+  constexpr int smem = TL<KB, VB, HILO>::total;
   auto kern = decode_tc_kernel<KB, VB, HILO>;
   static bool configured[64] = {};
   static int max_ctas[64][3] = {};   // co-resident CTAs with clusters of 1, 2, 4
@@ -1171,14 +1261,15 @@ size_t tq_tc_frag_bytes_max() { return (size_t)kMaxFragBlock; }
 
 // Power-of-two scales of the query operand: the largest index-plane value is at most
 // 0.5·max|coef| (|(Π q)_j| ≤ ‖q‖), the largest sign-plane value at most 1 (|(S q)_j| ≤
-// smax·‖q‖); each scale puts that bound in [224, 448), inside the e4m3 range.
+// smax·‖q‖); the operand holds twice them divided by b_r (|1/b_r| ≤ 2, see expand_inv_b), so
+// each scale puts four times the bound in [224, 448), inside the e4m3 range.
 void tq_tc_operand_scales(const tq_plane_decomp& kd, float* s_idx, float* s_sgn) {
   float m = 0.f;
   for (int v = 0; v < kd.n; ++v) m = fmaxf(m, 0.5f * fabsf(kd.coef[v]));
   int e = 0;
   frexpf(448.f / (m > 0.f ? m : 1.f), &e);   // 448/m = f·2^e, f in [0.5, 1)
-  *s_idx = ldexpf(1.f, e - 1);
-  *s_sgn = 256.f;
+  *s_idx = ldexpf(1.f, e - 3);
+  *s_sgn = 64.f;
 }
 
 tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream) {

@@ -93,7 +93,10 @@ __device__ __forceinline__ float ex2(float x) {
 // Online softmax over the fragments.  lg: base-2 logits; ok: the token is valid; vxn: the 32
 // tokens' value norms (index 16T + g + 8k), or null for plain values (norm 1).  Updates the
 // running maximum and sums (l: Σ p, lw: Σ p·‖v‖), rescales acc when the maximum grows, and
-// returns the value weights w = p·‖v‖ (exactly 0 for invalid tokens).
+// returns the value weights w = p·‖v‖ (exactly 0 for invalid tokens).  NH = 2: the lane's two
+// columns are two heads; NH = 1: both columns are the same head (its weight split into an fp16
+// pair for the value product), so only column 0 is computed and column 1 mirrors it.
+template <int NH>
 __device__ __forceinline__ void online_softmax(const float (&lg)[2][2][2], const bool (&ok)[2][2],
                                                const float* vxn, float (&acc)[8][4],
                                                float (&m_run)[2], float (&l_run)[2],
@@ -104,14 +107,14 @@ __device__ __forceinline__ void online_softmax(const float (&lg)[2][2][2], const
   // is rare: the common tile skips the shuffles.
   bool grow = false;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     const float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
     grow |= m > m_run[h];
   }
   if (__any_sync(0xffffffffu, grow)) {
     float mt[2], corr[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       float m = fmaxf(fmaxf(lg[0][0][h], lg[0][1][h]), fmaxf(lg[1][0][h], lg[1][1][h]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
@@ -122,6 +125,7 @@ __device__ __forceinline__ void online_softmax(const float (&lg)[2][2][2], const
       lw_run[h] *= corr[h];
       m_run[h] = mt[h];
     }
+    if (NH == 1) corr[1] = corr[0];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       acc[k][0] *= corr[0];
@@ -139,13 +143,25 @@ __device__ __forceinline__ void online_softmax(const float (&lg)[2][2][2], const
       const bool valid = ok[T][k];
       const float vn = vxn ? vxn[16 * T + g + 8 * k] : 1.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NH; ++h) {
         const float pr = valid ? ex2(lg[T][k][h] - m_run[h]) : 0.f;
         l_run[h] += pr;
         w[T][k][h] = valid ? pr * vn : 0.f;
         lw_run[h] += w[T][k][h];
       }
+      if (NH == 1) w[T][k][1] = w[T][k][0];
     }
+}
+
+// After the last tile: with NH = 1 the second column's statistics are the first's.
+template <int NH>
+__device__ __forceinline__ void mirror_stats(float (&m_run)[2], float (&l_run)[2],
+                                             float (&lw_run)[2]) {
+  if (NH == 1) {
+    m_run[1] = m_run[0];
+    l_run[1] = l_run[0];
+    lw_run[1] = lw_run[0];
+  }
 }
 
 // Values from codes: acc[coord][column] += Σ_t A[coord][t]·w[t][column].  vrows: the 32 tokens'
@@ -256,7 +272,7 @@ __device__ __forceinline__ void softmax_values_step(const float (&lg)[2][2][2], 
                                                     float (&m_run)[2], float (&l_run)[2],
                                                     float (&lw_run)[2], int lane) {
   float w[2][2][2];
-  online_softmax(lg, ok, vxn, acc, m_run, l_run, lw_run, w, lane);
+  online_softmax<HILO ? 1 : 2>(lg, ok, vxn, acc, m_run, l_run, lw_run, w, lane);
   values_from_codes<VB, HILO>(w, vrows, plane_stride, lut_lane, vcoef, acc, lane);
 }
 
