@@ -26,14 +26,12 @@
 // mma.sync m16n8k16 (4-bit codes through a pair table of fp16 levels, 1–3-bit codes as planes).
 //
 // Data path.  A producer warp streams 256-token stages of packed K/V through a 4-deep
-// shared-memory ring with bulk copies (TMA engine).  The splits of one (batch, KV head) run as
-// thread-block clusters of up to 4 CTAs, which build the query operand together at the start
-// (each computes a quarter of Π q and S q and stores its bytes into every CTA of the cluster
-// through distributed shared memory) while the ring fills.  At the end each CTA sends its
-// (m, l, acc) per head to every CTA of its cluster; every CTA merges the cluster's results and
-// rotates back its quarter of the output coordinates into the cluster's record.  The last CTA
-// of a (batch, KV head) to finish (a ticket counter in the workspace) adds up the records with
-// log-sum-exp weights.
+// shared-memory ring with bulk copies (TMA engine).  The query operand comes from a small
+// kernel that runs first (this grid's programmatic-launch primary) while the ring fills.
+// At the end each split writes its record (m, l, acc[128] per head, still in the rotated
+// domain) to the workspace and takes a ticket; the last split of a (batch, KV head) copies the
+// records and Π into shared memory, adds up the records with log-sum-exp weights and rotates
+// the sum back once (out = Πᵀ·acc / L).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -62,12 +60,11 @@ __host__ __device__ constexpr int kNof(bool hilo) { return hilo ? 16 : kPieces *
 // one plane's query operand (4 KB or 2 KB of e4m3)
 __host__ __device__ constexpr int kBImgOf(bool hilo) { return kNof(hilo) * 128; }
 constexpr int kBSbo = 8 * 128;                // 8-row groups of the operand image
-// score constants: 8 columns × {A, Cm, B, Cq}, then the operand offsets of the 4 slices
-// ([slice][index planes | sign plane][8 columns], see query_prep_tc_kernel)
+// score constants: 8 columns × {A, Cm, B, Cq}, then the operand offsets
+// ([16 slices][index planes | sign plane][8 columns], see query_prep_tc_kernel)
 constexpr int kCstFloats = 8 * 4;
-constexpr int kCstBytes = (kCstFloats + 4 * 2 * 8) * 4;
+constexpr int kCstBytes = (kCstFloats + 16 * 2 * 8) * 4;
 constexpr int kRec = TQ_REC;
-constexpr int kPrepThreads = 256;
 constexpr int kMaxSplits = 256;
 constexpr int kAccPitch = 140;
 // named barriers
@@ -155,132 +152,68 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
 }
 
-// ---------------------------------------------------------------- cluster helpers
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_ctas() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// the shared::cluster address of the same shared-memory offset in CTA `rank`
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void fence_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-// arrive on the mbarrier at `saddr` in CTA `rank`, ordering this thread's earlier writes
-__device__ __forceinline__ void arrive_remote(uint32_t saddr, uint32_t rank) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   map_rank(saddr, rank))
-               : "memory");
-}
-// bounded wait with cluster-scope acquire (the phase was completed by arrivals of peers)
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity) {
-  auto try1 = [&]() {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(s32(bar)), "r"(parity), "r"(10000000u)
-        : "memory");
-    return ok != 0;
-  };
-  if (try1()) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (try1()) return true;
-    if (global_ns() - t0 > 20000000ull) return false;
-  }
-}
-// cluster-wide barrier in two halves: every thread of every CTA arrives once (at kernel
-// start, after its mbarriers are initialised) and waits before its first remote mbarrier
-// access, so the barrier's latency hides behind the work in between
-__device__ __forceinline__ void cluster_arrive_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_all() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // ---------------------------------------------------------------- query operand kernel
-// Grid (4 slices, KV heads, batch).  The CTA for slice s computes (Π q_h)_j and (S q_h)_j
-// for the group's heads h and coordinates j = 32s..32s+31 (plane word s), and writes the
-// operand bytes of K positions 32s..32s+31 of every plane: row (piece p, column n) holds
-// piece p of coef_v·(Π q)_j/‖q‖·s_idx (index plane v) or 2·(S q)_j/(‖q‖·smax)·s_sgn (sign
-// plane), divided by the b_r of the K position's expanded A byte; column n = head n.  ‖q‖ and
-// the column sums (Πᵀ1)·q, (Sᵀ1)·q come straight from q, so no slice needs another slice's
-// results; each slice writes its share of the operand offsets Σ a_r·(operand).
+// Grid (kSlices, KV heads, batch), the split kernel's programmatic-launch primary.  The CTA for
+// slice s computes (Π q_h)_j and (S q_h)_j for the group's heads h and the 8 coordinates
+// j = 8s..8s+7, and writes the operand bytes of their K positions k (coord_of_k(k) = j) in
+// every plane: row (piece p, column n) holds piece p of coef_v·(Π q)_j/‖q‖·s_idx (index plane
+// v) or 2·(S q)_j/(‖q‖·smax)·s_sgn (sign plane), divided by the b_r of the K position's
+// expanded A byte; column n = head n.  It also writes its share of the operand offsets
+// Σ a_r·(operand) (the constant the MMAs add to each column) and, slice 0, the score
+// constants.  ‖q‖ and the column sums (Πᵀ1)·q, (Sᵀ1)·q come straight from q, so no slice
+// needs another slice's results.
+constexpr int kSlices = 16;
+constexpr int kPrepThreads = 256;
 template <int KB, bool HILO>
 __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mma_launch a) {
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
-  __shared__ float qf[8][TQ_D];
-  __shared__ float part[2][4][8][32];     // [Π|S][k quarter][head][j in slice]
-  __shared__ float qs[2][8][32];
+  constexpr int kBImg = kBImgOf(HILO);
+  constexpr int NCOL = HILO ? 4 : 8;
+  __shared__ __align__(16) float qf[8][TQ_D];
+  __shared__ float red[2][16][8][8];      // [Π|S][k chunk][j in slice][head]
+  __shared__ float prod[2][8][8];         // [Π|S][j in slice][head]
   __shared__ float s_nq[8], s_uq[8], s_wq[8];
+  __shared__ float s_off[2][8];           // [index planes | sign plane][column]
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the decode grid may start now; it waits for this grid before its first MMA
+  // the split kernel may start now; it waits for this grid before it copies the operand
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // thread (which, k chunk kq, j in slice jl): 8 entries of row j of M (M = Π or S, read from
+  // Mᵀ), requested before the queries are needed
+  const int which = tid >> 7, kq = (tid >> 3) & 15, jl = tid & 7;
+  const int j = 8 * s + jl;
+  const float* T = which ? a.sT : a.piT;
+  float t[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t[k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
   for (int i = tid; i < 8 * TQ_D; i += kPrepThreads) {
-    const int h = i >> 7, j = i & 127;
+    const int h = i >> 7, jq = i & 127;
     float v = 0.f;
     if (h < a.G) {
-      const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + j;
-      if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[e];
+      const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + jq;
+      if (a.q_dtype == TQ_F32) v = __ldg(static_cast<const float*>(a.q) + e);
       else if (a.q_dtype == TQ_BF16)
-        v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.q)[e] << 16);
-      else v = __half2float(__ushort_as_half(static_cast<const uint16_t*>(a.q)[e]));
+        v = __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(a.q) + e) << 16);
+      else v = __half2float(__ushort_as_half(__ldg(static_cast<const unsigned short*>(a.q) + e)));
     }
-    qf[h][j] = v;
+    qf[h][jq] = v;
   }
-  // thread (which, k quarter, j): 32 coalesced loads of Πᵀ or Sᵀ, issued together
-  const int which = tid >> 7, kq = (tid >> 5) & 3, jl = lane;
-  const float* T = which ? a.sT : a.piT;
-  float t[32];
-#pragma unroll
-  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * kq + k) * TQ_D + 32 * s + jl]);
-  float uk[4], wk[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uk[k] = __ldg(&a.u[lane + 32 * k]);
-    wk[k] = __ldg(&a.w[lane + 32 * k]);
-  }
+  if (tid < 16) s_off[tid >> 3][tid & 7] = 0.f;
   __syncthreads();
   if (warp < a.G) {
     // ‖q‖, (Πᵀ1)·q and (Sᵀ1)·q of head `warp`
     float n2 = 0.f, uq = 0.f, wq = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int j = lane + 32 * k;
-      const float x = qf[warp][j];
+      const int jq = lane + 32 * k;
+      const float x = qf[warp][jq];
       n2 = fmaf(x, x, n2);
-      uq = fmaf(uk[k], x, uq);
-      wq = fmaf(wk[k], x, wq);
+      uq = fmaf(__ldg(&a.u[jq]), x, uq);
+      wq = fmaf(__ldg(&a.w[jq]), x, wq);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -296,68 +229,60 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
   }
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    float acc = 0.f;
-    if (h < a.G) {
+    float x = 0.f;
+    if (h < NCOL) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc = fmaf(t[k], qf[h][32 * kq + k], acc);
+      for (int k = 0; k < 8; ++k) x = fmaf(t[k], qf[h][8 * kq + k], x);
     }
-    part[which][kq][h][jl] = acc;
+    red[which][kq][jl][h] = x;
   }
   __syncthreads();
-  for (int i = tid; i < 2 * 8 * 32; i += kPrepThreads) {
-    const int wh = i >> 8, h = (i >> 5) & 7, j = i & 31;
-    qs[wh][h][j] = (part[wh][0][h][j] + part[wh][1][h][j]) + (part[wh][2][h][j] + part[wh][3][h][j]);
+  if (tid < 2 * 8 * 8) {
+    const int wh = tid >> 6, jj = (tid >> 3) & 7, h = tid & 7;
+    float x = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x += red[wh][k][jj][h];
+    prod[wh][jj][h] = x;
   }
   __syncthreads();
-  constexpr int kBImg = kBImgOf(HILO);
   unsigned char* out = static_cast<unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO);
   float* cst = reinterpret_cast<float*>(out + NP * kBImg);
-  {
-    // Warp n: column n (head n); lane: K position 32s + lane; plane after plane.  A set bit
-    // must contribute 2x (x: the half-scaled operand value below), and the expanded A byte at
-    // this K position is a_r + b_r·bit, so the operand is y = 2x/b_r, stored as four e4m3
-    // pieces; the warp adds up a_r·(sum of the pieces) over its K positions: the constant the
-    // MMAs add to the column, which the softmax warps take off.
-    const int n = warp, kl = lane;
-    const int k = 32 * s + kl;
-    const int jl2 = coord_of_k(k) - 32 * s;
-    const int r = (k >> 2) & 7;
-    const float ar = expand_a(r), ib = expand_inv_b(r);
-    const bool col_ok = !HILO || n < 4;
-    float off_idx = 0.f, off_sgn = 0.f;
-    for (int v = 0; v < NP && col_ok; ++v) {
-      float x = 0.f;
-      if (n < a.G && s_nq[n] > 0.f) {
-        const float nq = s_nq[n];
-        x = v < NKV ? 0.5f * a.kd.coef[v] * qs[0][n][jl2] / nq * a.s_idx
-                    : qs[1][n][jl2] / (nq * a.smax) * a.s_sgn;
-      }
-      float y = 2.f * x * ib, yhat = 0.f;
+  // item (plane v, column n, j in slice): four piece bytes of K position k
+  for (int it = tid; it < NP * NCOL * 8; it += kPrepThreads) {
+    const int v = it / (NCOL * 8), n = (it / 8) % NCOL, jj = it & 7;
+    const int k = 32 * (s >> 2) + 4 * jj + (s & 3);   // coord_of_k(k) = 8s + jj
+    const int r = jj;                                  // (k >> 2) & 7
+    float x = 0.f;
+    if (n < a.G && s_nq[n] > 0.f) {
+      const float nq = s_nq[n];
+      x = v < NKV ? 0.5f * a.kd.coef[v] * prod[0][jj][n] / nq * a.s_idx
+                  : prod[1][jj][n] / (nq * a.smax) * a.s_sgn;
+    }
+    float y = 2.f * x * expand_inv_b(r), yhat = 0.f;
+    uint32_t e4 = 0u;
 #pragma unroll
-      for (int p = 0; p < kPieces; ++p) {
-        const __nv_fp8_storage_t e = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-        const float pv = e4m3_value(e);
-        y -= pv;
-        yhat += pv;
-        out[v * kBImg + bimg_off(bimg_row(HILO, p, n), k)] = e;
-      }
-      if (v < NKV) off_idx = fmaf(ar, yhat, off_idx);
-      else off_sgn = fmaf(ar, yhat, off_sgn);
+    for (int pc = 0; pc < kPieces; ++pc) {
+      const __nv_fp8_storage_t e = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+      const float pv = e4m3_value(e);
+      y -= pv;
+      yhat += pv;
+      e4 |= (uint32_t)e << (8 * pc);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      off_idx += __shfl_xor_sync(0xffffffffu, off_idx, o);
-      off_sgn += __shfl_xor_sync(0xffffffffu, off_sgn, o);
-    }
-    if (lane == 0 && col_ok) {
-      float* offp = cst + kCstFloats + s * 16;   // [index planes | sign plane][8 columns]
-      const int c0 = HILO ? 2 * n : n;
-      offp[c0] = off_idx;
-      offp[8 + c0] = off_sgn;
-      if (HILO) {
-        offp[c0 + 1] = off_idx;
-        offp[8 + c0 + 1] = off_sgn;
-      }
+    for (int pc = 0; pc < kPieces; ++pc)
+      out[v * kBImg + bimg_off(bimg_row(HILO, pc, n), k)] = (unsigned char)(e4 >> (8 * pc));
+    atomicAdd(&s_off[v < NKV ? 0 : 1][n], expand_a(r) * yhat);
+  }
+  __syncthreads();
+  if (tid < 2 * NCOL) {
+    // this slice's operand offsets: [slice][index planes | sign plane][column]
+    const int kind = tid / NCOL, n = tid % NCOL;
+    float* offp = cst + kCstFloats + s * 16 + kind * 8;
+    if (HILO) {
+      offp[2 * n] = s_off[kind][n];
+      offp[2 * n + 1] = s_off[kind][n];
+    } else {
+      offp[n] = s_off[kind][n];
     }
   }
   if (s == 0 && tid < 8) {
@@ -391,18 +316,20 @@ struct TL {
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
   static constexpr int frag = lut + lut_bytes;               // operand images + constants
   static constexpr int used = frag + frag_block(NP, HILO);
-  // the slots for the per-CTA results of the cluster (up to 4 × (16 + 8·128) floats)
-  static constexpr int slots = used;
-  static constexpr int total = slots + 4 * (16 + 8 * 128) * 4;
-  // after the main loop the ring is reused: softmax-warp accumulators and statistics (later
-  // the merged accumulators [8][128]), then rows of Πᵀ (512 bytes each) for the rotation back;
-  // the last CTA's merge keeps its weights [2][8][kMaxSplits] at the start
+  // after the main loop everything is reused: the softmax warps' accumulators and statistics
+  // (the last CTA's merged accumulators [8][128], merge weights [8][kMaxSplits] and rotation
+  // partials [2][8][128] after them), then Π (64 KB) for the rotation back
   static constexpr int comb_acc = 0;
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
+  static constexpr int mrg_acc = 0;
+  static constexpr int mrg_w = 8 * TQ_D * 4;
+  static constexpr int mrg_part = mrg_w + 8 * kMaxSplits * 4;
   static constexpr int pi_off = (comb_stats + (kSWarps * 4 + 3 + 4) * 8 * 4 + 127) / 128 * 128;
-  static constexpr int pi_rows = (ring - pi_off) / 512 / 32 * 32;   // rows per chunk
-  static_assert(pi_rows >= 32, "rotation rows");
-  static_assert(2 * 8 * kMaxSplits * 4 <= ring, "merge weights");
+  static_assert(mrg_part + 2 * 8 * TQ_D * 4 <= pi_off, "merge scratch");
+  // the last CTA copies the records into [rec_off, total) in chunks of whole splits
+  static constexpr int rec_off = pi_off + TQ_D * TQ_D * 4;
+  static constexpr int rec_min = rec_off + 16 * 8 * TQ_REC * 4;
+  static constexpr int total = used > rec_min ? used : rec_min;
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
   // D: index planes summed in pairs by the MMAs (block j = planes 2j, 2j + 1), then the sign
@@ -431,14 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   __shared__ __align__(8) uint64_t mma_done[2];
   __shared__ __align__(8) uint64_t d_free[2];
   __shared__ __align__(8) uint64_t a_full[2];
-  __shared__ __align__(8) uint64_t prol_bar;   // query operand (and value pair table) landed
-  __shared__ __align__(8) uint64_t comb_bar;   // every CTA's result is in this CTA's slots
-  __shared__ __align__(8) uint64_t pi_bar;     // rows of Πᵀ landed
-  __shared__ __align__(8) uint64_t rec_bar;    // (leader) every CTA of the cluster wrote its record part
-  __shared__ __align__(8) uint64_t last_bar;   // the leader's verdict (s_last) arrived
-  __shared__ __align__(8) uint64_t mrg_bar;    // a chunk of record slices landed
-  __shared__ float s_hM[8], s_hL[8];
-  __shared__ int s_last;
+  __shared__ __align__(8) uint64_t op_bar;     // query operand and constants landed
+  __shared__ __align__(8) uint64_t prol_bar;   // value pair table landed (4-bit values)
+  __shared__ __align__(8) uint64_t pi_bar;     // Π landed (rotation back)
+  __shared__ __align__(8) uint64_t rec_bar;    // a chunk of records landed (last split)
+  __shared__ float s_hL[8];
   __shared__ uint32_t s_tmem;
   __shared__ int s_ticket;
 
@@ -447,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   // the warp index through a shuffle: the compiler then knows it is warp-uniform and keeps
   // the TMEM addresses derived from it in uniform registers
   const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
-  const uint32_t rank = cluster_rank(), C = cluster_ctas();
   int len = a.seq_lens[b];
   if (len > a.cap) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
@@ -457,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   const int t_end = min(t_begin + a.split_len, len);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int nstages = (ntiles + 1) / 2;
-  // Without clusters only the splits that hold tokens take part (ragged batches launch many
-  // empty ones): an empty split leaves at once, and a sequence without tokens gets its zero
-  // output from split 0.
-  const int used = C == 1 ? (len + a.split_len - 1) / a.split_len : a.nsplit;
-  if (C == 1 && ntiles == 0) {
+  // Only the splits that hold tokens take part (ragged batches launch many empty ones): an
+  // empty split leaves at once, and a sequence without tokens gets its zero output from
+  // split 0.
+  const int used = (len + a.split_len - 1) / a.split_len;
+  if (ntiles == 0) {
     if (len == 0 && split == 0)
       for (int i = tid; i < a.G * TQ_D; i += kThreads) {
         const long long e = ((long long)b * a.Hq + kvh * a.G) * TQ_D + i;
@@ -471,7 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       }
     return;
   }
-  const int cid = split / (int)C, nclus = used / (int)C;
 
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -483,28 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       mbar_init(&d_free[i], kSWarps / 2);
       mbar_init(&a_full[i], kEWarps);
     }
+    mbar_init(&op_bar, 1);
     mbar_init(&prol_bar, 1);
-    mbar_init(&comb_bar, C);
     mbar_init(&pi_bar, 1);
-    mbar_init(&rec_bar, C);
-    mbar_init(&last_bar, 1);
-    mbar_init(&mrg_bar, 1);
+    mbar_init(&rec_bar, 1);
     mbar_init_fence();
-    s_ticket = -1;
+    s_ticket = 0;
   }
   if (warp == 0) tmem_alloc(&s_tmem, 512);
   tc_before();
   __syncthreads();
   tc_after();
-  // every CTA of the cluster initialises its barriers before any remote access (the wait half
-  // comes just before the first remote store, at the end of the split)
-  if (C > 1) cluster_arrive_all();
   const uint32_t tmem = s_tmem;
-
-  // output coordinates i0..i0+R of this CTA (the rotation back and the final merge), and the
-  // chunks of prow rows of Πᵀ that the rotation back stages in the ring
-  const int R = TQ_D / (int)C, i0 = (int)rank * R;
-  const int prow = R < L::pi_rows ? R : L::pi_rows;
 
   // ============================================================ producer warp
   if (warp == kEWarps + kSWarps + kIWarps) {
@@ -532,16 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         }
         bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
       };
+      if (VB == 4) {
+        mbar_expect_tx(&prol_bar, L::lut_bytes);
+        bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
+      }
       // the ring fills while the query-operand kernel (this grid's programmatic-launch
       // primary) runs; its output is copied in as soon as that grid has completed
       int c = 0;
       for (; c < nstages && c < kStages; ++c) issue(c);
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      mbar_expect_tx(&prol_bar, frag_block(NP, HILO) + L::lut_bytes);
+      mbar_expect_tx(&op_bar, frag_block(NP, HILO));
       bulk_g2s(smem + L::frag,
                static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO),
-               frag_block(NP, HILO), &prol_bar);
-      if (VB == 4) bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
+               frag_block(NP, HILO), &op_bar);
       for (; c < nstages; ++c) {
         const int st = c % kStages;
         if (!mbar_wait(&empty_bar[st], ((c / kStages) - 1) & 1)) {
@@ -553,9 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       // every copy issued lands before the CTA may finish
       for (int k = c - kStages > 0 ? c - kStages : 0; k < c; ++k)
         mbar_wait(&full_bar[k % kStages], (k / kStages) & 1);
-      mbar_wait(&prol_bar, 0);
+      if (VB == 4) mbar_wait(&prol_bar, 0);
+      mbar_wait(&op_bar, 0);
     }
-    if (C > 1) cluster_wait_all();
     return;
   }
 
@@ -630,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           bdesc[o][ks] = smem_desc(frag_s + (v0 + (o < nv ? o : 0)) * kBImg + ks * 256, 128, kBSbo);
-      bool ok = mbar_wait(&prol_bar, 0);
+      bool ok = mbar_wait(&op_bar, 0);
       for (int i = 0; i < ntiles && ok; ++i) {
         const int ab = L::abufs == 2 ? (i & 1) : 0;
         const int db = i & 1;
@@ -660,12 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   } else {
     // ========================================================== softmax / value warps
     const int sw_ = warp - kEWarps;                       // 0..7
+    const int stid = tid - kEWarps * 32;
     const int q = warp & 3;                               // TMEM lane quadrant
     const int grp = sw_ >> 2;                             // tiles i ≡ grp (mod 2)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int g = lane >> 2, c = lane & 3;
-    // the operand constants (and the cluster's stores into this CTA) are complete
-    bool okp = mbar_wait(&prol_bar, 0);
+    // the query operand and its constants (and the value pair table) have landed
+    bool okp = mbar_wait(&op_bar, 0) && (VB != 4 || mbar_wait(&prol_bar, 0));
     if (!okp) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
     float hA[2], hCm[2], hB[2], hCq[2];
     {
@@ -674,11 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int col = 2 * c + k;
+        float oi = 0.f, os = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < kSlices; ++sl) {
+          oi += offp[sl * 16 + col];
+          os += offp[sl * 16 + 8 + col];
+        }
         hA[k] = cst[col * 4 + 0];
-        hCm[k] = cst[col * 4 + 1] + ((offp[col] + offp[16 + col]) + (offp[32 + col] + offp[48 + col]));
+        hCm[k] = cst[col * 4 + 1] + oi;
         hB[k] = cst[col * 4 + 2];
-        hCq[k] = cst[col * 4 + 3] +
-                 ((offp[8 + col] + offp[24 + col]) + (offp[40 + col] + offp[56 + col]));
+        hCq[k] = cst[col * 4 + 3] + os;
       }
     }
     float acc[8][4];
@@ -791,16 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       }
     }
     named_sync(kBarS, kSWarps * 32);   // every softmax warp is done with the ring: reuse it
-    const int stid = tid - kEWarps * 32;
-    // the first chunk of Πᵀ rows is in flight during the combine
-    if (stid == 0) {
-      mbar_expect_tx(&pi_bar, (unsigned)prow * 512u);
-      bulk_g2s(smem + L::pi_off, a.vpiT + (long long)i0 * TQ_D, (unsigned)prow * 512u, &pi_bar);
-    }
     float* cacc = reinterpret_cast<float*>(smem + L::comb_acc);     // [warp][col][140]
     float* cstat = reinterpret_cast<float*>(smem + L::comb_stats);  // [warp][3][8]
     float* fac = cstat + kSWarps * 3 * 8;                           // [warp][8]
-    float* cML = fac + kSWarps * 8;                                 // M, L, LW [3][8], then [8][4]
+    float* cML = fac + kSWarps * 8;                                 // M, L, LW [3][8]
 #pragma unroll
     for (int k8 = 0; k8 < 8; ++k8) {
 #pragma unroll
@@ -847,13 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       cML[16 + col] = lw;
     }
     named_sync(kBarS, kSWarps * 32);
-    // ---- this CTA's per-head result (M, L, acc[128]) into slot `rank` of every CTA of the
-    // cluster
-    constexpr int kSlot = 16 + 8 * TQ_D;
-    float* slots = reinterpret_cast<float*>(smem + L::slots);  // [C][M[8], L[8], acc[8][128]]
-    const uint32_t slots_s = s32(slots);
-    if (C > 1) cluster_wait_all();   // every peer's barriers are initialised
-    // item (head, 4 coordinates): the combined values, stored as one 16-byte word per CTA
+    // ---- this split's record, in the rotated domain: (M, L, acc[128]) per head; item (head,
+    // 4 coordinates), one 16-byte store
+    float* rec = a.part + ((bh * a.nsplit + split) * a.G) * kRec;
     for (int it = stid; it < a.G * (TQ_D / 4); it += kSWarps * 32) {
       const int head = it >> 5, j0 = 4 * (it & 31);
       const int col = HILO ? 2 * head : head;
@@ -871,190 +782,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         if (VB != 4) acc_j -= a.vd.cst * cML[16 + col];
         v4[e] = acc_j;
       }
-      const uint4 u = make_uint4(__float_as_uint(v4[0]), __float_as_uint(v4[1]),
-                                 __float_as_uint(v4[2]), __float_as_uint(v4[3]));
-      const int off = (int)rank * kSlot + 16 + head * TQ_D + j0;
-      for (uint32_t d = 0; d < C; ++d) {
-        if (d == rank) *reinterpret_cast<uint4*>(slots + off) = u;
-        else st_cluster_v4(map_rank(slots_s + 4u * off, d), u);
-      }
+      *reinterpret_cast<float4*>(rec + head * kRec + 4 + j0) = make_float4(v4[0], v4[1], v4[2], v4[3]);
       if (j0 == 0) {
-        const int o = (int)rank * kSlot + head;
-        for (uint32_t d = 0; d < C; ++d) {
-          if (d == rank) {
-            slots[o] = cML[col];                       // base-2 maximum
-            slots[o + 8] = cML[8 + col];
-          } else {
-            st_cluster_f32(map_rank(slots_s + 4u * o, d), cML[col]);
-            st_cluster_f32(map_rank(slots_s + 4u * (o + 8), d), cML[8 + col]);
-          }
-        }
+        rec[head * kRec + 0] = cML[col];                       // base-2 maximum
+        rec[head * kRec + 1] = cML[8 + col];
       }
-    }
-    if (C > 1) fence_cluster();
-    named_sync(kBarS, kSWarps * 32);
-    if (stid < (int)C) {
-      if (stid == (int)rank) mbar_arrive(&comb_bar);
-      else arrive_remote(s32(&comb_bar), (uint32_t)stid);
-    }
-    // ---- merge the cluster's C results (every CTA does it; they agree bit for bit): weights
-    // per head first, then 4 coordinates per item
-    bool okc = C == 1 ? mbar_wait(&comb_bar, 0) : mbar_wait_cluster(&comb_bar, 0);
-    if (!okc && stid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    float* cw = cML + 24;                                         // [8][4] slot weights
-    if (stid < a.G) {
-      const int head = stid;
-      float M = -INFINITY;
-      for (uint32_t r = 0; r < C; ++r)
-        if (slots[r * kSlot + 8 + head] > 0.f) M = fmaxf(M, slots[r * kSlot + head]);
-      float Ls = 0.f;
-      for (uint32_t r = 0; r < C; ++r) {
-        const float l = slots[r * kSlot + 8 + head];
-        const float wr = (M == -INFINITY || !(l > 0.f)) ? 0.f : exp2f(slots[r * kSlot + head] - M);
-        cw[head * 4 + r] = wr;
-        Ls = fmaf(wr, l, Ls);
-      }
-      s_hM[head] = M;
-      s_hL[head] = Ls;
-    }
-    named_sync(kBarS, kSWarps * 32);
-    float* mrg = reinterpret_cast<float*>(smem + L::comb_acc);   // [8][128], after cacc is read
-    for (int it = stid; it < a.G * (TQ_D / 4); it += kSWarps * 32) {
-      const int head = it >> 5, j0 = 4 * (it & 31);
-      float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (uint32_t r = 0; r < C; ++r) {
-        const float wr = cw[head * 4 + r];
-        const float4 v = *reinterpret_cast<const float4*>(slots + r * kSlot + 16 + head * TQ_D + j0);
-        m4.x = fmaf(wr, v.x, m4.x);
-        m4.y = fmaf(wr, v.y, m4.y);
-        m4.z = fmaf(wr, v.z, m4.z);
-        m4.w = fmaf(wr, v.w, m4.w);
-      }
-      *reinterpret_cast<float4*>(mrg + head * TQ_D + j0) = m4;
     }
   }
 
   // ============================================================ end of the split
-  // every compute warp: rotate back this CTA's output rows of the merged accumulators into the
-  // cluster's record, then the ticket
+  // the records are released at device scope; the split that takes the last ticket of its
+  // (batch, KV head) merges them
   tc_before();
   named_sync(kBarAll, kCompute);
   tc_after();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  {
-    const float* mrg = reinterpret_cast<const float*>(smem + L::comb_acc);   // [8][128]
-    float* rec_base = a.part + ((bh * (a.nsplit / (int)C) + cid) * a.G) * kRec;
-    const float4* pis = reinterpret_cast<const float4*>(smem + L::pi_off);  // [prow][32]
-    for (int c0 = 0, ph = 0; c0 < R; c0 += prow, ph ^= 1) {
-      if (c0 > 0) {
-        named_sync(kBarAll, kCompute);   // the previous chunk is consumed
-        if (tid == 0) {
-          mbar_expect_tx(&pi_bar, (unsigned)prow * 512u);
-          bulk_g2s(smem + L::pi_off, a.vpiT + (long long)(i0 + c0) * TQ_D, (unsigned)prow * 512u,
-                   &pi_bar);
-        }
-      }
-      const bool okp2 = mbar_wait(&pi_bar, (unsigned)ph);
-      if (!okp2 && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-      // task (head, 32-row group) per warp; lane = output row; the j loop starts at a
-      // lane-dependent offset so that the float4 reads of both operands are free of bank
-      // conflicts
-      const int ngrp = prow / 32;
-      for (int task = warp; okp2 && task < a.G * ngrp; task += kCompute / 32) {
-        const int h = task / ngrp, r = (task - h * ngrp) * 32 + lane;
-        const float4* mh = reinterpret_cast<const float4*>(mrg + h * TQ_D);
-        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll 8
-        for (int jj = 0; jj < 32; ++jj) {
-          const int jq = (jj + lane) & 31;
-          const float4 pv = pis[r * 32 + jq];
-          const float4 mv = mh[jq];
-          o0 = fmaf(pv.x, mv.x, o0);
-          o1 = fmaf(pv.y, mv.y, o1);
-          o2 = fmaf(pv.z, mv.z, o2);
-          o3 = fmaf(pv.w, mv.w, o3);
-        }
-        rec_base[h * kRec + 4 + i0 + c0 + r] = (o0 + o1) + (o2 + o3);
-      }
-    }
-    if (rank == 0 && tid < a.G) {
-      rec_base[tid * kRec] = s_hM[tid];
-      rec_base[tid * kRec + 1] = s_hL[tid];
-    }
-  }
-  named_sync(kBarAll, kCompute);
   if (tid == 0) {
-    // this CTA's part of the record is released at device scope; the leader, once every CTA
-    // of the cluster has reported, takes the cluster's ticket and tells the cluster whether
-    // it was the last one of the (batch, KV head)
     fence_gpu();
-    if (rank == 0) mbar_arrive(&rec_bar);
-    else arrive_remote(s32(&rec_bar), 0);
-    bool okt = true;
-    if (rank == 0) {
-      okt = C == 1 ? mbar_wait(&rec_bar, 0) : mbar_wait_cluster(&rec_bar, 0);
-      fence_gpu();
-      const int last = atomicAdd(&a.counters[bh], 1) == nclus - 1 ? 1 : 0;
-      for (uint32_t d = 0; d < C; ++d) {
-        if (d == 0) {
-          s_last = last;
-          mbar_arrive(&last_bar);
-        } else {
-          st_cluster_s32(map_rank(s32(&s_last), d), last);
-          arrive_remote(s32(&last_bar), d);
-        }
-      }
-    }
-    okt = (C == 1 ? mbar_wait(&last_bar, 0) : mbar_wait_cluster(&last_bar, 0)) && okt;
-    if (!okt) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    s_ticket = okt ? s_last : 0;
+    s_ticket = atomicAdd(&a.counters[bh], 1) == used - 1 ? 1 : 0;
+    fence_gpu();
   }
   named_sync(kBarAll, kCompute);
   if (s_ticket != 1) return;
-  // Every record (one per cluster) is rotated back already: out_h = Σ_r w_r·rec_r / Σ_r w_r·L_r
-  // with w_r = 2^(M_r − max M).  CTA `rank` of the last cluster produces output coordinates
-  // i0..i0+R.  Without clusters the records are contiguous and arrive by bulk copy, in chunks
-  // that fit in shared memory; in a cluster each CTA loads its 128-byte slices directly (few
-  // small bulk copies would cost more than they save).  Warp h computes the weights of head h.
+  // out_h = Πᵀ·(Σ_r w_r·acc_r) / Σ_r w_r·L_r with w_r = 2^(M_r − max M).  The records come
+  // into shared memory by bulk copies, in chunks of whole splits; warp h computes the weights
+  // of head h from the records' (M, L) meanwhile.
+  const float* recs = a.part + bh * (long long)a.nsplit * a.G * kRec;
+  float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [8][128]
+  float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [8][kMaxSplits]
+  float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [2][8][128]
+  float* srec = reinterpret_cast<float*>(smem + L::rec_off);    // [chunk][G][kRec]
+  const int rec_bytes = a.G * kRec * 4;
+  const int chunk = (L::total - L::rec_off) / rec_bytes;
+  auto issue_chunk = [&](int r0) {
+    const int n = min(chunk, used - r0);
+    mbar_expect_tx(&rec_bar, (unsigned)(n * rec_bytes));
+    bulk_g2s(srec, recs + (long long)r0 * a.G * kRec, (unsigned)(n * rec_bytes), &rec_bar);
+  };
   if (tid == 0) {
     fence_gpu();
-    fence_proxy_async_global();
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // records → bulk copies
+    // Π for the rotation back (its region is free: the ring's data is consumed and the
+    // operand images are read), then the first chunk of records
+    fence_async_smem();
+    mbar_expect_tx(&pi_bar, TQ_D * TQ_D * 4);
+    bulk_g2s(smem + L::pi_off, a.pi, TQ_D * TQ_D * 4, &pi_bar);
+    issue_chunk(0);
   }
-  named_sync(kBarAll, kCompute);
-  const float* recs = a.part + bh * (long long)(a.nsplit / (int)C) * a.G * kRec;
-  float* sa = reinterpret_cast<float*>(smem);                          // C == 1: [chunk][G][kRec]
-  float* s_w = reinterpret_cast<float*>(smem + L::slots);              // [2][8][kMaxSplits]
-  const int chunk = C == 1 ? min(nclus, (int)(L::slots / (a.G * kRec * 4))) : nclus;
-  auto issue_chunk = [&](int r0) {
-    const int n = min(chunk, nclus - r0);
-    const unsigned bytes = (unsigned)(n * a.G * kRec * 4);
-    mbar_expect_tx(&mrg_bar, bytes);
-    bulk_g2s(sa, recs + (long long)r0 * a.G * kRec, bytes, &mrg_bar);
-  };
-  if (C == 1 && tid == 0) issue_chunk(0);
-  constexpr int kPre = 16;
-  float pv[kPre];
-  const bool slice_item = C > 1 && tid < a.G * R;   // R ≤ 64 here: one item per thread
-  const int sh = slice_item ? tid / R : 0, si = slice_item ? tid - sh * R : 0;
-#pragma unroll
-  for (int r = 0; r < kPre; ++r)
-    pv[r] = (slice_item && r < nclus)
-                ? __ldcg(&recs[((long long)r * a.G + sh) * kRec + 4 + i0 + si]) : 0.f;
   if (warp < a.G) {
-    float mx = -INFINITY;
-#pragma unroll 4
-    for (int r = lane; r < nclus; r += 32) {
+    // every (M, L) of the head requested at once
+    float mv[kMaxSplits / 32], lv[kMaxSplits / 32];
+#pragma unroll
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
+      const int r = lane + 32 * u;
       const long long o = ((long long)r * a.G + warp) * kRec;
-      const float m = __ldcg(&recs[o]), l = __ldcg(&recs[o + 1]);
-      const float mm = l > 0.f ? m : -INFINITY;
-      s_w[warp * kMaxSplits + r] = mm;
-      mx = fmaxf(mx, mm);
-      s_w[(8 + warp) * kMaxSplits + r] = l;
+      mv[u] = r < used ? __ldcg(&recs[o]) : 0.f;
+      lv[u] = r < used ? __ldcg(&recs[o + 1]) : 0.f;
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
+      const int r = lane + 32 * u;
+      if (r < used) {
+        const float mm = lv[u] > 0.f ? mv[u] : -INFINITY;
+        s_w[warp * kMaxSplits + r] = mm;
+        s_w[(8 + warp) * kMaxSplits + r] = lv[u];
+        mx = fmaxf(mx, mm);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float Ls = 0.f;
-    for (int r = lane; r < nclus; r += 32) {
+    for (int r = lane; r < used; r += 32) {
       const float mm = s_w[warp * kMaxSplits + r];
       const float wgt = (mx == -INFINITY || mm == -INFINITY) ? 0.f : exp2f(mm - mx);
       s_w[warp * kMaxSplits + r] = wgt;
@@ -1066,84 +865,98 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   }
   named_sync(kBarAll, kCompute);   // weights ready
   constexpr int kItems = (8 * TQ_D + kCompute - 1) / kCompute;
-  float x[kItems] = {};
-  if (C > 1) {
-    if (slice_item) {
-      const float* wv = s_w + sh * kMaxSplits;
-      float x0 = 0.f, x1 = 0.f;
+  float x[kItems];
 #pragma unroll
-      for (int r = 0; r < kPre; r += 2) {
-        if (r < nclus) x0 = fmaf(wv[r], pv[r], x0);
-        if (r + 1 < nclus) x1 = fmaf(wv[r + 1], pv[r + 1], x1);
+  for (int it = 0; it < kItems; ++it) x[it] = 0.f;
+  for (int r0 = 0, ph = 0; r0 < used; r0 += chunk, ph ^= 1) {
+    const bool okr = mbar_wait(&rec_bar, (unsigned)ph);
+    if (!okr && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    const int n = min(chunk, used - r0);
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int item = tid + it * kCompute;
+      if (okr && item < a.G * TQ_D) {
+        const int h = item >> 7, j = item & 127;
+        const float* wv = s_w + h * kMaxSplits + r0;
+        const float* av = srec + h * kRec + 4 + j;
+        const int step = a.G * kRec;
+        float x0 = 0.f, x1 = 0.f;
+        int r = 0;
+        for (; r + 2 <= n; r += 2) {
+          x0 = fmaf(wv[r], av[r * step], x0);
+          x1 = fmaf(wv[r + 1], av[(r + 1) * step], x1);
+        }
+        if (r < n) x0 = fmaf(wv[r], av[r * step], x0);
+        x[it] += x0 + x1;
       }
-      for (int r0 = kPre; r0 < nclus; r0 += kPre) {   // beyond the prefetched records
-#pragma unroll
-        for (int r = 0; r < kPre; ++r)
-          pv[r] = r0 + r < nclus ? __ldcg(&recs[((long long)(r0 + r) * a.G + sh) * kRec + 4 + i0 + si]) : 0.f;
-#pragma unroll
-        for (int r = 0; r < kPre; ++r)
-          if (r0 + r < nclus) x0 = fmaf(wv[r0 + r], pv[r], x0);
-      }
-      x[0] = x0 + x1;
     }
-  } else {
-    uint32_t mphase = 0;
-    for (int r0 = 0; r0 < nclus; r0 += chunk) {
-      const bool okm = mbar_wait(&mrg_bar, mphase);
-      if (!okm && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-      mphase ^= 1;
-      const int n = min(chunk, nclus - r0);
-#pragma unroll
-      for (int it = 0; it < kItems; ++it) {
-        const int item = tid + it * kCompute;
-        if (item < a.G * TQ_D) {
-          const int h = item >> 7, i = item & 127;
-          const float* wv = s_w + h * kMaxSplits + r0;
-          const float* av = sa + h * kRec + 4 + i;
-          const int step = a.G * kRec;
-          float x0 = 0.f, x1 = 0.f;
-          int r = 0;
-          for (; r + 2 <= n; r += 2) {
-            x0 = fmaf(wv[r], av[r * step], x0);
-            x1 = fmaf(wv[r + 1], av[(r + 1) * step], x1);
-          }
-          if (r < n) x0 = fmaf(wv[r], av[r * step], x0);
-          x[it] += x0 + x1;
-        }
-      }
-      if (r0 + chunk < nclus) {
-        named_sync(kBarAll, kCompute);   // the chunk buffer is consumed
-        if (tid == 0) {
-          fence_async_smem();
-          issue_chunk(r0 + chunk);
-        }
+    if (r0 + chunk < used) {
+      named_sync(kBarAll, kCompute);   // the chunk is consumed
+      if (tid == 0) {
+        fence_async_smem();
+        issue_chunk(r0 + chunk);
       }
     }
   }
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
-    const int item = C > 1 ? (it == 0 && slice_item ? tid : -1) : tid + it * kCompute;
-    if (item >= 0 && item < a.G * R) {
-      const int h = item / R, i = item - h * R;
-      const float Lh = s_hL[h];
-      const float v = Lh > 0.f ? x[it] / Lh : 0.f;
-      const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + i0 + i;
-      if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = v;
-      else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(v);
-      else static_cast<__half*>(a.out)[e] = __float2half_rn(v);
-    }
+    const int item = tid + it * kCompute;
+    if (item < 8 * TQ_D) mrg[item] = item < a.G * TQ_D ? x[it] : 0.f;
   }
-  if (rank == 0 && tid == 0) a.counters[bh] = 0;   // ready for the next call
+  named_sync(kBarAll, kCompute);
+  // rotation back: thread (i, half) adds Π[j][i]·mrg[h][j] over its half of j for every head
+  if (tid < 2 * TQ_D) {
+    const bool okpi = mbar_wait(&pi_bar, 0);
+    if (!okpi) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    const int i = tid & 127, half = tid >> 7;
+    const float* pis = reinterpret_cast<const float*>(smem + L::pi_off);
+    constexpr int NH = HILO ? 4 : 8;               // heads ≥ G have mrg = 0
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (okpi) {
+#pragma unroll 2
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const int j = 64 * half + 4 * j4;
+        const float p0 = pis[j * TQ_D + i], p1 = pis[(j + 1) * TQ_D + i];
+        const float p2 = pis[(j + 2) * TQ_D + i], p3 = pis[(j + 3) * TQ_D + i];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mrg + h * TQ_D + j);
+          o[h] = fmaf(p0, m4.x, o[h]);
+          o[h] = fmaf(p1, m4.y, o[h]);
+          o[h] = fmaf(p2, m4.z, o[h]);
+          o[h] = fmaf(p3, m4.w, o[h]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h) rpart[(half * 8 + h) * TQ_D + i] = o[h];
+  } else if (tid == 2 * TQ_D) {
+    // the other threads need not wait for the copy of Π, but the CTA may not finish before it
+    if (!mbar_wait(&pi_bar, 0)) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+  }
+  named_sync(kBarAll, kCompute);
+  for (int item = tid; item < a.G * TQ_D; item += kCompute) {
+    const int h = item >> 7, i = item & 127;
+    const float Lh = s_hL[h];
+    const float x = rpart[h * TQ_D + i] + rpart[(8 + h) * TQ_D + i];
+    const float v = Lh > 0.f ? x / Lh : 0.f;
+    const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + i;
+    if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = v;
+    else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(v);
+    else static_cast<__half*>(a.out)[e] = __float2half_rn(v);
+  }
+  if (tid == 0) a.counters[bh] = 0;   // ready for the next call
 }
 
-// Cluster size and split count: as many CTAs as can be co-resident (one per SM), in clusters
-// of 4, 2 or 1 consecutive splits of one (batch, KV head).
+// Split count: as many CTAs as can be co-resident (one per SM) when every (batch, KV head)
+// gets at least two, else the plan's splits in several waves; splits are whole tiles and only
+// those that cover the longest sequence are launched.
 template <int KB, int VB, bool HILO>
 tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
   constexpr int smem = TL<KB, VB, HILO>::total;
   auto kern = decode_tc_kernel<KB, VB, HILO>;
   static bool configured[64] = {};
-  static int max_ctas[64][3] = {};   // co-resident CTAs with clusters of 1, 2, 4
+  static int max_ctas[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
   if (!configured[dev]) {
@@ -1152,84 +965,33 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    max_ctas[dev][0] = per_sm * tq_num_sms();
-    for (int k = 1; k < 3; ++k) {
-      const int csz = 1 << k;
-      cudaLaunchConfig_t q = {};
-      q.gridDim = dim3(csz, 1, 1);
-      q.blockDim = dim3(kThreads);
-      q.dynamicSmemBytes = smem;
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = csz;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      q.attrs = at;
-      q.numAttrs = 1;
-      int nclusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &q) != cudaSuccess) nclusters = 0;
-      max_ctas[dev][k] = nclusters * csz;
-    }
-    cudaGetLastError();
+    max_ctas[dev] = per_sm * tq_num_sms();
     configured[dev] = true;
   }
-  // the choice with the shortest estimated critical path: tiles per CTA plus the end of the
-  // split, which costs about three tiles more without clusters and one and a half more with
-  // clusters of two than with clusters of four (each CTA rotates back a smaller share); on a
-  // tie the larger cluster
   const int units = a0.B * a0.Hkv;
-  const long long len = a0.max_len > 0 ? a0.max_len : 1;
-  int best_c = 1, best_n = 1;
-  long long best_cost = -1;
-  for (int k = 0; k < 3; ++k) {
-    const int csz = 1 << k;
-    int ns = max_ctas[dev][k] / units;
-    if (ns > a0.nsplit) ns = a0.nsplit;
-    ns -= ns % csz;
-    if (ns < csz) {
-      if (csz > 1) continue;
-      ns = 1;
-    }
-    const long long tiles = ((len + ns - 1) / ns + kTile - 1) / kTile;
-    const long long cost = 2 * tiles + (csz == 1 ? 6 : csz == 2 ? 3 : 0);
-    if (best_cost < 0 || cost <= best_cost) {
-      best_cost = cost;
-      best_c = csz;
-      best_n = ns;
-    }
-  }
-  if (max_ctas[dev][0] / units < 2 && a0.nsplit > 1) {
-    // fewer SMs than two splits per unit: the plan's splits, in several waves
-    best_c = 1;
-    best_n = a0.nsplit;
-  }
+  int ns = max_ctas[dev] / units;
+  if (ns > a0.nsplit || ns < 2) ns = a0.nsplit;
+  if (ns < 1) ns = 1;
   tq_mma_launch a = a0;
-  long long sl = a.max_len > 0 ? (a.max_len + best_n - 1) / best_n : 1;
+  long long sl = a.max_len > 0 ? (a.max_len + ns - 1) / ns : 1;
   sl = (sl + kTile - 1) / kTile * kTile;
-  // splits rounded to whole tiles may cover the context with fewer of them: launch only those
-  // (whole clusters), which leaves SMs to the query-operand kernel running alongside
   if (a.max_len > 0) {
-    int used = (int)((a.max_len + sl - 1) / sl);
-    used = (used + best_c - 1) / best_c * best_c;
-    if (used < best_n) best_n = used;
+    const int used = (int)((a.max_len + sl - 1) / sl);
+    if (used < ns) ns = used;
   }
-  a.nsplit = best_n;
+  a.nsplit = ns;
   a.split_len = (int)sl;
-  query_prep_tc_kernel<KB, HILO><<<dim3(4, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
+  query_prep_tc_kernel<KB, HILO><<<dim3(kSlices, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.Hkv, a.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = best_c;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = best_c > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TQ_ERR_CUDA;
   return tq_cuda_status(cudaGetLastError());
 }

@@ -270,40 +270,64 @@ def test_decode_group_of_eight():
     run_decode(1, 16, 2, [640], 3, 4, torch.float16, torch.float32, 600)
 
 
-def test_decode_qwen7b_32k():
-    """One decode step, B=1, 28/4 heads, 32768 tokens, K 3-bit prod, V 4-bit MSE, bf16."""
-    w = synth.DECODE_32K
+def run_workload_decode(w, pairs):
+    """A decode workload at its full size, in the configuration the benchmark times (one plan
+    for the whole batch, its longest sequence as the plan's maximum); the oracle checks the
+    listed (batch row, KV head) pairs."""
     kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
     k, v = synth.make_kv(w, device="cuda")
     q = synth.make_queries(w, device="cuda")[:, :, 0]
-    lens = synth.seq_lengths(w)
+    lens = [min(int(x), w.context) for x in synth.seq_lengths(w)]
     kcache = api.ProdCache.empty(w.batch, w.kv_heads, w.context, w.k_bits)
     vcache = api.MSECache.empty(w.batch, w.kv_heads, w.context, w.v_bits)
-    api.quantize_prod(kc, k, kcache)
-    api.quantize_mse(vc, v, vcache)
     lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, w.context, q.dtype, w.out_dtype)
-    out = plan.run(kc, vc, q, kcache, vcache, lens_t, plan.new_out()).double().cpu().numpy()
+    api.quantize_prod(kc, k, kcache, count=lens_t)
+    api.quantize_mse(vc, v, vcache, count=lens_t)
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, max(lens), q.dtype, w.out_dtype)
+    out = plan.new_out().fill_(float("nan"))
+    out = plan.run(kc, vc, q, kcache, vcache, lens_t, out).double().cpu().numpy()
     check_flags_clear()
+    assert not np.isnan(out).any()
     pi, s = oracle_constants()
     ck, cv = oracle_codebook(w.k_bits - 1), oracle_codebook(w.v_bits)
     g = w.group
     stats = CodeStats()
-    for h in range(w.kv_heads):
-        n = int(lens[0])
-        gi, gs, gx, gr = unpack_prod(kcache, 0, h, n, w.k_bits - 1)
-        kcodes = match_prod_codes(k[0, h, :n].double().cpu().numpy(), gi, gs, gx, gr, pi, s, ck, stats)
-        vi, vx = unpack_mse(vcache, 0, h, n, w.v_bits)
-        vcodes = match_mse_codes(v[0, h, :n].double().cpu().numpy(), vi, vx, pi, cv, stats)
+    for b, h in pairs:
+        n = lens[b]
+        gi, gs, gx, gr = unpack_prod(kcache, b, h, n, w.k_bits - 1)
+        kcodes = match_prod_codes(k[b, h, :n].double().cpu().numpy(), gi, gs, gx, gr, pi, s, ck, stats)
+        vi, vx = unpack_mse(vcache, b, h, n, w.v_bits)
+        vcodes = match_mse_codes(v[b, h, :n].double().cpu().numpy(), vi, vx, pi, cv, stats)
         kd = {key: kcodes[key][None, None] for key in ("idx", "sign", "n", "gamma")}
         vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
-        ref = o.decode_attention(q[0:1, h * g:(h + 1) * g].double().cpu().numpy(), kd, vd, [n],
+        ref = o.decode_attention(q[b:b + 1, h * g:(h + 1) * g].double().cpu().numpy(), kd, vd, [n],
                                  pi, s, ck, cv)[0]
-        err = rel_l2(out[0, h * g:(h + 1) * g], ref)
-        assert err < 1e-3, f"kv head {h}: rel L2 {err:.3g}"
+        err = rel_l2(out[b, h * g:(h + 1) * g], ref)
+        assert err < out_tol(w.out_dtype), f"(b={b}, kv head={h}): rel L2 {err:.3g}"
     assert stats.idx_excluded < 1e-4 * stats.coords, stats
     assert stats.sign_excluded < 1e-4 * stats.coords, stats
-    print(f"qwen7b 32k code stats: {stats}")
+    print(f"{w.name} code stats: {stats}")
+
+
+def test_decode_qwen7b_32k():
+    """One decode step, B=1, 28/4 heads, 32768 tokens, K 3-bit prod, V 4-bit MSE, bf16."""
+    run_workload_decode(synth.DECODE_32K, [(0, h) for h in range(4)])
+
+
+def test_decode_longctx_262k():
+    """B=1, 32/8 heads, 262144 tokens, K 3-bit prod (4 outlier channels), V 2-bit MSE: two of
+    the eight KV heads checked against the oracle."""
+    run_workload_decode(synth.LONG_262K, [(0, 0), (0, 5)])
+
+
+def test_decode_serving_ragged_b32():
+    """B=32 ragged 4096–16384 tokens, 28/4 heads, K 4-bit prod, V 4-bit MSE: the longest and
+    the shortest sequences and two others checked against the oracle."""
+    w = synth.SERVE_B32
+    lens = [int(x) for x in synth.seq_lengths(w)]
+    order = np.argsort(lens)
+    pairs = [(int(order[-1]), 0), (int(order[0]), 3), (int(order[len(order) // 2]), 1), (7, 2)]
+    run_workload_decode(w, pairs)
 
 
 # ------------------------------------------------------------------ asymmetric mode
