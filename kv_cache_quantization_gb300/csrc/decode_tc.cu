@@ -152,7 +152,6 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
 }
 
-__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ---------------------------------------------------------------- query operand kernel
 // Grid (kSlices, KV heads, batch), the split kernel's programmatic-launch primary.  The CTA for
@@ -316,20 +315,20 @@ struct TL {
   static constexpr int lut_bytes = VB == 4 ? 256 * 32 * 4 : 0;
   static constexpr int frag = lut + lut_bytes;               // operand images + constants
   static constexpr int used = frag + frag_block(NP, HILO);
-  // after the main loop everything is reused: the softmax warps' accumulators and statistics
-  // (the last CTA's merged accumulators [8][128], merge weights [8][kMaxSplits] and rotation
-  // partials [2][8][128] after them), then Π (64 KB) for the rotation back
+  // after the main loop everything is reused: first the softmax warps' accumulators and
+  // statistics; then, in the split that merges, the merged accumulators [8][128], merge
+  // weights and sums [2][8][kMaxSplits], rotation partials [2][8][128], Π (64 KB) and the
+  // records, copied in chunks of whole splits into [rec_off, total); the dynamic shared memory
+  // is sized so that one chunk holds the records of every split at the usual split counts
   static constexpr int comb_acc = 0;
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
   static constexpr int mrg_acc = 0;
   static constexpr int mrg_w = 8 * TQ_D * 4;
-  static constexpr int mrg_part = mrg_w + 8 * kMaxSplits * 4;
-  static constexpr int pi_off = (comb_stats + (kSWarps * 4 + 3 + 4) * 8 * 4 + 127) / 128 * 128;
-  static_assert(mrg_part + 2 * 8 * TQ_D * 4 <= pi_off, "merge scratch");
-  // the last CTA copies the records into [rec_off, total) in chunks of whole splits
+  static constexpr int mrg_part = mrg_w + 2 * 8 * kMaxSplits * 4;
+  static constexpr int pi_off = mrg_part + 2 * 8 * TQ_D * 4;
   static constexpr int rec_off = pi_off + TQ_D * TQ_D * 4;
-  static constexpr int rec_min = rec_off + 16 * 8 * TQ_REC * 4;
-  static constexpr int total = used > rec_min ? used : rec_min;
+  static constexpr int total = 226 * 1024;
+  static_assert(used <= total && rec_off + 16 * 8 * TQ_REC * 4 <= total, "shared memory");
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
   // D: index planes summed in pairs by the MMAs (block j = planes 2j, 2j + 1), then the sign
@@ -798,9 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   tc_after();
   if (warp == 0) tmem_dealloc(tmem, 512);
   if (tid == 0) {
-    fence_gpu();
-    s_ticket = atomicAdd(&a.counters[bh], 1) == used - 1 ? 1 : 0;
-    fence_gpu();
+    // acquire-release: releases the CTA's records (ordered before by the barrier) and, for
+    // the last split, acquires every other split's
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + bh) : "memory");
+    s_ticket = old == used - 1 ? 1 : 0;
   }
   named_sync(kBarAll, kCompute);
   if (s_ticket != 1) return;
@@ -809,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   // of head h from the records' (M, L) meanwhile.
   const float* recs = a.part + bh * (long long)a.nsplit * a.G * kRec;
   float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [8][128]
-  float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [8][kMaxSplits]
+  float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [2][8][kMaxSplits]
   float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [2][8][128]
   float* srec = reinterpret_cast<float*>(smem + L::rec_off);    // [chunk][G][kRec]
   const int rec_bytes = a.G * kRec * 4;
@@ -820,7 +821,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     bulk_g2s(srec, recs + (long long)r0 * a.G * kRec, (unsigned)(n * rec_bytes), &rec_bar);
   };
   if (tid == 0) {
-    fence_gpu();
     asm volatile("fence.proxy.async.global;" ::: "memory");   // records → bulk copies
     // Π for the rotation back (its region is free: the ring's data is consumed and the
     // operand images are read), then the first chunk of records
