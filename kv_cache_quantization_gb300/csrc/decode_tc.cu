@@ -179,16 +179,19 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the split kernel may start now; it waits for this grid before it copies the operand
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // thread (which, k chunk kq, j in slice jl): 8 entries of row j of M (M = Π or S, read from
-  // Mᵀ), requested before the queries are needed
+  // Mᵀ: the codec's constants), requested at once
   const int which = tid >> 7, kq = (tid >> 3) & 15, jl = tid & 7;
   const int j = 8 * s + jl;
   const float* T = which ? a.sT : a.piT;
   float t[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) t[k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
+  // This grid is a programmatic-launch secondary of the previous kernel in the stream: the
+  // queries (and the cache that the split grid streams before it waits for this grid) may be
+  // that kernel's output, so the split grid may start only once every CTA is past this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = tid; i < 8 * TQ_D; i += kPrepThreads) {
     const int h = i >> 7, jq = i & 127;
     float v = 0.f;
@@ -981,7 +984,20 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
   }
   a.nsplit = ns;
   a.split_len = (int)sl;
-  query_prep_tc_kernel<KB, HILO><<<dim3(kSlices, a.Hkv, a.B), kPrepThreads, 0, stream>>>(a);
+  {
+    // the operand kernel's start overlaps the end of the previous kernel in the stream
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(kSlices, a.Hkv, a.B);
+    pc.blockDim = dim3(kPrepThreads);
+    pc.stream = stream;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&pc, query_prep_tc_kernel<KB, HILO>, a) != cudaSuccess)
+      return TQ_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.Hkv, a.B);
   cfg.blockDim = dim3(kThreads);

@@ -283,12 +283,16 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
   const int t = (int)(i % a.tokens);
   const int bh = (int)(i / a.tokens);
   const int b = bh / a.heads, h = bh % a.heads;
-  // every global input first: the vector, Πᵀ and Mᵀ, the count and the position
-  float vals[8];
-  if (tid < 16) load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
+  // Launched as a programmatic-launch secondary of the previous kernel in the stream: the
+  // codec's constants (Πᵀ, Mᵀ) are requested at once, everything the previous kernel may
+  // produce or read (the vector, the count, the position, the cache) only after it completed.
   float tp[32], tm[32];
   small_load(a.piT, tp, tid);
   if constexpr (kProd) small_load(a.mT, tm, tid);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  float vals[8];
+  if (tid < 16) load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
   const int cnt = a.count ? a.count[b] : a.tokens;
   const int pos = a.pos ? a.pos[b] : 0;
   if (t >= cnt) return;
@@ -381,7 +385,17 @@ tq_status launch(const QuantArgs& a, cudaStream_t stream) {
   if (total == 0) return TQ_OK;
   const int sms = tq_num_sms();
   if (total <= 2LL * (sms > 0 ? sms : 148)) {
-    quantize_small_kernel<kProd><<<(unsigned)total, kSmallThreads, 0, stream>>>(a);
+    // programmatic launch: this kernel's start overlaps the end of the previous one
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)total);
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, quantize_small_kernel<kProd>, a) != cudaSuccess) return TQ_ERR_CUDA;
     return tq_cuda_status(cudaGetLastError());
   }
   const size_t smem = (size_t)(kProd ? 2 : 1) * TQ_D * TQ_D * sizeof(float) +
