@@ -270,6 +270,14 @@ def test_decode_group_of_eight():
     run_decode(1, 16, 2, [640], 3, 4, torch.float16, torch.float32, 600)
 
 
+@pytest.mark.parametrize("hq,hkv,n,vbits", [(16, 2, 20000, 4), (7, 1, 30000, 2)])
+def test_decode_records_in_several_chunks(hq, hkv, n, vbits):
+    """Few (batch, KV head) units and a long context: many splits per sequence (53 of 8 heads,
+    118 of 7 heads), so the merging split brings the records into shared memory in several
+    chunks."""
+    run_decode(1, hq, hkv, [n], 3, vbits, torch.bfloat16, torch.float32, 620 + hq)
+
+
 def run_workload_decode(w, pairs):
     """A decode workload at its full size, in the configuration the benchmark times (one plan
     for the whole batch, its longest sequence as the plan's maximum); the oracle checks the
