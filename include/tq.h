@@ -234,8 +234,9 @@ tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,
  *   with that device current, so make the first call on each device before capturing any
  *   stream.  All calls on a device share the one array: calls that may overlap on the GPU
  *   (different streams without ordering between them) race and must not be issued; calls
- *   ordered on one stream are safe.  The array keeps the previous call's data; nothing in it
- *   needs to start at zero. */
+ *   ordered on one stream are safe.  The array keeps the previous call's data; each call
+ *   first clears the few bytes of it that must start at zero (its split tickets), on its
+ *   stream, then runs. */
 tq_status tq_decode_attention_noalloc(const tq_attn_desc* desc, const tq_codec* kc,
                                       const tq_codec* vc, const void* q, tq_prod_cache k,
                                       tq_mse_cache v, const int32_t* seq_lens, void* out,

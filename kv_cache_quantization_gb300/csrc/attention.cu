@@ -459,6 +459,17 @@ extern "C" size_t tq_decode_workspace_bytes(const tq_attn_desc* desc) {
   return p.bytes;
 }
 
+// Byte range of the workspace that must be zero when a symmetric decode call starts (the
+// split tickets).
+tq_status tq_decode_ticket_span(const tq_attn_desc* desc, size_t* offset, size_t* bytes) {
+  Plan p;
+  const tq_status st = plan(desc, false, &p);
+  if (st != TQ_OK) return st;
+  *offset = p.ctr_off;
+  *bytes = p.bytes - p.ctr_off;
+  return TQ_OK;
+}
+
 extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc,
                                          const tq_codec* vc, const void* q, tq_prod_cache k,
                                          tq_mse_cache v, const int32_t* seq_lens, void* out,

@@ -57,7 +57,16 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_attn_desc* desc, const
     return tq_decode_attention(desc, kc, vc, q, k, v, seq_lens, out, nullptr, 0, stream);
   if (need > kScratchBytes) return TQ_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  const tq_status st = scratch_address(&scratch);
+  tq_status st = scratch_address(&scratch);
   if (st != TQ_OK) return st;
+  // The array keeps the previous call's contents.  The split tickets must start at zero;
+  // every completed call leaves them so, but one that gave up on a wait may not: clear them
+  // (a few bytes, on the call's stream) before every call.
+  size_t off = 0, bytes = 0;
+  st = tq_decode_ticket_span(desc, &off, &bytes);
+  if (st != TQ_OK) return st;
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + off, 0, bytes,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TQ_ERR_CUDA;
   return tq_decode_attention(desc, kc, vc, q, k, v, seq_lens, out, scratch, kScratchBytes, stream);
 }
