@@ -21,9 +21,11 @@
 // image brings them in once per CTA.  Raw activations arrive by per-vector bulk copies
 // (the TMA engine) one tile ahead of the tile being computed.
 //
-// Thread r of the 128-thread CTA owns vector r of the tile (TMEM lane r): it reads its row of
-// D1 / D2, decides indices and signs, builds whole code planes in registers and writes each
-// plane with one 128-bit store.  One CTA per SM, persistent over tiles.
+// Two threads own vector r of the tile (TMEM lane r): thread r of warps 0–3 its coordinates
+// 0–63, the same lane of warps 4–7 (same TMEM lane quadrant) coordinates 64–127.  Each reads
+// its half of the row of D1 / D2, decides indices and signs, builds its half of every code
+// plane in registers and writes it with one 64-bit store; the two halves of ‖ρ‖² meet in
+// shared memory.  One CTA of 256 threads per SM, persistent over tiles.
 #include <cuda_fp16.h>
 
 #include "tc_ptx.h"
@@ -33,7 +35,7 @@ TQ_DEFINE_FLAGS(tq_take_flags_quantize_tc)
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kTileV = 128;                    // vectors per tile (MMA M)
 constexpr int kImg = 128 * 128 * 2;            // one 128×128 fp16 operand image (32 KB)
 constexpr int kLBO = 128;                      // K-adjacent core matrices
@@ -51,7 +53,8 @@ struct QL {
   static constexpr int raw = kProd ? rho_lo + kImg : a + kImg;   // raw vectors of the next tile
   static constexpr int norm = raw + kTileV * kRawPitch;          // float ‖x‖ [128]
   static constexpr int ysc = norm + 4 * kTileV;                  // float D1 → y scale [128]
-  static constexpr int bars = ysc + 4 * kTileV;                  // 3 mbarriers + TMEM slot
+  static constexpr int rr = ysc + 4 * kTileV;                    // float ‖ρ‖² halves [2][128]
+  static constexpr int bars = rr + 2 * 4 * kTileV;               // 3 mbarriers + TMEM slot
   static constexpr int total = bars + 32;
   static constexpr int tmem_cols = kProd ? 256 : 128;
 };
@@ -187,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   float* s_norm = reinterpret_cast<float*>(smem + L::norm);
   float* s_ysc = reinterpret_cast<float*>(smem + L::ysc);
+  float* s_rr = reinterpret_cast<float*>(smem + L::rr);
   uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* bar_x = bar_const + 1;
   uint64_t* bar_mma = bar_const + 2;
@@ -213,7 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
   tc_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t d1 = tmem, d2 = tmem + 128;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  // TMEM lane quadrant (rows 32·quad..) and column half (coordinates 64·half..) of this warp
+  const int quad = warp & 3, half = warp >> 2;
+  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
 
   if (warp == 0 && blockIdx.x < ntiles) {
     if (lane == 0) {
@@ -239,14 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     px ^= 1;
     x_pending = false;
     // ---- raw → X̂ (fp16, per-vector power-of-two scale) and ‖x‖.  Warp w converts vectors
-    // 32w..32w+31, eight at a time: lane (i = lane & 7, g = lane >> 3) takes chunks
+    // 16w..16w+15, eight at a time: lane (i = lane & 7, g = lane >> 3) takes chunks
     // (g + 4j + i) mod 16 of vector i, so that both the staging reads and the canonical
     // writes of a quarter-warp fall in distinct banks.
     {
       const int i = lane & 7, g = lane >> 3;
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
-        const int v = 32 * warp + 8 * pass + i;
+      for (int pass = 0; pass < 2; ++pass) {
+        const int v = 16 * warp + 8 * pass + i;
         const bool valid = v < nvalid;
         uint32_t w[4][4];
 #pragma unroll
@@ -338,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     mma_pending = false;
     tc_after();
 
-    // ---- epilogue 1 (thread r = vector r): index planes, residual, ‖ρ‖
-    const int r = tid;
+    // ---- epilogue 1 (vector r, coordinates 64·half..64·half+63): index planes, residual, ‖ρ‖²
+    const int r = 32 * quad + lane;
     const long long gi = first + r;
     int dst = -1;
     long long bh = 0;
@@ -358,13 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     const float n = s_norm[r];
     const float ysc = s_ysc[r];
     constexpr bool kNib = !kProd && IB == 4;
-    constexpr int kWords = kNib ? 16 : 4 * IB;
+    // this thread's words: nibbles 8 (coordinates 8w'..8w'+7, w' = 8·half + k), or per plane
+    // the two 32-coordinate words of its half
+    constexpr int kWords = kNib ? 8 : 2 * IB;
     uint32_t code[kWords];
 #pragma unroll
     for (int k = 0; k < kWords; ++k) code[k] = 0;
     float rr = 0.f;
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
+    for (int hb = 0; hb < 2; ++hb) {
+      const int blk = 2 * half + hb;
       float dv[32];
       tmem_ld32(d1 + lane_base + 32 * blk, dv);
 #pragma unroll
@@ -373,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
         float level;
         const int q = cell_of<IB>(y, a.lv, level);
         if constexpr (kNib) {
-          code[4 * blk + (e >> 3)] |= (uint32_t)q << (4 * (e & 7));
+          code[4 * hb + (e >> 3)] |= (uint32_t)q << (4 * (e & 7));
         } else {
 #pragma unroll
-          for (int p = 0; p < IB; ++p) code[4 * p + blk] |= (uint32_t)((q >> p) & 1) << e;
+          for (int p = 0; p < IB; ++p) code[2 * p + hb] |= (uint32_t)((q >> p) & 1) << e;
         }
         const float rho = y - level;
         rr = fmaf(rho, rho, rr);
@@ -403,19 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
         }
       }
     }
+    s_rr[half * kTileV + r] = rr;
     if (dst >= 0) {
       if constexpr (kNib) {
-        uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64);
+        uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 32 * half);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 2; ++k)
           dp[k] = make_uint4(code[4 * k], code[4 * k + 1], code[4 * k + 2], code[4 * k + 3]);
       } else {
 #pragma unroll
         for (int p = 0; p < IB; ++p)
-          *reinterpret_cast<uint4*>(a.idx + ((bh * IB + p) * a.capacity + dst) * 16) =
-              make_uint4(code[4 * p], code[4 * p + 1], code[4 * p + 2], code[4 * p + 3]);
+          *reinterpret_cast<uint2*>(a.idx + ((bh * IB + p) * a.capacity + dst) * 16 + 8 * half) =
+              make_uint2(code[2 * p], code[2 * p + 1]);
       }
-      a.xnorm[slot] = n;
+      if (half == 0) a.xnorm[slot] = n;
     }
     if constexpr (kProd) {
       async_proxy_fence();   // ρ̂ (generic writes) → tensor-core reads
@@ -444,19 +454,19 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
       pm ^= 1;
       mma_pending = false;
       tc_after();
-      uint32_t sw[4];
+      uint32_t sw[2];
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int hb = 0; hb < 2; ++hb) {
         float dv[32];
-        tmem_ld32(d2 + lane_base + 32 * blk, dv);
+        tmem_ld32(d2 + lane_base + 32 * (2 * half + hb), dv);
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 32; ++e) word |= (dv[e] >= 0.f ? 1u : 0u) << e;
-        sw[blk] = n > 0.f ? word : 0xffffffffu;   // zero vector: zero residual, all signs +1
+        sw[hb] = n > 0.f ? word : 0xffffffffu;   // zero vector: zero residual, all signs +1
       }
       if (dst >= 0) {
-        *reinterpret_cast<uint4*>(a.sgn + slot * 16) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-        a.rnorm[slot] = n * sqrtf(rr);
+        *reinterpret_cast<uint2*>(a.sgn + slot * 16 + 8 * half) = make_uint2(sw[0], sw[1]);
+        if (half == 0) a.rnorm[slot] = n * sqrtf(s_rr[r] + s_rr[kTileV + r]);
       }
     }
     tc_before();
