@@ -21,11 +21,11 @@
 // image brings them in once per CTA.  Raw activations arrive by per-vector bulk copies
 // (the TMA engine) one tile ahead of the tile being computed.
 //
-// Two threads own vector r of the tile (TMEM lane r): thread r of warps 0–3 its coordinates
-// 0–63, the same lane of warps 4–7 (same TMEM lane quadrant) coordinates 64–127.  Each reads
-// its half of the row of D1 / D2, decides indices and signs, builds its half of every code
-// plane in registers and writes it with one 64-bit store; the two halves of ‖ρ‖² meet in
-// shared memory.  One CTA of 256 threads per SM, persistent over tiles.
+// kParts threads own vector r of the tile (TMEM lane r): lane r % 32 of warps q, q + 4, ...
+// (the same TMEM lane quadrant q = r / 32), part p taking coordinates 128p/kParts onwards.
+// Each reads its part of the row of D1 / D2, decides indices and signs, builds its part of
+// every code plane in registers and writes it with one store; the parts of ‖ρ‖² meet in
+// shared memory.  One CTA of 128·kParts threads per SM, persistent over tiles.
 #include <cuda_fp16.h>
 
 #include "tc_ptx.h"
@@ -35,7 +35,9 @@ TQ_DEFINE_FLAGS(tq_take_flags_quantize_tc)
 
 namespace {
 
-constexpr int kThreads = 256;
+// threads per vector: 2 for the product quantiser (its shared memory holds one more operand
+// pair), 4 for the MSE quantiser
+__host__ __device__ constexpr int parts_of(bool prod) { return prod ? 2 : 4; }
 constexpr int kTileV = 128;                    // vectors per tile (MMA M)
 constexpr int kImg = 128 * 128 * 2;            // one 128×128 fp16 operand image (32 KB)
 constexpr int kLBO = 128;                      // K-adjacent core matrices
@@ -53,8 +55,8 @@ struct QL {
   static constexpr int raw = kProd ? rho_lo + kImg : a + kImg;   // raw vectors of the next tile
   static constexpr int norm = raw + kTileV * kRawPitch;          // float ‖x‖ [128]
   static constexpr int ysc = norm + 4 * kTileV;                  // float D1 → y scale [128]
-  static constexpr int rr = ysc + 4 * kTileV;                    // float ‖ρ‖² halves [2][128]
-  static constexpr int bars = rr + 2 * 4 * kTileV;               // 3 mbarriers + TMEM slot
+  static constexpr int rr = ysc + 4 * kTileV;                    // float ‖ρ‖² parts [2][128]
+  static constexpr int bars = rr + (kProd ? 2 : 0) * 4 * kTileV; // 3 mbarriers + TMEM slot
   static constexpr int total = bars + 32;
   static constexpr int tmem_cols = kProd ? 256 : 128;
 };
@@ -185,8 +187,10 @@ __device__ __forceinline__ int cell_of(float y, const tq_levels& lv, float& leve
 }
 
 template <bool kProd, int IB>
-__global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(TcArgs a) {
   using L = QL<kProd>;
+  constexpr int kParts = parts_of(kProd);
+  constexpr int kBlkPart = 4 / kParts;           // 32-coordinate blocks per thread
   extern __shared__ __align__(128) unsigned char smem[];
   float* s_norm = reinterpret_cast<float*>(smem + L::norm);
   float* s_ysc = reinterpret_cast<float*>(smem + L::ysc);
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
   tc_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t d1 = tmem, d2 = tmem + 128;
-  // TMEM lane quadrant (rows 32·quad..) and column half (coordinates 64·half..) of this warp
+  // TMEM lane quadrant (rows 32·quad..) and coordinate part (blocks kBlkPart·half..) of this
+  // warp
   const int quad = warp & 3, half = warp >> 2;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
 
@@ -245,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     px ^= 1;
     x_pending = false;
     // ---- raw → X̂ (fp16, per-vector power-of-two scale) and ‖x‖.  Warp w converts vectors
-    // 16w..16w+15, eight at a time: lane (i = lane & 7, g = lane >> 3) takes chunks
+    // 32w/kParts.., eight at a time: lane (i = lane & 7, g = lane >> 3) takes chunks
     // (g + 4j + i) mod 16 of vector i, so that both the staging reads and the canonical
     // writes of a quarter-warp fall in distinct banks.
     {
       const int i = lane & 7, g = lane >> 3;
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        const int v = 16 * warp + 8 * pass + i;
+      for (int pass = 0; pass < 4 / kParts; ++pass) {
+        const int v = (32 / kParts) * warp + 8 * pass + i;
         const bool valid = v < nvalid;
         uint32_t w[4][4];
 #pragma unroll
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     mma_pending = false;
     tc_after();
 
-    // ---- epilogue 1 (vector r, coordinates 64·half..64·half+63): index planes, residual, ‖ρ‖²
+    // ---- epilogue 1 (vector r, this thread's coordinate blocks): index planes, residual, ‖ρ‖²
     const int r = 32 * quad + lane;
     const long long gi = first + r;
     int dst = -1;
@@ -364,16 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
     const float n = s_norm[r];
     const float ysc = s_ysc[r];
     constexpr bool kNib = !kProd && IB == 4;
-    // this thread's words: nibbles 8 (coordinates 8w'..8w'+7, w' = 8·half + k), or per plane
-    // the two 32-coordinate words of its half
-    constexpr int kWords = kNib ? 8 : 2 * IB;
+    // this thread's words: its nibble words (8 coordinates each), or per plane its
+    // 32-coordinate words
+    constexpr int kWords = kNib ? 4 * kBlkPart : kBlkPart * IB;
     uint32_t code[kWords];
 #pragma unroll
     for (int k = 0; k < kWords; ++k) code[k] = 0;
     float rr = 0.f;
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      const int blk = 2 * half + hb;
+    for (int hb = 0; hb < kBlkPart; ++hb) {
+      const int blk = kBlkPart * half + hb;
       float dv[32];
       tmem_ld32(d1 + lane_base + 32 * blk, dv);
 #pragma unroll
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
           code[4 * hb + (e >> 3)] |= (uint32_t)q << (4 * (e & 7));
         } else {
 #pragma unroll
-          for (int p = 0; p < IB; ++p) code[2 * p + hb] |= (uint32_t)((q >> p) & 1) << e;
+          for (int p = 0; p < IB; ++p) code[kBlkPart * p + hb] |= (uint32_t)((q >> p) & 1) << e;
         }
         const float rho = y - level;
         rr = fmaf(rho, rho, rr);
@@ -412,18 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
         }
       }
     }
-    s_rr[half * kTileV + r] = rr;
+    if constexpr (kProd) s_rr[half * kTileV + r] = rr;
     if (dst >= 0) {
       if constexpr (kNib) {
-        uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 32 * half);
+        uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 16 * kBlkPart * half);
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < kBlkPart; ++k)
           dp[k] = make_uint4(code[4 * k], code[4 * k + 1], code[4 * k + 2], code[4 * k + 3]);
       } else {
 #pragma unroll
-        for (int p = 0; p < IB; ++p)
-          *reinterpret_cast<uint2*>(a.idx + ((bh * IB + p) * a.capacity + dst) * 16 + 8 * half) =
-              make_uint2(code[2 * p], code[2 * p + 1]);
+        for (int p = 0; p < IB; ++p) {
+          unsigned char* row = a.idx + ((bh * IB + p) * a.capacity + dst) * 16 + 4 * kBlkPart * half;
+          if (kBlkPart == 2) *reinterpret_cast<uint2*>(row) = make_uint2(code[2 * p], code[2 * p + 1]);
+          else *reinterpret_cast<uint32_t*>(row) = code[p];
+        }
       }
       if (half == 0) a.xnorm[slot] = n;
     }
@@ -454,19 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(TcArgs a) {
       pm ^= 1;
       mma_pending = false;
       tc_after();
-      uint32_t sw[2];
+      uint32_t sw[kBlkPart];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
+      for (int hb = 0; hb < kBlkPart; ++hb) {
         float dv[32];
-        tmem_ld32(d2 + lane_base + 32 * (2 * half + hb), dv);
+        tmem_ld32(d2 + lane_base + 32 * (kBlkPart * half + hb), dv);
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 32; ++e) word |= (dv[e] >= 0.f ? 1u : 0u) << e;
         sw[hb] = n > 0.f ? word : 0xffffffffu;   // zero vector: zero residual, all signs +1
       }
       if (dst >= 0) {
-        *reinterpret_cast<uint2*>(a.sgn + slot * 16 + 8 * half) = make_uint2(sw[0], sw[1]);
-        if (half == 0) a.rnorm[slot] = n * sqrtf(s_rr[r] + s_rr[kTileV + r]);
+        unsigned char* srow = a.sgn + slot * 16 + 4 * kBlkPart * half;
+        if (kBlkPart == 2) *reinterpret_cast<uint2*>(srow) = make_uint2(sw[0], sw[kBlkPart - 1]);
+        else *reinterpret_cast<uint32_t*>(srow) = sw[0];
+        if (half == 0) {
+          float rt = 0.f;
+#pragma unroll
+          for (int pp = 0; pp < kParts; ++pp) rt += s_rr[pp * kTileV + r];
+          a.rnorm[slot] = n * sqrtf(rt);
+        }
       }
     }
     tc_before();
@@ -500,7 +514,7 @@ tq_status launch_tc(const TcArgs& a, int grid, cudaStream_t stream) {
       return TQ_ERR_CUDA;
     configured[dev] = true;
   }
-  quantize_tc_kernel<kProd, IB><<<grid, kThreads, QL<kProd>::total, stream>>>(a);
+  quantize_tc_kernel<kProd, IB><<<grid, 128 * parts_of(kProd), QL<kProd>::total, stream>>>(a);
   return tq_cuda_status(cudaGetLastError());
 }
 
