@@ -154,39 +154,50 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
 
 
 // ---------------------------------------------------------------- query operand kernel
-// Grid (kSlices, KV heads, batch), the split kernel's programmatic-launch primary.  The CTA for
-// slice s computes (Π q_h)_j and (S q_h)_j for the group's heads h and the 8 coordinates
-// j = 8s..8s+7, and writes the operand bytes of their K positions k (coord_of_k(k) = j) in
-// every plane: row (piece p, column n) holds piece p of coef_v·(Π q)_j/‖q‖·s_idx (index plane
-// v) or 2·(S q)_j/(‖q‖·smax)·s_sgn (sign plane), divided by the b_r of the K position's
-// expanded A byte; column n = head n.  It also writes its share of the operand offsets
-// Σ a_r·(operand) (the constant the MMAs add to each column) and, slice 0, the score
-// constants.  ‖q‖ and the column sums (Πᵀ1)·q, (Sᵀ1)·q come straight from q, so no slice
-// needs another slice's results.
+// Grid (kSlices / SPC, KV heads, batch), the split kernel's programmatic-launch primary.  The
+// work for slice s (SPC slices a CTA) computes (Π q_h)_j and (S q_h)_j for the group's heads h
+// and the 8 coordinates j = 8s..8s+7, and writes the operand bytes of their K positions k
+// (coord_of_k(k) = j) in every plane: row (piece p, column n) holds piece p of
+// coef_v·(Π q)_j/‖q‖·s_idx (index plane v) or 2·(S q)_j/(‖q‖·smax)·s_sgn (sign plane), divided
+// by the b_r of the K position's expanded A byte; column n = head n.  It also writes the
+// slice's share of the operand offsets Σ a_r·(operand) (the constant the MMAs add to each
+// column) and, slice 0, the score constants.  ‖q‖ and the column sums (Πᵀ1)·q, (Sᵀ1)·q come
+// straight from q, so no slice needs another slice's results.
 constexpr int kSlices = 16;
 constexpr int kPrepThreads = 256;
-template <int KB, bool HILO>
-__global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mma_launch a) {
+// SPC slices per CTA (grid kSlices / SPC × KV heads × batch): one slice a CTA while the grid
+// stays small; large batches take 2 or 4, so that the operand kernel runs in one short wave
+// and frees the SMs for the split grid.
+template <int KB, bool HILO, int SPC>
+__global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
+    query_prep_tc_kernel(const tq_mma_launch a) {
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
   constexpr int kBImg = kBImgOf(HILO);
+  constexpr int kN = kNof(HILO);
   constexpr int NCOL = HILO ? 4 : 8;
+  // SPC = 4: the CTA holds K positions 32·blockIdx.x .. +31 of every operand row whole, so
+  // they are gathered here and leave as 16-byte stores
+  __shared__ __align__(16) unsigned char stage[SPC == 4 ? NP * kN * 32 : 16];
   __shared__ __align__(16) float qf[8][TQ_D];
-  __shared__ float red[2][16][8][8];      // [Π|S][k chunk][j in slice][head]
-  __shared__ float prod[2][8][8];         // [Π|S][j in slice][head]
-  __shared__ float s_nq[8], s_uq[8], s_wq[8];
-  __shared__ float s_off[2][8];           // [index planes | sign plane][column]
-  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  __shared__ float red[SPC][2][16][8][8];   // [slice][Π|S][k chunk][j in slice][head]
+  __shared__ float prod[SPC][2][8][8];      // [slice][Π|S][j in slice][head]
+  __shared__ float s_nq[8], s_inq[8], s_uq[8], s_wq[8];
+  __shared__ float s_off[SPC][2][8];        // [slice][index planes | sign plane][column]
+  const int kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // thread (which, k chunk kq, j in slice jl): 8 entries of row j of M (M = Π or S, read from
-  // Mᵀ: the codec's constants), requested at once
+  // Mᵀ: the codec's constants) for each of its slices, requested at once
   const int which = tid >> 7, kq = (tid >> 3) & 15, jl = tid & 7;
-  const int j = 8 * s + jl;
   const float* T = which ? a.sT : a.piT;
-  float t[8];
+  float t[SPC][8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) t[k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
+  for (int u = 0; u < SPC; ++u) {
+    const int j = 8 * (SPC * (int)blockIdx.x + u) + jl;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[u][k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
+  }
   // This grid is a programmatic-launch secondary of the previous kernel in the stream: the
   // queries (and the cache that the split grid streams before it waits for this grid) may be
   // that kernel's output, so the split grid may start only once every CTA is past this wait.
@@ -204,7 +215,7 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
     }
     qf[h][jq] = v;
   }
-  if (tid < 16) s_off[tid >> 3][tid & 7] = 0.f;
+  if (tid < 8) s_inq[tid] = 0.f;
   __syncthreads();
   if (warp < a.G) {
     // ‖q‖, (Πᵀ1)·q and (Sᵀ1)·q of head `warp`
@@ -224,70 +235,101 @@ __global__ void __launch_bounds__(kPrepThreads) query_prep_tc_kernel(const tq_mm
       wq += __shfl_xor_sync(0xffffffffu, wq, o);
     }
     if (lane == 0) {
-      s_nq[warp] = sqrtf(n2);
+      const float nq = sqrtf(n2);
+      s_nq[warp] = nq;
+      s_inq[warp] = nq > 0.f ? 1.f / nq : 0.f;
       s_uq[warp] = uq;
       s_wq[warp] = wq;
     }
   }
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    float x = 0.f;
-    if (h < NCOL) {
+  for (int u = 0; u < SPC; ++u)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x = fmaf(t[k], qf[h][8 * kq + k], x);
+    for (int h = 0; h < 8; ++h) {
+      float x = 0.f;
+      if (h < NCOL) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x = fmaf(t[u][k], qf[h][8 * kq + k], x);
+      }
+      red[u][which][kq][jl][h] = x;
     }
-    red[which][kq][jl][h] = x;
-  }
   __syncthreads();
-  if (tid < 2 * 8 * 8) {
-    const int wh = tid >> 6, jj = (tid >> 3) & 7, h = tid & 7;
+  for (int it = tid; it < SPC * 2 * 8 * 8; it += kPrepThreads) {
+    const int u = it >> 7, wh = (it >> 6) & 1, jj = (it >> 3) & 7, h = it & 7;
     float x = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) x += red[wh][k][jj][h];
-    prod[wh][jj][h] = x;
+    for (int k = 0; k < 16; ++k) x += red[u][wh][k][jj][h];
+    prod[u][wh][jj][h] = x;
   }
   __syncthreads();
   unsigned char* out = static_cast<unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO);
   float* cst = reinterpret_cast<float*>(out + NP * kBImg);
-  // item (plane v, column n, j in slice): four piece bytes of K position k
-  for (int it = tid; it < NP * NCOL * 8; it += kPrepThreads) {
-    const int v = it / (NCOL * 8), n = (it / 8) % NCOL, jj = it & 7;
+  // item (slice u, column n, j in slice jj), every plane: the four piece bytes of K position k;
+  // the 8 items of a (slice, column) are adjacent lanes and add up its offsets by shuffles
+  // (item counts are multiples of 32: whole warps take part)
+  const float sgn_scale = a.s_sgn / a.smax;
+  for (int it = tid; it < SPC * NCOL * 8; it += kPrepThreads) {
+    const int u = it / (NCOL * 8), n = (it >> 3) % NCOL, jj = it & 7;
+    const int s = SPC * (int)blockIdx.x + u;
     const int k = 32 * (s >> 2) + 4 * jj + (s & 3);   // coord_of_k(k) = 8s + jj
     const int r = jj;                                  // (k >> 2) & 7
-    float x = 0.f;
-    if (n < a.G && s_nq[n] > 0.f) {
-      const float nq = s_nq[n];
-      x = v < NKV ? 0.5f * a.kd.coef[v] * prod[0][jj][n] / nq * a.s_idx
-                  : prod[1][jj][n] / (nq * a.smax) * a.s_sgn;
-    }
-    float y = 2.f * x * expand_inv_b(r), yhat = 0.f;
-    uint32_t e4 = 0u;
+    const float inq = s_inq[n];                        // 1/‖q‖; 0 for a zero or absent head
+    const float xi = 0.5f * a.s_idx * inq * prod[u][0][jj][n];
+    const float xs = sgn_scale * inq * prod[u][1][jj][n];
+    const float ib2 = 2.f * expand_inv_b(r), ar = expand_a(r);
+    float oi = 0.f, os = 0.f;
 #pragma unroll
-    for (int pc = 0; pc < kPieces; ++pc) {
-      const __nv_fp8_storage_t e = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-      const float pv = e4m3_value(e);
-      y -= pv;
-      yhat += pv;
-      e4 |= (uint32_t)e << (8 * pc);
+    for (int v = 0; v < NP; ++v) {
+      float y = ib2 * (v < NKV ? a.kd.coef[v] * xi : xs), yhat = 0.f;
+      uint32_t e4 = 0u;
+#pragma unroll
+      for (int pc = 0; pc < kPieces; ++pc) {
+        const __nv_fp8_storage_t e = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+        const float pv = e4m3_value(e);
+        y -= pv;
+        yhat += pv;
+        e4 |= (uint32_t)e << (8 * pc);
+      }
+#pragma unroll
+      for (int pc = 0; pc < kPieces; ++pc) {
+        const unsigned char byte = (unsigned char)(e4 >> (8 * pc));
+        if constexpr (SPC == 4) stage[(v * kN + bimg_row(HILO, pc, n)) * 32 + 4 * jj + u] = byte;
+        else out[v * kBImg + bimg_off(bimg_row(HILO, pc, n), k)] = byte;
+      }
+      if (v < NKV) oi = fmaf(ar, yhat, oi);
+      else os = fmaf(ar, yhat, os);
     }
 #pragma unroll
-    for (int pc = 0; pc < kPieces; ++pc)
-      out[v * kBImg + bimg_off(bimg_row(HILO, pc, n), k)] = (unsigned char)(e4 >> (8 * pc));
-    atomicAdd(&s_off[v < NKV ? 0 : 1][n], expand_a(r) * yhat);
+    for (int o = 1; o < 8; o <<= 1) {
+      oi += __shfl_xor_sync(0xffffffffu, oi, o);
+      os += __shfl_xor_sync(0xffffffffu, os, o);
+    }
+    if (jj == 0) {
+      s_off[u][0][n] = oi;
+      s_off[u][1][n] = os;
+    }
   }
   __syncthreads();
-  if (tid < 2 * NCOL) {
-    // this slice's operand offsets: [slice][index planes | sign plane][column]
-    const int kind = tid / NCOL, n = tid % NCOL;
-    float* offp = cst + kCstFloats + s * 16 + kind * 8;
-    if (HILO) {
-      offp[2 * n] = s_off[kind][n];
-      offp[2 * n + 1] = s_off[kind][n];
-    } else {
-      offp[n] = s_off[kind][n];
+  if constexpr (SPC == 4) {
+    for (int c = tid; c < NP * kN * 2; c += kPrepThreads) {
+      const int v = c / (kN * 2), row = (c >> 1) % kN, hf = c & 1;
+      *reinterpret_cast<uint4*>(out + v * kBImg + bimg_off(row, 32 * (int)blockIdx.x + 16 * hf)) =
+          *reinterpret_cast<const uint4*>(stage + (v * kN + row) * 32 + 16 * hf);
     }
   }
-  if (s == 0 && tid < 8) {
+  if (tid < SPC * 2 * NCOL) {
+    // the slices' operand offsets: [slice][index planes | sign plane][column]
+    const int u = tid / (2 * NCOL), kind = (tid / NCOL) & 1, n = tid % NCOL;
+    const int s = SPC * (int)blockIdx.x + u;
+    float* offp = cst + kCstFloats + s * 16 + kind * 8;
+    if (HILO) {
+      offp[2 * n] = s_off[u][kind][n];
+      offp[2 * n + 1] = s_off[u][kind][n];
+    } else {
+      offp[n] = s_off[u][kind][n];
+    }
+  }
+  if (blockIdx.x == 0 && tid < 8) {
     // score constants of column n: A, Cm, B, Cq (see the softmax warps)
     const int n = tid, head = HILO ? n >> 1 : n;
     const float nq = head < a.G ? s_nq[head] : 0.f;
@@ -320,9 +362,10 @@ struct TL {
   static constexpr int used = frag + frag_block(NP, HILO);
   // after the main loop everything is reused: first the softmax warps' accumulators and
   // statistics; then, in the split that merges, the merged accumulators [8][128], merge
-  // weights and sums [2][8][kMaxSplits], rotation partials [2][8][128], Π (64 KB) and the
-  // records, copied in chunks of whole splits into [rec_off, total); the dynamic shared memory
-  // is sized so that one chunk holds the records of every split at the usual split counts
+  // weights and sums [2][8][kMaxSplits] (later the rotation's partial sums [3][8][128]), the
+  // merge's partial sums [at most 15][128], Π (64 KB) and the records, copied in chunks of
+  // whole splits into [rec_off, total); the dynamic shared memory is sized so that one chunk
+  // holds the records of every split at the usual split counts
   static constexpr int comb_acc = 0;
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
   static constexpr int mrg_acc = 0;
@@ -367,13 +410,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   __shared__ float s_hL[8];
   __shared__ uint32_t s_tmem;
   __shared__ int s_ticket;
+  __shared__ int s_item;
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const long long bh = (long long)b * a.Hkv + kvh;
   // the warp index through a shuffle: the compiler then knows it is warp-uniform and keeps
   // the TMEM addresses derived from it in uniform registers
   const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
+  // CTAs are dispatched in blockIdx order.  For a batch, the work items (sequence, split) are
+  // taken largest first (ties by index), the KV heads of an item side by side: the long splits
+  // start in the first wave and the short ones fill in behind them (longest-processing-time-
+  // first list scheduling).  The ranking uses the dynamic shared memory, not yet in use.
+  int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int nitems = a.B * (int)gridDim.x;
+  if (a.B > 1 && nitems <= kThreads) {
+    int* sc_len = reinterpret_cast<int*>(smem);
+    int* sc_work = sc_len + kThreads;
+    if (tid < a.B) sc_len[tid] = min(a.seq_lens[tid], a.cap);
+    __syncthreads();
+    if (tid < nitems) {
+      const int ib = tid / (int)gridDim.x, is = tid - ib * (int)gridDim.x;
+      sc_work[tid] = max(0, min(a.split_len, sc_len[ib] - is * a.split_len));
+    }
+    __syncthreads();
+    const int pos = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (tid < nitems) {
+      const int wt = sc_work[tid];
+      int rank = 0;
+      for (int o = 0; o < nitems; ++o) {
+        const int wo = sc_work[o];
+        rank += (wo > wt || (wo == wt && o < tid)) ? 1 : 0;
+      }
+      if (rank == pos / a.Hkv) s_item = tid;
+    }
+    fence_async_smem();   // the scratch is the ring: bulk copies write it next
+    __syncthreads();
+    b = s_item / (int)gridDim.x;
+    split = s_item - b * (int)gridDim.x;
+    kvh = pos % a.Hkv;
+  }
   int len = a.seq_lens[b];
+  const long long bh = (long long)b * a.Hkv + kvh;
   if (len > a.cap) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
     len = a.cap;
@@ -446,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
         }
         bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
       };
+      // Π is read again only by the split that merges: have it in L2 by then
+      if (split == 0) bulk_prefetch_l2(a.pi, TQ_D * TQ_D * 4);
       if (VB == 4) {
         mbar_expect_tx(&prol_bar, L::lut_bytes);
         bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
@@ -814,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   const float* recs = a.part + bh * (long long)a.nsplit * a.G * kRec;
   float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [8][128]
   float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [2][8][kMaxSplits]
-  float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [2][8][128]
+  float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [parts·G][128]
   float* srec = reinterpret_cast<float*>(smem + L::rec_off);    // [chunk][G][kRec]
   const int rec_bytes = a.G * kRec * 4;
   const int chunk = (L::total - L::rec_off) / rec_bytes;
@@ -867,30 +944,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     if (lane == 0) s_hL[warp] = Ls;
   }
   named_sync(kBarAll, kCompute);   // weights ready
-  constexpr int kItems = (8 * TQ_D + kCompute - 1) / kCompute;
-  float x[kItems];
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) x[it] = 0.f;
+  // Warp (part, head) adds up the records r ≡ part (mod parts) of its head, four coordinates
+  // a lane (16-byte shared loads; the weight is one broadcast load per record); the parts'
+  // sums meet in shared memory.
+  const int parts = (kCompute / 32) / a.G;                     // G ≤ 8: at least one
+  const bool mact = warp < parts * a.G;
+  const int mp = warp / a.G, mh = warp - (warp / a.G) * a.G;
+  float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
   for (int r0 = 0, ph = 0; r0 < used; r0 += chunk, ph ^= 1) {
     const bool okr = mbar_wait(&rec_bar, (unsigned)ph);
     if (!okr && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
     const int n = min(chunk, used - r0);
-#pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-      const int item = tid + it * kCompute;
-      if (okr && item < a.G * TQ_D) {
-        const int h = item >> 7, j = item & 127;
-        const float* wv = s_w + h * kMaxSplits + r0;
-        const float* av = srec + h * kRec + 4 + j;
-        const int step = a.G * kRec;
-        float x0 = 0.f, x1 = 0.f;
-        int r = 0;
-        for (; r + 2 <= n; r += 2) {
-          x0 = fmaf(wv[r], av[r * step], x0);
-          x1 = fmaf(wv[r + 1], av[(r + 1) * step], x1);
-        }
-        if (r < n) x0 = fmaf(wv[r], av[r * step], x0);
-        x[it] += x0 + x1;
+    if (okr && mact) {
+      const float* wv = s_w + mh * kMaxSplits + r0;
+      const float4* av = reinterpret_cast<const float4*>(srec + mh * kRec + 4) + lane;
+      const int step4 = a.G * kRec / 4;
+      int r = mp;
+      for (; r + parts < n; r += 2 * parts) {
+        const float w0 = wv[r], w1 = wv[r + parts];
+        const float4 v0 = av[r * step4], v1 = av[(r + parts) * step4];
+        x0.x = fmaf(w0, v0.x, x0.x); x0.y = fmaf(w0, v0.y, x0.y);
+        x0.z = fmaf(w0, v0.z, x0.z); x0.w = fmaf(w0, v0.w, x0.w);
+        x1.x = fmaf(w1, v1.x, x1.x); x1.y = fmaf(w1, v1.y, x1.y);
+        x1.z = fmaf(w1, v1.z, x1.z); x1.w = fmaf(w1, v1.w, x1.w);
+      }
+      if (r < n) {
+        const float w0 = wv[r];
+        const float4 v0 = av[r * step4];
+        x0.x = fmaf(w0, v0.x, x0.x); x0.y = fmaf(w0, v0.y, x0.y);
+        x0.z = fmaf(w0, v0.z, x0.z); x0.w = fmaf(w0, v0.w, x0.w);
       }
     }
     if (r0 + chunk < used) {
@@ -901,24 +983,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       }
     }
   }
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int item = tid + it * kCompute;
-    if (item < 8 * TQ_D) mrg[item] = item < a.G * TQ_D ? x[it] : 0.f;
+  if (mact)
+    reinterpret_cast<float4*>(rpart + (mp * a.G + mh) * TQ_D)[lane] =
+        make_float4(x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w);
+  named_sync(kBarAll, kCompute);
+  for (int item = tid; item < 8 * TQ_D; item += kCompute) {
+    const int h = item >> 7, j = item & 127;
+    float v = 0.f;
+    if (h < a.G)
+      for (int p = 0; p < parts; ++p) v += rpart[(p * a.G + h) * TQ_D + j];
+    mrg[item] = v;
   }
   named_sync(kBarAll, kCompute);
-  // rotation back: thread (i, half) adds Π[j][i]·mrg[h][j] over its half of j for every head
-  if (tid < 2 * TQ_D) {
+  // rotation back: thread (i, part) adds Π[j][i]·mrg[h][j] over its third of j (44, 44 and 40
+  // rows) for every head; the partial sums go where the merge weights were
+  float* rot = s_w;                                             // [3][8][128]
+  if (tid < 3 * TQ_D) {
     const bool okpi = mbar_wait(&pi_bar, 0);
     if (!okpi) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    const int i = tid & 127, half = tid >> 7;
+    const int i = tid & 127, part = tid >> 7;
+    const int jb = 44 * part, nj4 = part == 2 ? 10 : 11;
     const float* pis = reinterpret_cast<const float*>(smem + L::pi_off);
     constexpr int NH = HILO ? 4 : 8;               // heads ≥ G have mrg = 0
     float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (okpi) {
 #pragma unroll 2
-      for (int j4 = 0; j4 < 16; ++j4) {
-        const int j = 64 * half + 4 * j4;
+      for (int j4 = 0; j4 < nj4; ++j4) {
+        const int j = jb + 4 * j4;
         const float p0 = pis[j * TQ_D + i], p1 = pis[(j + 1) * TQ_D + i];
         const float p2 = pis[(j + 2) * TQ_D + i], p3 = pis[(j + 3) * TQ_D + i];
 #pragma unroll
@@ -932,8 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       }
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h) rpart[(half * 8 + h) * TQ_D + i] = o[h];
-  } else if (tid == 2 * TQ_D) {
+    for (int h = 0; h < 8; ++h) rot[(part * 8 + h) * TQ_D + i] = o[h];
+  } else if (tid == 3 * TQ_D) {
     // the other threads need not wait for the copy of Π, but the CTA may not finish before it
     if (!mbar_wait(&pi_bar, 0)) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
   }
@@ -941,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   for (int item = tid; item < a.G * TQ_D; item += kCompute) {
     const int h = item >> 7, i = item & 127;
     const float Lh = s_hL[h];
-    const float x = rpart[h * TQ_D + i] + rpart[(8 + h) * TQ_D + i];
+    const float x = rot[h * TQ_D + i] + rot[(8 + h) * TQ_D + i] + rot[(16 + h) * TQ_D + i];
     const float v = Lh > 0.f ? x / Lh : 0.f;
     const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + i;
     if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = v;
@@ -986,8 +1077,11 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
   a.split_len = (int)sl;
   {
     // the operand kernel's start overlaps the end of the previous kernel in the stream
+    const long long units = (long long)a.B * a.Hkv;
+    const int spc = units * kSlices <= 2LL * tq_num_sms() ? 1
+                    : units * (kSlices / 2) <= 2LL * tq_num_sms() ? 2 : 4;
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(kSlices, a.Hkv, a.B);
+    pc.gridDim = dim3(kSlices / spc, a.Hkv, a.B);
     pc.blockDim = dim3(kPrepThreads);
     pc.stream = stream;
     cudaLaunchAttribute pa[1];
@@ -995,8 +1089,9 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&pc, query_prep_tc_kernel<KB, HILO>, a) != cudaSuccess)
-      return TQ_ERR_CUDA;
+    auto prep = spc == 1 ? query_prep_tc_kernel<KB, HILO, 1>
+                : spc == 2 ? query_prep_tc_kernel<KB, HILO, 2> : query_prep_tc_kernel<KB, HILO, 4>;
+    if (cudaLaunchKernelEx(&pc, prep, a) != cudaSuccess) return TQ_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.Hkv, a.B);

@@ -64,6 +64,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       ::"r"(s32(dst)), "l"(src), "r"(bytes), "r"(s32(bar))
       : "memory");
 }
+// fetch `bytes` (a multiple of 16, 16-byte aligned source) into L2 without waiting
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // generic-proxy shared-memory writes → later async-proxy (tensor core / bulk copy) accesses
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
