@@ -198,6 +198,13 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
 #pragma unroll
     for (int k = 0; k < 8; ++k) t[u][k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
   }
+  // the column sums Πᵀ1 and Sᵀ1 at the lane's coordinates (for the norm warps)
+  float cu[4], cw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    cu[k] = __ldg(&a.u[lane + 32 * k]);
+    cw[k] = __ldg(&a.w[lane + 32 * k]);
+  }
   // This grid is a programmatic-launch secondary of the previous kernel in the stream: the
   // queries (and the cache that the split grid streams before it waits for this grid) may be
   // that kernel's output, so the split grid may start only once every CTA is past this wait.
@@ -225,8 +232,8 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
       const int jq = lane + 32 * k;
       const float x = qf[warp][jq];
       n2 = fmaf(x, x, n2);
-      uq = fmaf(__ldg(&a.u[jq]), x, uq);
-      wq = fmaf(__ldg(&a.w[jq]), x, wq);
+      uq = fmaf(cu[k], x, uq);
+      wq = fmaf(cw[k], x, wq);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -361,11 +368,11 @@ struct TL {
   static constexpr int frag = lut + lut_bytes;               // operand images + constants
   static constexpr int used = frag + frag_block(NP, HILO);
   // after the main loop everything is reused: first the softmax warps' accumulators and
-  // statistics; then, in the split that merges, the merged accumulators [8][128], merge
-  // weights and sums [2][8][kMaxSplits] (later the rotation's partial sums [3][8][128]), the
-  // merge's partial sums [at most 15][128], Π (64 KB) and the records, copied in chunks of
-  // whole splits into [rec_off, total); the dynamic shared memory is sized so that one chunk
-  // holds the records of every split at the usual split counts
+  // statistics; then, in the split that merges, the merged accumulators [128][8], merge
+  // weights and sums [2][8][kMaxSplits], the merge's partial sums [at most 15][128], Π (64 KB)
+  // and the records, copied in chunks of whole splits into [rec_off, total) (then the rotation's
+  // 15 partial sums [15][8][128]); the dynamic shared memory is sized so that one chunk holds
+  // the records of every split at the usual split counts
   static constexpr int comb_acc = 0;
   static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
   static constexpr int mrg_acc = 0;
@@ -375,6 +382,7 @@ struct TL {
   static constexpr int rec_off = pi_off + TQ_D * TQ_D * 4;
   static constexpr int total = 226 * 1024;
   static_assert(used <= total && rec_off + 16 * 8 * TQ_REC * 4 <= total, "shared memory");
+  static_assert(rec_off + (kCompute / 32) * 8 * TQ_D * 4 <= total, "rotation partial sums");
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
   // D: index planes summed in pairs by the MMAs (block j = planes 2j, 2j + 1), then the sign
@@ -447,31 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     split = s_item - b * (int)gridDim.x;
     kvh = pos % a.Hkv;
   }
-  int len = a.seq_lens[b];
-  const long long bh = (long long)b * a.Hkv + kvh;
-  if (len > a.cap) {
-    if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
-    len = a.cap;
-  }
-  const int t_begin = split * a.split_len;
-  const int t_end = min(t_begin + a.split_len, len);
-  const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
-  const int nstages = (ntiles + 1) / 2;
-  // Only the splits that hold tokens take part (ragged batches launch many empty ones): an
-  // empty split leaves at once, and a sequence without tokens gets its zero output from
-  // split 0.
-  const int used = (len + a.split_len - 1) / a.split_len;
-  if (ntiles == 0) {
-    if (len == 0 && split == 0)
-      for (int i = tid; i < a.G * TQ_D; i += kThreads) {
-        const long long e = ((long long)b * a.Hq + kvh * a.G) * TQ_D + i;
-        if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = 0.f;
-        else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(0.f);
-        else static_cast<__half*>(a.out)[e] = __float2half_rn(0.f);
-      }
-    return;
-  }
-
+  int len = a.seq_lens[b];   // in flight during the setup
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full_bar[st], 1);
@@ -493,6 +477,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   tc_before();
   __syncthreads();
   tc_after();
+  const long long bh = (long long)b * a.Hkv + kvh;
+  if (len > a.cap) {
+    if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
+    len = a.cap;
+  }
+  const int t_begin = split * a.split_len;
+  const int t_end = min(t_begin + a.split_len, len);
+  const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
+  const int nstages = (ntiles + 1) / 2;
+  // Only the splits that hold tokens take part (ragged batches launch many empty ones): an
+  // empty split leaves right after the setup, and a sequence without tokens gets its zero
+  // output from split 0.
+  const int used = (len + a.split_len - 1) / a.split_len;
+  if (ntiles == 0) {
+    if (len == 0 && split == 0)
+      for (int i = tid; i < a.G * TQ_D; i += kThreads) {
+        const long long e = ((long long)b * a.Hq + kvh * a.G) * TQ_D + i;
+        if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = 0.f;
+        else if (a.out_dtype == TQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(0.f);
+        else static_cast<__half*>(a.out)[e] = __float2half_rn(0.f);
+      }
+    if (warp == 0) tmem_dealloc(s_tmem, 512);
+    return;
+  }
+
   const uint32_t tmem = s_tmem;
 
   // ============================================================ producer warp
@@ -523,19 +532,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       };
       // Π is read again only by the split that merges: have it in L2 by then
       if (split == 0) bulk_prefetch_l2(a.pi, TQ_D * TQ_D * 4);
+      // the first stage and the value pair table come in while the query-operand kernel (this
+      // grid's programmatic-launch primary) runs; its output is copied in as soon as that grid
+      // has completed, ahead of the other stages
+      issue(0);
       if (VB == 4) {
         mbar_expect_tx(&prol_bar, L::lut_bytes);
         bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
       }
-      // the ring fills while the query-operand kernel (this grid's programmatic-launch
-      // primary) runs; its output is copied in as soon as that grid has completed
-      int c = 0;
-      for (; c < nstages && c < kStages; ++c) issue(c);
       asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_expect_tx(&op_bar, frag_block(NP, HILO));
       bulk_g2s(smem + L::frag,
                static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO),
                frag_block(NP, HILO), &op_bar);
+      int c = 1;
+      for (; c < nstages && c < kStages; ++c) issue(c);
       for (; c < nstages; ++c) {
         const int st = c % kStages;
         if (!mbar_wait(&empty_bar[st], ((c / kStages) - 1) & 1)) {
@@ -889,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   // into shared memory by bulk copies, in chunks of whole splits; warp h computes the weights
   // of head h from the records' (M, L) meanwhile.
   const float* recs = a.part + bh * (long long)a.nsplit * a.G * kRec;
-  float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [8][128]
+  float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [128][8]
   float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [2][8][kMaxSplits]
   float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [parts·G][128]
   float* srec = reinterpret_cast<float*>(smem + L::rec_off);    // [chunk][G][kRec]
@@ -900,14 +911,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     mbar_expect_tx(&rec_bar, (unsigned)(n * rec_bytes));
     bulk_g2s(srec, recs + (long long)r0 * a.G * kRec, (unsigned)(n * rec_bytes), &rec_bar);
   };
-  if (tid == 0) {
+  // the copies are issued by a thread of the last compute warp, which has no weights to compute
+  const bool issuer = tid == kCompute - 32;
+  if (issuer) {
     asm volatile("fence.proxy.async.global;" ::: "memory");   // records → bulk copies
-    // Π for the rotation back (its region is free: the ring's data is consumed and the
-    // operand images are read), then the first chunk of records
+    // the first chunk of records, then Π for the rotation back (its region is free: the
+    // ring's data is consumed and the operand images are read)
     fence_async_smem();
+    issue_chunk(0);
     mbar_expect_tx(&pi_bar, TQ_D * TQ_D * 4);
     bulk_g2s(smem + L::pi_off, a.pi, TQ_D * TQ_D * 4, &pi_bar);
-    issue_chunk(0);
   }
   if (warp < a.G) {
     // every (M, L) of the head requested at once
@@ -960,15 +973,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       const float4* av = reinterpret_cast<const float4*>(srec + mh * kRec + 4) + lane;
       const int step4 = a.G * kRec / 4;
       int r = mp;
-      for (; r + parts < n; r += 2 * parts) {
-        const float w0 = wv[r], w1 = wv[r + parts];
-        const float4 v0 = av[r * step4], v1 = av[(r + parts) * step4];
-        x0.x = fmaf(w0, v0.x, x0.x); x0.y = fmaf(w0, v0.y, x0.y);
-        x0.z = fmaf(w0, v0.z, x0.z); x0.w = fmaf(w0, v0.w, x0.w);
-        x1.x = fmaf(w1, v1.x, x1.x); x1.y = fmaf(w1, v1.y, x1.y);
-        x1.z = fmaf(w1, v1.z, x1.z); x1.w = fmaf(w1, v1.w, x1.w);
+      for (; r + 3 * parts < n; r += 4 * parts) {   // four records' loads in flight
+        float w[4];
+        float4 v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          w[e] = wv[r + e * parts];
+          v[e] = av[(r + e * parts) * step4];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float4& xx = (e & 1) ? x1 : x0;
+          xx.x = fmaf(w[e], v[e].x, xx.x); xx.y = fmaf(w[e], v[e].y, xx.y);
+          xx.z = fmaf(w[e], v[e].z, xx.z); xx.w = fmaf(w[e], v[e].w, xx.w);
+        }
       }
-      if (r < n) {
+      for (; r < n; r += parts) {
         const float w0 = wv[r];
         const float4 v0 = av[r * step4];
         x0.x = fmaf(w0, v0.x, x0.x); x0.y = fmaf(w0, v0.y, x0.y);
@@ -977,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     }
     if (r0 + chunk < used) {
       named_sync(kBarAll, kCompute);   // the chunk is consumed
-      if (tid == 0) {
+      if (issuer) {
         fence_async_smem();
         issue_chunk(r0 + chunk);
       }
@@ -987,52 +1007,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     reinterpret_cast<float4*>(rpart + (mp * a.G + mh) * TQ_D)[lane] =
         make_float4(x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w);
   named_sync(kBarAll, kCompute);
+  // the merged accumulators, coordinate-major: mrg[j][h] (heads ≥ G are 0)
   for (int item = tid; item < 8 * TQ_D; item += kCompute) {
-    const int h = item >> 7, j = item & 127;
+    const int j = item >> 3, h = item & 7;
     float v = 0.f;
     if (h < a.G)
       for (int p = 0; p < parts; ++p) v += rpart[(p * a.G + h) * TQ_D + j];
     mrg[item] = v;
   }
   named_sync(kBarAll, kCompute);
-  // rotation back: thread (i, part) adds Π[j][i]·mrg[h][j] over its third of j (44, 44 and 40
-  // rows) for every head; the partial sums go where the merge weights were
-  float* rot = s_w;                                             // [3][8][128]
-  if (tid < 3 * TQ_D) {
-    const bool okpi = mbar_wait(&pi_bar, 0);
-    if (!okpi) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    const int i = tid & 127, part = tid >> 7;
-    const int jb = 44 * part, nj4 = part == 2 ? 10 : 11;
+  // rotation back, out_h = Πᵀ·mrg_h: warp w takes the rows j of Π in [128w/15, 128(w+1)/15),
+  // lane l the output coordinates 4l..4l+3 of every head (one 16-byte load of Π and one or two
+  // of mrg per 16 or 32 FMAs); the 15 partial sums go to the record area, free by now
+  constexpr int kRotParts = kCompute / 32;
+  float* rot = srec;                                            // [15][8][128]
+  {
+    const bool okpi = mbar_wait(&pi_bar, 0);   // every thread: the CTA may not finish before it
+    if (!okpi && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    constexpr int NH = HILO ? 4 : 8;                            // heads ≥ G have mrg = 0
+    const int j0 = (TQ_D * warp) / kRotParts, j1 = (TQ_D * (warp + 1)) / kRotParts;
     const float* pis = reinterpret_cast<const float*>(smem + L::pi_off);
-    constexpr int NH = HILO ? 4 : 8;               // heads ≥ G have mrg = 0
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float o[4][NH];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int h = 0; h < NH; ++h) o[e][h] = 0.f;
     if (okpi) {
-#pragma unroll 2
-      for (int j4 = 0; j4 < nj4; ++j4) {
-        const int j = jb + 4 * j4;
-        const float p0 = pis[j * TQ_D + i], p1 = pis[(j + 1) * TQ_D + i];
-        const float p2 = pis[(j + 2) * TQ_D + i], p3 = pis[(j + 3) * TQ_D + i];
+      for (int j = j0; j < j1; ++j) {
+        const float4 p4 = *reinterpret_cast<const float4*>(pis + j * TQ_D + 4 * lane);
+        float m[8];
+        const float4 ma = *reinterpret_cast<const float4*>(mrg + 8 * j);
+        m[0] = ma.x; m[1] = ma.y; m[2] = ma.z; m[3] = ma.w;
+        if (NH == 8) {
+          const float4 mb = *reinterpret_cast<const float4*>(mrg + 8 * j + 4);
+          m[4] = mb.x; m[5] = mb.y; m[6] = mb.z; m[7] = mb.w;
+        }
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          const float4 m4 = *reinterpret_cast<const float4*>(mrg + h * TQ_D + j);
-          o[h] = fmaf(p0, m4.x, o[h]);
-          o[h] = fmaf(p1, m4.y, o[h]);
-          o[h] = fmaf(p2, m4.z, o[h]);
-          o[h] = fmaf(p3, m4.w, o[h]);
+          o[0][h] = fmaf(p4.x, m[h], o[0][h]);
+          o[1][h] = fmaf(p4.y, m[h], o[1][h]);
+          o[2][h] = fmaf(p4.z, m[h], o[2][h]);
+          o[3][h] = fmaf(p4.w, m[h], o[3][h]);
         }
       }
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h) rot[(part * 8 + h) * TQ_D + i] = o[h];
-  } else if (tid == 3 * TQ_D) {
-    // the other threads need not wait for the copy of Π, but the CTA may not finish before it
-    if (!mbar_wait(&pi_bar, 0)) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    for (int h = 0; h < NH; ++h)
+      *reinterpret_cast<float4*>(rot + (warp * 8 + h) * TQ_D + 4 * lane) =
+          make_float4(o[0][h], o[1][h], o[2][h], o[3][h]);
   }
   named_sync(kBarAll, kCompute);
   for (int item = tid; item < a.G * TQ_D; item += kCompute) {
     const int h = item >> 7, i = item & 127;
     const float Lh = s_hL[h];
-    const float x = rot[h * TQ_D + i] + rot[(8 + h) * TQ_D + i] + rot[(16 + h) * TQ_D + i];
+    float x = 0.f;
+#pragma unroll
+    for (int p = 0; p < kRotParts; ++p) x += rot[(p * 8 + h) * TQ_D + i];
     const float v = Lh > 0.f ? x / Lh : 0.f;
     const long long e = ((long long)b * a.Hq + kvh * a.G + h) * TQ_D + i;
     if (a.out_dtype == TQ_F32) static_cast<float*>(a.out)[e] = v;
