@@ -902,14 +902,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   const float* recs = a.part + bh * (long long)a.nsplit * a.G * kRec;
   float* mrg = reinterpret_cast<float*>(smem + L::mrg_acc);     // [128][8]
   float* s_w = reinterpret_cast<float*>(smem + L::mrg_w);       // [2][8][kMaxSplits]
-  float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);  // [parts·G][128]
+  // [parts·G][kPartPitch]: the pitch of 132 floats keeps the coordinate-major reads below free
+  // of bank conflicts
+  constexpr int kPartPitch = TQ_D + 4;
+  static_assert((kCompute / 32) * kPartPitch * 4 <= L::pi_off - L::mrg_part, "merge partials");
+  float* rpart = reinterpret_cast<float*>(smem + L::mrg_part);
   float* srec = reinterpret_cast<float*>(smem + L::rec_off);    // [chunk][G][kRec]
   const int rec_bytes = a.G * kRec * 4;
   const int chunk = (L::total - L::rec_off) / rec_bytes;
+  // a chunk comes in as up to 8 bulk copies of whole records, all in flight at once
   auto issue_chunk = [&](int r0) {
     const int n = min(chunk, used - r0);
     mbar_expect_tx(&rec_bar, (unsigned)(n * rec_bytes));
-    bulk_g2s(srec, recs + (long long)r0 * a.G * kRec, (unsigned)(n * rec_bytes), &rec_bar);
+    const int per = (n + 7) / 8;
+    for (int q0 = 0; q0 < n; q0 += per) {
+      const int m = min(per, n - q0);
+      bulk_g2s(srec + (long long)q0 * a.G * kRec, recs + (long long)(r0 + q0) * a.G * kRec,
+               (unsigned)(m * rec_bytes), &rec_bar);
+    }
   };
   // the copies are issued by a thread of the last compute warp, which has no weights to compute
   const bool issuer = tid == kCompute - 32;
@@ -1004,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     }
   }
   if (mact)
-    reinterpret_cast<float4*>(rpart + (mp * a.G + mh) * TQ_D)[lane] =
+    reinterpret_cast<float4*>(rpart + (mp * a.G + mh) * kPartPitch)[lane] =
         make_float4(x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w);
   named_sync(kBarAll, kCompute);
   // the merged accumulators, coordinate-major: mrg[j][h] (heads ≥ G are 0)
@@ -1012,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     const int j = item >> 3, h = item & 7;
     float v = 0.f;
     if (h < a.G)
-      for (int p = 0; p < parts; ++p) v += rpart[(p * a.G + h) * TQ_D + j];
+      for (int p = 0; p < parts; ++p) v += rpart[(p * a.G + h) * kPartPitch + j];
     mrg[item] = v;
   }
   named_sync(kBarAll, kCompute);
