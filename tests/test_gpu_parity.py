@@ -266,6 +266,23 @@ def test_decode_many_ragged_units():
     run_decode(40, 8, 4, lens, 3, 4, torch.bfloat16, torch.float32, 650, sample=pairs)
 
 
+def test_decode_operand_two_slices_per_cta():
+    """24 (batch, KV head) units: the query-operand kernel takes two slices a CTA, here with
+    one operand column per head (G = 7); ragged lengths taken largest first."""
+    run_decode(6, 28, 4, [0, 5, 333, 1000, 2047, 64], 3, 4, torch.bfloat16, torch.float32, 660)
+
+
+def test_decode_large_batch_natural_order():
+    """180 sequences × 3 splits: more work items than the split kernel ranks, so the CTAs keep
+    their natural order; the operand kernel takes four slices a CTA."""
+    rng = np.random.default_rng(181)
+    lens = [int(x) for x in rng.integers(0, 700, size=180)]
+    lens[7] = 0
+    lens[11] = 700
+    pairs = [(b, h) for b in (0, 7, 11, 90, 179) for h in range(2)]
+    run_decode(180, 4, 2, lens, 3, 2, torch.bfloat16, torch.float32, 670, sample=pairs)
+
+
 def test_decode_group_of_eight():
     run_decode(1, 16, 2, [640], 3, 4, torch.float16, torch.float32, 600)
 
