@@ -348,6 +348,14 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   }
 }
 
+// A sequence of len tokens is cut into ceil(len / split_len) splits of equal size in whole tiles
+// (at most split_len, a multiple of the tile): every one of them holds tokens, and a ragged
+// batch's splits are as even as its lengths allow.
+__device__ __forceinline__ int seq_split_len(int len, int split_len) {
+  const int ns = len > 0 ? (len + split_len - 1) / split_len : 1;
+  return ((len + ns - 1) / ns + kTile - 1) / kTile * kTile;
+}
+
 // ---------------------------------------------------------------- shared memory and TMEM
 template <int KB, int VB, bool HILO>
 struct TL {
@@ -436,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     __syncthreads();
     if (tid < nitems) {
       const int ib = tid / (int)gridDim.x, is = tid - ib * (int)gridDim.x;
-      sc_work[tid] = max(0, min(a.split_len, sc_len[ib] - is * a.split_len));
+      const int lb = sc_len[ib], slb = seq_split_len(lb, a.split_len);
+      sc_work[tid] = max(0, min(slb, lb - is * slb));
     }
     __syncthreads();
     const int pos = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
@@ -482,14 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
     len = a.cap;
   }
-  const int t_begin = split * a.split_len;
-  const int t_end = min(t_begin + a.split_len, len);
+  const int slb = seq_split_len(len, a.split_len);
+  const int t_begin = split * slb;
+  const int t_end = min(t_begin + slb, len);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int nstages = (ntiles + 1) / 2;
   // Only the splits that hold tokens take part (ragged batches launch many empty ones): an
   // empty split leaves right after the setup, and a sequence without tokens gets its zero
   // output from split 0.
-  const int used = (len + a.split_len - 1) / a.split_len;
+  const int used = (len + a.split_len - 1) / a.split_len;   // the splits with tokens
   if (ntiles == 0) {
     if (len == 0 && split == 0)
       for (int i = tid; i < a.G * TQ_D; i += kThreads) {
