@@ -21,7 +21,7 @@ Sources (cited by page title and section):
   (Algorithm 2), values the MSE-only quantiser (Algorithm 1); "对称 vs 非对称":
   asymmetric mode keeps K in FP16 and quantises V only.
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
 
 * index = number of decision boundaries <= y (a tie goes to the upper cell);
 * sign bit = 1 iff (S r)_j >= 0, so a zero residual stores all ones;
