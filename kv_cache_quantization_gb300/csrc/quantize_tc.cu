@@ -21,11 +21,15 @@
 // image brings them in once per CTA.  Raw activations arrive by per-vector bulk copies
 // (the TMA engine) one tile ahead of the tile being computed.
 //
-// kParts threads own vector r of the tile (TMEM lane r): lane r % 32 of warps q, q + 4, ...
-// (the same TMEM lane quadrant q = r / 32), part p taking coordinates 128p/kParts onwards.
-// Each reads its part of the row of D1 / D2, decides indices and signs, builds its part of
-// every code plane in registers and writes it with one store; the parts of ‖ρ‖² meet in
-// shared memory.  One CTA of 128·kParts threads per SM, persistent over tiles.
+// Two threads own vector r of the tile (TMEM lane r): lane r % 32 of warps q and q + 4 of a
+// group (the same TMEM lane quadrant q = r / 32), part p taking coordinates 64p onwards.  Each
+// reads its part of the row of D1 / D2, decides indices and signs, builds its part of every
+// code plane in registers and writes it with one store; the parts of ‖ρ‖² meet in shared
+// memory.  One CTA per SM, persistent over tiles, made of groups of 256 threads that take
+// alternate tiles, each with its own operand and staging buffers, accumulator columns and
+// barriers: one group for the product quantiser (its shared memory holds Π̂ and M̂), two for
+// the MSE quantiser, so that one group's conversion and epilogue overlap the other's product
+// and copies.
 #include <cuda_fp16.h>
 
 #include "tc_ptx.h"
@@ -35,9 +39,9 @@ TQ_DEFINE_FLAGS(tq_take_flags_quantize_tc)
 
 namespace {
 
-// threads per vector: 2 for the product quantiser (its shared memory holds one more operand
-// pair), 4 for the MSE quantiser
-__host__ __device__ constexpr int parts_of(bool prod) { return prod ? 2 : 4; }
+constexpr int kParts = 2;                      // threads per vector
+constexpr int kGT = 128 * kParts;              // threads per group
+__host__ __device__ constexpr int groups_of(bool prod) { return prod ? 1 : 2; }
 constexpr int kTileV = 128;                    // vectors per tile (MMA M)
 constexpr int kImg = 128 * 128 * 2;            // one 128×128 fp16 operand image (32 KB)
 constexpr int kLBO = 128;                      // K-adjacent core matrices
@@ -45,22 +49,29 @@ constexpr int kSBO = 16 * 128;                 // 8-row groups: 16 core matrices
 constexpr int kRawPitch = 256;                 // one raw bf16/fp16 vector
 constexpr float kPiScale = 64.f, kMScale = 8.f, kRhoScale = 256.f;
 
-// shared-memory map (bytes from the dynamic base)
+// shared-memory map (bytes from the dynamic base): the codec's images, then one area per group
 template <bool kProd>
 struct QL {
+  static constexpr int kGroups = groups_of(kProd);
   static constexpr int pi = 0;                                   // Π̂ hi | lo
   static constexpr int m = 2 * kImg;                             // M̂ hi | lo (prod)
-  static constexpr int a = kProd ? 4 * kImg : 2 * kImg;          // X̂, then ρ̂ hi (prod)
-  static constexpr int rho_lo = a + kImg;                        // ρ̂ lo (prod)
-  static constexpr int raw = kProd ? rho_lo + kImg : a + kImg;   // raw vectors of the next tile
+  static constexpr int area = kProd ? 4 * kImg : 2 * kImg;       // group 0's area
+  // offsets inside a group's area
+  static constexpr int a = 0;                                    // X̂, then ρ̂ hi (prod)
+  static constexpr int rho_lo = kImg;                            // ρ̂ lo (prod)
+  static constexpr int raw = kProd ? 2 * kImg : kImg;            // raw vectors of the next tile
   static constexpr int norm = raw + kTileV * kRawPitch;          // float ‖x‖ [128]
   static constexpr int ysc = norm + 4 * kTileV;                  // float D1 → y scale [128]
   static constexpr int rr = ysc + 4 * kTileV;                    // float ‖ρ‖² parts [2][128]
-  static constexpr int bars = rr + (kProd ? 2 : 0) * 4 * kTileV; // 3 mbarriers + TMEM slot
-  static constexpr int total = bars + 32;
-  static constexpr int tmem_cols = kProd ? 256 : 128;
+  static constexpr int gsize = rr + (kProd ? 2 : 0) * 4 * kTileV;
+  // mbarriers: the codec's images, then (raw tile, MMA) per group; then the TMEM slot
+  static constexpr int bars = area + kGroups * gsize;
+  static constexpr int total = bars + 8 * (1 + 2 * kGroups) + 8;
+  static constexpr int tmem_cols = 256;                          // D1 | D2, or D1 per group
 };
-static_assert(QL<true>::total <= 227 * 1024, "shared memory budget");
+static_assert(QL<true>::total <= 227 * 1024 && QL<false>::total <= 227 * 1024,
+              "shared memory budget");
+static_assert(QL<true>::gsize % 1024 == 0 && QL<false>::gsize % 1024 == 0, "area alignment");
 
 __device__ __forceinline__ uint32_t s32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -116,6 +127,20 @@ __device__ __forceinline__ void tc_after() {
 }
 __device__ __forceinline__ void async_proxy_fence() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// barrier of one group (named barrier 1 + group, kGT threads), and its AND-reduction
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kGT) : "memory");
+}
+__device__ __forceinline__ bool group_sync_and(int group, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + group), "r"(kGT)
+      : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
                                          uint64_t* bar) {
@@ -187,27 +212,33 @@ __device__ __forceinline__ int cell_of(float y, const tq_levels& lv, float& leve
 }
 
 template <bool kProd, int IB>
-__global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kGT * groups_of(kProd), 1) quantize_tc_kernel(TcArgs a) {
   using L = QL<kProd>;
-  constexpr int kParts = parts_of(kProd);
+  constexpr int kGroups = L::kGroups;
   constexpr int kBlkPart = 4 / kParts;           // 32-coordinate blocks per thread
   extern __shared__ __align__(128) unsigned char smem[];
-  float* s_norm = reinterpret_cast<float*>(smem + L::norm);
-  float* s_ysc = reinterpret_cast<float*>(smem + L::ysc);
-  float* s_rr = reinterpret_cast<float*>(smem + L::rr);
-  uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* bar_x = bar_const + 1;
-  uint64_t* bar_mma = bar_const + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + 3);
-  unsigned char* raw = smem + L::raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // this thread's group, and its warp inside the group
+  const int group = warp / (kGT / 32), gw = warp % (kGT / 32);
+  unsigned char* area = smem + L::area + group * L::gsize;
+  float* s_norm = reinterpret_cast<float*>(area + L::norm);
+  float* s_ysc = reinterpret_cast<float*>(area + L::ysc);
+  float* s_rr = reinterpret_cast<float*>(area + L::rr);
+  uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* bar_x = bar_const + 1 + 2 * group;
+  uint64_t* bar_mma = bar_x + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + 1 + 2 * kGroups);
+  unsigned char* raw = area + L::raw;
   const long long total = (long long)a.batch * a.heads * a.tokens;
   const long long ntiles = (total + kTileV - 1) / kTileV;
+  // the CTA's tiles blockIdx.x + k·gridDim.x go to its groups in turn
+  const long long tile0 = blockIdx.x + (long long)group * gridDim.x;
+  const long long tstep = (long long)kGroups * gridDim.x;
 
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s32(bar_const)));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s32(bar_x)));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s32(bar_mma)));
+    for (int b = 1; b < 1 + 2 * kGroups; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s32(bar_const + b)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -220,44 +251,44 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
   __syncthreads();
   tc_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t d1 = tmem, d2 = tmem + 128;
+  const uint32_t d1 = tmem + 128 * group, d2 = tmem + 128;   // D2: the product quantiser's
   // TMEM lane quadrant (rows 32·quad..) and coordinate part (blocks kBlkPart·half..) of this
   // warp
-  const int quad = warp & 3, half = warp >> 2;
+  const int quad = gw & 3, half = gw >> 2;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
 
-  if (warp == 0 && blockIdx.x < ntiles) {
-    if (lane == 0) {
+  if (gw == 0) {
+    if (warp == 0 && lane == 0 && blockIdx.x < ntiles) {
       const unsigned bytes = kProd ? 4 * kImg : 2 * kImg;
       arrive_expect(bar_const, bytes);
       bulk_g2s(smem + L::pi, a.img, 2 * kImg, bar_const);
       if (kProd) bulk_g2s(smem + L::m, static_cast<const unsigned char*>(a.img) + 2 * kImg,
                           2 * kImg, bar_const);
     }
-    issue_tile(a, blockIdx.x, total, raw, bar_x, lane);
+    if (tile0 < ntiles) issue_tile(a, tile0, total, raw, bar_x, lane);
   }
   bool ok = blockIdx.x >= ntiles || bar_wait(bar_const, 0);
   ok = __syncthreads_and(ok);
-  bool x_pending = blockIdx.x < ntiles;   // a raw-tile copy is in flight
+  bool x_pending = tile0 < ntiles;        // a raw-tile copy is in flight
   bool mma_pending = false;               // an MMA group is in flight
   uint32_t px = 0, pm = 0;
 
-  for (long long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+  for (long long tile = tile0; tile < ntiles && ok; tile += tstep) {
     const long long first = tile * kTileV;
     const int nvalid = (int)min((long long)kTileV, total - first);
-    ok = __syncthreads_and(bar_wait(bar_x, px));
+    ok = group_sync_and(group, bar_wait(bar_x, px));
     if (!ok) break;
     px ^= 1;
     x_pending = false;
-    // ---- raw → X̂ (fp16, per-vector power-of-two scale) and ‖x‖.  Warp w converts vectors
-    // 32w/kParts.., eight at a time: lane (i = lane & 7, g = lane >> 3) takes chunks
-    // (g + 4j + i) mod 16 of vector i, so that both the staging reads and the canonical
+    // ---- raw → X̂ (fp16, per-vector power-of-two scale) and ‖x‖.  Warp w of the group
+    // converts vectors 32w/kParts.., eight at a time: lane (i = lane & 7, g = lane >> 3) takes
+    // chunks (g + 4j + i) mod 16 of vector i, so that both the staging reads and the canonical
     // writes of a quarter-warp fall in distinct banks.
     {
       const int i = lane & 7, g = lane >> 3;
 #pragma unroll 1
       for (int pass = 0; pass < 4 / kParts; ++pass) {
-        const int v = (32 / kParts) * warp + 8 * pass + i;
+        const int v = (32 / kParts) * gw + 8 * pass + i;
         const bool valid = v < nvalid;
         uint32_t w[4][4];
 #pragma unroll
@@ -304,7 +335,7 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
             const __half2 h2 = __floats2half2_rn(x0, x1);
             hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(smem + L::a + canon(v, 8 * ch)) =
+          *reinterpret_cast<uint4*>(area + L::a + canon(v, 8 * ch)) =
               make_uint4(hw[0], hw[1], hw[2], hw[3]);
         }
         ss += __shfl_xor_sync(0xffffffffu, ss, 8);
@@ -319,18 +350,18 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
     }
     async_proxy_fence();   // X̂ (generic writes) → tensor-core reads
     tc_before();
-    __syncthreads();
+    group_sync(group);
     tc_after();
-    if (warp == 0) {
-      // the staging buffer is free: fetch the next tile while this one is computed
-      const long long next = tile + gridDim.x;
+    if (gw == 0) {
+      // the staging buffer is free: fetch the group's next tile while this one is computed
+      const long long next = tile + tstep;
       if (next < ntiles) {
         async_proxy_fence();
         issue_tile(a, next, total, raw, bar_x, lane);
       }
       // ---- GEMM 1: D1 = X̂ · (Π̂hi + Π̂lo)ᵀ
       if (lane == 0) {
-        const uint32_t sa = s32(smem + L::a), sp = s32(smem + L::pi);
+        const uint32_t sa = s32(area + L::a), sp = s32(smem + L::pi);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t ad = sdesc(sa + ks * 2 * kLBO);
@@ -341,9 +372,9 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
       }
       __syncwarp();
     }
-    x_pending = tile + gridDim.x < ntiles;
+    x_pending = tile + tstep < ntiles;
     mma_pending = true;
-    ok = __syncthreads_and(bar_wait(bar_mma, pm));
+    ok = group_sync_and(group, bar_wait(bar_mma, pm));
     if (!ok) break;
     pm ^= 1;
     mma_pending = false;
@@ -411,8 +442,8 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
             lo[e2] = *reinterpret_cast<const uint32_t*>(&ll);
           }
           const int off = canon(r, 32 * blk + 8 * c8);
-          *reinterpret_cast<uint4*>(smem + L::a + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(smem + L::rho_lo + off) =
+          *reinterpret_cast<uint4*>(area + L::a + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(area + L::rho_lo + off) =
               make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
@@ -437,12 +468,12 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
     if constexpr (kProd) {
       async_proxy_fence();   // ρ̂ (generic writes) → tensor-core reads
       tc_before();
-      __syncthreads();
+      group_sync(group);
       tc_after();
       // ---- GEMM 2: D2 = ρ̂hi·M̂hiᵀ + ρ̂hi·M̂loᵀ + ρ̂lo·M̂hiᵀ
-      if (warp == 0) {
+      if (gw == 0) {
         if (lane == 0) {
-          const uint32_t sh = s32(smem + L::a), sl = s32(smem + L::rho_lo);
+          const uint32_t sh = s32(area + L::a), sl = s32(area + L::rho_lo);
           const uint32_t smh = s32(smem + L::m), sml = smh + kImg;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -456,7 +487,7 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
         __syncwarp();
       }
       mma_pending = true;
-      ok = __syncthreads_and(bar_wait(bar_mma, pm));
+      ok = group_sync_and(group, bar_wait(bar_mma, pm));
       if (!ok) break;
       pm ^= 1;
       mma_pending = false;
@@ -484,13 +515,13 @@ __global__ void __launch_bounds__(128 * parts_of(kProd), 1) quantize_tc_kernel(T
       }
     }
     tc_before();
-    __syncthreads();   // D1 / D2 read and X̂ / ρ̂ consumed before the next tile reuses them
+    group_sync(group);   // D1 / D2 read and X̂ / ρ̂ consumed before the next tile reuses them
     tc_after();
   }
   if (!ok) {
     // a bounded wait gave up: report it, let in-flight copies and MMAs land (bounded) and
     // release the accumulator columns before leaving
-    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+    if (tid == group * kGT) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
     if (x_pending) bar_wait(bar_x, px);
     if (mma_pending) bar_wait(bar_mma, pm);
   }
@@ -514,7 +545,7 @@ tq_status launch_tc(const TcArgs& a, int grid, cudaStream_t stream) {
       return TQ_ERR_CUDA;
     configured[dev] = true;
   }
-  quantize_tc_kernel<kProd, IB><<<grid, 128 * parts_of(kProd), QL<kProd>::total, stream>>>(a);
+  quantize_tc_kernel<kProd, IB><<<grid, kGT * groups_of(kProd), QL<kProd>::total, stream>>>(a);
   return tq_cuda_status(cudaGetLastError());
 }
 
