@@ -133,9 +133,10 @@ def rotation_from_gaussian(g):
 # ---------------------------------------------------------------------------------------
 
 def quantize_mse(x, pi, centroids):
-    """TurboQuant-MSE (Algorithm 1): n = ||x||; y = Π x / n; idx_j = #{boundaries <= y_j}.
-    The comparison itself is taken in float32 (y and the boundaries rounded to float32), the
-    precision the GPU kernel decides in; y is computed in float64.
+    """TurboQuant-MSE (Algorithm 1): n = ||x||; y = Π x / n; idx_j = #{boundaries <= y_j},
+    everything in float64.  (A float32 implementation may pick the neighbouring cell only
+    where y_j lies within float32 rounding of a boundary, far inside the 1e-6 band that
+    ``boundary_exclusion`` marks.)
     Returns (idx int64 [..., d], n float64 [...], y float64 [..., d])."""
     x = np.asarray(x, dtype=np.float64)
     c = np.asarray(centroids, dtype=np.float64)
@@ -145,7 +146,7 @@ def quantize_mse(x, pi, centroids):
     u = x / safe[..., None]
     u = np.where((n > 0)[..., None], u, 0.0)
     y = u @ np.asarray(pi, dtype=np.float64).T
-    idx = np.searchsorted(bnd.astype(np.float32), y.astype(np.float32), side="right")
+    idx = np.searchsorted(bnd, y, side="right")
     return idx.astype(np.int64), n, y
 
 
@@ -346,16 +347,18 @@ def boundary_exclusion(y, centroids, eps=1e-6):
     dist = np.abs(y[..., None] - bnd)
     k = np.argmin(dist, axis=-1)            # nearest boundary separates cells k and k+1
     excluded = np.take_along_axis(dist, k[..., None], axis=-1)[..., 0] < eps
-    idx = np.searchsorted(bnd.astype(np.float32), y.astype(np.float32), side="right")
+    idx = np.searchsorted(bnd, y, side="right")
     alt = np.where(idx == k, k + 1, k)
     return excluded, alt.astype(np.int64)
 
 
 def sign_exclusion(z, n, d, eps=1e-6):
-    """True where a QJL sign bit is not decided robustly in float32.  The decision quantity
-    is the sketch of the unit-sphere residual, (S r)_j / ||x||; it sums d residual
-    coordinates, each known to eps, through unit-variance weights, so the same eps becomes
-    eps·√d on it."""
+    """True where a QJL sign bit lies within eps of its decision boundary.  The sign decides
+    on z_j = (S r)_j.  Measured in the same unit-sphere units as the index band, the decision
+    quantity is the projection of the unit-sphere residual r/||x|| onto the unit direction of
+    row j of S, i.e. z_j / (||x||·||S_j||), and E||S_j||² = d for a Gaussian S.  So a bit is
+    excluded when |z_j| < eps·√d·||x||.  For a Gaussian S independent of x, z_j ~ N(0, ||r||²)
+    and the excluded share of a vector's bits is erf(eps·√d·||x|| / (√2·||r||))."""
     z = np.asarray(z, dtype=np.float64)
     n = np.asarray(n, dtype=np.float64)[..., None]
     return np.abs(z) < eps * math.sqrt(d) * n

@@ -343,11 +343,43 @@ def pin_boundary_exclusion_rate(o):
         assert np.all(np.abs(alt - idx) == 1)
 
 
+def pin_sign_exclusion_rate(o):
+    """The share of QJL sign bits that the parity checks skip matches its closed form.  With a
+    fresh Gaussian sketch S for every vector (independent of x), (S r)_j ~ N(0, ||r||²)
+    exactly, so the share of the vector's bits inside the band |z_j| < eps·√d·||x|| is
+    erf(eps·√d·||x|| / (√2·||r||)).  Checked per index width with a wide eps (so the count is
+    large) and for the 1e-6 band: the expected share stays below 1e-4.  A band with d in
+    place of √d, ||r|| in place of ||x||, or a tenfold width misses the closed form."""
+    from scipy import special
+    rng = np.random.default_rng(31)
+    d = 128
+    pi = _rotation(o, 42)
+    nvec = 1500
+    for ibits in (1, 2, 3):
+        c, _ = o.lloyd_max_codebook(d, ibits)
+        eps = 1e-3
+        got = 0
+        expect = 0.0
+        expect_1e6 = 0.0
+        for v in range(nvec):
+            x = rng.standard_normal((1, d)) * np.exp(0.5 * rng.standard_normal(d))
+            s = rng.standard_normal((d, d))
+            k = o.quantize_prod(x, pi, s, c)
+            got += int(o.sign_exclusion(k["z"], k["n"], d, eps=eps).sum())
+            ratio = math.sqrt(d) * k["n"][0] / (math.sqrt(2.0) * k["gamma"][0])
+            expect += d * special.erf(eps * ratio)
+            expect_1e6 += d * special.erf(1e-6 * ratio)
+        total = nvec * d
+        sd = math.sqrt(expect * (1 - expect / total))
+        assert abs(got - expect) < 5 * sd + 0.02 * expect, (ibits, got, expect)
+        assert expect_1e6 / total < 1e-4, (ibits, expect_1e6 / total)
+
+
 ALL_PINS = [
     pin_rotation, pin_codebook_closed_form_1bit, pin_codebook_centroid_condition,
     pin_codebook_gaussian_limit, pin_codebook_mse_monotone, pin_mse_index_is_nearest_level,
     pin_mse_distortion, pin_value_cos_sim_pages, pin_qjl_identity, pin_estimator_unbiased,
     pin_estimator_equals_dequantized_dot, pin_residual_definition, pin_zero_vector,
     pin_packing_golden, pin_attention_brute_force, pin_asym_concatenation,
-    pin_boundary_exclusion_rate,
+    pin_boundary_exclusion_rate, pin_sign_exclusion_rate,
 ]

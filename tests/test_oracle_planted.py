@@ -102,10 +102,30 @@ def plant_ties_down_and_shift(o):
     o.quantize_mse = f
 
 
+def plant_sign_band_power_of_d(o):
+    """Sign band eps·d·||x|| instead of eps·√d·||x||."""
+    o.sign_exclusion = lambda z, n, d, eps=1e-6: np.abs(np.asarray(z)) < eps * d * np.asarray(n)[..., None]
+
+
+def plant_sign_band_residual_norm(o):
+    """Sign band scaled by the residual's norm (||r|| ≈ ||S r|| / √d) instead of ||x||."""
+    def band(z, n, d, eps=1e-6):
+        z = np.asarray(z, dtype=np.float64)
+        rn = np.linalg.norm(z, axis=-1, keepdims=True) / math.sqrt(d)
+        return np.abs(z) < eps * math.sqrt(d) * rn
+    o.sign_exclusion = band
+
+
+def plant_sign_band_tenfold(o):
+    orig = o.sign_exclusion
+    o.sign_exclusion = lambda z, n, d, eps=1e-6: orig(z, n, d, eps * 10)
+
+
 PLANTS = [plant_drop_qjl, plant_flip_qjl_sign, plant_wrong_qjl_constant,
           plant_transposed_rotation, plant_no_sign_fix, plant_cell_midpoint_levels,
           plant_residual_sign, plant_gqa_mapping, plant_msb_first, plant_mse_norm_dropped,
-          plant_ties_down_and_shift]
+          plant_ties_down_and_shift, plant_sign_band_power_of_d, plant_sign_band_residual_norm,
+          plant_sign_band_tenfold]
 
 
 @pytest.mark.parametrize("plant", PLANTS, ids=lambda p: p.__name__)
