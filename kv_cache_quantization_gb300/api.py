@@ -213,9 +213,8 @@ class DecodePlan:
         nbytes = B.tq_decode_workspace_bytes(self.desc)
         if nbytes == 0:
             raise ValueError("invalid decode-attention configuration")
-        # zero-filled once: the library keeps its split tickets there, and every call
-        # leaves them at zero again
-        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        # caller-owned scratch; the library clears what must start at zero on every call
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.out_dtype = out_dtype
         self.shape = (batch, q_heads, HEAD_DIM)
 

@@ -79,7 +79,8 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   const size_t pf = (size_t)d->batch * d->kv_heads * p->nsplit * p->G * kRec;
   p->q_off = 0;
   p->part_off = (qbytes + 255) / 256 * 256;
-  // split tickets of the tensor-core path: one int per (batch, KV head), zero between calls
+  // split tickets of the tensor-core path: one int per (batch, KV head), cleared by the
+  // query-operand kernel at the start of every call
   p->ctr_off = (p->part_off + pf * sizeof(float) + 255) / 256 * 256;
   p->bytes = p->ctr_off + (size_t)d->batch * d->kv_heads * sizeof(int);
   return TQ_OK;
@@ -457,17 +458,6 @@ extern "C" size_t tq_decode_workspace_bytes(const tq_attn_desc* desc) {
   if (!desc) return 0;
   if (plan(desc, desc->tail_capacity > 0, &p) != TQ_OK) return 0;
   return p.bytes;
-}
-
-// Byte range of the workspace that must be zero when a symmetric decode call starts (the
-// split tickets).
-tq_status tq_decode_ticket_span(const tq_attn_desc* desc, size_t* offset, size_t* bytes) {
-  Plan p;
-  const tq_status st = plan(desc, false, &p);
-  if (st != TQ_OK) return st;
-  *offset = p.ctr_off;
-  *bytes = p.bytes - p.ctr_off;
-  return TQ_OK;
 }
 
 extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc,

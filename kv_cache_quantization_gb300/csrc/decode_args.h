@@ -46,7 +46,7 @@ struct tq_mma_launch {
   const float* vpiT;           // Πᵀ of the value codec (row-major)
   void* out;                   // [B][Hq][128]
   int out_dtype;
-  int* counters;               // [B][Hkv] split tickets (zero between calls)
+  int* counters;               // [B][Hkv] split tickets (cleared by the operand kernel)
   int max_len;                 // longest sequence (tokens) of the call
   float s_idx, s_sgn;          // power-of-two scales of the e4m3 query operand
 };

@@ -12,7 +12,9 @@
 // The array is a file-scope __device__ object, so every GPU that loads the library holds
 // it (kScratchBytes) until the process exits.  Host code may not use the array's name as a
 // device address (on the host it is only a stand-in symbol), so the device address is
-// looked up once per device with cudaGetSymbolAddress and cached.
+// looked up once per device with cudaGetSymbolAddress and cached.  The cached address
+// belongs to the device's primary context: after cudaDeviceReset it is stale, as are the
+// codecs created before the reset, and the library must not be used on that device again.
 #include <mutex>
 
 #include "tq_internal.h"
@@ -59,14 +61,7 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_attn_desc* desc, const
   void* scratch = nullptr;
   tq_status st = scratch_address(&scratch);
   if (st != TQ_OK) return st;
-  // The array keeps the previous call's contents.  The split tickets must start at zero;
-  // every completed call leaves them so, but one that gave up on a wait may not: clear them
-  // (a few bytes, on the call's stream) before every call.
-  size_t off = 0, bytes = 0;
-  st = tq_decode_ticket_span(desc, &off, &bytes);
-  if (st != TQ_OK) return st;
-  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + off, 0, bytes,
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  // The array keeps the previous call's contents; the decode path clears its split tickets
+  // itself at the start of every call, so nothing needs resetting here.
   return tq_decode_attention(desc, kc, vc, q, k, v, seq_lens, out, scratch, kScratchBytes, stream);
 }

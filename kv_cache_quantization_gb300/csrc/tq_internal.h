@@ -77,7 +77,5 @@ tq_status tq_launch_quantize_tc(bool prod, const void* x, int dtype, int batch, 
                                 float* xnorm, float* rnorm, int capacity, const tq_codec* c,
                                 cudaStream_t stream);
 size_t tq_operand_image_bytes(bool prod);
-// Byte range of a symmetric decode call's workspace that must be zero when the call starts.
-tq_status tq_decode_ticket_span(const tq_attn_desc* desc, size_t* offset, size_t* bytes);
 void tq_build_operand_image(const double* mat, bool sketch, uint16_t* img);
 float tq_fp16_friendly_scale(const float* levels, int n);
