@@ -1,11 +1,20 @@
-"""Benchmark: one decode step of compressed-KV attention (quantise the new token's K and V
-into the packed cache, then decode attention over the whole packed context), on the
-Qwen2.5-7B-shaped GQA layer: batch 1, 28 query / 4 KV heads, head_dim 128, 32768 tokens,
-K 3-bit product code, V 4-bit MSE code, bf16 inputs.
+"""Benchmark of compressed-KV decode attention (TurboQuant codes: product-quantised keys, MSE
+values, attention on the packed bits).
+
+The headline line is the long-context workload, the largest that fits one GPU: batch 1,
+32 query / 8 KV heads, head_dim 128, 262144 cached tokens, K 3-bit product code (4 outlier
+channels), V 2-bit MSE code, bf16 inputs.  One step = quantise the new token's K and V into
+the packed cache, then decode attention over all 262144 tokens.  A ``per_workload`` block adds
+the other decode workloads, each timed the same way:
+
+* ``decode_gqa28x4_ctx32768_k3v4``: batch 1, 28/4 heads, 32768 tokens, K3/V4 (one step);
+* ``asym_b8_ctx8192_kfp16_v4_tail255``: batch 8, FP16 keys, V 4-bit, FP16 tail of 255 tokens;
+* ``serving_b32_ragged4k-16k_k4v4``: 32 ragged sequences, K4/V4, the workload's 128 decode
+  steps: each appends one token per (sequence, KV head) and attends the grown cache.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
 Metric: KV tokens/s = (tokens attended per sequence, summed over the batch) / step time.
-Multi-GPU (torchrun): every rank runs its own independent batch (weak scaling, no
+Multi-GPU (torchrun): every rank runs its own independent replica (weak scaling, no
 data-path collective); timing is the max over ranks.
 """
 from __future__ import annotations
@@ -25,14 +34,18 @@ sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode attention: KV tokens/s and % of GB300 HBM roofline"
 UNIT = "KV tokens/s"
+HEADLINE = "longctx_gqa32x8_ctx262144_k3v2"
+PER_WORKLOAD = ["decode_gqa28x4_ctx32768_k3v4", "asym_b8_ctx8192_kfp16_v4_tail255",
+                "serving_b32_ragged4k-16k_k4v4"]
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
 
 
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy test)"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
 
@@ -40,7 +53,11 @@ def read_peaks():
 # ------------------------------------------------------------------ clocks sampling
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock, utilisation and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
@@ -50,13 +67,11 @@ class ClockSampler:
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -86,12 +101,22 @@ class ClockSampler:
                 pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[4]) or 0) >= 50]
+        use = loaded or rows
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "what": "median SM clock over samples with GPU utilisation >= 50%"}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -119,12 +144,339 @@ def barrier(ws):
         dist.barrier()
 
 
+# ------------------------------------------------------------------ timing helpers
+
+class Graphs:
+    """Captures a sequence of library calls once as a CUDA graph and replays it, so that the
+    measurement is the GPU's time and not the Python launch loop's."""
+
+    def __init__(self, dev):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.stream = torch.cuda.current_stream(dev)
+
+    def capture(self, fn, n):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.dev)
+        cap.wait_stream(self.stream)
+        with torch.cuda.graph(g, stream=cap):
+            cs = torch.cuda.current_stream(self.dev)
+            for i in range(n):
+                fn(i, cs)
+        self.stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def time(self, g, ws):
+        """Milliseconds of one replay of g (CUDA events on the replaying stream), max over
+        ranks."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0.record(self.stream)
+        g.replay()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return max_over_ranks(e0.elapsed_time(e1), ws, self.dev)
+
+    def busy(self, g, seconds):
+        """Replays g for about `seconds` (untimed), so the clock sampler sees the GPU under
+        load around a timed region."""
+        torch = self.torch
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            g.replay()
+            torch.cuda.synchronize()
+
+
+def _elem_bytes(dt):
+    import torch
+    return torch.finfo(dt).bits // 8
+
+
+def decode_bytes(w, tokens_total, out_dtype):
+    """Algorithmic bytes of one decode-attention call: the packed K and V codes of every
+    attended token and KV head, the queries and the outputs."""
+    from kv_cache_quantization_gb300 import _binding as Bn
+    code = Bn.tq_code_bytes(Bn.TQ_PROD, w.k_bits) + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits)
+    return (w.kv_heads * tokens_total * code
+            + w.batch * w.q_heads * 128 * (_elem_bytes(w.in_dtype) + _elem_bytes(out_dtype)))
+
+
+def roofline(bytes_, ms, workload, peak):
+    from kv_cache_quantization_gb300.profiling import measured_traffic
+    achieved = bytes_ / (ms * 1e-3) / 1e9
+    traffic, note = measured_traffic(workload)
+    return {"bound": "hbm", "achieved": achieved, "peak": peak[0], "unit": "GB/s",
+            "frac": achieved / peak[0], "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+            "traffic": traffic, "traffic_note": note, "algorithmic_bytes": bytes_, "ms": ms,
+            "peak_source": peak[1]}
+
+
+# ------------------------------------------------------------------ symmetric workloads
+
+class SymWorkload:
+    """Codecs, packed caches and per-step inputs of a symmetric workload, quantised once (the
+    prefill compaction, also timed)."""
+
+    def __init__(self, w, dev):
+        import torch
+
+        from kv_cache_quantization_gb300 import api, synth
+        self.w = w
+        self.dev = dev
+        self.api = api
+        cap = synth.cache_capacity(w)
+        lens0 = [min(int(x), w.context) for x in synth.seq_lengths(w)]
+        # tokens in the cache before the timed steps: one-step workloads append their step's
+        # token at len - 1; the decode loop appends at len, len + 1, ...
+        self.loop = w.decode_steps > 0
+        pre = lens0 if self.loop else [x - 1 for x in lens0]
+        self.lens0 = lens0
+        self.kc, self.vc = api.Codec.prod(w.k_bits, w.layer), api.Codec.mse(w.v_bits, w.layer)
+        k, v = synth.make_kv(w, device=dev)
+        self.kcache = api.ProdCache.empty(w.batch, w.kv_heads, cap, w.k_bits, device=dev)
+        self.vcache = api.MSECache.empty(w.batch, w.kv_heads, cap, w.v_bits, device=dev)
+        pre_t = torch.tensor(pre, dtype=torch.int32, device=dev)
+        api.quantize_prod(self.kc, k, self.kcache, count=pre_t)
+        api.quantize_mse(self.vc, v, self.vcache, count=pre_t)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.quantize_prod(self.kc, k, self.kcache, count=pre_t)
+        api.quantize_mse(self.vc, v, self.vcache, count=pre_t)
+        e1.record()
+        torch.cuda.synchronize()
+        self.compaction_ms = e0.elapsed_time(e1)
+        self.compaction_vectors = 2 * w.kv_heads * sum(pre)
+        self.compaction_bytes = w.kv_heads * sum(pre) * (
+            2 * 128 * _elem_bytes(w.in_dtype) + api.B.tq_code_bytes(api.B.TQ_PROD, w.k_bits)
+            + api.B.tq_code_bytes(api.B.TQ_MSE, w.v_bits))
+        del k, v
+        self.cap = cap
+        nsteps = w.decode_steps if self.loop else 4
+        self.queries = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(nsteps)]
+        self.new_kv = [synth.make_new_tokens(w, device=dev, step=i) for i in range(nsteps)]
+        if self.loop:
+            # append positions of step s are lens0 + s, the attended lengths lens0 + s + 1
+            self.lens = [torch.tensor([x + s for x in lens0], dtype=torch.int32, device=dev)
+                         for s in range(nsteps + 1)]
+            self.caches = [(self.kcache, self.vcache)]
+        else:
+            self.pos = pre_t
+            self.lens = torch.tensor(lens0, dtype=torch.int32, device=dev)
+            # rotating copies: every step reads its cache from HBM, not L2
+            l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            per = self.kcache.nbytes() + self.vcache.nbytes()
+            self.copies = max(3, math.ceil(3 * l2 / per))
+            self.caches = [(self.kcache, self.vcache)] + [
+                (api.ProdCache(*(t.clone() for t in (self.kcache.idx, self.kcache.sgn,
+                                                      self.kcache.xnorm, self.kcache.rnorm))),
+                 api.MSECache(self.vcache.idx.clone(), self.vcache.xnorm.clone(), w.v_bits))
+                for _ in range(self.copies - 1)]
+            self.per_copy = per
+        self.plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, cap,
+                                   max(lens0) + (w.decode_steps if self.loop else 0),
+                                   w.in_dtype, w.out_dtype, device=dev)
+        self.out = self.plan.new_out(dev)
+        self.nsteps = nsteps
+
+    def tokens(self, i):
+        """Tokens attended (summed over the batch) at step i."""
+        return sum(self.lens0) + (i + 1) * self.w.batch if self.loop else sum(self.lens0)
+
+    def step(self, i, stream, kv=None, q=None):
+        api = self.api
+        s = i % self.nsteps
+        kn, vn = kv if kv is not None else self.new_kv[s]
+        q = self.queries[s] if q is None else q
+        if self.loop:
+            kcache, vcache = self.caches[0]
+            pos, lens = self.lens[s], self.lens[s + 1]
+        else:
+            kcache, vcache = self.caches[i % self.copies]
+            pos, lens = self.pos, self.lens
+        api.quantize_prod(self.kc, kn, kcache, pos=pos, stream=stream)
+        api.quantize_mse(self.vc, vn, vcache, pos=pos, stream=stream)
+        self.plan.run(self.kc, self.vc, q, kcache, vcache, lens, self.out, stream=stream)
+
+    def decode_only(self, i, stream):
+        s = i % self.nsteps
+        if self.loop:
+            kcache, vcache = self.caches[0]
+            lens = self.lens[s + 1]
+        else:
+            kcache, vcache = self.caches[i % self.copies]
+            lens = self.lens
+        self.plan.run(self.kc, self.vc, self.queries[s], kcache, vcache, lens, self.out,
+                      stream=stream)
+
+    def l2_note(self):
+        if self.loop:
+            return (f"one cache of {self.kcache.nbytes() + self.vcache.nbytes() >> 20} MiB "
+                    f"(> L2), appended in place by the decode loop")
+        return f"{self.copies} rotating cache copies ({self.copies * self.per_copy >> 20} MiB > 3x L2)"
+
+    def compaction(self, peak):
+        ms = self.compaction_ms
+        return {"vectors": self.compaction_vectors, "ms": ms,
+                "vectors_per_s": self.compaction_vectors / (ms * 1e-3),
+                "what": "quantise the cached K (product code) and V (MSE code) once",
+                "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak[0],
+                             "achieved": self.compaction_bytes / (ms * 1e-3) / 1e9,
+                             "frac": self.compaction_bytes / (ms * 1e-3) / 1e9 / peak[0],
+                             "algorithmic_bytes": self.compaction_bytes,
+                             "note": "input vectors read once, codes and norms written"}}
+
+
+def measure_sym(w, args, dev, ws, peak, headline, clk=None):
+    import torch
+    g = Graphs(dev)
+    S = SymWorkload(w, dev)
+    n = w.decode_steps if S.loop else args.steps
+    for i in range(max(args.warmup, 3)):
+        S.step(i, g.stream)
+    torch.cuda.synchronize()
+    g_step = g.capture(S.step, n)
+    g_dec = g.capture(S.decode_only, n)
+    if headline:
+        g.busy(g_step, 1.0)
+    step_ms = g.time(g_step, ws) / n
+    if headline:
+        g.busy(g_step, 0.5)
+    dec_ms = g.time(g_dec, ws) / n
+    tokens = [S.tokens(i) for i in range(n)]
+    mean_tokens = sum(tokens) / n
+    dec_bytes = decode_bytes(w, mean_tokens, w.out_dtype)
+    res = {
+        "value": mean_tokens * ws / (step_ms * 1e-3), "unit": UNIT, "ms_per_step": step_ms,
+        "steps": n, "tokens_attended_per_step": mean_tokens,
+        "step": ("append one new K,V token per (sequence, KV head) at its length, then decode "
+                 "attention over the grown cache; the workload's 128 steps" if S.loop else
+                 "quantise the new K,V token at position len-1, then decode attention over len "
+                 "tokens; the workload's one decode step, repeated"),
+        "l2": S.l2_note(),
+        "decode_call": roofline(dec_bytes, dec_ms, w.name, peak),
+        "compaction": S.compaction(peak),
+        "gpu_launches": 4 * n,
+    }
+    if not headline:
+        return res
+    # ---------------- end to end through the public API with host buffers: a step's inputs
+    # (query, new key and value) travel as one packed pinned buffer, the output comes back
+    parts = [S.queries[0], S.new_kv[0][0], S.new_kv[0][1]]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [0, sizes[0], sizes[0] + sizes[1]]
+    h2d = sum(sizes)
+    in_dev = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    q_dev, k_dev, v_dev = (in_dev[o:o + m].view(t.dtype).view(t.shape)
+                           for o, m, t in zip(offs, sizes, parts))
+    in_host = []
+    for i in range(4):
+        buf = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+        for o, m, t in zip(offs, sizes, (S.queries[i], S.new_kv[i][0], S.new_kv[i][1])):
+            buf[o:o + m].copy_(t.contiguous().cpu().view(-1).view(torch.uint8))
+        in_host.append(buf)
+    out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+    d2h = S.out.numel() * S.out.element_size()
+
+    def e2e_step(i, stream):
+        in_dev.copy_(in_host[i % 4], non_blocking=True)
+        S.step(i, stream, (k_dev, v_dev), q_dev)
+        out_host.copy_(S.out, non_blocking=True)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0.record(g.stream)
+    for i in range(n):
+        e2e_step(i, g.stream)
+    e1.record(g.stream)
+    torch.cuda.synchronize()
+    eager_ms = max_over_ranks(e0.elapsed_time(e1) / n, ws, dev)
+    graph_ms = g.time(g.capture(e2e_step, n), ws) / n
+    res["e2e"] = {"value": mean_tokens * ws / (eager_ms * 1e-3), "unit": UNIT,
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "ms_per_step": eager_ms,
+                  "timing": "eager Python loop over the steps; every step one pinned-host copy "
+                            "in (query, new key and value packed), the library calls, the "
+                            "output copied out",
+                  "graph_value": mean_tokens * ws / (graph_ms * 1e-3),
+                  "graph_ms_per_step": graph_ms,
+                  "graph_timing": "the same steps captured once as a CUDA graph and replayed"}
+    return res
+
+
+# ------------------------------------------------------------------ asymmetric workload
+
+def measure_asym(w, args, dev, ws, peak):
+    """FP16 keys, 4-bit MSE values and an FP16 tail of 255 tokens per sequence.  The step is
+    one decode-attention call over the compressed part and the tail."""
+    import torch
+
+    from kv_cache_quantization_gb300 import _binding as Bn
+    from kv_cache_quantization_gb300 import api, synth
+    g = Graphs(dev)
+    lens_np = synth.seq_lengths(w)
+    n_tok = int(sum(lens_np)) + w.batch * w.tail
+    vc = api.Codec.mse(w.v_bits, w.layer)
+    k, v = synth.make_kv(w, device=dev)
+    kt, vt = synth.asym_tail(w, k, v)
+    lens = torch.tensor([int(x) for x in lens_np], dtype=torch.int32, device=dev)
+    tl = torch.full((w.batch,), w.tail, dtype=torch.int32, device=dev)
+    base_v = api.MSECache.empty(w.batch, w.kv_heads, w.context, w.v_bits, device=dev)
+    api.quantize_mse(vc, v, base_v, count=lens)
+    k16 = k.to(torch.float16)
+    del k, v
+    torch.cuda.synchronize()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per = k16.numel() * 2 + base_v.nbytes() + kt.numel() * 4
+    copies = max(3, math.ceil(3 * l2 / per))
+    sets = [(k16, base_v, kt, vt)] + [
+        (k16.clone(), api.MSECache(base_v.idx.clone(), base_v.xnorm.clone(), w.v_bits),
+         kt.clone(), vt.clone()) for _ in range(copies - 1)]
+    queries = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, int(max(lens_np)),
+                          w.in_dtype, w.out_dtype, device=dev,
+                          tail_capacity=synth.TAIL_CAPACITY)
+    out = plan.new_out(dev)
+
+    def step(i, stream):
+        kk, vv, ktt, vtt = sets[i % copies]
+        plan.run_asym(vc, queries[i % 4], kk, vv, lens, ktt, vtt, tl, out, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i, g.stream)
+    ms = g.time(g.capture(step, args.steps), ws) / args.steps
+    dec_bytes = (w.kv_heads * (int(sum(lens_np)) * (256 + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
+                               + w.batch * w.tail * 512)
+                 + w.batch * w.q_heads * 128 * (_elem_bytes(w.in_dtype) + _elem_bytes(w.out_dtype)))
+    return {"value": n_tok * ws / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "steps": args.steps, "tokens_attended_per_step": n_tok,
+            "step": "decode attention over the compressed part (FP16 keys, 4-bit values) and "
+                    "the FP16 tail",
+            "l2": f"{copies} rotating copies ({copies * per >> 20} MiB > 3x L2)",
+            "decode_call": roofline(dec_bytes, ms, w.name, peak), "gpu_launches": 2 * args.steps}
+
+
 # ------------------------------------------------------------------ our implementation
+
+def describe(w, ws):
+    return {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
+            "head_dim": 128, "context": w.context, "k_bits": w.k_bits, "v_bits": w.v_bits,
+            "tail": w.tail, "decode_steps": w.decode_steps, "layer": w.layer,
+            "parallelism": f"replicas x{ws} (independent batches)"}
+
 
 def run_ours(args):
     import torch
 
-    from kv_cache_quantization_gb300 import api, synth
+    from kv_cache_quantization_gb300 import synth
 
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -132,366 +484,45 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    peak = read_peaks()
     w = synth.WORKLOADS[args.workload]
-    if w.k_bits == 0:
-        return run_ours_asym(args, w, ws, rank, dev)
-    ctx = w.context
-    # tokens attended per sequence this step (ragged for the serving workload); the cache
-    # holds lens - 1 of them and the step appends the last one
-    lens_np = synth.seq_lengths(w)
-    lens_np[:] = [min(int(x), ctx) for x in lens_np]
-    n_tok = int(sum(lens_np))
-    kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
-
-    # Prefill compaction: quantise the cached tokens once (not part of the timed step).
-    k, v = synth.make_kv(w, device=dev)
-    base_k = api.ProdCache.empty(w.batch, w.kv_heads, ctx, w.k_bits, device=dev)
-    base_v = api.MSECache.empty(w.batch, w.kv_heads, ctx, w.v_bits, device=dev)
-    pre = torch.tensor([int(x) - 1 for x in lens_np], dtype=torch.int32, device=dev)
-    api.quantize_prod(kc, k, base_k, count=pre)
-    api.quantize_mse(vc, v, base_v, count=pre)
-    torch.cuda.synchronize()
-    # compaction throughput (full cache, K and V), reported as an extra
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    api.quantize_prod(kc, k, base_k, count=pre)
-    api.quantize_mse(vc, v, base_v, count=pre)
-    ev1.record()
-    torch.cuda.synchronize()
-    compaction_ms = ev0.elapsed_time(ev1)
-    del k, v
-
-    # Rotate several cache copies so that each timed step reads from HBM, not L2.
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_copy = base_k.nbytes() + base_v.nbytes()
-    copies = max(3, math.ceil(3 * l2 / per_copy))
-    kcs = [base_k] + [api.ProdCache(*(t.clone() for t in (base_k.idx, base_k.sgn, base_k.xnorm,
-                                                          base_k.rnorm))) for _ in range(copies - 1)]
-    vcs = [base_v] + [api.MSECache(base_v.idx.clone(), base_v.xnorm.clone(), w.v_bits)
-                      for _ in range(copies - 1)]
-    steps_q = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
-    steps_kv = [synth.make_new_tokens(w, device=dev, step=i) for i in range(4)]
-    pos = pre.clone()
-    lens = torch.tensor([int(x) for x in lens_np], dtype=torch.int32, device=dev)
-    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, ctx, int(max(lens_np)), w.in_dtype, w.out_dtype,
-                          device=dev)
-    out = plan.new_out(dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i, kv_new=None, q=None, stream=stream):
-        kn, vn = kv_new if kv_new is not None else steps_kv[i % 4]
-        c = i % copies
-        api.quantize_prod(kc, kn, kcs[c], pos=pos, stream=stream)
-        api.quantize_mse(vc, vn, vcs[c], pos=pos, stream=stream)
-        plan.run(kc, vc, steps_q[i % 4] if q is None else q, kcs[c], vcs[c], lens, out,
-                 stream=stream)
-
-    def decode_only(i, stream=stream):
-        c = i % copies
-        plan.run(kc, vc, steps_q[i % 4], kcs[c], vcs[c], lens, out, stream=stream)
-
-    # quantise K, quantise V, query fragments, split decode (its last CTA per head merges)
-    launches_per_step = 4
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
-    # The timed steps replay CUDA graphs captured from the same library calls, so that the
-    # measurement is the GPU's time and not the Python launch loop's.
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            cs = torch.cuda.current_stream(dev)
-            for i in range(args.steps):
-                fn(i, stream=cs)
-        stream.wait_stream(cap)
-        return g
-
-    g_step = capture(step)
-    g_dec = capture(decode_only)
-    g_step.replay()
-    g_dec.replay()
-    torch.cuda.synchronize()
-    barrier(ws)
-
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
-        for _ in range(3):                 # untimed replays keep the clock sampler busy
-            g_step.replay()
-        torch.cuda.synchronize()
-        barrier(ws)
-        t0.record(stream)
-        g_step.replay()                    # exactly args.steps steps
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-        d0.record(stream)
-        g_dec.replay()                     # the same decode-attention calls alone
-        d1.record(stream)
-        torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
-    ms_per_step = max_over_ranks(total_ms / args.steps, ws, dev)
-    dec_mean = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws, dev)
-
-    tokens_per_step = n_tok
-    value = tokens_per_step * ws / (ms_per_step * 1e-3)
-    # algorithmic bytes of one decode-attention call: packed K and V codes of every cached
-    # token and head, the query and the output
-    from kv_cache_quantization_gb300 import _binding as Bn
-    code_bytes = (Bn.tq_code_bytes(Bn.TQ_PROD, w.k_bits) + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
-    dec_bytes = (w.kv_heads * n_tok * code_bytes
-                 + w.batch * w.q_heads * 128 * (2 + torch.finfo(w.out_dtype).bits // 8))
-    peak, peak_kind = read_peaks()
-    achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
-    # compaction bytes: every cached vector read once (bf16) and its code written
-    in_bytes = torch.finfo(w.in_dtype).bits // 8 * 128
-    comp_bytes = w.kv_heads * (n_tok - w.batch) * (2 * in_bytes + code_bytes)
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get(args.workload)
-        except Exception:
-            traffic = None
-
-    # ---------------- end to end through the public API with host buffers
-    # a step's inputs (query, new key, new value) travel as one packed pinned buffer: one
-    # host-to-device copy a step, the tensors the library sees are views into its device copy
-    parts = [steps_q[0], steps_kv[0][0], steps_kv[0][1]]
-    sizes = [t.numel() * t.element_size() for t in parts]
-    offs = [0, sizes[0], sizes[0] + sizes[1]]
-    h2d = sum(sizes)
-    in_dev = torch.empty(h2d, dtype=torch.uint8, device=dev)
-    q_dev, k_dev, v_dev = (in_dev[o:o + n].view(t.dtype).view(t.shape)
-                           for o, n, t in zip(offs, sizes, parts))
-    in_host = []
-    for i in range(4):
-        buf = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-        for o, n, t in zip(offs, sizes, (steps_q[i], steps_kv[i][0], steps_kv[i][1])):
-            buf[o:o + n].copy_(t.contiguous().cpu().view(-1).view(torch.uint8))
-        in_host.append(buf)
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d2h = out.numel() * out.element_size()
-    def e2e_step(i, stream=stream):
-        in_dev.copy_(in_host[i % 4], non_blocking=True)
-        step(i, (k_dev, v_dev), q_dev, stream=stream)
-        out_host.copy_(out, non_blocking=True)
-
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_eager_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    # the same steps (copies in, library calls, copy out) captured once and replayed
-    g_e2e = capture(e2e_step)
-    g_e2e.replay()
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0.record(stream)
-    g_e2e.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_graph_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    e2e_ms = min(e2e_graph_ms, e2e_eager_ms)
-
+        if w.k_bits == 0:
+            head = measure_asym(w, args, dev, ws, peak)
+        else:
+            head = measure_sym(w, args, dev, ws, peak, headline=True)
+    clocks = clk.summary()
+    per = {}
+    if not args.no_per_workload:
+        for name in PER_WORKLOAD:
+            if name == w.name:
+                continue
+            wl = synth.WORKLOADS[name]
+            with ClockSampler(torch.cuda.current_device()) as c2:
+                r = (measure_asym(wl, args, dev, ws, peak) if wl.k_bits == 0
+                     else measure_sym(wl, args, dev, ws, peak, headline=False))
+            r["config"] = describe(wl, ws)
+            r["clocks"] = c2.summary()
+            per[name] = r
+            torch.cuda.empty_cache()
     result = {
-        "metric": METRIC,
-        "value": value,
-        "unit": UNIT,
-        "n_gpus": ws,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 in / fp32 accumulate on packed K3/V4 codes",
-        "data": "synthetic (seeded N(0,1) x lognormal(0,0.5) per channel)",
-        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
-                   "kv_heads": w.kv_heads, "head_dim": 128, "context": ctx, "tokens_attended": n_tok,
-                   "k_bits": w.k_bits, "v_bits": w.v_bits,
-                   "parallelism": f"replicas x{ws} (independent batches)",
-                   "l2": f"{copies} rotating cache copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
-                   "step": "quantise new K,V token + decode attention over all tokens",
-                   "timing": "CUDA-graph replay of the K steps, CUDA events around it"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "tq_decode_attention (query prep + split decode + merge)",
-                     "algorithmic_bytes": dec_bytes, "ms": dec_mean,
-                     "peak_source": peak_kind},
-        "e2e": {"value": tokens_per_step * ws / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "timing": "every step: one pinned-host copy in (query, new key and value "
-                          "packed), library calls, copy out; the faster of an eager Python "
-                          "loop and one CUDA graph of the K steps",
-                "ms_per_step_eager": e2e_eager_ms, "ms_per_step_graph": e2e_graph_ms},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
-        "compaction": {"vectors": 2 * w.kv_heads * (n_tok - w.batch), "ms": compaction_ms,
-                       "vectors_per_s": 2 * w.kv_heads * (n_tok - w.batch) / (compaction_ms * 1e-3),
-                       "what": "quantise the cached K (product code) and V (MSE code) once",
-                       "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak,
-                                    "achieved": comp_bytes / (compaction_ms * 1e-3) / 1e9,
-                                    "frac": comp_bytes / (compaction_ms * 1e-3) / 1e9 / peak,
-                                    "algorithmic_bytes": comp_bytes,
-                                    "note": "input vectors read once, codes and norms written"}},
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(result), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-
-
-def run_ours_asym(args, w, ws, rank, dev):
-    """Asymmetric workload: FP16 keys, 4-bit MSE values and an FP16 tail of 255 tokens per
-    sequence.  The timed step is one decode-attention call over the compressed part and the
-    tail (the tail's FP16 append is a copy, not part of this path)."""
-    import torch
-
-    from kv_cache_quantization_gb300 import api, synth
-
-    lens_np = synth.seq_lengths(w)                       # compressed tokens per sequence
-    tail = w.tail
-    n_tok = int(sum(lens_np)) + w.batch * tail
-    vc = api.Codec.mse(w.v_bits)
-    k, v = synth.make_kv(w, device=dev)
-    lens = torch.tensor([int(x) for x in lens_np], dtype=torch.int32, device=dev)
-    tl = torch.full((w.batch,), tail, dtype=torch.int32, device=dev)
-    tail_cap = 256
-    base_v = api.MSECache.empty(w.batch, w.kv_heads, w.context, w.v_bits, device=dev)
-    api.quantize_mse(vc, v, base_v, count=lens)
-    k16 = k.to(torch.float16)
-    kt = k16[:, :, w.context - tail_cap:].contiguous()
-    vt = v[:, :, w.context - tail_cap:].to(torch.float16).contiguous()
-    del k, v
-    torch.cuda.synchronize()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_copy = k16.numel() * 2 + base_v.nbytes() + kt.numel() * 4
-    copies = max(3, math.ceil(3 * l2 / per_copy))
-    sets = [(k16, base_v, kt, vt)] + [
-        (k16.clone(), api.MSECache(base_v.idx.clone(), base_v.xnorm.clone(), w.v_bits), kt.clone(),
-         vt.clone()) for _ in range(copies - 1)]
-    steps_q = [synth.make_queries(w, device=dev, step=i)[:, :, 0] for i in range(4)]
-    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, w.context, int(max(lens_np)), w.in_dtype,
-                          w.out_dtype, device=dev, tail_capacity=tail_cap)
-    out = plan.new_out(dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i, q=None, stream=stream):
-        kk, vv, ktt, vtt = sets[i % copies]
-        plan.run_asym(vc, steps_q[i % 4] if q is None else q, kk, vv, lens, ktt, vtt, tl, out,
-                      stream=stream)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.graph(g, stream=cap):
-        cs = torch.cuda.current_stream(dev)
-        for i in range(args.steps):
-            step(i, stream=cs)
-    stream.wait_stream(cap)
-    g.replay()
-    torch.cuda.synchronize()
-    barrier(ws)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        barrier(ws)
-        t0.record(stream)
-        g.replay()
-        t1.record(stream)
-        torch.cuda.synchronize()
-    ms_per_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, ws, dev)
-    value = n_tok * ws / (ms_per_step * 1e-3)
-    from kv_cache_quantization_gb300 import _binding as Bn
-    dec_bytes = (w.kv_heads * (int(sum(lens_np)) * (256 + Bn.tq_code_bytes(Bn.TQ_MSE, w.v_bits))
-                               + w.batch * tail * 512)
-                 + w.batch * w.q_heads * 128 * (2 + torch.finfo(w.out_dtype).bits // 8))
-    peak, peak_kind = read_peaks()
-    achieved = dec_bytes / (ms_per_step * 1e-3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get(args.workload)
-        except Exception:
-            traffic = None
-    # end to end: the query from pinned host memory in, the output back, every step
-    q_host = [steps_q[i].cpu().pin_memory() for i in range(4)]
-    q_dev = torch.empty_like(steps_q[0])
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    def e2e_step(i, stream=stream):
-        q_dev.copy_(q_host[i % 4], non_blocking=True)
-        step(i, q_dev, stream=stream)
-        out_host.copy_(out, non_blocking=True)
-
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_eager_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    g_e2e = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.graph(g_e2e, stream=cap):
-        cs = torch.cuda.current_stream(dev)
-        for i in range(args.steps):
-            e2e_step(i, stream=cs)
-    stream.wait_stream(cap)
-    g_e2e.replay()
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0.record(stream)
-    g_e2e.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_graph_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    e2e_ms = min(e2e_graph_ms, e2e_eager_ms)
-    result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 queries, fp16 keys, 4-bit value codes / fp32 accumulate, bf16 out",
-        "data": "synthetic (seeded N(0,1) x lognormal(0,0.5) per channel)",
-        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
-                   "kv_heads": w.kv_heads, "head_dim": 128, "context": w.context,
-                   "tokens_attended": n_tok, "k_bits": 0, "v_bits": w.v_bits, "tail": tail,
-                   "parallelism": f"replicas x{ws} (independent batches)",
-                   "l2": f"{copies} rotating copies ({copies * per_copy / 2**20:.0f} MiB > 3x L2)",
-                   "step": "decode attention over the compressed part and the FP16 tail",
-                   "timing": "CUDA-graph replay of the K steps, CUDA events around it"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "tq_decode_attention_asym (split decode + merge)",
-                     "algorithmic_bytes": dec_bytes, "ms": ms_per_step, "peak_source": peak_kind},
-        "e2e": {"value": n_tok * ws / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": q_dev.numel() * q_dev.element_size(),
-                "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e2e_ms,
-                "timing": "every step: pinned-host copy in, library call, copy out; the faster "
-                          "of an eager Python loop and one CUDA graph of the K steps",
-                "ms_per_step_eager": e2e_eager_ms, "ms_per_step_graph": e2e_graph_ms},
-        "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(),
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": ws,
+        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in; fp32 accumulation on packed codes (e4m3 x e4m3 key products, fp16 "
+                 "value products)",
+        "data": "synthetic (seeded N(0,1); keys with 4 outlier channels x10)",
+        "config": dict(describe(w, ws), tokens_attended=head["tokens_attended_per_step"],
+                       l2=head["l2"], step=head["step"],
+                       timing="CUDA-graph replay of the K steps, CUDA events around it"),
+        "roofline": dict(head["decode_call"],
+                         kernel="tq_decode_attention (query operand + split decode with its "
+                                "merge)"),
+        "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": clocks,
+        "compaction": head.get("compaction"),
+        "per_workload": per,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)
@@ -528,10 +559,11 @@ class OracleSample:
         self.q = q[0:1, :w.group].double().numpy()
         if not w.k_bits:
             # asymmetric: FP16 keys, and an FP16 tail of w.tail tokens after the sample
+            import torch
             kt, vt = synth.make_kv(w, device="cpu", tokens=max(w.tail, 1))
-            self.kx = k[0, 0].to(torch_f16()).double().numpy()
-            self.kt = kt[0:1, 0:1].to(torch_f16()).double().numpy()
-            self.vt = vt[0:1, 0:1].to(torch_f16()).double().numpy()
+            self.kx = k[0, 0].to(torch.float16).double().numpy()
+            self.kt = kt[0:1, 0:1].to(torch.float16).double().numpy()
+            self.vt = vt[0:1, 0:1].to(torch.float16).double().numpy()
 
     def rep(self):
         o = self.o
@@ -556,9 +588,7 @@ class OracleSample:
                 f"{self.w.context} tokens; {what}; {reps} reps in {el:.1f} s")
 
 
-def oracle_baseline(w, budget_s=15.0):
-    """cpu_baseline object: the oracle timed on its bounded sample for about budget_s."""
-    smp = OracleSample(w)
+def _timed_reps(smp, budget_s):
     smp.rep()
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -566,14 +596,33 @@ def oracle_baseline(w, budget_s=15.0):
         reps += 1
         el = time.perf_counter() - t0
         if el > budget_s:
-            break
-    return {"value": smp.tokens_per_s(el / reps), "unit": UNIT, "cores": _blas_threads(),
-            "kind": "oracle", "sample": smp.describe(reps, el)}
+            return reps, el
 
 
-def torch_f16():
-    import torch
-    return torch.float16
+def oracle_baseline(w, budget_s=15.0):
+    """cpu_baseline object: the oracle timed on its bounded sample for about budget_s with the
+    BLAS threads it has, and for a shorter while on one thread."""
+    smp = OracleSample(w)
+    reps, el = _timed_reps(smp, budget_s)
+    out = {"value": smp.tokens_per_s(el / reps), "unit": UNIT, "cores": _blas_threads(),
+           "kind": "oracle", "sample": smp.describe(reps, el)}
+    # one thread: a fresh interpreter whose BLAS is limited to one thread from the start
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--single-thread-oracle",
+                            "--workload", w.name, "--cpu-seconds", str(budget_s / 3)],
+                           env=env, capture_output=True, text=True, timeout=300)
+        out["single_thread_value"] = float(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        out["single_thread_value"] = None
+    return out
+
+
+def single_thread_oracle(args):
+    from kv_cache_quantization_gb300 import synth
+    smp = OracleSample(synth.WORKLOADS[args.workload])
+    reps, el = _timed_reps(smp, args.cpu_seconds)
+    print(smp.tokens_per_s(el / reps))
 
 
 def _blas_threads():
@@ -586,8 +635,8 @@ def _blas_threads():
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle on the host cores, W warm-up and K timed steps,
-    each step one repetition of the bounded sample.  Only rank 0 runs."""
+    """The reference arm: the CPU oracle on the host cores, W warm-up and K timed steps, each
+    step one repetition of the bounded sample.  Only rank 0 runs."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
@@ -602,12 +651,14 @@ def run_reference(args):
         smp.rep()
     el = time.perf_counter() - t0
     value = smp.tokens_per_s(el / args.steps)
-    ms = w.batch * w.context / value * 1e3
+    tokens = int(sum(min(int(x), w.context) for x in synth.seq_lengths(w))) + w.batch * w.tail
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "ms_per_step_what": "one repetition of the bounded sample (measured)",
+        "full_step_ms_extrapolated": tokens / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(describe(w, ws), tokens_attended=tokens),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                          "sample": smp.describe(args.steps, el)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -620,13 +671,17 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_gqa28x4_ctx32768_k3v4")
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--single-thread-oracle", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.single_thread_oracle:
+        single_thread_oracle(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -191,12 +191,11 @@ size_t tq_decode_workspace_bytes(const tq_attn_desc* desc);
  *   seq_lens : device int32[batch]; tokens t < seq_lens[b] are attended (clamped to
  *              capacity, flagged if larger).  A zero length gives a zero output row.
  *   out      : device [batch][q_heads][128] of desc->out_dtype.
- *   workspace: device, ≥ tq_decode_workspace_bytes(desc) bytes, 256-byte aligned, and
- *              zero-filled before its first use: the call keeps per-(batch, KV head)
- *              split tickets in it and leaves them at zero when it completes, so one
- *              zero fill serves every later call (with any descriptor that fits).  After a
- *              call whose device status reports TQ_FLAG_TIMEOUT, zero it again.  Calls that
- *              share a workspace must be serialised on one stream. */
+ *   workspace: device, ≥ tq_decode_workspace_bytes(desc) bytes, 256-byte aligned, scratch
+ *              owned by the caller.  It needs no initialisation: the call clears the
+ *              per-(batch, KV head) split tickets it keeps there at its start, so one
+ *              workspace may serve calls with different descriptors and asymmetric calls in
+ *              turn.  Calls that share a workspace must be serialised on one stream. */
 tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
                               const void* q, tq_prod_cache k, tq_mse_cache v,
                               const int32_t* seq_lens, void* out, void* workspace,
@@ -232,11 +231,12 @@ tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,
  *   entry point there).
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *   with that device current, so make the first call on each device before capturing any
- *   stream.  All calls on a device share the one array: calls that may overlap on the GPU
- *   (different streams without ordering between them) race and must not be issued; calls
- *   ordered on one stream are safe.  The array keeps the previous call's data; each call
- *   first clears the few bytes of it that must start at zero (its split tickets), on its
- *   stream, then runs. */
+ *   stream.  The address is cached for the device's primary context: after cudaDeviceReset
+ *   (which also destroys every codec on the device) the library must not be used on that
+ *   device again.  All calls on a device share the one array: calls that may overlap on the
+ *   GPU (different streams without ordering between them) race and must not be issued;
+ *   calls ordered on one stream are safe.  The array keeps the previous call's data; the
+ *   decode path clears the part that must start at zero (its split tickets) itself. */
 tq_status tq_decode_attention_noalloc(const tq_attn_desc* desc, const tq_codec* kc,
                                       const tq_codec* vc, const void* q, tq_prod_cache k,
                                       tq_mse_cache v, const int32_t* seq_lens, void* out,
@@ -253,8 +253,18 @@ size_t tq_decode_noalloc_scratch_bytes(void);
 #define TQ_FLAG_TIMEOUT      0x4u   /* a bounded device-side wait gave up */
 
 /* Synchronises the current device, returns the status word in *flags (host) and clears
- * it.  Returns TQ_ERR_DEVICE_STATUS if any bit was set, TQ_OK otherwise. */
+ * it.  Returns TQ_ERR_TIMEOUT if TQ_FLAG_TIMEOUT was set, else TQ_ERR_DEVICE_STATUS if any
+ * other bit was set, TQ_OK otherwise. */
 tq_status tq_device_status(uint32_t* flags);
+
+/* Exercises the bounded device-side wait that every kernel of the library uses on its
+ * barriers (no counterpart on the pages: failure detection of this implementation).  Launches
+ * one warp on `stream` that waits on a barrier nothing arrives at, with a limit of `limit_us`
+ * microseconds (1..1000000) of GPU time; the wait gives up, raises TQ_FLAG_TIMEOUT and the
+ * kernel returns, leaving the context usable.  A following tq_device_status() then returns
+ * TQ_ERR_TIMEOUT and clears the flag.  Returns TQ_ERR_INVALID_ARG for a limit out of range,
+ * TQ_ERR_CUDA if the launch fails. */
+tq_status tq_check_bounded_wait(uint32_t limit_us, tq_stream_t stream);
 
 /* Library version string. */
 const char* tq_version(void);

@@ -68,6 +68,7 @@ SIGNATURES = {
                                                    tq_prod_cache, tq_mse_cache, _vp, _vp, _vp]),
     "tq_decode_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "tq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "tq_check_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _vp]),
 }
 
 _lib = None
@@ -188,6 +189,10 @@ def tq_decode_attention_noalloc(desc: tq_attn_desc, kc, vc, q, k: tq_prod_cache,
 
 def tq_decode_noalloc_scratch_bytes() -> int:
     return load().tq_decode_noalloc_scratch_bytes()
+
+
+def tq_check_bounded_wait(limit_us: int, stream) -> int:
+    return load().tq_check_bounded_wait(limit_us, ptr(stream))
 
 
 def tq_device_status():

@@ -210,6 +210,10 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   // that kernel's output, so the split grid may start only once every CTA is past this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The split tickets of this (batch, KV head) start the call at zero whatever the workspace
+  // held before (another descriptor's records, an asymmetric call, a call that gave up on a
+  // wait): the split grid takes tickets only after this grid has completed.
+  if (blockIdx.x == 0 && tid == 0) a.counters[bh] = 0;
   for (int i = tid; i < 8 * TQ_D; i += kPrepThreads) {
     const int h = i >> 7, jq = i & 127;
     float v = 0.f;
@@ -1173,7 +1177,28 @@ tq_status launch_k(const tq_mma_launch& a, cudaStream_t stream) {
   return TQ_ERR_UNSUPPORTED;
 }
 
+// A barrier that nothing ever arrives at, waited on with the kernels' bounded wait: the wait
+// gives up after limit_ns of global time and raises TQ_FLAG_TIMEOUT, and the kernel returns.
+// No copy, MMA or TMEM allocation is outstanding while it waits.
+__global__ void bounded_wait_check_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, limit_ns);
+  if (!__any_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+}
+
 }  // namespace
+
+extern "C" tq_status tq_check_bounded_wait(uint32_t limit_us, tq_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return TQ_ERR_INVALID_ARG;
+  bounded_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      (unsigned long long)limit_us * 1000ull);
+  return tq_cuda_status(cudaGetLastError());
+}
 
 bool tq_tc_decode_supported(int kbits, int vbits, int G, int nsplit) {
   return kbits >= 1 && kbits <= 3 && vbits >= 1 && vbits <= 4 && G >= 1 && G <= 8 &&

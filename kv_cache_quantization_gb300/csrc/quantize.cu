@@ -476,5 +476,6 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   const unsigned int f = tq_take_flags_decode_asym();
   if (a == ~0u || b == ~0u || d == ~0u || e == ~0u || f == ~0u) return TQ_ERR_CUDA;
   *flags = a | b | d | e | f;
+  if (*flags & TQ_FLAG_TIMEOUT) return TQ_ERR_TIMEOUT;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

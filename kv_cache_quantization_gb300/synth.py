@@ -133,3 +133,27 @@ def make_new_tokens(w: Workload, device="cpu", step: int = 0):
     k = _draw(w, "k", shape, gen, device)
     v = _draw(w, "v", shape, gen, device)
     return k.to(w.in_dtype), v.to(w.in_dtype)
+
+
+def cache_capacity(w: Workload) -> int:
+    """Tokens per (sequence, KV head) a cache for the workload must hold: its context, or its
+    longest sequence after the decode steps' appends if that is more, in whole 64-token
+    blocks."""
+    need = max(w.context, int(seq_lengths(w).max()) + w.decode_steps)
+    return (need + 63) // 64 * 64
+
+
+TAIL_CAPACITY = 256   # FP16 tail slots per (sequence, KV head): at most min_compress - 1 used
+
+
+def asym_tail(w: Workload, k: torch.Tensor, v: torch.Tensor):
+    """FP16 tail of the asymmetric workload, [B, Hkv, TAIL_CAPACITY, d]: slots t < w.tail hold
+    the last w.tail tokens of each sequence (the ones not in the compressed part), the rest
+    are zero."""
+    shape = (w.batch, w.kv_heads, TAIL_CAPACITY, HEAD_DIM)
+    kt = torch.zeros(shape, dtype=torch.float16, device=k.device)
+    vt = torch.zeros(shape, dtype=torch.float16, device=v.device)
+    start = w.context - w.tail
+    kt[:, :, :w.tail] = k[:, :, start:w.context].to(torch.float16)
+    vt[:, :, :w.tail] = v[:, :, start:w.context].to(torch.float16)
+    return kt, vt

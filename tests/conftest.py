@@ -8,3 +8,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter):
+    parity = sys.modules.get("parity")
+    if parity is None or not getattr(parity, "REPORT", None):
+        return
+    terminalreporter.write_sep("-", "boundary exclusions of the full-size workloads")
+    for name, (stats, extra) in sorted(parity.REPORT.items()):
+        terminalreporter.write_line(f"{name}: {stats} {extra}".rstrip())

@@ -22,6 +22,15 @@ D = 128
 MAX_AMBIGUOUS = 6
 
 
+# Exclusion counts of the full-size workloads, by workload name (printed at the end of the
+# test session by conftest.py so that a quiet run still shows them).
+REPORT = {}
+
+
+def report(name, stats, extra=""):
+    REPORT[name] = (stats, extra)
+
+
 def oracle_constants(layer=0):
     sp, ss = layer_seeds(layer)
     return o.rotation_from_gaussian(gaussian_matrix(sp)), gaussian_matrix(ss)
@@ -40,8 +49,10 @@ class CodeStats:
         self.vectors_dropped = 0
 
     def __repr__(self):
+        c = max(self.coords, 1)
         return (f"coords={self.coords} idx_excluded={self.idx_excluded} "
-                f"idx_flipped={self.idx_flipped} sign_excluded={self.sign_excluded} "
+                f"({self.idx_excluded / c:.2e}) idx_flipped={self.idx_flipped} "
+                f"sign_excluded={self.sign_excluded} ({self.sign_excluded / c:.2e}) "
                 f"vectors_dropped={self.vectors_dropped}")
 
 
@@ -134,6 +145,17 @@ def rel_l2(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def check_heads(got, ref, tol, where):
+    """Relative L2 error of every query head's output row (got, ref: [G, d]) against tol;
+    returns the worst."""
+    worst = 0.0
+    for j in range(ref.shape[0]):
+        err = rel_l2(got[j], ref[j])
+        assert err < tol, f"{where}, query head {j} of the group: rel L2 {err:.3g}"
+        worst = max(worst, err)
+    return worst
 
 
 def unpack_prod_at(cache, b, h, toks, ibits):

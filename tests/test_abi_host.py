@@ -74,6 +74,11 @@ def test_code_bytes(lib):
     assert B.tq_code_bytes(B.TQ_PROD, 1) == 0 and B.tq_code_bytes(B.TQ_MSE, 5) == 0
 
 
+def test_bounded_wait_check_rejects_limits_out_of_range(lib):
+    assert B.tq_check_bounded_wait(0, None) == B.TQ_ERR_INVALID_ARG
+    assert B.tq_check_bounded_wait(1000001, None) == B.TQ_ERR_INVALID_ARG
+
+
 def test_invalid_arguments_rejected(lib):
     pi = np.eye(128)
     c = np.array([-0.1, 0.1])

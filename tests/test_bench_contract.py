@@ -18,7 +18,11 @@ def _check_line(d, n_gpus):
     assert d["unit"] == "KV tokens/s" and d["higher_is_better"] is True
     assert d["n_gpus"] == n_gpus and d["steps"] == 1 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
-    assert d["config"]["workload"] == "decode_gqa28x4_ctx32768_k3v4"
+    assert d["config"]["workload"] == "longctx_gqa32x8_ctx262144_k3v2"
+    assert d["config"]["context"] == 262144 and d["config"]["kv_heads"] == 8
+    # the step time is the measured repetition of the bounded sample; the projection to the
+    # whole workload is reported apart
+    assert d["full_step_ms_extrapolated"] > d["ms_per_step"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,

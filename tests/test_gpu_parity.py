@@ -13,8 +13,8 @@ import torch
 import oracle.turboquant as o
 from kv_cache_quantization_gb300 import _binding as B
 from kv_cache_quantization_gb300 import api, synth
-from parity import (CodeStats, match_mse_codes, match_prod_codes, oracle_codebook,
-                    oracle_constants, rel_l2, unpack_mse, unpack_prod)
+from parity import (CodeStats, check_heads, match_mse_codes, match_prod_codes,
+                    oracle_codebook, oracle_constants, rel_l2, report, unpack_mse, unpack_prod)
 
 pytestmark = pytest.mark.gpu
 
@@ -226,9 +226,8 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
         kd = {key: kcodes[key][None, None] for key in ("idx", "sign", "n", "gamma")}
         vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
         ref = o.decode_attention(qq, kd, vd, [n], pi, s, ck, cv)[0]
-        err = rel_l2(got[b, h * g:(h + 1) * g], ref)
-        worst = max(worst, err)
-        assert err < out_tol(out_dtype), f"(b={b}, kv head={h}) rel L2 {err:.3g}"
+        worst = max(worst, check_heads(got[b, h * g:(h + 1) * g], ref, out_tol(out_dtype),
+                                       f"(b={b}, kv head={h})"))
     assert stats.idx_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
     assert stats.sign_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
     return worst
@@ -327,11 +326,10 @@ def run_workload_decode(w, pairs):
         vd = {key: vcodes[key][None, None] for key in ("idx", "n")}
         ref = o.decode_attention(q[b:b + 1, h * g:(h + 1) * g].double().cpu().numpy(), kd, vd, [n],
                                  pi, s, ck, cv)[0]
-        err = rel_l2(out[b, h * g:(h + 1) * g], ref)
-        assert err < out_tol(w.out_dtype), f"(b={b}, kv head={h}): rel L2 {err:.3g}"
+        check_heads(out[b, h * g:(h + 1) * g], ref, out_tol(w.out_dtype), f"(b={b}, kv head={h})")
+    report(w.name, stats, f"pairs={len(pairs)}")
     assert stats.idx_excluded < 1e-4 * stats.coords, stats
     assert stats.sign_excluded < 1e-4 * stats.coords, stats
-    print(f"{w.name} code stats: {stats}")
 
 
 def test_decode_qwen7b_32k():
@@ -357,22 +355,30 @@ def test_decode_serving_ragged_b32():
 
 # ------------------------------------------------------------------ asymmetric mode
 
-def run_asym(batch, hq, hkv, lens, tlens, vbits, out_dtype, seed, tail_cap=256, sample=None):
+def run_asym(batch, hq, hkv, lens, tlens, vbits, out_dtype, seed, tail_cap=256, sample=None,
+             tensors=None, name=None):
+    """Asymmetric decode against the oracle.  tensors = (k fp16, v, k_tail fp16, v_tail fp16,
+    q) of a workload recipe, or None for test-local draws."""
     cap = max(64, (max(lens) + 63) // 64 * 64)
-    k = rand_x((batch, hkv, cap, D), seed, torch.bfloat16).to(torch.float16)
-    v = rand_x((batch, hkv, cap, D), seed + 1, torch.bfloat16)
-    kt = rand_x((batch, hkv, tail_cap, D), seed + 2, torch.bfloat16).to(torch.float16)
-    vt = rand_x((batch, hkv, tail_cap, D), seed + 3, torch.bfloat16).to(torch.float16)
-    q = rand_x((batch, hq, D), seed + 4, torch.bfloat16)
+    if tensors is None:
+        k = rand_x((batch, hkv, cap, D), seed, torch.bfloat16).to(torch.float16)
+        v = rand_x((batch, hkv, cap, D), seed + 1, torch.bfloat16)
+        kt = rand_x((batch, hkv, tail_cap, D), seed + 2, torch.bfloat16).to(torch.float16)
+        vt = rand_x((batch, hkv, tail_cap, D), seed + 3, torch.bfloat16).to(torch.float16)
+        q = rand_x((batch, hq, D), seed + 4, torch.bfloat16)
+    else:
+        k, v, kt, vt, q = tensors
+        cap = k.shape[2]
     vc = api.Codec.mse(vbits)
     vcache = api.MSECache.empty(batch, hkv, cap, vbits)
     lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
     tl_t = torch.tensor(tlens, dtype=torch.int32, device="cuda")
     api.quantize_mse(vc, v, vcache, count=lens_t)
     plan = api.DecodePlan(batch, hq, hkv, cap, max(lens), q.dtype, out_dtype, tail_capacity=tail_cap)
-    out = plan.run_asym(vc, q, k, vcache, lens_t, kt, vt, tl_t, plan.new_out())
+    out = plan.run_asym(vc, q, k, vcache, lens_t, kt, vt, tl_t, plan.new_out().fill_(float("nan")))
     got = out.double().cpu().numpy()
     check_flags_clear()
+    assert not np.isnan(got).any()
     pi, _ = oracle_constants()
     cv = oracle_codebook(vbits)
     g = hq // hkv
@@ -389,8 +395,10 @@ def run_asym(batch, hq, hkv, lens, tlens, vbits, out_dtype, seed, tail_cap=256, 
         if n + tl == 0:
             assert np.all(got[b, h * g:(h + 1) * g] == 0)
             continue
-        err = rel_l2(got[b, h * g:(h + 1) * g], ref)
-        assert err < out_tol(out_dtype), f"(b={b}, kv head={h}) rel L2 {err:.3g}"
+        check_heads(got[b, h * g:(h + 1) * g], ref, out_tol(out_dtype), f"(b={b}, kv head={h})")
+    if name:
+        report(name, stats, f"pairs={len(sample or [])}")
+    assert stats.idx_excluded < 1e-4 * max(stats.coords, 1) + 4, stats
 
 
 def test_asym_small():
@@ -406,8 +414,125 @@ def test_asym_value_bits_and_groups(vbits, hq, hkv):
 
 
 def test_asym_b8_8k():
-    """B=8, 28/4 heads, 7937 FP16-key / 4-bit-value tokens + 255 FP16 tail tokens, bf16 out."""
+    """B=8, 28/4 heads, the workload's own inputs: 7937 FP16-key / 4-bit-value tokens and the
+    last 255 tokens held as the FP16 tail, bf16 out; 8 of the 32 (batch, KV head) pairs checked
+    against the oracle, every query head on its own."""
     w = synth.ASYM_8K
     lens = [int(x) for x in synth.seq_lengths(w)]
-    run_asym(w.batch, w.q_heads, w.kv_heads, lens, [w.tail] * w.batch, w.v_bits, w.out_dtype, 800,
-             sample=[(0, 0), (3, 1), (7, 3)])
+    k, v = synth.make_kv(w, device="cuda")
+    kt, vt = synth.asym_tail(w, k, v)
+    q = synth.make_queries(w, device="cuda")[:, :, 0]
+    pairs = [(0, 0), (1, 3), (2, 1), (3, 2), (4, 0), (5, 3), (6, 2), (7, 1)]
+    run_asym(w.batch, w.q_heads, w.kv_heads, lens, [w.tail] * w.batch, w.v_bits, w.out_dtype, 0,
+             sample=pairs, tensors=(k.to(torch.float16), v, kt, vt, q), name=w.name)
+
+
+# ------------------------------------------------------------------ workspace reuse
+
+def test_workspace_reuse_across_descriptors():
+    """One workspace serves a larger symmetric call, an asymmetric call and a smaller call in
+    turn (each leaves its own data where the next keeps its split tickets); the smaller call's
+    output is bit for bit that of a fresh workspace."""
+    def case(batch, hq, hkv, n, seed):
+        k = rand_x((batch, hkv, n, D), seed, torch.bfloat16)
+        v = rand_x((batch, hkv, n, D), seed + 1, torch.bfloat16)
+        q = rand_x((batch, hq, D), seed + 2, torch.bfloat16)
+        kc, vc = api.Codec.prod(3), api.Codec.mse(4)
+        kcache = api.ProdCache.empty(batch, hkv, n, 3)
+        vcache = api.MSECache.empty(batch, hkv, n, 4)
+        api.quantize_prod(kc, k, kcache)
+        api.quantize_mse(vc, v, vcache)
+        lens = torch.full((batch,), n, dtype=torch.int32, device="cuda")
+        return kc, vc, q, kcache, vcache, lens, k, v
+    big = case(16, 28, 4, 2048, 950)
+    small = case(2, 14, 2, 1500, 960)
+    big_plan = api.DecodePlan(16, 28, 4, 2048, 2048, torch.bfloat16, torch.float32)
+    asym_plan = api.DecodePlan(16, 28, 4, 2048, 2048, torch.bfloat16, torch.float32,
+                               tail_capacity=256)
+    n = max(big_plan.workspace.numel(), asym_plan.workspace.numel())
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda").fill_(0xA5)
+    big_plan.workspace = ws
+    asym_plan.workspace = ws
+    big_plan.run(*big[:6], big_plan.new_out())
+    tl = torch.full((16,), 200, dtype=torch.int32, device="cuda")
+    kt = big[6][:, :, :256].to(torch.float16).contiguous()
+    vt = big[7][:, :, :256].to(torch.float16).contiguous()
+    asym_plan.run_asym(big[1], big[2], big[6].to(torch.float16), big[4], big[5], kt, vt, tl,
+                       asym_plan.new_out())
+    fresh = api.DecodePlan(2, 14, 2, 1500, 1500, torch.bfloat16, torch.float32)
+    ref = fresh.run(*small[:6], fresh.new_out())
+    out = torch.full(fresh.shape, float("nan"), device="cuda")
+    kc, vc, q, kcache, vcache, lens = small[:6]
+    B.check(B.tq_decode_attention(fresh.desc, kc.handle, vc.handle, q, kcache.c(), vcache.c(),
+                                  lens, out, ws, ws.numel(), torch.cuda.current_stream().cuda_stream),
+            "tq_decode_attention")
+    torch.cuda.synchronize()
+    check_flags_clear()
+    assert torch.equal(out, ref)
+
+
+# ------------------------------------------------------------------ serving loop
+
+def test_decode_serving_loop():
+    """The ragged serving batch (B=32, 4096–16384 tokens, 28/4 heads, K 4-bit prod, V 4-bit
+    MSE) for its 128 decode steps: every step appends one new key and value per (sequence, KV
+    head) at position len (tq_quantize_*, one token), the lengths grow by one, and decode
+    attention runs over the grown cache.  The oracle replays the appends and checks four
+    (sequence, KV head) pairs at steps 0, 1, 64 and 127, every query head on its own."""
+    w = synth.SERVE_B32
+    steps = w.decode_steps
+    lens0 = [int(x) for x in synth.seq_lengths(w)]
+    cap = synth.cache_capacity(w)
+    kc, vc = api.Codec.prod(w.k_bits), api.Codec.mse(w.v_bits)
+    k, v = synth.make_kv(w, device="cuda")
+    kcache = api.ProdCache.empty(w.batch, w.kv_heads, cap, w.k_bits)
+    vcache = api.MSECache.empty(w.batch, w.kv_heads, cap, w.v_bits)
+    lens_t = torch.tensor(lens0, dtype=torch.int32, device="cuda")
+    api.quantize_prod(kc, k, kcache, count=lens_t)
+    api.quantize_mse(vc, v, vcache, count=lens_t)
+    plan = api.DecodePlan(w.batch, w.q_heads, w.kv_heads, cap, max(lens0) + steps, w.in_dtype,
+                          w.out_dtype)
+    order = np.argsort(lens0)
+    pairs = [(int(order[-1]), 0), (int(order[0]), 3), (int(order[len(order) // 2]), 1), (7, 2)]
+    checkpoints = (0, 1, 64, steps - 1)
+    new_kv, queries, outs = [], {}, {}
+    for st in range(steps):
+        kn, vn = synth.make_new_tokens(w, device="cuda", step=st)
+        q = synth.make_queries(w, device="cuda", step=st)[:, :, 0]
+        api.quantize_prod(kc, kn, kcache, pos=lens_t)
+        api.quantize_mse(vc, vn, vcache, pos=lens_t)
+        lens_t = lens_t + 1
+        out = plan.run(kc, vc, q, kcache, vcache, lens_t, plan.new_out().fill_(float("nan")))
+        new_kv.append((kn[:, :, 0].double().cpu().numpy(), vn[:, :, 0].double().cpu().numpy()))
+        if st in checkpoints:
+            outs[st] = out.double().cpu().numpy()
+            queries[st] = q.double().cpu().numpy()
+    torch.cuda.synchronize()
+    check_flags_clear()
+    pi, s = oracle_constants(w.layer)
+    ck, cv = oracle_codebook(w.k_bits - 1), oracle_codebook(w.v_bits)
+    g = w.group
+    stats = CodeStats()
+    for b, h in pairs:
+        n0 = lens0[b]
+        n = n0 + steps
+        xk = np.concatenate([k[b, h, :n0].double().cpu().numpy(),
+                             np.stack([new_kv[t][0][b, h] for t in range(steps)])])
+        xv = np.concatenate([v[b, h, :n0].double().cpu().numpy(),
+                             np.stack([new_kv[t][1][b, h] for t in range(steps)])])
+        gi, gs, gx, gr = unpack_prod(kcache, b, h, n, w.k_bits - 1)
+        kcodes = match_prod_codes(xk, gi, gs, gx, gr, pi, s, ck, stats)
+        assert not kcodes["drop"].any()
+        vi, vx = unpack_mse(vcache, b, h, n, w.v_bits)
+        vcodes = match_mse_codes(xv, vi, vx, pi, cv, stats)
+        for st in checkpoints:
+            m = n0 + st + 1
+            kd = {key: kcodes[key][None, None, :m] for key in ("idx", "sign", "n", "gamma")}
+            vd = {key: vcodes[key][None, None, :m] for key in ("idx", "n")}
+            ref = o.decode_attention(queries[st][b:b + 1, h * g:(h + 1) * g], kd, vd, [m], pi, s,
+                                     ck, cv)[0]
+            check_heads(outs[st][b, h * g:(h + 1) * g], ref, out_tol(w.out_dtype),
+                        f"step {st}, (b={b}, kv head={h})")
+    report(w.name + " (128-step loop)", stats, f"pairs={len(pairs)}")
+    assert stats.idx_excluded < 1e-4 * stats.coords, stats
+    assert stats.sign_excluded < 1e-4 * stats.coords, stats
