@@ -291,19 +291,19 @@ class SymWorkload:
         return sum(self.lens0) + (i + 1) * self.w.batch if self.loop else sum(self.lens0)
 
     def step(self, i, stream, kv=None, q=None):
-        api = self.api
+        """One decode step through tq_decode_step: the new token's key and value are appended
+        at pos and pos + 1 tokens are attended."""
         s = i % self.nsteps
         kn, vn = kv if kv is not None else self.new_kv[s]
         q = self.queries[s] if q is None else q
         if self.loop:
             kcache, vcache = self.caches[0]
-            pos, lens = self.lens[s], self.lens[s + 1]
+            pos = self.lens[s]
         else:
             kcache, vcache = self.caches[i % self.copies]
-            pos, lens = self.pos, self.lens
-        api.quantize_prod(self.kc, kn, kcache, pos=pos, stream=stream)
-        api.quantize_mse(self.vc, vn, vcache, pos=pos, stream=stream)
-        self.plan.run(self.kc, self.vc, q, kcache, vcache, lens, self.out, stream=stream)
+            pos = self.pos
+        self.plan.step(self.kc, self.vc, q, kn[:, :, 0], vn[:, :, 0], kcache, vcache, pos,
+                       self.out, stream=stream)
 
     def decode_only(self, i, stream):
         s = i % self.nsteps
@@ -363,7 +363,7 @@ def measure_sym(w, args, dev, ws, peak, headline, clk=None):
         "l2": S.l2_note(),
         "decode_call": roofline(dec_bytes, dec_ms, w.name, peak),
         "compaction": S.compaction(peak),
-        "gpu_launches": 4 * n,
+        "gpu_launches": 2 * n,
     }
     if not headline:
         return res
@@ -517,7 +517,8 @@ def run_ours(args):
                        timing="CUDA-graph replay of the K steps, CUDA events around it"),
         "roofline": dict(head["decode_call"],
                          kernel="tq_decode_attention (query operand + split decode with its "
-                                "merge)"),
+                                "merge); the step is tq_decode_step (appends + operand in one "
+                                "prologue launch, then the split decode)"),
         "e2e": head.get("e2e"),
         "gpu_launches": head["gpu_launches"],
         "clocks": clocks,

@@ -201,6 +201,25 @@ tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc, cons
                               const int32_t* seq_lens, void* out, void* workspace,
                               size_t workspace_bytes, tq_stream_t stream);
 
+/* One decode step in a single call ([QJL] §六: the compressed store appends each new token's
+ * codes, then the read path attends the whole store; [MLX] quick start: append, then decode):
+ * quantises the step's new key (product code) and value (MSE code) of every (batch, KV head)
+ * into the caches at position pos[b], then runs decode attention over pos[b] + 1 tokens.  The
+ * result equals tq_quantize_prod + tq_quantize_mse (one token at pos) followed by
+ * tq_decode_attention with seq_lens = pos + 1; on the tensor-core path the appends and the
+ * query operand share one launch.
+ *   k_new, v_new : device [batch][kv_heads][128] of kv_dtype (F32, F16 or BF16), 16-byte
+ *                  aligned.
+ *   pos      : device int32[batch], the append positions (< capacity; a position out of range
+ *              is skipped and flagged TQ_FLAG_POS_OVERFLOW).  desc->max_seq_len must be at
+ *              least max(pos) + 1.
+ *   lens_out : device int32[batch] or NULL; receives pos[b] + 1 (must not alias pos).
+ *   Other arguments as tq_decode_attention (same workspace size). */
+tq_status tq_decode_step(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
+                         const void* q, const void* k_new, const void* v_new, tq_dtype kv_dtype,
+                         tq_prod_cache k, tq_mse_cache v, const int32_t* pos, int32_t* lens_out,
+                         void* out, void* workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* Asymmetric mode ([MLX] "对称 vs 非对称": K = FP16, V = turbo): keys stay FP16, values
  * are MSE-coded, and the most recent tokens sit uncompressed in an FP16 tail that joins
  * the same softmax.

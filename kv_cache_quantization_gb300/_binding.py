@@ -61,6 +61,9 @@ SIGNATURES = {
     "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp,
                                            tq_prod_cache, tq_mse_cache, _vp, _vp, _vp,
                                            ctypes.c_size_t, _vp]),
+    "tq_decode_step": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp, _vp, _vp,
+                                      ctypes.c_int, tq_prod_cache, tq_mse_cache, _vp, _vp, _vp,
+                                      _vp, ctypes.c_size_t, _vp]),
     "tq_decode_attention_asym": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp,
                                                 tq_mse_cache, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 ctypes.c_size_t, _vp]),
@@ -170,6 +173,14 @@ def tq_decode_attention(desc: tq_attn_desc, kc, vc, q, k: tq_prod_cache, v: tq_m
                         seq_lens, out, workspace, workspace_bytes, stream) -> int:
     return load().tq_decode_attention(ctypes.byref(desc), kc, vc, ptr(q), k, v, ptr(seq_lens),
                                       ptr(out), ptr(workspace), workspace_bytes, ptr(stream))
+
+
+def tq_decode_step(desc: tq_attn_desc, kc, vc, q, k_new, v_new, kv_dtype, k: tq_prod_cache,
+                   v: tq_mse_cache, pos, lens_out, out, workspace, workspace_bytes,
+                   stream) -> int:
+    return load().tq_decode_step(ctypes.byref(desc), kc, vc, ptr(q), ptr(k_new), ptr(v_new),
+                                 kv_dtype, k, v, ptr(pos), ptr(lens_out), ptr(out),
+                                 ptr(workspace), workspace_bytes, ptr(stream))
 
 
 def tq_decode_attention_asym(desc: tq_attn_desc, vc, q, k_f16, v: tq_mse_cache, seq_lens,

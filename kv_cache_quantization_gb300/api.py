@@ -227,6 +227,17 @@ class DecodePlan:
                                       _stream(stream)), "tq_decode_attention")
         return out
 
+    def step(self, kc: Codec, vc: Codec, q, k_new, v_new, k: ProdCache, v: MSECache, pos, out,
+             lens_out=None, stream=None):
+        """Appends k_new, v_new [batch, kv_heads, 128] at pos[b] and attends pos[b] + 1 tokens."""
+        if k_new.dtype != v_new.dtype or not (k_new.is_contiguous() and v_new.is_contiguous()):
+            raise ValueError("k_new and v_new must be contiguous and of one dtype")
+        B.check(B.tq_decode_step(self.desc, kc.handle, vc.handle, q, k_new, v_new,
+                                 tq_dtype(k_new.dtype), k.c(), v.c(), pos, lens_out, out,
+                                 self.workspace, self.workspace.numel(), _stream(stream)),
+                "tq_decode_step")
+        return out
+
     def run_asym(self, vc: Codec, q, k_f16, v: MSECache, seq_lens, k_tail, v_tail, tail_lens,
                  out, stream=None):
         B.check(B.tq_decode_attention_asym(self.desc, vc.handle, q, k_f16, v.c(), seq_lens,

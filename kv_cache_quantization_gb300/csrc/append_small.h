@@ -1,0 +1,198 @@
+// Quantisation of one vector by one CTA of 512 threads: the path of a decode step's append
+// (one new key or value per sequence and KV head), where a whole tile of the tensor-core
+// quantiser would idle.  QJL deep-dive §二 steps 1–3 in the unit-sphere domain: y = Π x/‖x‖,
+// idx = #{boundaries ≤ y}, ρ = y − c[idx], sign(M ρ) with M = S Πᵀ, ‖r‖ = ‖x‖·‖ρ‖.
+//
+// Included by the translation units that launch it; each has its own device status word
+// g_tq_flags, defined (TQ_DEFINE_FLAGS) before this header is included.  Internal to the
+// library.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "append_args.h"
+#include "tq_internal.h"
+
+namespace tq {
+
+constexpr int kAppendThreads = 512;
+
+// One vector to quantise into a cache.
+struct AppendArgs {
+  const void* x;        // the vector's 128 coordinates (dtype), 16-byte aligned
+  int dtype;
+  int dst;              // cache position
+  long long bh;         // (batch, head) row of the cache
+  int capacity;
+  uint8_t* idx;         // plane-major index codes, or nibbles (nibbles != 0)
+  uint8_t* sgn;         // product code: sign plane (null for MSE codes)
+  float* xnorm;
+  float* rnorm;
+  tq_levels lv;
+  int ibits;
+  int nibbles;
+};
+
+// 8 consecutive elements of x (dtype F32, F16 or BF16) from element `off`, as floats.
+__device__ __forceinline__ void append_load8(const void* base, int dtype, long long off,
+                                             float* out) {
+  if (dtype == TQ_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+  } else {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (dtype == TQ_BF16) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      } else {
+        __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+        float2 f = __half22float2(h);
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+      }
+    }
+  }
+}
+
+// Thread (k quarter q, output j) of the 512 owns T[32q..32q+31][j] of T = Πᵀ or Mᵀ (row-major
+// [128][128]); the values are requested at kernel start, before the programmatic wait.
+__device__ __forceinline__ void append_load_t(const float* __restrict__ T, float (&t)[32],
+                                              int tid) {
+  const int j = tid & 127, q = tid >> 7;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * q + k) * TQ_D + j]);
+}
+
+// (T v)_j for j = tid < 128 (other threads get 0): four partial sums over k quarters meet in
+// `part` [4][128].  Contains two __syncthreads.
+__device__ __forceinline__ float append_matvec(const float (&t)[32], const float* v, float* part,
+                                               int tid) {
+  const int j = tid & 127, q = tid >> 7;
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) acc = fmaf(t[k], v[32 * q + k], acc);
+  part[q * TQ_D + j] = acc;
+  __syncthreads();
+  float r = 0.f;
+  if (tid < TQ_D) r = (part[j] + part[TQ_D + j]) + (part[2 * TQ_D + j] + part[3 * TQ_D + j]);
+  __syncthreads();
+  return r;
+}
+
+// Shared memory of one append CTA.
+struct AppendSmem {
+  float xs[TQ_D], rho[TQ_D], part[4 * TQ_D];
+  float red[4];
+};
+
+// Quantises the vector into the cache: every thread of the CTA calls it (it synchronises the
+// CTA); tp (and tm for a product code) were loaded by append_load_t.  The caller has checked
+// that a.dst lies inside the capacity.
+template <bool kProd>
+__device__ __forceinline__ void append_quantize(const AppendArgs& a, const float (&tp)[32],
+                                                const float (&tm)[32], AppendSmem& sm, int tid) {
+  float vals[8];
+  if (tid < 16) append_load8(a.x, a.dtype, tid * 8, vals);
+  const long long slot = a.bh * a.capacity + a.dst;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < 16) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm.xs[tid * 8 + e] = vals[e];
+  }
+  __syncthreads();
+  float x2 = 0.f;
+  if (tid < TQ_D) x2 = sm.xs[tid] * sm.xs[tid];
+  if (warp < 4) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x2 += __shfl_xor_sync(0xffffffffu, x2, o);
+    if (lane == 0) sm.red[warp] = x2;
+  }
+  __syncthreads();
+  const float n = sqrtf((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3]));
+  const float acc = append_matvec(tp, sm.xs, sm.part, tid);
+  int q = 0;
+  float r = 0.f;
+  if (tid < TQ_D) {
+    const float y = n > 0.f ? acc / n : 0.f;
+    for (int bnd = 0; bnd < a.lv.levels - 1; ++bnd) q += (a.lv.b[bnd] <= y) ? 1 : 0;
+    r = y - a.lv.c[q];
+    sm.rho[tid] = r;
+  }
+  // index codes: warp w < 4 owns coordinates 32w..32w+31
+  if (warp < 4) {
+    if (a.nibbles) {
+      // byte k = idx(2k) | idx(2k+1) << 4: lane pairs combine through a shuffle
+      const int other = __shfl_xor_sync(0xffffffffu, q, 1);
+      if ((lane & 1) == 0) a.idx[slot * 64 + (tid >> 1)] = (uint8_t)(q | (other << 4));
+    } else {
+      for (int p = 0; p < a.ibits; ++p) {
+        const unsigned word = __ballot_sync(0xffffffffu, (q >> p) & 1);
+        if (lane == 0)
+          reinterpret_cast<uint32_t*>(
+              a.idx + ((a.bh * a.ibits + p) * a.capacity + a.dst) * 16)[warp] = word;
+      }
+    }
+    if (tid == 0) a.xnorm[slot] = n;
+  }
+  if constexpr (kProd) {
+    float r2 = r * r;
+    if (warp < 4) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, o);
+    }
+    __syncthreads();   // rho complete; red reused
+    if (warp < 4 && lane == 0) sm.red[warp] = r2;
+    const float z = append_matvec(tm, sm.rho, sm.part, tid);   // contains __syncthreads
+    if (warp < 4) {
+      const unsigned word = n > 0.f ? __ballot_sync(0xffffffffu, z >= 0.f) : 0xffffffffu;
+      if (lane == 0) reinterpret_cast<uint32_t*>(a.sgn + slot * 16)[warp] = word;
+      if (tid == 0) a.rnorm[slot] = n * sqrtf((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3]));
+    }
+  }
+}
+
+// One CTA of 512 threads appends the key (key = true) or the value of (batch b, KV head kvh).
+// The codec's constants are requested before the programmatic wait, everything the previous
+// kernel in the stream may write (the vectors, the positions, the caches) after it.
+__device__ __forceinline__ void append_kv_role(const AppendKV& a, bool key, int kvh, int b) {
+  __shared__ AppendSmem sm;
+  const int tid = threadIdx.x;
+  float tp[32], tm[32];
+  append_load_t(key ? a.kpiT : a.vpiT, tp, tid);
+  if (key) append_load_t(a.kmT, tm, tid);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long bh = (long long)b * a.Hkv + kvh;
+  const int pos = a.pos[b];
+  if (key && kvh == 0 && tid == 0 && a.lens_out) a.lens_out[b] = pos + 1;
+  if (pos < 0 || pos >= a.cap) {
+    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
+    return;
+  }
+  AppendArgs aa;
+  const long long off = bh * TQ_D;
+  aa.x = a.dtype == TQ_F32
+             ? static_cast<const void*>(static_cast<const float*>(key ? a.k_new : a.v_new) + off)
+             : static_cast<const void*>(static_cast<const uint16_t*>(key ? a.k_new : a.v_new) + off);
+  aa.dtype = a.dtype;
+  aa.dst = pos;
+  aa.bh = bh;
+  aa.capacity = a.cap;
+  if (key) {
+    aa.idx = a.kidx; aa.sgn = a.ksgn; aa.xnorm = a.kxn; aa.rnorm = a.krn;
+    aa.lv = a.klv; aa.ibits = a.kbits; aa.nibbles = 0;
+    append_quantize<true>(aa, tp, tm, sm, tid);
+  } else {
+    aa.idx = a.vidx; aa.sgn = nullptr; aa.xnorm = a.vxn; aa.rnorm = nullptr;
+    aa.lv = a.vlv; aa.ibits = a.vbits; aa.nibbles = a.v_nibbles;
+    append_quantize<false>(aa, tp, tm, sm, tid);
+  }
+}
+
+}  // namespace tq

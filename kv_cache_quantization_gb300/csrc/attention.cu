@@ -29,7 +29,7 @@ constexpr float kQjlNum = 1.2533141373155003f;   // √(π/2)
 
 struct Plan {
   int G, nsplit_main, nsplit_tail, nsplit, split_len;
-  size_t q_off, part_off, ctr_off, bytes;
+  size_t q_off, part_off, ctr_off, lens_off, bytes;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -82,7 +82,9 @@ tq_status plan(const tq_attn_desc* d, bool asym, Plan* p) {
   // split tickets of the tensor-core path: one int per (batch, KV head), cleared by the
   // query-operand kernel at the start of every call
   p->ctr_off = (p->part_off + pf * sizeof(float) + 255) / 256 * 256;
-  p->bytes = p->ctr_off + (size_t)d->batch * d->kv_heads * sizeof(int);
+  // a decode step on the CUDA-core path: the attended lengths pos + 1
+  p->lens_off = (p->ctr_off + (size_t)d->batch * d->kv_heads * sizeof(int) + 255) / 256 * 256;
+  p->bytes = p->lens_off + (size_t)d->batch * sizeof(int);
   return TQ_OK;
 }
 
@@ -460,11 +462,47 @@ extern "C" size_t tq_decode_workspace_bytes(const tq_attn_desc* desc) {
   return p.bytes;
 }
 
-extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc,
-                                         const tq_codec* vc, const void* q, tq_prod_cache k,
-                                         tq_mse_cache v, const int32_t* seq_lens, void* out,
-                                         void* workspace, size_t workspace_bytes,
-                                         tq_stream_t stream_) {
+namespace {
+
+// Inputs of a decode step that the plain decode call does not have.
+struct StepIn {
+  const void* k_new;
+  const void* v_new;
+  tq_dtype kv_dtype;
+  int32_t* lens_out;
+};
+
+// The appends of a decode step (the caches' pointers and the codecs' constants).
+tq::AppendKV append_args(const StepIn& in, const tq_attn_desc* desc, const tq_codec* kc,
+                         const tq_codec* vc, const tq_prod_cache& k, const tq_mse_cache& v,
+                         const int32_t* pos, const DecodeArgs& a) {
+  tq::AppendKV ap{};
+  ap.k_new = in.k_new; ap.v_new = in.v_new; ap.dtype = in.kv_dtype;
+  ap.pos = pos; ap.lens_out = in.lens_out;
+  ap.Hkv = desc->kv_heads; ap.cap = desc->capacity;
+  ap.kidx = k.idx; ap.ksgn = k.sgn; ap.kxn = k.xnorm; ap.krn = k.rnorm;
+  ap.vidx = v.idx; ap.vxn = v.xnorm;
+  ap.kpiT = kc->d_piT; ap.kmT = kc->d_mT; ap.vpiT = vc->d_piT;
+  ap.klv = a.kl; ap.vlv = a.vl;
+  ap.kbits = kc->ibits; ap.vbits = vc->ibits; ap.v_nibbles = vc->ibits == 4;
+  return ap;
+}
+
+// Attended lengths of a decode step on the CUDA-core path: pos + 1.
+__global__ void step_lens_kernel(const int32_t* pos, int n, int32_t* lens, int32_t* lens_out) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < n; b += gridDim.x * blockDim.x) {
+    const int32_t l = pos[b] + 1;
+    lens[b] = l;
+    if (lens_out) lens_out[b] = l;
+  }
+}
+
+// Symmetric decode attention, optionally preceded by a decode step's append (step != null:
+// seq_lens holds the append positions and pos + 1 tokens are attended).
+tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
+                     const void* q, tq_prod_cache k, tq_mse_cache v, const int32_t* seq_lens,
+                     void* out, void* workspace, size_t workspace_bytes, tq_stream_t stream_,
+                     const StepIn* step) {
   Plan p;
   tq_status st = plan(desc, false, &p);
   if (st != TQ_OK) return st;
@@ -475,6 +513,14 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   if (!q || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < p.bytes)
     return TQ_ERR_INVALID_ARG;
+  if (step) {
+    if (!step->k_new || !step->v_new || !aligned16(step->k_new) || !aligned16(step->v_new))
+      return TQ_ERR_INVALID_ARG;
+    if (step->kv_dtype != TQ_F32 && step->kv_dtype != TQ_F16 && step->kv_dtype != TQ_BF16)
+      return TQ_ERR_UNSUPPORTED;
+    if (step->lens_out && static_cast<const void*>(step->lens_out) == seq_lens)
+      return TQ_ERR_INVALID_ARG;
+  }
   if (desc->batch == 0) return TQ_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -514,7 +560,30 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
     m.counters = reinterpret_cast<int*>(ws + p.ctr_off);
     m.max_len = desc->max_seq_len;
     tq_tc_operand_scales(m.kd, &m.s_idx, &m.s_sgn);
-    return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
+    if (!step) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
+    m.app = append_args(*step, desc, kc, vc, k, v, seq_lens, a);
+    m.len_add = 1;
+    if (tq_step_prologue_fits(desc->batch, desc->kv_heads)) {
+      // the appends and the query operand in one prologue launch, then the split decode; the
+      // split grid reads the appended token only after the prologue has completed
+      m.fresh = 1;
+      return tq_launch_decode_step_tc(m, stream);
+    }
+    // many (batch, KV head) units: the appends as one launch, then the operand kernel and the
+    // split decode (the cache is final when the split grid starts)
+    m.fresh = 0;
+    if ((st = tq_launch_append_kv(m.app, desc->batch, stream)) != TQ_OK) return st;
+    return tq_launch_decode_tc(m, stream);
+  }
+  if (step) {
+    // CUDA-core path: the appends, then attention over pos + 1 tokens
+    if ((st = tq_launch_append_kv(append_args(*step, desc, kc, vc, k, v, seq_lens, a),
+                                  desc->batch, stream)) != TQ_OK)
+      return st;
+    int32_t* lens = reinterpret_cast<int32_t*>(ws + p.lens_off);
+    step_lens_kernel<<<(desc->batch + 255) / 256, 256, 0, stream>>>(seq_lens, desc->batch, lens,
+                                                                    nullptr);
+    a.seq_lens = lens;
   }
   query_prep_kernel<<<rows, kPrepThreads, 0, stream>>>(q, desc->q_dtype, kc->d_piT, kc->d_sT,
                                                    reinterpret_cast<float*>(ws + p.q_off));
@@ -522,6 +591,27 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
   merge_kernel<<<rows, kMergeThreads, 0, stream>>>(a.part, a.Hq, a.Hkv, a.G, p.nsplit_main, p.nsplit,
                                               vc->d_pi, out, desc->out_dtype);
   return tq_cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc,
+                                         const tq_codec* vc, const void* q, tq_prod_cache k,
+                                         tq_mse_cache v, const int32_t* seq_lens, void* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         tq_stream_t stream) {
+  return run_decode(desc, kc, vc, q, k, v, seq_lens, out, workspace, workspace_bytes, stream,
+                    nullptr);
+}
+
+extern "C" tq_status tq_decode_step(const tq_attn_desc* desc, const tq_codec* kc,
+                                    const tq_codec* vc, const void* q, const void* k_new,
+                                    const void* v_new, tq_dtype kv_dtype, tq_prod_cache k,
+                                    tq_mse_cache v, const int32_t* pos, int32_t* lens_out,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    tq_stream_t stream) {
+  const StepIn in{k_new, v_new, kv_dtype, lens_out};
+  return run_decode(desc, kc, vc, q, k, v, pos, out, workspace, workspace_bytes, stream, &in);
 }
 
 extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include "append_args.h"
 #include "tq_internal.h"
 
 // A codebook written as a sum over "virtual bit planes": with s_i = 2·bit_i − 1 the
@@ -49,6 +50,12 @@ struct tq_mma_launch {
   int* counters;               // [B][Hkv] split tickets (cleared by the operand kernel)
   int max_len;                 // longest sequence (tokens) of the call
   float s_idx, s_sgn;          // power-of-two scales of the e4m3 query operand
+  // attended tokens of batch b: seq_lens[b] + len_add; the last `fresh` of them may be written
+  // by the programmatic-launch primary, so the split kernel reads them only after its wait
+  int len_add, fresh;
+  // decode step with the appends in the prologue kernel: the step's new key and value,
+  // appended at seq_lens[b]
+  tq::AppendKV app;
 };
 
 // Odd-Walsh decomposition of a codec's levels (index bits ≤ 3).
@@ -56,6 +63,13 @@ tq_plane_decomp tq_decompose_levels(const tq_codec* c);
 // Tensor-core (tcgen05) split decode with in-kernel query operand and last-CTA merge.
 bool tq_tc_decode_supported(int kbits, int vbits, int G, int nsplit);
 tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream);
+// The same after a prologue kernel that appends the step's new key and value and builds the
+// query operand in one launch.
+tq_status tq_launch_decode_step_tc(const tq_mma_launch& a, cudaStream_t stream);
+// Whether that prologue fits in one wave of CTAs (else the appends run as their own launch).
+bool tq_step_prologue_fits(int batch, int kv_heads);
+// The appends of a decode step as one launch (quantize.cu), a programmatic-launch secondary.
+tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t stream);
 // Workspace bytes per (batch, KV head) for its query operand images.
 size_t tq_tc_frag_bytes_max();
 // Power-of-two scales of the e4m3 query operand for a key codec's decomposition.

@@ -43,6 +43,8 @@
 
 TQ_DEFINE_FLAGS(tq_take_flags_decode_tc)
 
+#include "append_small.h"
+
 namespace {
 using namespace tq;
 
@@ -50,10 +52,16 @@ constexpr int kTile = 128;                    // tokens per tile = TMEM lanes
 constexpr int kStageTok = 256;                // tokens per ring stage (two tiles)
 constexpr int kStages = 4;
 constexpr int kEWarps = 4;                    // expand planes into TMEM
-constexpr int kSWarps = 8;                    // softmax + values (two groups of four)
-constexpr int kIWarps = 3;                    // issue MMAs (one thread each)
-constexpr int kCompute = (kEWarps + kSWarps + kIWarps) * 32;
-constexpr int kThreads = kCompute + 32;       // + producer warp
+// Warp roles of a split CTA with NG softmax groups: 4 expander warps, NG groups of four
+// softmax + value warps (group g takes the tiles i ≡ g mod NG), one MMA-issue warp, and the
+// producer warp last.
+template <int NG>
+struct Roles {
+  static constexpr int S = 4 * NG;                           // softmax + value warps
+  static constexpr int issuer = kEWarps + S;                 // the MMA-issue warp
+  static constexpr int compute = (kEWarps + S + 1) * 32;    // every warp but the producer
+  static constexpr int threads = compute + 32;
+};
 constexpr int kPieces = 4;                    // e4m3 pieces per query value
 // MMA N: 4 pieces × 8 head columns, or (group of at most 4 heads) 4 pieces × 4 heads
 __host__ __device__ constexpr int kNof(bool hilo) { return hilo ? 16 : kPieces * 8; }
@@ -168,15 +176,16 @@ constexpr int kPrepThreads = 256;
 // SPC slices per CTA (grid kSlices / SPC × KV heads × batch): one slice a CTA while the grid
 // stays small; large batches take 2 or 4, so that the operand kernel runs in one short wave
 // and frees the SMs for the split grid.
+// The operand work of CTA `bx` for slices SPC·bx .. SPC·bx + SPC − 1, by the first kPrepThreads
+// threads of the CTA; any further threads only take part in the CTA barriers.
 template <int KB, bool HILO, int SPC>
-__global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
-    query_prep_tc_kernel(const tq_mma_launch a) {
+__device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) {
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
   constexpr int kBImg = kBImgOf(HILO);
   constexpr int kN = kNof(HILO);
   constexpr int NCOL = HILO ? 4 : 8;
-  // SPC = 4: the CTA holds K positions 32·blockIdx.x .. +31 of every operand row whole, so
+  // SPC = 4: the CTA holds K positions 32·bx .. +31 of every operand row whole, so
   // they are gathered here and leave as 16-byte stores
   __shared__ __align__(16) unsigned char stage[SPC == 4 ? NP * kN * 32 : 16];
   __shared__ __align__(16) float qf[8][TQ_D];
@@ -187,14 +196,15 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   const int kvh = blockIdx.y, b = blockIdx.z;
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool act = tid < kPrepThreads;
   // thread (which, k chunk kq, j in slice jl): 8 entries of row j of M (M = Π or S, read from
   // Mᵀ: the codec's constants) for each of its slices, requested at once
-  const int which = tid >> 7, kq = (tid >> 3) & 15, jl = tid & 7;
+  const int which = (tid >> 7) & 1, kq = (tid >> 3) & 15, jl = tid & 7;
   const float* T = which ? a.sT : a.piT;
   float t[SPC][8];
 #pragma unroll
   for (int u = 0; u < SPC; ++u) {
-    const int j = 8 * (SPC * (int)blockIdx.x + u) + jl;
+    const int j = 8 * (SPC * bx + u) + jl;
 #pragma unroll
     for (int k = 0; k < 8; ++k) t[u][k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
   }
@@ -213,8 +223,8 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   // The split tickets of this (batch, KV head) start the call at zero whatever the workspace
   // held before (another descriptor's records, an asymmetric call, a call that gave up on a
   // wait): the split grid takes tickets only after this grid has completed.
-  if (blockIdx.x == 0 && tid == 0) a.counters[bh] = 0;
-  for (int i = tid; i < 8 * TQ_D; i += kPrepThreads) {
+  if (bx == 0 && tid == 0) a.counters[bh] = 0;
+  for (int i = tid; act && i < 8 * TQ_D; i += kPrepThreads) {
     const int h = i >> 7, jq = i & 127;
     float v = 0.f;
     if (h < a.G) {
@@ -258,14 +268,14 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
       float x = 0.f;
-      if (h < NCOL) {
+      if (h < NCOL && act) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) x = fmaf(t[u][k], qf[h][8 * kq + k], x);
       }
-      red[u][which][kq][jl][h] = x;
+      if (act) red[u][which][kq][jl][h] = x;
     }
   __syncthreads();
-  for (int it = tid; it < SPC * 2 * 8 * 8; it += kPrepThreads) {
+  for (int it = tid; act && it < SPC * 2 * 8 * 8; it += kPrepThreads) {
     const int u = it >> 7, wh = (it >> 6) & 1, jj = (it >> 3) & 7, h = it & 7;
     float x = 0.f;
 #pragma unroll
@@ -279,9 +289,9 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   // the 8 items of a (slice, column) are adjacent lanes and add up its offsets by shuffles
   // (item counts are multiples of 32: whole warps take part)
   const float sgn_scale = a.s_sgn / a.smax;
-  for (int it = tid; it < SPC * NCOL * 8; it += kPrepThreads) {
+  for (int it = tid; act && it < SPC * NCOL * 8; it += kPrepThreads) {
     const int u = it / (NCOL * 8), n = (it >> 3) % NCOL, jj = it & 7;
-    const int s = SPC * (int)blockIdx.x + u;
+    const int s = SPC * bx + u;
     const int k = 32 * (s >> 2) + 4 * jj + (s & 3);   // coord_of_k(k) = 8s + jj
     const int r = jj;                                  // (k >> 2) & 7
     const float inq = s_inq[n];                        // 1/‖q‖; 0 for a zero or absent head
@@ -322,16 +332,16 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   }
   __syncthreads();
   if constexpr (SPC == 4) {
-    for (int c = tid; c < NP * kN * 2; c += kPrepThreads) {
+    for (int c = tid; act && c < NP * kN * 2; c += kPrepThreads) {
       const int v = c / (kN * 2), row = (c >> 1) % kN, hf = c & 1;
-      *reinterpret_cast<uint4*>(out + v * kBImg + bimg_off(row, 32 * (int)blockIdx.x + 16 * hf)) =
+      *reinterpret_cast<uint4*>(out + v * kBImg + bimg_off(row, 32 * bx + 16 * hf)) =
           *reinterpret_cast<const uint4*>(stage + (v * kN + row) * 32 + 16 * hf);
     }
   }
   if (tid < SPC * 2 * NCOL) {
     // the slices' operand offsets: [slice][index planes | sign plane][column]
     const int u = tid / (2 * NCOL), kind = (tid / NCOL) & 1, n = tid % NCOL;
-    const int s = SPC * (int)blockIdx.x + u;
+    const int s = SPC * bx + u;
     float* offp = cst + kCstFloats + s * 16 + kind * 8;
     if (HILO) {
       offp[2 * n] = s_off[u][kind][n];
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
       offp[n] = s_off[u][kind][n];
     }
   }
-  if (blockIdx.x == 0 && tid < 8) {
+  if (bx == 0 && tid < 8) {
     // score constants of column n: A, Cm, B, Cq (see the softmax warps)
     const int n = tid, head = HILO ? n >> 1 : n;
     const float nq = head < a.G ? s_nq[head] : 0.f;
@@ -352,6 +362,25 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
   }
 }
 
+template <int KB, bool HILO, int SPC>
+__global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
+    query_prep_tc_kernel(const tq_mma_launch a) {
+  query_prep_role<KB, HILO, SPC>(a, blockIdx.x);
+}
+
+// Prologue of a decode step, the split kernel's programmatic-launch primary in place of the
+// operand kernel.  Grid (kSlices / SPC + 2, KV heads, batch): the first kSlices / SPC CTAs of a
+// (batch, KV head) build its query operand; the next one quantises the step's new key into the
+// key cache at position seq_lens[b] (product code), the last one the new value (MSE code).  One
+// launch does the work of the two appends and the operand kernel, which would otherwise run
+// one after the other.
+template <int KB, bool HILO, int SPC>
+__global__ void __launch_bounds__(kAppendThreads, 1) step_prologue_kernel(const tq_mma_launch a) {
+  constexpr int nsl = kSlices / SPC;
+  if ((int)blockIdx.x < nsl) query_prep_role<KB, HILO, SPC>(a, blockIdx.x);
+  else append_kv_role(a.app, (int)blockIdx.x == nsl, blockIdx.y, blockIdx.z);
+}
+
 // A sequence of len tokens is cut into ceil(len / split_len) splits of equal size in whole tiles
 // (at most split_len, a multiple of the tile): every one of them holds tokens, and a ragged
 // batch's splits are as even as its lengths allow.
@@ -361,7 +390,7 @@ __device__ __forceinline__ int seq_split_len(int len, int split_len) {
 }
 
 // ---------------------------------------------------------------- shared memory and TMEM
-template <int KB, int VB, bool HILO>
+template <int KB, int VB, bool HILO, int NG>
 struct TL {
   static constexpr int NP = num_vplanes(KB) + 1;             // planes incl. the sign plane
   static constexpr int kN = kNof(HILO);                      // MMA N (D columns per block)
@@ -386,42 +415,47 @@ struct TL {
   // 15 partial sums [15][8][128]); the dynamic shared memory is sized so that one chunk holds
   // the records of every split at the usual split counts
   static constexpr int comb_acc = 0;
-  static constexpr int comb_stats = kSWarps * 8 * kAccPitch * 4;
+  static constexpr int comb_stats = Roles<NG>::S * 8 * kAccPitch * 4;
   static constexpr int mrg_acc = 0;
   static constexpr int mrg_w = 8 * TQ_D * 4;
   static constexpr int mrg_part = mrg_w + 2 * 8 * kMaxSplits * 4;
-  static constexpr int pi_off = mrg_part + 2 * 8 * TQ_D * 4;
+  static constexpr int pi_off = mrg_part + (Roles<NG>::compute / 32) * (TQ_D + 4) * 4;
   static constexpr int rec_off = pi_off + TQ_D * TQ_D * 4;
   static constexpr int total = 226 * 1024;
   static_assert(used <= total && rec_off + 16 * 8 * TQ_REC * 4 <= total, "shared memory");
-  static_assert(rec_off + (kCompute / 32) * 8 * TQ_D * 4 <= total, "rotation partial sums");
+  static_assert(rec_off + (Roles<NG>::compute / 32) * 8 * TQ_D * 4 <= total,
+                "rotation partial sums");
   // TMEM: A (one tile: NP planes × 32 columns of e4m3), D (NP planes × 32 columns)
   static constexpr int a_cols = NP * 32;
   // D: index planes summed in pairs by the MMAs (block j = planes 2j, 2j + 1), then the sign
   // plane's block
   static constexpr int d_blocks = (NP - 1 + 1) / 2 + 1;
   static constexpr int d_cols = d_blocks * kN;
-  static constexpr int abufs = (2 * a_cols + 2 * d_cols <= 512) ? 2 : 1;
+  // one D buffer per softmax group
+  static constexpr int abufs = (2 * a_cols + NG * d_cols <= 512) ? 2 : 1;
   static constexpr int d_col = abufs * a_cols;
-  static_assert(d_col + 2 * d_cols <= 512, "TMEM columns");
+  static_assert(d_col + NG * d_cols <= 512, "TMEM columns");
 };
 
 // ---------------------------------------------------------------- the split kernel
-template <int KB, int VB, bool HILO>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_launch a) {
-  using L = TL<KB, VB, HILO>;
+template <int KB, int VB, bool HILO, int NG>
+__global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const tq_mma_launch a) {
+  using L = TL<KB, VB, HILO, NG>;
+  using R = Roles<NG>;
+  constexpr int kThreads = R::threads;
+  constexpr int kCompute = R::compute;
+  constexpr int kSWarps = R::S;
   constexpr int kN = L::kN;
   constexpr int kBImg = kBImgOf(HILO);
   constexpr int NKV = num_vplanes(KB);
   constexpr int NP = NKV + 1;
   constexpr int NVV = VB == 4 ? 0 : num_vplanes(VB);
-  constexpr int NI = L::d_blocks;                              // issuer warps: one per D block
-  static_assert(L::d_blocks <= kIWarps, "issuer warps");
+  constexpr int NB = L::d_blocks;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t mma_done[2];
-  __shared__ __align__(8) uint64_t d_free[2];
+  __shared__ __align__(8) uint64_t mma_done[NG];   // key scores of group g's tile in D[g]
+  __shared__ __align__(8) uint64_t d_free[NG];
   __shared__ __align__(8) uint64_t a_full[2];
   __shared__ __align__(8) uint64_t op_bar;     // query operand and constants landed
   __shared__ __align__(8) uint64_t prol_bar;   // value pair table landed (4-bit values)
@@ -444,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   if (a.B > 1 && nitems <= kThreads) {
     int* sc_len = reinterpret_cast<int*>(smem);
     int* sc_work = sc_len + kThreads;
-    if (tid < a.B) sc_len[tid] = min(a.seq_lens[tid], a.cap);
+    if (tid < a.B) sc_len[tid] = min(a.seq_lens[tid] + a.len_add, a.cap);
     __syncthreads();
     if (tid < nitems) {
       const int ib = tid / (int)gridDim.x, is = tid - ib * (int)gridDim.x;
@@ -468,17 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     split = s_item - b * (int)gridDim.x;
     kvh = pos % a.Hkv;
   }
-  int len = a.seq_lens[b];   // in flight during the setup
+  int len = a.seq_lens[b] + a.len_add;   // in flight during the setup
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full_bar[st], 1);
-      mbar_init(&empty_bar[st], 2 * (kEWarps + kSWarps / 2));   // two tiles per stage
+      mbar_init(&empty_bar[st], 2 * (kEWarps + 4));   // two tiles per stage
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&mma_done[i], NI);
-      mbar_init(&d_free[i], kSWarps / 2);
-      mbar_init(&a_full[i], kEWarps);
+    for (int i = 0; i < NG; ++i) {
+      mbar_init(&mma_done[i], 1);
+      mbar_init(&d_free[i], 4);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&a_full[i], kEWarps);
     mbar_init(&op_bar, 1);
     mbar_init(&prol_bar, 1);
     mbar_init(&pi_bar, 1);
@@ -519,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   const uint32_t tmem = s_tmem;
 
   // ============================================================ producer warp
-  if (warp == kEWarps + kSWarps + kIWarps) {
+  if (warp == R::issuer + 1) {
     if (lane == 0) {
       auto issue = [&](int c) {
         const int st = c % kStages;
@@ -546,10 +580,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       };
       // Π is read again only by the split that merges: have it in L2 by then
       if (split == 0) bulk_prefetch_l2(a.pi, TQ_D * TQ_D * 4);
-      // the first stage and the value pair table come in while the query-operand kernel (this
-      // grid's programmatic-launch primary) runs; its output is copied in as soon as that grid
-      // has completed, ahead of the other stages
-      issue(0);
+      // The ring's first stages and the value pair table come in while this grid's programmatic-
+      // launch primary (the operand kernel, or a decode step's prologue) runs: the cache is final
+      // by then, except for the last `fresh` tokens that a step's prologue appends, whose stages
+      // are requested after the wait.  The operand is copied in as soon as the primary grid has
+      // completed, ahead of the remaining stages.
+      int c = 0;
+      for (; c < nstages && c < kStages; ++c) {
+        const int t0 = t_begin + c * kStageTok;
+        if (a.fresh > 0 && t0 + min(kStageTok, a.cap - t0) > len - a.fresh) break;
+        issue(c);
+      }
       if (VB == 4) {
         mbar_expect_tx(&prol_bar, L::lut_bytes);
         bulk_g2s(smem + L::lut, a.lut, L::lut_bytes, &prol_bar);
@@ -559,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       bulk_g2s(smem + L::frag,
                static_cast<const unsigned char*>(a.qfrag) + bh * (long long)frag_block(NP, HILO),
                frag_block(NP, HILO), &op_bar);
-      int c = 1;
       for (; c < nstages && c < kStages; ++c) issue(c);
       for (; c < nstages; ++c) {
         const int st = c % kStages;
@@ -602,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       if (lane == 0) mbar_arrive(&empty_bar[st]);
       // the A buffer is free once the MMAs of the tile that used it last have completed
       const int prev = i - L::abufs;
-      if (okl && prev >= 0) okl = mbar_wait(&mma_done[prev & 1], (prev >> 1) & 1);
+      if (okl && prev >= 0) okl = mbar_wait(&mma_done[prev % NG], (prev / NG) & 1);
       if (!__all_sync(0xffffffffu, okl)) {   // the TMEM stores below are warp-collective
         if (lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
         break;
@@ -630,46 +670,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[ab]);
     }
-  } else if (warp >= kEWarps + kSWarps) {
-    // ========================================================== MMA-issue warps
-    // Issuer iw owns D block iw: index planes 2iw and 2iw + 1 accumulated into one block, or
-    // (last block) the sign plane; 4 MMAs of K = 32 per plane and tile, D[i & 1].  The whole
-    // warp waits and forms the (warp-uniform) descriptors; one elected lane issues the MMAs
-    // and their commit.
-    const int iw = warp - kEWarps - kSWarps;
-    if (iw < NI && ntiles > 0) {
+  } else if (warp == R::issuer) {
+    // ========================================================== MMA-issue warp
+    // D block j accumulates index planes 2j and 2j + 1, the last block the sign plane; 4 MMAs
+    // of K = 32 per plane and tile, into group g's D buffer for the tiles i ≡ g (mod NG).  The
+    // whole warp waits and forms the (warp-uniform) descriptors; one elected lane issues the
+    // MMAs and their commit.
+    if (warp == R::issuer && ntiles > 0) {
       const uint32_t idesc = idesc_f16(128, kN);   // e4m3 × e4m3 → f32 has the same fields
       const uint32_t frag_s = s32(smem + L::frag);
-      const bool sign_blk = iw == NI - 1;
-      const int v0 = sign_blk ? NKV : 2 * iw;
-      const int nv = sign_blk ? 1 : (2 * iw + 1 < NKV ? 2 : 1);
-      uint64_t bdesc[2][4];
-#pragma unroll
-      for (int o = 0; o < 2; ++o)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          bdesc[o][ks] = smem_desc(frag_s + (v0 + (o < nv ? o : 0)) * kBImg + ks * 256, 128, kBSbo);
       bool ok = mbar_wait(&op_bar, 0);
       for (int i = 0; i < ntiles && ok; ++i) {
         const int ab = L::abufs == 2 ? (i & 1) : 0;
-        const int db = i & 1;
+        const int g = i % NG;
         ok = mbar_wait(&a_full[ab], (i / L::abufs) & 1) &&
-             (i < 2 || mbar_wait(&d_free[db], ((i - 2) >> 1) & 1));
+             (i < NG || mbar_wait(&d_free[g], ((i / NG) - 1) & 1));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_after();
         if (elect_one()) {
-          const uint32_t d = tmem + L::d_col + db * L::d_cols + iw * kN;
 #pragma unroll
-          for (int o = 0; o < 2; ++o) {
-            if (o < nv) {
-              const uint32_t a0 = tmem + ab * L::a_cols + 32 * (v0 + o);
+          for (int j = 0; j < NB; ++j) {
+            const uint32_t d = tmem + L::d_col + g * L::d_cols + j * kN;
+            const int v0 = j == NB - 1 ? NKV : 2 * j;
+            const int nv = j == NB - 1 ? 1 : (2 * j + 1 < NKV ? 2 : 1);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_f8(d, a0 + 8 * ks, bdesc[o][ks], idesc, (o > 0 || ks > 0) ? 1u : 0u);
+            for (int o = 0; o < 2; ++o) {
+              if (o < nv) {
+                const uint32_t a0 = tmem + ab * L::a_cols + 32 * (v0 + o);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_f8(d, a0 + 8 * ks,
+                         smem_desc(frag_s + (v0 + o) * kBImg + ks * 256, 128, kBSbo), idesc,
+                         (o > 0 || ks > 0) ? 1u : 0u);
+              }
             }
           }
-          mma_commit(&mma_done[db]);
+          mma_commit(&mma_done[g]);
         }
         __syncwarp();
       }
@@ -678,10 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     __syncwarp();
   } else {
     // ========================================================== softmax / value warps
-    const int sw_ = warp - kEWarps;                       // 0..7
+    const int sw_ = warp - kEWarps;                       // 0 .. 4·NG − 1
     const int stid = tid - kEWarps * 32;
     const int q = warp & 3;                               // TMEM lane quadrant
-    const int grp = sw_ >> 2;                             // tiles i ≡ grp (mod 2)
+    const int grp = sw_ >> 2;                             // tiles i ≡ grp (mod NG)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int g = lane >> 2, c = lane & 3;
     // the query operand and its constants (and the value pair table) have landed
@@ -712,11 +749,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, lw_run[2] = {0.f, 0.f};
     const uint32_t* lut_lane = reinterpret_cast<const uint32_t*>(smem + L::lut) + lane;
 
-    for (int i = grp; i < ntiles && okp; i += 2) {
+    for (int i = grp; i < ntiles && okp; i += NG) {
       const int st = (i >> 1) % kStages;
       const int hrow = (i & 1) * kTile;                   // the tile's first row in the stage
-      const int db = i & 1;
-      const bool okw = mbar_wait(&mma_done[db], (i >> 1) & 1) &&
+      const int db = grp;
+      const bool okw = mbar_wait(&mma_done[db], (i / NG) & 1) &&
                        mbar_wait(&full_bar[st], ((i >> 1) / kStages) & 1);
       if (!__all_sync(0xffffffffu, okw)) {   // the TMEM loads below are warp-collective
         if (lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
@@ -895,6 +932,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
   }
 
   // ============================================================ end of the split
+  // The main loop is over: the next kernel in the stream may launch now and fetch its
+  // constants while the records are merged (it waits for this grid to complete before it
+  // touches anything this grid reads or writes).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the records are released at device scope; the split that takes the last ticket of its
   // (batch, KV head) merges them
   tc_before();
@@ -1100,9 +1141,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const tq_mma_lau
 // gets at least two, else the plan's splits in several waves; splits are whole tiles and only
 // those that cover the longest sequence are launched.
 template <int KB, int VB, bool HILO>
-tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
-  constexpr int smem = TL<KB, VB, HILO>::total;
-  auto kern = decode_tc_kernel<KB, VB, HILO>;
+tq_status launch_one(const tq_mma_launch& a0, bool step, cudaStream_t stream) {
+  // two softmax groups: a third (tried) adds no speed, the main loop being bound by the
+  // SM's issue and integer-ALU throughput rather than by one warp's latency
+  constexpr int NG = 2;
+  constexpr int kThreads = Roles<NG>::threads;
+  constexpr int smem = TL<KB, VB, HILO, NG>::total;
+  auto kern = decode_tc_kernel<KB, VB, HILO, NG>;
   static bool configured[64] = {};
   static int max_ctas[64] = {};
   int dev = 0;
@@ -1130,21 +1175,26 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
   a.nsplit = ns;
   a.split_len = (int)sl;
   {
-    // the operand kernel's start overlaps the end of the previous kernel in the stream
+    // the operand kernel (or the step's prologue) starts while the previous kernel in the
+    // stream ends
     const long long units = (long long)a.B * a.Hkv;
     const int spc = units * kSlices <= 2LL * tq_num_sms() ? 1
                     : units * (kSlices / 2) <= 2LL * tq_num_sms() ? 2 : 4;
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(kSlices / spc, a.Hkv, a.B);
-    pc.blockDim = dim3(kPrepThreads);
+    pc.gridDim = dim3(kSlices / spc + (step ? 2 : 0), a.Hkv, a.B);
+    pc.blockDim = dim3(step ? kAppendThreads : kPrepThreads);
     pc.stream = stream;
     cudaLaunchAttribute pa[1];
     pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    auto prep = spc == 1 ? query_prep_tc_kernel<KB, HILO, 1>
-                : spc == 2 ? query_prep_tc_kernel<KB, HILO, 2> : query_prep_tc_kernel<KB, HILO, 4>;
+    auto prep = step ? (spc == 1   ? step_prologue_kernel<KB, HILO, 1>
+                        : spc == 2 ? step_prologue_kernel<KB, HILO, 2>
+                                   : step_prologue_kernel<KB, HILO, 4>)
+                     : (spc == 1   ? query_prep_tc_kernel<KB, HILO, 1>
+                        : spc == 2 ? query_prep_tc_kernel<KB, HILO, 2>
+                                   : query_prep_tc_kernel<KB, HILO, 4>);
     if (cudaLaunchKernelEx(&pc, prep, a) != cudaSuccess) return TQ_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1162,17 +1212,29 @@ tq_status launch_one(const tq_mma_launch& a0, cudaStream_t stream) {
 }
 
 template <int KB, int VB>
-tq_status launch_kv(const tq_mma_launch& a, cudaStream_t stream) {
-  return a.G <= 4 ? launch_one<KB, VB, true>(a, stream) : launch_one<KB, VB, false>(a, stream);
+tq_status launch_kv(const tq_mma_launch& a, bool step, cudaStream_t stream) {
+  return a.G <= 4 ? launch_one<KB, VB, true>(a, step, stream)
+                  : launch_one<KB, VB, false>(a, step, stream);
 }
 
 template <int KB>
-tq_status launch_k(const tq_mma_launch& a, cudaStream_t stream) {
+tq_status launch_k(const tq_mma_launch& a, bool step, cudaStream_t stream) {
   switch (a.vbits) {
-    case 1: return launch_kv<KB, 1>(a, stream);
-    case 2: return launch_kv<KB, 2>(a, stream);
-    case 3: return launch_kv<KB, 3>(a, stream);
-    case 4: return launch_kv<KB, 4>(a, stream);
+    case 1: return launch_kv<KB, 1>(a, step, stream);
+    case 2: return launch_kv<KB, 2>(a, step, stream);
+    case 3: return launch_kv<KB, 3>(a, step, stream);
+    case 4: return launch_kv<KB, 4>(a, step, stream);
+  }
+  return TQ_ERR_UNSUPPORTED;
+}
+
+tq_status launch_kbits(const tq_mma_launch& a, bool step, cudaStream_t stream) {
+  if (!tq_tc_decode_supported(a.kbits, a.vbits, a.G, a.nsplit)) return TQ_ERR_UNSUPPORTED;
+  if (!a.counters || !a.qfrag) return TQ_ERR_INVALID_ARG;
+  switch (a.kbits) {
+    case 1: return launch_k<1>(a, step, stream);
+    case 2: return launch_k<2>(a, step, stream);
+    case 3: return launch_k<3>(a, step, stream);
   }
   return TQ_ERR_UNSUPPORTED;
 }
@@ -1221,12 +1283,19 @@ void tq_tc_operand_scales(const tq_plane_decomp& kd, float* s_idx, float* s_sgn)
 }
 
 tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream) {
-  if (!tq_tc_decode_supported(a.kbits, a.vbits, a.G, a.nsplit)) return TQ_ERR_UNSUPPORTED;
-  if (!a.counters || !a.qfrag) return TQ_ERR_INVALID_ARG;
-  switch (a.kbits) {
-    case 1: return launch_k<1>(a, stream);
-    case 2: return launch_k<2>(a, stream);
-    case 3: return launch_k<3>(a, stream);
-  }
-  return TQ_ERR_UNSUPPORTED;
+  return launch_kbits(a, false, stream);
+}
+
+tq_status tq_launch_decode_step_tc(const tq_mma_launch& a, cudaStream_t stream) {
+  if (!a.app.k_new || !a.app.v_new || !a.app.kmT) return TQ_ERR_INVALID_ARG;
+  return launch_kbits(a, true, stream);
+}
+
+bool tq_step_prologue_fits(int batch, int kv_heads) {
+  // the prologue runs one CTA of 512 threads per SM (its append CTAs' registers): use it when
+  // all its CTAs fit in one wave
+  const long long units = (long long)batch * kv_heads;
+  const int sms = tq_num_sms();
+  const int spc = units * kSlices <= 2LL * sms ? 1 : units * (kSlices / 2) <= 2LL * sms ? 2 : 4;
+  return units * (kSlices / spc + 2) <= sms;
 }

@@ -18,6 +18,8 @@
 
 TQ_DEFINE_FLAGS(tq_take_flags_quantize)
 
+#include "append_small.h"
+
 namespace {
 
 constexpr int kTile = 64;       // vectors per tile
@@ -250,34 +252,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
 // threads per vector.  Each 128×128 product is split four ways over k, so every thread
 // issues 32 independent coalesced loads of Πᵀ (or Mᵀ) from L2 instead of a 128-long chain;
 // codes are assembled with warp ballots.
-constexpr int kSmallThreads = 512;
-
-// Thread (k quarter q, output j) of the 512 owns T[32q..32q+31][j]: its 32 values are loaded
-// at kernel start, together with every other global input, so that the kernel waits for one
-// round trip only.
-__device__ __forceinline__ void small_load(const float* __restrict__ T, float (&t)[32], int tid) {
-  const int j = tid & 127, q = tid >> 7;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) t[k] = __ldg(&T[(32 * q + k) * TQ_D + j]);
-}
-__device__ __forceinline__ float small_matvec(const float (&t)[32], const float* v, float* part,
-                                              int tid) {
-  const int j = tid & 127, q = tid >> 7;
-  float acc = 0.f;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) acc = fmaf(t[k], v[32 * q + k], acc);
-  part[q * TQ_D + j] = acc;
-  __syncthreads();
-  float r = 0.f;
-  if (tid < TQ_D) r = (part[j] + part[TQ_D + j]) + (part[2 * TQ_D + j] + part[3 * TQ_D + j]);
-  __syncthreads();
-  return r;
-}
-
 template <bool kProd>
-__global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs a) {
-  __shared__ float xs[TQ_D], rho[TQ_D], part[4 * TQ_D];
-  __shared__ float red[4];
+__global__ void __launch_bounds__(tq::kAppendThreads) quantize_small_kernel(QuantArgs a) {
+  __shared__ tq::AppendSmem sm;
   const int tid = threadIdx.x;
   const long long i = blockIdx.x;
   const int t = (int)(i % a.tokens);
@@ -287,12 +264,10 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
   // codec's constants (Πᵀ, Mᵀ) are requested at once, everything the previous kernel may
   // produce or read (the vector, the count, the position, the cache) only after it completed.
   float tp[32], tm[32];
-  small_load(a.piT, tp, tid);
-  if constexpr (kProd) small_load(a.mT, tm, tid);
+  tq::append_load_t(a.piT, tp, tid);
+  if constexpr (kProd) tq::append_load_t(a.mT, tm, tid);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  float vals[8];
-  if (tid < 16) load8(a.x, a.dtype, b * a.sb + h * a.sh + t * a.st + tid * 8, vals);
   const int cnt = a.count ? a.count[b] : a.tokens;
   const int pos = a.pos ? a.pos[b] : 0;
   if (t >= cnt) return;
@@ -301,61 +276,28 @@ __global__ void __launch_bounds__(kSmallThreads) quantize_small_kernel(QuantArgs
     if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
     return;
   }
-  const long long slot = (long long)bh * a.capacity + dst;
-  const int warp = tid >> 5, lane = tid & 31;
-  if (tid < 16) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) xs[tid * 8 + e] = vals[e];
-  }
-  __syncthreads();
-  float x2 = 0.f;
-  if (tid < TQ_D) x2 = xs[tid] * xs[tid];
-  if (warp < 4) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x2 += __shfl_xor_sync(0xffffffffu, x2, o);
-    if (lane == 0) red[warp] = x2;
-  }
-  __syncthreads();
-  const float n = sqrtf((red[0] + red[1]) + (red[2] + red[3]));
-  const float acc = small_matvec(tp, xs, part, tid);
-  int q = 0;
-  float r = 0.f;
-  if (tid < TQ_D) {
-    const float y = n > 0.f ? acc / n : 0.f;
-    for (int bnd = 0; bnd < a.lv.levels - 1; ++bnd) q += (a.lv.b[bnd] <= y) ? 1 : 0;
-    r = y - a.lv.c[q];
-    rho[tid] = r;
-  }
-  // index codes: warp w < 4 owns coordinates 32w..32w+31
-  if (warp < 4) {
-    if (a.nibbles) {
-      // byte k = idx(2k) | idx(2k+1) << 4: lane pairs combine through a shuffle
-      const int other = __shfl_xor_sync(0xffffffffu, q, 1);
-      if ((lane & 1) == 0) a.idx[slot * 64 + (tid >> 1)] = (uint8_t)(q | (other << 4));
-    } else {
-      for (int p = 0; p < a.ibits; ++p) {
-        const unsigned word = __ballot_sync(0xffffffffu, (q >> p) & 1);
-        if (lane == 0)
-          reinterpret_cast<uint32_t*>(a.idx + (((long long)bh * a.ibits + p) * a.capacity + dst) * 16)[warp] = word;
-      }
-    }
-    if (tid == 0) a.xnorm[slot] = n;
-  }
-  if constexpr (kProd) {
-    float r2 = r * r;
-    if (warp < 4) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, o);
-    }
-    __syncthreads();   // rho complete; red reused
-    if (warp < 4 && lane == 0) red[warp] = r2;
-    const float z = small_matvec(tm, rho, part, tid);   // contains __syncthreads
-    if (warp < 4) {
-      const unsigned word = n > 0.f ? __ballot_sync(0xffffffffu, z >= 0.f) : 0xffffffffu;
-      if (lane == 0) reinterpret_cast<uint32_t*>(a.sgn + slot * 16)[warp] = word;
-      if (tid == 0) a.rnorm[slot] = n * sqrtf((red[0] + red[1]) + (red[2] + red[3]));
-    }
-  }
+  tq::AppendArgs aa;
+  aa.x = a.dtype == TQ_F32
+             ? static_cast<const void*>(static_cast<const float*>(a.x) + b * a.sb + h * a.sh + t * a.st)
+             : static_cast<const void*>(static_cast<const uint16_t*>(a.x) + b * a.sb + h * a.sh + t * a.st);
+  aa.dtype = a.dtype;
+  aa.dst = dst;
+  aa.bh = bh;
+  aa.capacity = a.capacity;
+  aa.idx = a.idx;
+  aa.sgn = a.sgn;
+  aa.xnorm = a.xnorm;
+  aa.rnorm = a.rnorm;
+  aa.lv = a.lv;
+  aa.ibits = a.ibits;
+  aa.nibbles = a.nibbles;
+  tq::append_quantize<kProd>(aa, tp, tm, sm, tid);
+}
+
+// The appends of a decode step in one launch: grid (2, KV heads, batch), CTA x = 0 the key,
+// x = 1 the value of (batch, KV head).
+__global__ void __launch_bounds__(tq::kAppendThreads) append_kv_kernel(const tq::AppendKV a) {
+  tq::append_kv_role(a, blockIdx.x == 0, blockIdx.y, blockIdx.z);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -388,7 +330,7 @@ tq_status launch(const QuantArgs& a, cudaStream_t stream) {
     // programmatic launch: this kernel's start overlaps the end of the previous one
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)total);
-    cfg.blockDim = dim3(kSmallThreads);
+    cfg.blockDim = dim3(tq::kAppendThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -466,6 +408,20 @@ extern "C" tq_status tq_quantize_mse(const tq_codec* vc, const void* x, tq_dtype
   a.capacity = capacity; a.piT = vc->d_piT; a.mT = nullptr; a.lv = tq_make_levels(vc);
   a.ibits = vc->ibits; a.nibbles = vc->ibits == 4;
   return launch<false>(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, a.Hkv, batch);
+  cfg.blockDim = dim3(tq::kAppendThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, append_kv_kernel, a) != cudaSuccess) return TQ_ERR_CUDA;
+  return tq_cuda_status(cudaGetLastError());
 }
 
 extern "C" tq_status tq_device_status(uint32_t* flags) {

@@ -475,9 +475,8 @@ def test_workspace_reuse_across_descriptors():
 
 def test_decode_serving_loop():
     """The ragged serving batch (B=32, 4096–16384 tokens, 28/4 heads, K 4-bit prod, V 4-bit
-    MSE) for its 128 decode steps: every step appends one new key and value per (sequence, KV
-    head) at position len (tq_quantize_*, one token), the lengths grow by one, and decode
-    attention runs over the grown cache.  The oracle replays the appends and checks four
+    MSE) for its 128 decode steps: every step (tq_decode_step) appends one new key and value
+    per (sequence, KV head) at position len, attends the grown cache and returns len + 1.  The oracle replays the appends and checks four
     (sequence, KV head) pairs at steps 0, 1, 64 and 127, every query head on its own."""
     w = synth.SERVE_B32
     steps = w.decode_steps
@@ -496,13 +495,14 @@ def test_decode_serving_loop():
     pairs = [(int(order[-1]), 0), (int(order[0]), 3), (int(order[len(order) // 2]), 1), (7, 2)]
     checkpoints = (0, 1, 64, steps - 1)
     new_kv, queries, outs = [], {}, {}
+    lens_next = torch.empty_like(lens_t)
     for st in range(steps):
         kn, vn = synth.make_new_tokens(w, device="cuda", step=st)
         q = synth.make_queries(w, device="cuda", step=st)[:, :, 0]
-        api.quantize_prod(kc, kn, kcache, pos=lens_t)
-        api.quantize_mse(vc, vn, vcache, pos=lens_t)
-        lens_t = lens_t + 1
-        out = plan.run(kc, vc, q, kcache, vcache, lens_t, plan.new_out().fill_(float("nan")))
+        # one call: append at lens, attend lens + 1 tokens, lens + 1 written to lens_next
+        out = plan.step(kc, vc, q, kn[:, :, 0].contiguous(), vn[:, :, 0].contiguous(), kcache,
+                        vcache, lens_t, plan.new_out().fill_(float("nan")), lens_out=lens_next)
+        lens_t, lens_next = lens_next, lens_t
         new_kv.append((kn[:, :, 0].double().cpu().numpy(), vn[:, :, 0].double().cpu().numpy()))
         if st in checkpoints:
             outs[st] = out.double().cpu().numpy()
@@ -536,3 +536,53 @@ def test_decode_serving_loop():
     report(w.name + " (128-step loop)", stats, f"pairs={len(pairs)}")
     assert stats.idx_excluded < 1e-4 * stats.coords, stats
     assert stats.sign_excluded < 1e-4 * stats.coords, stats
+
+
+@pytest.mark.parametrize("kbits,vbits,hq,hkv,batch", [
+    (3, 2, 32, 8, 1),     # the long-context shape (4-head groups, value planes)
+    (3, 4, 28, 4, 3),     # the 32K shape (7-head groups, value pair table)
+    (4, 4, 28, 4, 6),     # the serving shape (3-bit key indices)
+    (5, 3, 8, 2, 2),      # 4-bit key indices: the CUDA-core path
+    (3, 2, 16, 4, 40),    # 160 units: the appends as their own launch before the operand kernel
+])
+def test_decode_step_equals_separate_calls(kbits, vbits, hq, hkv, batch):
+    """tq_decode_step gives bit for bit the caches and outputs of tq_quantize_prod +
+    tq_quantize_mse (one token at pos) + tq_decode_attention over pos + 1 tokens, over three
+    chained steps (lens_out feeding the next step), with ragged lengths."""
+    rng = np.random.default_rng(1700 + kbits * 10 + vbits)
+    lens = [int(x) for x in rng.integers(1, 1500, size=batch)]
+    cap = 1600
+    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits)
+    k = rand_x((batch, hkv, cap, D), 1701, torch.bfloat16)
+    v = rand_x((batch, hkv, cap, D), 1702, torch.bfloat16)
+    caches = []
+    for _ in range(2):
+        kcache = api.ProdCache.empty(batch, hkv, cap, kbits)
+        vcache = api.MSECache.empty(batch, hkv, cap, vbits)
+        lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        api.quantize_prod(kc, k, kcache, count=lt)
+        api.quantize_mse(vc, v, vcache, count=lt)
+        caches.append((kcache, vcache))
+    plan = api.DecodePlan(batch, hq, hkv, cap, max(lens) + 3, torch.bfloat16, torch.float32)
+    pos_a = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    pos_b = pos_a.clone()
+    nxt = torch.empty_like(pos_a)
+    for st in range(3):
+        kn = rand_x((batch, hkv, D), 1710 + st, torch.bfloat16)
+        vn = rand_x((batch, hkv, D), 1720 + st, torch.bfloat16)
+        q = rand_x((batch, hq, D), 1730 + st, torch.bfloat16)
+        out_a = plan.step(kc, vc, q, kn, vn, *caches[0], pos_a, plan.new_out(), lens_out=nxt)
+        pos_a, nxt = nxt, pos_a
+        api.quantize_prod(kc, kn[:, :, None], caches[1][0], pos=pos_b)
+        api.quantize_mse(vc, vn[:, :, None], caches[1][1], pos=pos_b)
+        pos_b = pos_b + 1
+        out_b = plan.run(kc, vc, q, *caches[1], pos_b, plan.new_out())
+        torch.cuda.synchronize()
+        assert torch.equal(pos_a, pos_b)
+        assert torch.equal(out_a, out_b), f"step {st}: max diff {(out_a - out_b).abs().max()}"
+    check_flags_clear()
+    for ta, tb in zip((caches[0][0].idx, caches[0][0].sgn, caches[0][0].xnorm, caches[0][0].rnorm,
+                       caches[0][1].idx, caches[0][1].xnorm),
+                      (caches[1][0].idx, caches[1][0].sgn, caches[1][0].xnorm, caches[1][0].rnorm,
+                       caches[1][1].idx, caches[1][1].xnorm)):
+        assert torch.equal(ta, tb)
