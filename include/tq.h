@@ -235,6 +235,38 @@ tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq_codec* vc,
                                    const uint16_t* v_tail, const int32_t* tail_lens, void* out,
                                    void* workspace, size_t workspace_bytes, tq_stream_t stream);
 
+/* ------------------------------------------------------------------ store with an FP16 tail */
+
+/* Bytes of workspace tq_store_append needs for `batch` sequences (0 if batch ≤ 0). */
+size_t tq_store_workspace_bytes(int32_t batch);
+
+/* Appends one token per sequence to a cache kept in the asymmetric layout: a compressed part
+ * (FP16 keys, MSE-coded values) and an FP16 tail of the most recent tokens ([QJL] §六: the
+ * store appends in chunks and keeps recent tokens in full precision; [MLX] quick start:
+ * `min_compress_tokens`, and `key_bits=0` for FP16 keys).  For each sequence b the new key and
+ * value go to tail slot tail_lens[b]; the append that fills the last of the tail_capacity slots
+ * compacts the tail: its keys are copied to k_f16 and its values MSE-coded into v, at positions
+ * comp_lens[b] .. comp_lens[b] + tail_capacity − 1, comp_lens[b] grows by tail_capacity and
+ * tail_lens[b] returns to 0; otherwise tail_lens[b] grows by one.  The cache is then read with
+ * tq_decode_attention_asym (seq_lens = comp_lens, tail_lens = tail_lens, desc->capacity =
+ * capacity, desc->tail_capacity = tail_capacity).
+ *   vc        : value codec (TQ_MSE).
+ *   k_new, v_new : device [batch][kv_heads][128] of dtype (F32, F16 or BF16).
+ *   k_f16     : device fp16 [batch][kv_heads][capacity][128], keys of the compressed part.
+ *   v         : MSE cache [batch][kv_heads][capacity], values of the compressed part.
+ *   k_tail, v_tail : device fp16 [batch][kv_heads][tail_capacity][128].
+ *   comp_lens, tail_lens : device int32[batch], read and updated.
+ *   workspace : device, ≥ tq_store_workspace_bytes(batch) bytes (no initialisation needed).
+ * capacity must be a positive multiple of 64 and tail_capacity a positive multiple of 8; arrays
+ * 16-byte aligned.  A sequence whose tail length is out of range, or whose compaction would
+ * pass the capacity, is left unchanged and TQ_FLAG_LEN_OVERFLOW is raised.  Several launches on
+ * `stream`; allocates nothing. */
+tq_status tq_store_append(const tq_codec* vc, int32_t batch, int32_t kv_heads, const void* k_new,
+                          const void* v_new, tq_dtype dtype, uint16_t* k_f16, tq_mse_cache v,
+                          int32_t capacity, uint16_t* k_tail, uint16_t* v_tail,
+                          int32_t tail_capacity, int32_t* comp_lens, int32_t* tail_lens,
+                          void* workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* Decode attention for callers that cannot allocate device memory (no counterpart on the
  * pages: this is a deployment variant of tq_decode_attention, computing exactly the same
  * result).  Callers such as an inference runtime's plugin whose enqueue call may not

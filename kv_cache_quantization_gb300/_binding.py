@@ -71,6 +71,9 @@ SIGNATURES = {
                                                    tq_prod_cache, tq_mse_cache, _vp, _vp, _vp]),
     "tq_decode_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "tq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "tq_store_workspace_bytes": (ctypes.c_size_t, [_i32]),
+    "tq_store_append": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, ctypes.c_int, _vp, tq_mse_cache,
+                                       _i32, _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "tq_check_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _vp]),
 }
 
@@ -204,6 +207,19 @@ def tq_decode_noalloc_scratch_bytes() -> int:
 
 def tq_check_bounded_wait(limit_us: int, stream) -> int:
     return load().tq_check_bounded_wait(limit_us, ptr(stream))
+
+
+def tq_store_workspace_bytes(batch: int) -> int:
+    return load().tq_store_workspace_bytes(batch)
+
+
+def tq_store_append(vc, batch, kv_heads, k_new, v_new, dtype, k_f16, v: tq_mse_cache, capacity,
+                    k_tail, v_tail, tail_capacity, comp_lens, tail_lens, workspace,
+                    workspace_bytes, stream) -> int:
+    return load().tq_store_append(vc, batch, kv_heads, ptr(k_new), ptr(v_new), dtype, ptr(k_f16),
+                                  v, capacity, ptr(k_tail), ptr(v_tail), tail_capacity,
+                                  ptr(comp_lens), ptr(tail_lens), ptr(workspace), workspace_bytes,
+                                  ptr(stream))
 
 
 def tq_device_status():

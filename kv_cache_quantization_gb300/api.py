@@ -247,6 +247,42 @@ class DecodePlan:
         return out
 
 
+class TailStore:
+    """A cache in the asymmetric layout: a compressed part (FP16 keys, MSE-coded values) and an
+    FP16 tail of the most recent tokens that compacts into the compressed part when it fills
+    (tq_store_append); read with DecodePlan.run_asym."""
+
+    def __init__(self, vc: Codec, batch, kv_heads, capacity, tail_capacity=256, device="cuda"):
+        cap = _cap(capacity)
+        self.vc = vc
+        self.batch, self.kv_heads, self.capacity, self.tail_capacity = batch, kv_heads, cap, tail_capacity
+        self.k_f16 = torch.zeros(batch, kv_heads, cap, HEAD_DIM, dtype=torch.float16, device=device)
+        self.v = MSECache.empty(batch, kv_heads, cap, vc.bits, device=device)
+        self.k_tail = torch.zeros(batch, kv_heads, tail_capacity, HEAD_DIM, dtype=torch.float16,
+                                  device=device)
+        self.v_tail = torch.zeros_like(self.k_tail)
+        self.comp_lens = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.tail_lens = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.workspace = torch.empty(max(B.tq_store_workspace_bytes(batch), 256), dtype=torch.uint8,
+                                     device=device)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """k_new, v_new: [batch, kv_heads, 128] contiguous, one dtype."""
+        B.check(B.tq_store_append(self.vc.handle, self.batch, self.kv_heads, k_new, v_new,
+                                  tq_dtype(k_new.dtype), self.k_f16, self.v.c(), self.capacity,
+                                  self.k_tail, self.v_tail, self.tail_capacity, self.comp_lens,
+                                  self.tail_lens, self.workspace, self.workspace.numel(),
+                                  _stream(stream)), "tq_store_append")
+
+    def plan(self, q_heads, q_dtype=torch.bfloat16, out_dtype=torch.float32, device="cuda"):
+        return DecodePlan(self.batch, q_heads, self.kv_heads, self.capacity, self.capacity, q_dtype,
+                          out_dtype, tail_capacity=self.tail_capacity, device=device)
+
+    def decode(self, plan: "DecodePlan", q, out, stream=None):
+        return plan.run_asym(self.vc, q, self.k_f16, self.v, self.comp_lens, self.k_tail,
+                             self.v_tail, self.tail_lens, out, stream=stream)
+
+
 def device_status():
     """(status, flags) of the device status word (synchronises the device)."""
     return B.tq_device_status()

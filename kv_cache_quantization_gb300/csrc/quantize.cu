@@ -43,6 +43,7 @@ struct QuantArgs {
   tq_levels lv;
   int ibits;
   int nibbles;
+  int sparse;      // one tile per CTA; a tile without a vector to write leaves at once
 };
 
 __device__ __forceinline__ void load8(const void* base, int dtype, long long off, float* out) {
@@ -113,6 +114,23 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   __shared__ int s_bh[kTile];
 
   const int tid = threadIdx.x;
+  if (a.sparse) {
+    // (the caller launches one CTA per tile) most tiles have nothing to write: leave before
+    // fetching the codec's constants
+    __shared__ int s_any;
+    if (tid == 0) s_any = 0;
+    __syncthreads();
+    if (tid < kTile) {
+      const long long i = (long long)blockIdx.x * kTile + tid;
+      if (i < (long long)a.batch * a.heads * a.tokens) {
+        const int t = (int)(i % a.tokens);
+        const int b = (int)(i / a.tokens) / a.heads;
+        if (t < (a.count ? a.count[b] : a.tokens)) s_any = 1;
+      }
+    }
+    __syncthreads();
+    if (!s_any) return;
+  }
   for (int i = tid; i < TQ_D * TQ_D / 4; i += kThreads) {
     reinterpret_cast<float4*>(PT)[i] = __ldg(reinterpret_cast<const float4*>(a.piT) + i);
     if (kProd) reinterpret_cast<float4*>(MT)[i] = __ldg(reinterpret_cast<const float4*>(a.mT) + i);
@@ -410,6 +428,40 @@ extern "C" tq_status tq_quantize_mse(const tq_codec* vc, const void* x, tq_dtype
   return launch<false>(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// The FFMA tile quantiser with one CTA per tile of 64 vectors, for inputs where few vectors are
+// written (count[b] = 0 for most rows): empty tiles cost a CTA start and no more.
+tq_status tq_launch_quantize_tiles(const tq_codec* c, bool prod, const void* x, tq_dtype dt,
+                                   int batch, int heads, int tokens, long long sb, long long sh,
+                                   long long st, const int* pos, const int* count, uint8_t* idx,
+                                   uint8_t* sgn, float* xnorm, float* rnorm, int capacity,
+                                   cudaStream_t stream) {
+  QuantArgs a{};
+  a.x = x; a.dtype = dt; a.batch = batch; a.heads = heads; a.tokens = tokens;
+  a.sb = sb; a.sh = sh; a.st = st; a.pos = pos; a.count = count;
+  a.idx = idx; a.sgn = sgn; a.xnorm = xnorm; a.rnorm = rnorm;
+  a.capacity = capacity; a.piT = c->d_piT; a.mT = prod ? c->d_mT : nullptr;
+  a.lv = tq_make_levels(c); a.ibits = c->ibits; a.nibbles = !prod && c->ibits == 4;
+  a.sparse = 1;
+  const long long total = (long long)batch * heads * tokens;
+  if (total == 0) return TQ_OK;
+  const long long ntiles = (total + kTile - 1) / kTile;
+  if (ntiles > (1LL << 30)) return TQ_ERR_INVALID_ARG;
+  const size_t smem = (size_t)(prod ? 2 : 1) * TQ_D * TQ_D * sizeof(float) +
+                      (size_t)kTile * kXStride * sizeof(float);
+  auto kern = prod ? quantize_kernel<true> : quantize_kernel<false>;
+  static bool configured[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
+  if (!configured[prod][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return TQ_ERR_CUDA;
+    configured[prod][dev] = true;
+  }
+  kern<<<(unsigned)ntiles, kThreads, smem, stream>>>(a);
+  return tq_cuda_status(cudaGetLastError());
+}
+
 tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, a.Hkv, batch);
@@ -429,9 +481,9 @@ extern "C" tq_status tq_device_status(uint32_t* flags) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int a = tq_take_flags_quantize(), b = tq_take_flags_attention();
   const unsigned int d = tq_take_flags_quantize_tc(), e = tq_take_flags_decode_tc();
-  const unsigned int f = tq_take_flags_decode_asym();
-  if (a == ~0u || b == ~0u || d == ~0u || e == ~0u || f == ~0u) return TQ_ERR_CUDA;
-  *flags = a | b | d | e | f;
+  const unsigned int f = tq_take_flags_decode_asym(), g = tq_take_flags_store();
+  if (a == ~0u || b == ~0u || d == ~0u || e == ~0u || f == ~0u || g == ~0u) return TQ_ERR_CUDA;
+  *flags = a | b | d | e | f | g;
   if (*flags & TQ_FLAG_TIMEOUT) return TQ_ERR_TIMEOUT;
   return *flags ? TQ_ERR_DEVICE_STATUS : TQ_OK;
 }

@@ -58,6 +58,7 @@ unsigned int tq_take_flags_attention();
 unsigned int tq_take_flags_quantize_tc();
 unsigned int tq_take_flags_decode_tc();
 unsigned int tq_take_flags_decode_asym();
+unsigned int tq_take_flags_store();
 
 static inline tq_status tq_cuda_status(cudaError_t e) {
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -77,5 +78,12 @@ tq_status tq_launch_quantize_tc(bool prod, const void* x, int dtype, int batch, 
                                 float* xnorm, float* rnorm, int capacity, const tq_codec* c,
                                 cudaStream_t stream);
 size_t tq_operand_image_bytes(bool prod);
+// FFMA tile quantiser, one CTA per tile of 64 vectors; tiles without a vector to write (count)
+// leave at once (quantize.cu).
+tq_status tq_launch_quantize_tiles(const tq_codec* c, bool prod, const void* x, tq_dtype dt,
+                                   int batch, int heads, int tokens, long long sb, long long sh,
+                                   long long st, const int* pos, const int* count, uint8_t* idx,
+                                   uint8_t* sgn, float* xnorm, float* rnorm, int capacity,
+                                   cudaStream_t stream);
 void tq_build_operand_image(const double* mat, bool sketch, uint16_t* img);
 float tq_fp16_friendly_scale(const float* levels, int n);
