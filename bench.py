@@ -464,6 +464,39 @@ def measure_asym(w, args, dev, ws, peak):
             "decode_call": roofline(dec_bytes, ms, w.name, peak), "gpu_launches": 2 * args.steps}
 
 
+# ------------------------------------------------------------------ quality report
+
+def quality_report(dev):
+    """Attention-level KL divergence and top-1 agreement of compressed keys against exact keys
+    (tq_attention_quality) on the 32K workload's data: every query head against its KV head's
+    32768 keys, for 3-bit and 4-bit product codes; FP16 keys (the asymmetric mode) attend
+    exactly up to FP16 rounding."""
+    import torch
+
+    from kv_cache_quantization_gb300 import api, synth
+    w = synth.DECODE_32K
+    k, _ = synth.make_kv(w, device=dev)
+    q = synth.make_queries(w, device=dev)[0, :, 0].float()
+    rep = {"workload": w.name, "queries": w.q_heads, "keys_per_query": w.context}
+    for bits in (3, 4):
+        kc = api.Codec.prod(bits, w.layer)
+        cache = api.ProdCache.empty(1, w.kv_heads, w.context, bits, device=dev)
+        api.quantize_prod(kc, k, cache)
+        kls, agree = [], 0
+        for h in range(w.kv_heads):
+            one = api.ProdCache(cache.idx[:, h:h + 1], cache.sgn[:, h:h + 1],
+                                cache.xnorm[:, h:h + 1], cache.rnorm[:, h:h + 1])
+            one = api.ProdCache(*(t.contiguous() for t in (one.idx, one.sgn, one.xnorm, one.rnorm)))
+            kl, te, tc = api.attention_quality(kc, q[h * w.group:(h + 1) * w.group], k[0, h],
+                                               one, w.context)
+            kls += kl.tolist()
+            agree += int((te == tc).sum())
+        rep[f"k{bits}_prod"] = {"kl_mean": sum(kls) / len(kls), "kl_max": max(kls),
+                                "top1_agreement": agree / w.q_heads}
+    torch.cuda.synchronize()
+    return rep
+
+
 # ------------------------------------------------------------------ our implementation
 
 def describe(w, ws):
@@ -525,6 +558,8 @@ def run_ours(args):
         "compaction": head.get("compaction"),
         "per_workload": per,
     }
+    if not args.no_per_workload:
+        result["quality"] = quality_report(dev)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = oracle_baseline(w, budget_s=args.cpu_seconds)
     if rank == 0:

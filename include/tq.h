@@ -164,6 +164,29 @@ tq_status tq_prod_scores(const tq_codec* kc, const float* q, int32_t nq, int64_t
                          tq_prod_cache keys, int32_t capacity, int32_t n, float* scores,
                          int64_t scores_stride, tq_stream_t stream);
 
+/* ------------------------------------------------------------------ quality report */
+
+/* Scratch bytes tq_attention_quality needs (0 if nq ≤ 0 or n ≤ 0). */
+size_t tq_attention_quality_scratch_bytes(int32_t nq, int32_t n);
+
+/* How far attention on compressed keys is from attention on the exact keys, per query: the
+ * KL divergence KL(p ‖ p̂) of p = softmax(scale·⟨q_i, k_t⟩) over the exact keys and p̂ =
+ * softmax(scale·ŝ_t) over the estimator scores of their product codes ([QJL] §五), and the
+ * positions of both maxima (top-1 agreement where they are equal).  The attention-level
+ * counterpart of [MLX] "对称 vs 非对称"'s KLD / Top-1 comparison.
+ *   q       : device float32 [nq][128].
+ *   k       : device [n][128] of k_dtype (F32, F16 or BF16), the exact keys.
+ *   codes   : the keys' product codes, a cache with batch = heads = 1 and this capacity (n ≤
+ *             capacity).
+ *   softmax_scale : ≤ 0 selects 1/√128.
+ *   scratch : device, ≥ tq_attention_quality_scratch_bytes(nq, n) bytes.
+ *   kl      : device float32 [nq]; top1_exact, top1_comp : device int32 [nq] (first position of
+ *             the maximum). */
+tq_status tq_attention_quality(const tq_codec* kc, const float* q, int32_t nq, const void* k,
+                               tq_dtype k_dtype, tq_prod_cache codes, int32_t capacity, int32_t n,
+                               float softmax_scale, void* scratch, size_t scratch_bytes, float* kl,
+                               int32_t* top1_exact, int32_t* top1_comp, tq_stream_t stream);
+
 /* ------------------------------------------------------------------ decode attention */
 
 typedef struct {

@@ -72,6 +72,10 @@ SIGNATURES = {
     "tq_decode_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "tq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "tq_store_workspace_bytes": (ctypes.c_size_t, [_i32]),
+    "tq_attention_quality_scratch_bytes": (ctypes.c_size_t, [_i32, _i32]),
+    "tq_attention_quality": (ctypes.c_int, [_vp, _vp, _i32, _vp, ctypes.c_int, tq_prod_cache, _i32,
+                                            _i32, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp,
+                                            _vp, _vp]),
     "tq_store_append": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, ctypes.c_int, _vp, tq_mse_cache,
                                        _i32, _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "tq_check_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _vp]),
@@ -207,6 +211,17 @@ def tq_decode_noalloc_scratch_bytes() -> int:
 
 def tq_check_bounded_wait(limit_us: int, stream) -> int:
     return load().tq_check_bounded_wait(limit_us, ptr(stream))
+
+
+def tq_attention_quality_scratch_bytes(nq: int, n: int) -> int:
+    return load().tq_attention_quality_scratch_bytes(nq, n)
+
+
+def tq_attention_quality(kc, q, nq, k, k_dtype, codes: tq_prod_cache, capacity, n, softmax_scale,
+                         scratch, scratch_bytes, kl, top1_exact, top1_comp, stream) -> int:
+    return load().tq_attention_quality(kc, ptr(q), nq, ptr(k), k_dtype, codes, capacity, n,
+                                       softmax_scale, ptr(scratch), scratch_bytes, ptr(kl),
+                                       ptr(top1_exact), ptr(top1_comp), ptr(stream))
 
 
 def tq_store_workspace_bytes(batch: int) -> int:

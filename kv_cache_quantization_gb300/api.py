@@ -201,6 +201,25 @@ def prod_scores(codec: Codec, q: torch.Tensor, keys: ProdCache, n: int, out=None
     return out
 
 
+def attention_quality(codec: Codec, q: torch.Tensor, k: torch.Tensor, keys: ProdCache, n: int,
+                      softmax_scale=None, stream=None):
+    """(KL [nq], top-1 position over exact keys [nq], over compressed keys [nq]) for fp32
+    queries q [nq, 128] against the exact keys k [n, 128] and their codes keys[0, 0, :n]."""
+    q = q.contiguous()
+    k = k.contiguous()
+    nq = q.shape[0]
+    scratch = torch.empty(B.tq_attention_quality_scratch_bytes(nq, n), dtype=torch.uint8,
+                          device=q.device)
+    kl = torch.empty(nq, dtype=torch.float32, device=q.device)
+    te = torch.empty(nq, dtype=torch.int32, device=q.device)
+    tc = torch.empty(nq, dtype=torch.int32, device=q.device)
+    B.check(B.tq_attention_quality(codec.handle, q, nq, k, tq_dtype(k.dtype), keys.c(),
+                                   keys.capacity, n, softmax_scale or 0.0, scratch,
+                                   scratch.numel(), kl, te, tc, _stream(stream)),
+            "tq_attention_quality")
+    return kl, te, tc
+
+
 class DecodePlan:
     """A decode-attention configuration with its workspace (allocated once, reused)."""
 

@@ -17,7 +17,7 @@ LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libtq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["host.cpp", "quantize.cu", "quantize_tc.cu", "attention.cu", "scores.cu",
-           "decode_tc.cu", "decode_asym.cu", "decode_noalloc.cu", "store.cu"]
+           "decode_tc.cu", "decode_asym.cu", "decode_noalloc.cu", "store.cu", "quality.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -19,7 +19,8 @@ Sources (cited by page title and section):
   - §六: read path rotates the query forward (q Πᵀ) and pre-sketches it (q Sᵀ).
 * [MLX] MLX-port article (cf-1.com), "背景": keys use the full two-stage quantiser
   (Algorithm 2), values the MSE-only quantiser (Algorithm 1); "对称 vs 非对称":
-  asymmetric mode keeps K in FP16 and quantises V only.
+  asymmetric mode keeps K in FP16 and quantises V only, and compression is judged by the KL
+  divergence and top-1 agreement of the distributions with and without it.
 
 Readings where the pages are silent:
 
@@ -268,6 +269,33 @@ def decode_attention_asym(q, k_plain, v_codes, seq_lens, k_tail, v_tail, tail_le
                 h = kh * g + j
                 out[b, h] = softmax_attention(q[b, h], keys, vals, scale)
     return out
+
+
+# ---------------------------------------------------------------------------------------
+# Quality of compressed attention        [MLX] "对称 vs 非对称": KL divergence and top-1
+# ---------------------------------------------------------------------------------------
+
+def softmax_kl(a, b):
+    """KL(softmax(a) ‖ softmax(b)) along the last axis: Σ_t p_t (log p_t − log q_t) with
+    log p = a − log Σ e^a and log q = b − log Σ e^b."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    la = a - special.logsumexp(a, axis=-1, keepdims=True)
+    lb = b - special.logsumexp(b, axis=-1, keepdims=True)
+    return np.sum(np.exp(la) * (la - lb), axis=-1)
+
+
+def attention_quality(q, keys, idx, sign, n, gamma, pi, s, centroids, scale=None):
+    """Attention-level counterpart of the pages' KLD / top-1 comparison: for each query q_i,
+    the attention weights over exact keys, softmax(scale·⟨q_i, k_t⟩), against those over the
+    estimator scores of the compressed keys ([QJL] §五).  Returns (KL(exact ‖ compressed),
+    argmax over exact, argmax over compressed) per query."""
+    q = np.asarray(q, dtype=np.float64)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    exact = scale * (q @ np.asarray(keys, dtype=np.float64).T)
+    comp = scale * prod_scores(q, idx, sign, n, gamma, pi, s, centroids)
+    return softmax_kl(exact, comp), np.argmax(exact, axis=-1), np.argmax(comp, axis=-1)
 
 
 # ---------------------------------------------------------------------------------------

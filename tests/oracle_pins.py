@@ -375,11 +375,57 @@ def pin_sign_exclusion_rate(o):
         assert expect_1e6 / total < 1e-4, (ibits, expect_1e6 / total)
 
 
+def pin_softmax_kl(o):
+    """KL of softmax distributions: zero for equal inputs and invariant to a shift of either
+    input; the two-token case equals the Bernoulli KL written out; random small vectors equal
+    a pure-Python double loop; never negative."""
+    assert abs(o.softmax_kl([0.3, -1.2, 2.0], [0.3, -1.2, 2.0])) < 1e-15
+    a, b = 0.7, -0.4
+    pa, pb = 1 / (1 + math.exp(-a)), 1 / (1 + math.exp(-b))
+    bern = pa * math.log(pa / pb) + (1 - pa) * math.log((1 - pa) / (1 - pb))
+    assert abs(o.softmax_kl([a, 0.0], [b, 0.0]) - bern) < 1e-14
+    rng = np.random.default_rng(37)
+    for _ in range(20):
+        x = rng.standard_normal(5) * 3
+        y = rng.standard_normal(5) * 3
+        zx = sum(math.exp(v) for v in x)
+        zy = sum(math.exp(v) for v in y)
+        brute = sum(math.exp(x[t]) / zx * (math.log(math.exp(x[t]) / zx) - math.log(math.exp(y[t]) / zy))
+                    for t in range(5))
+        assert abs(o.softmax_kl(x, y) - brute) < 1e-12
+        assert abs(o.softmax_kl(x + 4.0, y - 2.5) - brute) < 1e-12
+        assert o.softmax_kl(x, y) >= 0
+
+
+def pin_attention_quality(o):
+    """attention_quality: exact scores are scale·⟨q, k⟩ and compressed scores the estimator
+    (checked against a loop over the dequantised keys); the argmaxes match brute force."""
+    rng = np.random.default_rng(41)
+    pi = _rotation(o, 42)
+    s = _sketch(43)
+    c, _ = o.lloyd_max_codebook(128, 2)
+    keys = rng.standard_normal((12, 128))
+    q = rng.standard_normal((3, 128))
+    k = o.quantize_prod(keys, pi, s, c)
+    kl, te, tc = o.attention_quality(q, keys, k["idx"], k["sign"], k["n"], k["gamma"], pi, s, c)
+    kh = o.dequantize_prod(k["idx"], k["sign"], k["n"], k["gamma"], pi, s, c)
+    scale = 1 / math.sqrt(128)
+    for i in range(3):
+        ex = [scale * float(np.dot(q[i], keys[t])) for t in range(12)]
+        cp = [scale * float(np.dot(q[i], kh[t])) for t in range(12)]
+        assert te[i] == max(range(12), key=lambda t: ex[t])
+        assert tc[i] == max(range(12), key=lambda t: cp[t])
+        zx = sum(math.exp(v) for v in ex)
+        zy = sum(math.exp(v) for v in cp)
+        brute = sum(math.exp(ex[t]) / zx * (ex[t] - cp[t]) for t in range(12)) - math.log(zx) + math.log(zy)
+        assert abs(kl[i] - brute) < 1e-10
+
+
 ALL_PINS = [
     pin_rotation, pin_codebook_closed_form_1bit, pin_codebook_centroid_condition,
     pin_codebook_gaussian_limit, pin_codebook_mse_monotone, pin_mse_index_is_nearest_level,
     pin_mse_distortion, pin_value_cos_sim_pages, pin_qjl_identity, pin_estimator_unbiased,
     pin_estimator_equals_dequantized_dot, pin_residual_definition, pin_zero_vector,
     pin_packing_golden, pin_attention_brute_force, pin_asym_concatenation,
-    pin_boundary_exclusion_rate, pin_sign_exclusion_rate,
+    pin_boundary_exclusion_rate, pin_sign_exclusion_rate, pin_softmax_kl, pin_attention_quality,
 ]

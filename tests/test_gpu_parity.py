@@ -586,3 +586,38 @@ def test_decode_step_equals_separate_calls(kbits, vbits, hq, hkv, batch):
                       (caches[1][0].idx, caches[1][0].sgn, caches[1][0].xnorm, caches[1][0].rnorm,
                        caches[1][1].idx, caches[1][1].xnorm)):
         assert torch.equal(ta, tb)
+
+
+# ------------------------------------------------------------------ quality report
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_attention_quality_report(bits):
+    """KL divergence and top-1 positions of attention on compressed keys against exact keys
+    (tq_attention_quality) match the oracle on the 1024-key workload's inputs: KL within
+    2e-5 + 1e-3·KL, top-1 equal unless the oracle's two best scores are within rounding."""
+    w = synth.SCORES_1K
+    k, _ = synth.make_kv(w, device="cuda")
+    q = synth.make_queries(w, device="cuda")[0, 0]
+    kc = api.Codec.prod(bits)
+    cache = api.ProdCache.empty(1, 1, w.context, bits)
+    api.quantize_prod(kc, k, cache)
+    kl, te, tc = api.attention_quality(kc, q, k[0, 0], cache, w.context)
+    kl, te, tc = kl.double().cpu().numpy(), te.cpu().numpy(), tc.cpu().numpy()
+    check_flags_clear()
+    pi, s = oracle_constants()
+    c = oracle_codebook(bits - 1)
+    gi, gs, gx, gr = unpack_prod(cache, 0, 0, w.context, bits - 1)
+    x = k[0, 0].double().cpu().numpy()
+    codes = match_prod_codes(x, gi, gs, gx, gr, pi, s, c, CodeStats())
+    qn = q.double().cpu().numpy()
+    rkl, rte, rtc = o.attention_quality(qn, x, codes["idx"], codes["sign"], codes["n"],
+                                        codes["gamma"], pi, s, c)
+    assert np.all(np.abs(kl - rkl) <= 2e-5 + 1e-3 * rkl), np.max(np.abs(kl - rkl))
+    exact = qn @ x.T
+    comp = o.prod_scores(qn, codes["idx"], codes["sign"], codes["n"], codes["gamma"], pi, s, c)
+    tol = 1e-4 * np.linalg.norm(qn, axis=1) * np.max(np.linalg.norm(x, axis=1))
+    for i in range(len(qn)):
+        assert te[i] == rte[i] or exact[i, te[i]] >= exact[i, rte[i]] - tol[i]
+        assert tc[i] == rtc[i] or comp[i, tc[i]] >= comp[i, rtc[i]] - tol[i]
+    # more key bits, closer attention
+    assert rkl.mean() > 0

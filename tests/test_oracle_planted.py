@@ -121,11 +121,28 @@ def plant_sign_band_tenfold(o):
     o.sign_exclusion = lambda z, n, d, eps=1e-6: orig(z, n, d, eps * 10)
 
 
+def plant_kl_reversed(o):
+    """KL(compressed ‖ exact) instead of KL(exact ‖ compressed)."""
+    orig = o.softmax_kl
+    o.softmax_kl = lambda a, b: orig(b, a)
+
+
+def plant_kl_unnormalised(o):
+    """Log-probabilities without the log-partition term."""
+    def f(a, b):
+        a = np.asarray(a, dtype=float)
+        b = np.asarray(b, dtype=float)
+        p = np.exp(a - np.max(a, axis=-1, keepdims=True))
+        p /= p.sum(axis=-1, keepdims=True)
+        return np.sum(p * (a - b), axis=-1)
+    o.softmax_kl = f
+
+
 PLANTS = [plant_drop_qjl, plant_flip_qjl_sign, plant_wrong_qjl_constant,
           plant_transposed_rotation, plant_no_sign_fix, plant_cell_midpoint_levels,
           plant_residual_sign, plant_gqa_mapping, plant_msb_first, plant_mse_norm_dropped,
           plant_ties_down_and_shift, plant_sign_band_power_of_d, plant_sign_band_residual_norm,
-          plant_sign_band_tenfold]
+          plant_sign_band_tenfold, plant_kl_reversed, plant_kl_unnormalised]
 
 
 @pytest.mark.parametrize("plant", PLANTS, ids=lambda p: p.__name__)
