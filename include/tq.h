@@ -224,6 +224,27 @@ tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_codec* kc, cons
                               const int32_t* seq_lens, void* out, void* workspace,
                               size_t workspace_bytes, tq_stream_t stream);
 
+/* Attention of a chunk of n_queries new queries per sequence over the compressed cache (the
+ * read path of [QJL] §六 for many queries: each query forward-rotated and pre-sketched once,
+ * scores on the packed bits, one softmax per query), e.g. a prefill chunk or several tokens
+ * proposed at once.
+ *   desc     : desc->batch sequences; desc->max_seq_len bounds the longest query row's attended
+ *              length (max(seq_lens) + n_queries when causal).
+ *   q, out   : device [batch][n_queries][q_heads][128] of desc->q_dtype / desc->out_dtype.
+ *   seq_lens : device int32[batch]: the history length of each sequence.  causal = 0: every
+ *              query of sequence b attends its seq_lens[b] tokens; causal = 1: query i attends
+ *              seq_lens[b] + i + 1 tokens, the chunk's own keys and values having been appended
+ *              to the caches after the history.
+ *   workspace: ≥ tq_prefill_workspace_bytes(desc, n_queries) bytes.
+ *   Other arguments as tq_decode_attention.  Each query row streams its attended tokens (rows
+ *   of one sequence read its cache from L2 after the first); key index widths of 1–3 bits and
+ *   group sizes up to 8 (the tcgen05 path), else TQ_ERR_UNSUPPORTED. */
+size_t tq_prefill_workspace_bytes(const tq_attn_desc* desc, int32_t n_queries);
+tq_status tq_prefill_attention(const tq_attn_desc* desc, int32_t n_queries, int32_t causal,
+                               const tq_codec* kc, const tq_codec* vc, const void* q,
+                               tq_prod_cache k, tq_mse_cache v, const int32_t* seq_lens, void* out,
+                               void* workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* One decode step in a single call ([QJL] §六: the compressed store appends each new token's
  * codes, then the read path attends the whole store; [MLX] quick start: append, then decode):
  * quantises the step's new key (product code) and value (MSE code) of every (batch, KV head)

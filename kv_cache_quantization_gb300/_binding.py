@@ -61,6 +61,10 @@ SIGNATURES = {
     "tq_decode_attention": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp,
                                            tq_prod_cache, tq_mse_cache, _vp, _vp, _vp,
                                            ctypes.c_size_t, _vp]),
+    "tq_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tq_attn_desc), _i32]),
+    "tq_prefill_attention": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _i32, _i32, _vp, _vp,
+                                            _vp, tq_prod_cache, tq_mse_cache, _vp, _vp, _vp,
+                                            ctypes.c_size_t, _vp]),
     "tq_decode_step": (ctypes.c_int, [ctypes.POINTER(tq_attn_desc), _vp, _vp, _vp, _vp, _vp,
                                       ctypes.c_int, tq_prod_cache, tq_mse_cache, _vp, _vp, _vp,
                                       _vp, ctypes.c_size_t, _vp]),
@@ -180,6 +184,18 @@ def tq_decode_attention(desc: tq_attn_desc, kc, vc, q, k: tq_prod_cache, v: tq_m
                         seq_lens, out, workspace, workspace_bytes, stream) -> int:
     return load().tq_decode_attention(ctypes.byref(desc), kc, vc, ptr(q), k, v, ptr(seq_lens),
                                       ptr(out), ptr(workspace), workspace_bytes, ptr(stream))
+
+
+def tq_prefill_workspace_bytes(desc: tq_attn_desc, n_queries: int) -> int:
+    return load().tq_prefill_workspace_bytes(ctypes.byref(desc), n_queries)
+
+
+def tq_prefill_attention(desc: tq_attn_desc, n_queries, causal, kc, vc, q, k: tq_prod_cache,
+                         v: tq_mse_cache, seq_lens, out, workspace, workspace_bytes,
+                         stream) -> int:
+    return load().tq_prefill_attention(ctypes.byref(desc), n_queries, causal, kc, vc, ptr(q), k, v,
+                                       ptr(seq_lens), ptr(out), ptr(workspace), workspace_bytes,
+                                       ptr(stream))
 
 
 def tq_decode_step(desc: tq_attn_desc, kc, vc, q, k_new, v_new, kv_dtype, k: tq_prod_cache,

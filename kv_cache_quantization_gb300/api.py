@@ -266,6 +266,34 @@ class DecodePlan:
         return out
 
 
+class PrefillPlan:
+    """Attention of chunks of n_queries queries per sequence over a compressed cache
+    (tq_prefill_attention), with its workspace."""
+
+    def __init__(self, batch, n_queries, q_heads, kv_heads, capacity, max_seq_len, causal=True,
+                 q_dtype=torch.bfloat16, out_dtype=torch.float32, device="cuda"):
+        self.desc = B.tq_attn_desc(batch, q_heads, kv_heads, HEAD_DIM, _cap(capacity), max_seq_len,
+                                   0, 0.0, tq_dtype(q_dtype), tq_dtype(out_dtype))
+        self.n_queries = n_queries
+        self.causal = 1 if causal else 0
+        nbytes = B.tq_prefill_workspace_bytes(self.desc, n_queries)
+        if nbytes == 0:
+            raise ValueError("invalid prefill-attention configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.out_dtype = out_dtype
+        self.shape = (batch, n_queries, q_heads, HEAD_DIM)
+
+    def new_out(self, device="cuda"):
+        return torch.empty(self.shape, dtype=self.out_dtype, device=device)
+
+    def run(self, kc: Codec, vc: Codec, q, k: ProdCache, v: MSECache, seq_lens, out, stream=None):
+        B.check(B.tq_prefill_attention(self.desc, self.n_queries, self.causal, kc.handle, vc.handle,
+                                       q, k.c(), v.c(), seq_lens, out, self.workspace,
+                                       self.workspace.numel(), _stream(stream)),
+                "tq_prefill_attention")
+        return out
+
+
 class TailStore:
     """A cache in the asymmetric layout: a compressed part (FP16 keys, MSE-coded values) and an
     FP16 tail of the most recent tokens that compacts into the compressed part when it fills

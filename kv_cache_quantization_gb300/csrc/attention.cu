@@ -502,7 +502,7 @@ __global__ void step_lens_kernel(const int32_t* pos, int n, int32_t* lens, int32
 tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_codec* vc,
                      const void* q, tq_prod_cache k, tq_mse_cache v, const int32_t* seq_lens,
                      void* out, void* workspace, size_t workspace_bytes, tq_stream_t stream_,
-                     const StepIn* step) {
+                     const StepIn* step, int qps = 1, int causal = 0) {
   Plan p;
   tq_status st = plan(desc, false, &p);
   if (st != TQ_OK) return st;
@@ -537,8 +537,11 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
   a.part = reinterpret_cast<float*>(ws + p.part_off);
   const int rows = desc->batch * desc->q_heads;
   const bool tc = tq_tc_decode_supported(kc->ibits, vc->ibits, p.G, p.nsplit);
+  if (!tc && qps > 1) return TQ_ERR_UNSUPPORTED;   // query rows sharing a cache row: tcgen05 path
   if (tc) {
     tq_mma_launch m{};
+    m.qps = qps;
+    m.causal = causal;
     m.B = a.B; m.Hq = a.Hq; m.Hkv = a.Hkv; m.G = a.G; m.cap = a.cap;
     m.nsplit = p.nsplit; m.split_len = p.split_len;
     m.scale_log2 = a.scale * 1.4426950408889634f;
@@ -602,6 +605,26 @@ extern "C" tq_status tq_decode_attention(const tq_attn_desc* desc, const tq_code
                                          tq_stream_t stream) {
   return run_decode(desc, kc, vc, q, k, v, seq_lens, out, workspace, workspace_bytes, stream,
                     nullptr);
+}
+
+extern "C" size_t tq_prefill_workspace_bytes(const tq_attn_desc* desc, int32_t n_queries) {
+  if (!desc || n_queries <= 0 || (long long)desc->batch * n_queries > (1 << 30)) return 0;
+  tq_attn_desc rows = *desc;
+  rows.batch = desc->batch * n_queries;
+  return tq_decode_workspace_bytes(&rows);
+}
+
+extern "C" tq_status tq_prefill_attention(const tq_attn_desc* desc, int32_t n_queries,
+                                          int32_t causal, const tq_codec* kc, const tq_codec* vc,
+                                          const void* q, tq_prod_cache k, tq_mse_cache v,
+                                          const int32_t* seq_lens, void* out, void* workspace,
+                                          size_t workspace_bytes, tq_stream_t stream) {
+  if (!desc || n_queries <= 0 || (causal != 0 && causal != 1)) return TQ_ERR_INVALID_ARG;
+  if ((long long)desc->batch * n_queries > (1 << 30)) return TQ_ERR_INVALID_ARG;
+  tq_attn_desc rows = *desc;
+  rows.batch = desc->batch * n_queries;
+  return run_decode(&rows, kc, vc, q, k, v, seq_lens, out, workspace, workspace_bytes, stream,
+                    nullptr, n_queries, causal);
 }
 
 extern "C" tq_status tq_decode_step(const tq_attn_desc* desc, const tq_codec* kc,

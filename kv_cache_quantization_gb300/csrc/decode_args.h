@@ -53,6 +53,10 @@ struct tq_mma_launch {
   // attended tokens of batch b: seq_lens[b] + len_add; the last `fresh` of them may be written
   // by the programmatic-launch primary, so the split kernel reads them only after its wait
   int len_add, fresh;
+  // query rows per sequence: row b attends cache row b / qps (1 for decode; a prefill chunk's
+  // length for tq_prefill_attention), and with causal = 1 row b also its chunk's first
+  // b % qps + 1 tokens (appended to the cache after the sequence's seq_lens tokens)
+  int qps, causal;
   // decode step with the appends in the prologue kernel: the step's new key and value,
   // appended at seq_lens[b]
   tq::AppendKV app;

@@ -381,6 +381,13 @@ __global__ void __launch_bounds__(kAppendThreads, 1) step_prologue_kernel(const 
   else append_kv_role(a.app, (int)blockIdx.x == nsl, blockIdx.y, blockIdx.z);
 }
 
+// Tokens that query row b attends: its sequence's length (+ len_add for a decode step), plus,
+// for row i of a causal prefill chunk, the chunk's own first i + 1 tokens.
+__device__ __forceinline__ int row_len(const tq_mma_launch& a, int b) {
+  const int s = b / a.qps;
+  return a.seq_lens[s] + a.len_add + (a.causal ? b - s * a.qps + 1 : 0);
+}
+
 // A sequence of len tokens is cut into ceil(len / split_len) splits of equal size in whole tiles
 // (at most split_len, a multiple of the tile): every one of them holds tokens, and a ragged
 // batch's splits are as even as its lengths allow.
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const 
   if (a.B > 1 && nitems <= kThreads) {
     int* sc_len = reinterpret_cast<int*>(smem);
     int* sc_work = sc_len + kThreads;
-    if (tid < a.B) sc_len[tid] = min(a.seq_lens[tid] + a.len_add, a.cap);
+    if (tid < a.B) sc_len[tid] = min(row_len(a, tid), a.cap);
     __syncthreads();
     if (tid < nitems) {
       const int ib = tid / (int)gridDim.x, is = tid - ib * (int)gridDim.x;
@@ -502,7 +509,7 @@ __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const 
     split = s_item - b * (int)gridDim.x;
     kvh = pos % a.Hkv;
   }
-  int len = a.seq_lens[b] + a.len_add;   // in flight during the setup
+  int len = row_len(a, b);   // in flight during the setup
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full_bar[st], 1);
@@ -524,7 +531,8 @@ __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const 
   tc_before();
   __syncthreads();
   tc_after();
-  const long long bh = (long long)b * a.Hkv + kvh;
+  const long long bh = (long long)b * a.Hkv + kvh;   // query row: operand, records, tickets
+  const long long ch = (long long)(b / a.qps) * a.Hkv + kvh;   // the cache row it attends
   if (len > a.cap) {
     if (tid == 0 && split == 0 && kvh == 0) atomicOr(&g_tq_flags, TQ_FLAG_LEN_OVERFLOW);
     len = a.cap;
@@ -565,18 +573,18 @@ __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const 
         mbar_expect_tx(&full_bar[st], bytes);
         for (int p = 0; p < KB; ++p)
           bulk_g2s(base + L::kplanes + p * kStageTok * 16,
-                   a.kidx + ((bh * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::ksgn, a.ksgn + (bh * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::kxn, a.kxn + bh * a.cap + t0, n * 4, &full_bar[st]);
-        bulk_g2s(base + L::krn, a.krn + bh * a.cap + t0, n * 4, &full_bar[st]);
+                   a.kidx + ((ch * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+        bulk_g2s(base + L::ksgn, a.ksgn + (ch * a.cap + t0) * 16, n * 16, &full_bar[st]);
+        bulk_g2s(base + L::kxn, a.kxn + ch * a.cap + t0, n * 4, &full_bar[st]);
+        bulk_g2s(base + L::krn, a.krn + ch * a.cap + t0, n * 4, &full_bar[st]);
         if (VB == 4) {
-          bulk_g2s(base + L::vcodes, a.vidx + (bh * a.cap + t0) * 64, n * 64, &full_bar[st]);
+          bulk_g2s(base + L::vcodes, a.vidx + (ch * a.cap + t0) * 64, n * 64, &full_bar[st]);
         } else {
           for (int p = 0; p < VB; ++p)
             bulk_g2s(base + L::vcodes + p * kStageTok * 16,
-                     a.vidx + ((bh * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+                     a.vidx + ((ch * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
         }
-        bulk_g2s(base + L::vxn, a.vxn + bh * a.cap + t0, n * 4, &full_bar[st]);
+        bulk_g2s(base + L::vxn, a.vxn + ch * a.cap + t0, n * 4, &full_bar[st]);
       };
       // Π is read again only by the split that merges: have it in L2 by then
       if (split == 0) bulk_prefetch_l2(a.pi, TQ_D * TQ_D * 4);

@@ -187,7 +187,7 @@ def test_scores_fp32_1k():
 # ------------------------------------------------------------------ decode attention
 
 def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sample=None,
-               q_dtype=None, zero_tokens=()):
+               q_dtype=None, zero_tokens=(), layer=0):
     cap = max(64, (max(lens) + 63) // 64 * 64)
     k = rand_x((batch, hkv, cap, D), seed, in_dtype)
     v = rand_x((batch, hkv, cap, D), seed + 1, in_dtype)
@@ -195,7 +195,7 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
         k[b, h, t] = 0
         v[b, h, t] = 0
     q = rand_x((batch, hq, D), seed + 2, q_dtype or in_dtype)
-    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits)
+    kc, vc = api.Codec.prod(kbits, layer), api.Codec.mse(vbits, layer)
     kcache = api.ProdCache.empty(batch, hkv, cap, kbits)
     vcache = api.MSECache.empty(batch, hkv, cap, vbits)
     lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
@@ -206,7 +206,7 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
     plan.run(kc, vc, q, kcache, vcache, lens_t, out)
     got = out.double().cpu().numpy()
     check_flags_clear()
-    pi, s = oracle_constants()
+    pi, s = oracle_constants(layer)
     ck, cv = oracle_codebook(kbits - 1), oracle_codebook(vbits)
     g = hq // hkv
     stats = CodeStats()
@@ -235,6 +235,7 @@ def run_decode(batch, hq, hkv, lens, kbits, vbits, in_dtype, out_dtype, seed, sa
 
 @pytest.mark.parametrize("kbits,vbits,hq", [
     (3, 4, 8), (3, 2, 8), (4, 4, 8), (2, 1, 8), (5, 3, 8),      # G = 4 (query hi/lo columns)
+    (4, 2, 8), (4, 2, 14),                                      # 4-bit keys, 2-bit values
     (4, 4, 14), (3, 3, 14), (2, 2, 12), (5, 4, 14),             # G = 7, 7, 6 (one column per head)
     (4, 1, 6), (2, 3, 4)])                                      # G = 3, 2
 def test_decode_small(kbits, vbits, hq):
@@ -621,3 +622,74 @@ def test_attention_quality_report(bits):
         assert tc[i] == rtc[i] or comp[i, tc[i]] >= comp[i, rtc[i]] - tol[i]
     # more key bits, closer attention
     assert rkl.mean() > 0
+
+
+@pytest.mark.parametrize("layer", [1, 5])
+def test_decode_other_layers(layer):
+    """Codecs of other layers (rotation seed 42 + 7ℓ, sketch seed 43 + 7ℓ: independent Π and S
+    per layer, QJL deep-dive §六): quantisation and decode attention match the oracle built from
+    the same layer's constants."""
+    run_decode(2, 8, 2, [500, 1200], 3, 4, torch.bfloat16, torch.float32, 1900 + layer,
+               layer=layer)
+
+
+def test_layers_have_independent_constants():
+    """Different layers get different rotations: the codes of one input differ between layer 0
+    and layer 1 codecs."""
+    x = rand_x((1, 1, 64, D), 1950, torch.bfloat16)
+    caches = []
+    for layer in (0, 1):
+        kc = api.Codec.prod(3, layer)
+        cache = api.ProdCache.empty(1, 1, 64, 3)
+        api.quantize_prod(kc, x, cache)
+        caches.append(cache)
+    torch.cuda.synchronize()
+    assert not torch.equal(caches[0].idx, caches[1].idx)
+    torch.testing.assert_close(caches[0].xnorm, caches[1].xnorm, rtol=1e-6, atol=0)
+
+
+# ------------------------------------------------------------------ prefill chunks
+
+@pytest.mark.parametrize("causal,kbits,vbits,hq,hkv,nq", [
+    (True, 3, 4, 8, 2, 5), (False, 3, 2, 14, 2, 3), (True, 4, 4, 28, 4, 16)])
+def test_prefill_attention(causal, kbits, vbits, hq, hkv, nq):
+    """A chunk of nq queries per sequence over the compressed cache (tq_prefill_attention): with
+    causal, query i attends the history and the chunk's first i + 1 tokens; without, the
+    history only.  Every query head of every row against the oracle."""
+    batch, hist = 2, [300, 1000]
+    cap = 1088
+    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits)
+    k = rand_x((batch, hkv, cap, D), 2100 + nq, torch.bfloat16)
+    v = rand_x((batch, hkv, cap, D), 2200 + nq, torch.bfloat16)
+    q = rand_x((batch, nq, hq, D), 2300 + nq, torch.bfloat16)
+    kcache = api.ProdCache.empty(batch, hkv, cap, kbits)
+    vcache = api.MSECache.empty(batch, hkv, cap, vbits)
+    full = torch.tensor([h + nq for h in hist], dtype=torch.int32, device="cuda")
+    api.quantize_prod(kc, k, kcache, count=full)
+    api.quantize_mse(vc, v, vcache, count=full)
+    lens = torch.tensor(hist, dtype=torch.int32, device="cuda")
+    plan = api.PrefillPlan(batch, nq, hq, hkv, cap, max(hist) + nq, causal=causal)
+    out = plan.run(kc, vc, q, kcache, vcache, lens, plan.new_out().fill_(float("nan")))
+    got = out.double().cpu().numpy()
+    check_flags_clear()
+    pi, s = oracle_constants()
+    ck, cv = oracle_codebook(kbits - 1), oracle_codebook(vbits)
+    g = hq // hkv
+    stats = CodeStats()
+    for b in range(batch):
+        n_all = hist[b] + nq
+        for h in range(hkv):
+            gi, gs, gx, gr = unpack_prod(kcache, b, h, n_all, kbits - 1)
+            kcodes = match_prod_codes(k[b, h, :n_all].double().cpu().numpy(), gi, gs, gx, gr, pi,
+                                      s, ck, stats)
+            vi, vx = unpack_mse(vcache, b, h, n_all, vbits)
+            vcodes = match_mse_codes(v[b, h, :n_all].double().cpu().numpy(), vi, vx, pi, cv, stats)
+            for i in range(nq):
+                n = hist[b] + (i + 1 if causal else 0)
+                kd = {key: kcodes[key][None, None, :n] for key in ("idx", "sign", "n", "gamma")}
+                vd = {key: vcodes[key][None, None, :n] for key in ("idx", "n")}
+                ref = o.decode_attention(q[b:b + 1, i, h * g:(h + 1) * g].double().cpu().numpy(),
+                                         kd, vd, [n], pi, s, ck, cv)[0]
+                check_heads(got[b, i, h * g:(h + 1) * g], ref, 1e-3,
+                            f"(b={b}, query {i}, kv head={h})")
+    assert stats.idx_excluded < 1e-4 * stats.coords + 4, stats
