@@ -5,12 +5,11 @@ written) of one decode-attention call as ncu counted them, together with a diges
 kernel sources they were counted on.  ``bench.py`` reports the figure only while the digest
 still matches the sources; once a kernel changes, the figure is stale and it reports null.
 
-    python -m kv_cache_quantization_gb300.profiling <ncu csv> <workload> [<workload> ...]
+    python -m kv_cache_quantization_gb300.profiling <ncu csv> <workload>
 
-reads an ncu ``--csv --page raw`` export with the metrics ``dram__bytes_read.sum`` and
-``dram__bytes_write.sum``, sums every launch of each decode call (the query-operand kernel
-and the split kernel, or the asymmetric split kernel and its merge) and records it under the
-given workload names, one call per name, in the order they were captured.
+reads an ncu ``--csv`` export with the metrics ``dram__bytes_read.sum`` and
+``dram__bytes_write.sum`` of one captured launch of the workload's split kernel (the dominant
+kernel of a decode call) and records its bytes under the workload's name.
 """
 from __future__ import annotations
 
@@ -53,50 +52,44 @@ def measured_traffic(workload: str):
 
 
 def _launch_bytes(path):
-    """[(kernel name, dram bytes)] of every launch in an ncu raw-page CSV export."""
+    """[(kernel name, dram bytes read + written)] of every launch in an ncu ``--csv`` export
+    (one row per launch and metric)."""
     with open(path, newline="") as f:
         rows = [r for r in csv.reader(f) if r]
-    head = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    head = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
     cols = rows[head]
-    name_i = cols.index("Kernel Name")
-    rd, wr = cols.index("dram__bytes_read.sum"), cols.index("dram__bytes_write.sum")
-    units = rows[head + 1] if not rows[head + 1][0].strip().isdigit() else None
-    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6,
-             "GB": 1e9, "B": 1}
-    out = []
-    for r in rows[head + (2 if units else 1):]:
-        def val(i):
-            s = float(r[i].replace(",", ""))
-            return s * (scale.get(units[i], 1) if units else 1)
-        out.append((r[name_i], val(rd) + val(wr)))
-    return out
+    ci, cn, cm, cu, cv = (cols.index(x) for x in ("ID", "Kernel Name", "Metric Name",
+                                                  "Metric Unit", "Metric Value"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    launches = {}
+    for r in rows[head + 1:]:
+        if len(r) <= cv or r[cm] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        name, total = launches.get(r[ci], (r[cn], 0.0))
+        launches[r[ci]] = (name, total + float(r[cv].replace(",", "")) * scale.get(r[cu], 1))
+    return [launches[k] for k in sorted(launches, key=int)]
 
 
-def record(csv_path, workloads, how):
+def record(csv_path, workload, how):
+    """Stores the DRAM bytes of the last launch in an ncu CSV export (one capture of the
+    workload's split kernel) under `workload`, with the current sources' digest."""
     launches = _launch_bytes(csv_path)
-    calls, cur = [], 0.0
-    for name, b in launches:
-        cur += b
-        # a call ends with its split kernel (symmetric) or the merge (asymmetric)
-        if "decode_tc_kernel" in name or "merge_kernel" in name:
-            calls.append(cur)
-            cur = 0.0
-    if len(calls) < len(workloads):
-        raise SystemExit(f"{len(calls)} decode calls in {csv_path}, {len(workloads)} names given")
+    if not launches:
+        raise SystemExit(f"no launch in {csv_path}")
     try:
         with open(TRAFFIC_FILE) as f:
             data = json.load(f)
     except (OSError, ValueError):
         data = {}
-    digest = kernel_sources_digest()
-    for w, b in zip(workloads, calls):
-        data[w] = {"bytes": int(round(b)), "sources": digest, "how": how}
+    name, nbytes = launches[-1]
+    data[workload] = {"bytes": int(round(nbytes)), "sources": kernel_sources_digest(),
+                      "kernel": name.split("(")[0][:80], "how": how}
     with open(TRAFFIC_FILE, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
         f.write("\n")
 
 
 if __name__ == "__main__":
-    if len(sys.argv) < 3:
+    if len(sys.argv) != 3:
         raise SystemExit(__doc__)
-    record(sys.argv[1], sys.argv[2:], "one capture of each call")
+    record(sys.argv[1], sys.argv[2], "one ncu capture of the split kernel")
