@@ -15,21 +15,17 @@
 // bits) need the rotated coordinates to about 1e-7 in unit-sphere units, which the pairs give
 // (2^-22 relative per operand, fp32 accumulation) and a single fp16 operand would not.
 //
-// Operands sit in shared memory in the canonical K-major layout without swizzle (8-row ×
+// Π̂, M̂ and X̂ sit in shared memory in the canonical K-major layout without swizzle (8-row ×
 // 16-byte core matrices; LBO = distance between K-adjacent core matrices, SBO = between
-// 8-row groups).  The codec keeps Π̂ and M̂ in exactly that image, so one bulk copy per
-// image brings them in once per CTA.  Raw activations arrive by bulk copies (the TMA engine;
-// one per run of contiguous vectors) one tile ahead of the tile being computed.
+// 8-row groups).  The codec keeps Π̂ and M̂ in exactly that image, so one bulk copy brings them
+// in once per CTA.  Raw activations arrive by bulk copies (the TMA engine; one per run of
+// contiguous vectors) into a ring of tile buffers, where they are converted to X̂ in place.
+// ρ̂ goes to tensor memory, the A operand of GEMM 2.
 //
-// Two threads own vector r of the tile (TMEM lane r): lane r % 32 of warps q and q + 4 of a
-// group (the same TMEM lane quadrant q = r / 32), part p taking coordinates 64p onwards.  Each
-// reads its part of the row of D1 / D2, decides indices and signs, builds its part of every
-// code plane in registers and writes it with one store; the parts of ‖ρ‖² meet in shared
-// memory.  One CTA per SM, persistent over tiles, made of groups of 256 threads that take
-// alternate tiles, each with its own operand and staging buffers, accumulator columns and
-// barriers: one group for the product quantiser (its shared memory holds Π̂ and M̂), two for
-// the MSE quantiser, so that one group's conversion and epilogue overlap the other's product
-// and copies.
+// The thread that owns vector r of a tile reads row r of D1 / D2 (TMEM lane r), decides its
+// part of the indices and signs, builds its part of every code plane in registers and writes
+// it with one store.  The warp roles and the pipeline across tiles are described at the
+// kernel.
 #include <cuda_fp16.h>
 
 #include "tc_ptx.h"
@@ -46,45 +42,42 @@ constexpr int kSBO = 16 * 128;                 // 8-row groups: 16 core matrices
 constexpr int kRawPitch = 256;                 // one raw bf16/fp16 vector
 constexpr float kPiScale = 64.f, kMScale = 8.f, kRhoScale = 256.f;
 
-// shared-memory map of the MSE quantiser (bytes from the dynamic base): the codec's Π̂ image,
-// then one area per group of 256 threads
-struct ML {
-  static constexpr int kGroups = 2;
-  static constexpr int kParts = 2;                               // threads per vector
-  static constexpr int pi = 0;                                   // Π̂ hi | lo
-  static constexpr int area = 2 * kImg;                          // group 0's area
-  // offsets inside a group's area
-  static constexpr int a = 0;                                    // X̂
-  static constexpr int raw = kImg;                               // raw vectors of the next tile
-  static constexpr int norm = raw + kTileV * kRawPitch;          // float ‖x‖ [128]
-  static constexpr int ysc = norm + 4 * kTileV;                  // float D1 → y scale [128]
-  static constexpr int gsize = ysc + 4 * kTileV;
-  // mbarriers: the codec's image, then (raw tile, MMA) per group; then the TMEM slot
-  static constexpr int bars = area + kGroups * gsize;
-  static constexpr int total = bars + 8 * (1 + 2 * kGroups) + 8;
-  static constexpr int tmem_cols = 256;                          // D1 per group
+// Roles of a quantiser CTA: epilogue warps (warp w reads TMEM lane quadrant w % 4, part w / 4 of
+// each vector's coordinates), converter warps and one issuer warp.  The product code's
+// epilogues, and those of MSE codes of 3 or 4 bits (longer cell searches), carry most of the
+// work: two parts of 64 coordinates per vector; for 1- and 2-bit MSE codes the conversion does.
+template <bool kProd, int IB>
+struct Roles {
+  static constexpr bool kHeavyEpi = kProd || IB >= 3;
+  static constexpr int kEpiWarps = kHeavyEpi ? 8 : 4, kConvWarps = kHeavyEpi ? 4 : 8;
+  static constexpr int kParts = kEpiWarps / 4;              // threads per vector
+  static constexpr int kBlocks = 4 / kParts;                // 32-coordinate blocks per thread
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kThreads = 32 * (kEpiWarps + kConvWarps + 1);
 };
-// shared-memory map of the product quantiser: the codec's Π̂ and M̂ images, two tile buffers
-// (each holds a tile's raw vectors, then X̂ in place, then ρ̂ hi), the ρ̂ lo image, and small
-// per-tile arrays
-struct PL {
-  static constexpr int kParts = 4;                               // threads per vector
-  static constexpr int kThreads = 128 * kParts + 32;             // compute warps + issuer warp
-  static constexpr int pi = 0;                                   // Π̂ hi | lo
-  static constexpr int m = 2 * kImg;                             // M̂ hi | lo
-  static constexpr int buf = 4 * kImg;                           // tile buffers [2]
-  static constexpr int lo = 6 * kImg;                            // ρ̂ lo
-  static constexpr int ns = 7 * kImg;                            // float ‖x‖·2^s [2][128]
-  static constexpr int rr = ns + 2 * 4 * kTileV;                 // float ‖ρ‖² of parts 1..3
-  static constexpr int sexp = rr + (kParts - 1) * 4 * kTileV;    // int8 s [2][128]
-  // mbarriers: the codec's images, raw tile [2], GEMM 1, GEMM 2, X̂ ready, ρ̂ ready; then the
-  // TMEM slot
-  static constexpr int bars = sexp + 2 * kTileV;
-  static constexpr int total = bars + 8 * 7 + 8;
-  static constexpr int tmem_cols = 256;                          // D1 | D2
+
+// Shared-memory map (bytes from the dynamic base): the codec's images (Π̂ hi | lo, and for the
+// product code M̂ hi | lo), the tile buffers (each holds a tile's raw vectors, then X̂ in place),
+// per-buffer ‖x‖·2^s and s, part 1's ‖ρ‖², the mbarriers and the TMEM slot.
+template <bool kProd>
+struct QL {
+  static constexpr int kBufs = kProd ? 3 : 4;
+  static constexpr int pi = 0;                                   // Π̂ hi | lo, then M̂ hi | lo
+  static constexpr int buf = (kProd ? 4 : 2) * kImg;             // tile buffers [kBufs]
+  static constexpr int ns = buf + kBufs * kImg;                  // float ‖x‖·2^s [kBufs][128]
+  static constexpr int rr = ns + kBufs * 4 * kTileV;             // float ‖ρ‖² of part 1 [128]
+  static constexpr int sexp = rr + 4 * kTileV;                   // int8 s [kBufs][128]
+  // codec images; per buffer: raw tile in, X̂ ready; per D1 slot: GEMM 1 done; then the
+  // epilogue done per D1 slot (MSE code), or epilogue 1 done, epilogue 2 done, GEMM 2 done
+  static constexpr int nbars = 1 + 2 * kBufs + 2 + (kProd ? 3 : 2);
+  static constexpr int bars = (sexp + kBufs * kTileV + 7) / 8 * 8;
+  static constexpr int total = bars + 8 * nbars + 8;
+  static constexpr int tmem_cols = kProd ? 512 : 256;
 };
-static_assert(ML::total <= 227 * 1024 && PL::total <= 227 * 1024, "shared memory budget");
-static_assert(ML::gsize % 1024 == 0 && PL::bars % 8 == 0, "alignment");
+// TMEM columns: D1 [2], then for the product code D2 | ρ̂ hi | ρ̂ lo
+constexpr int kD2Col = 256, kRhoCol = 384;
+static_assert(QL<true>::total <= 227 * 1024 && QL<false>::total <= 227 * 1024,
+              "shared memory budget");
 
 __device__ __forceinline__ uint32_t s32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -112,10 +105,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           s32(bar))
       : "memory");
-}
-// bounded wait (the thread is suspended, not spinning, while the phase is incomplete)
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-  return tq::mbar_wait(bar, parity);
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -205,11 +194,11 @@ __device__ __forceinline__ long long vec_offset(const TcArgs& a, long long gi) {
   return (long long)b * a.sb + (long long)(bh - b * a.heads) * a.sh + (long long)t * a.st;
 }
 
-// Warp 0: bring the raw vectors of `tile` into the staging buffer.  Where the token stride is
-// one vector, the tile's vectors of one (batch, head) are contiguous in memory and move as one
-// bulk copy (lane v issues the run that starts at vector v: the tile's first vector or a
-// sequence's token 0); otherwise each vector is its own copy.  The TMA engine takes a bulk
-// copy at a time, so 128 small copies would hold the issuing warp for microseconds.
+// Bring the raw vectors of `tile` into a tile buffer (one warp).  Where the token stride is one
+// vector, the tile's vectors of one (batch, head) are contiguous in memory and move as one bulk
+// copy: for sequences of at least 32 tokens lane 0 walks the tile's runs (at most a few), else
+// lane v issues the run that starts at vector v (the tile's first vector or a sequence's token 0).
+// Otherwise each vector is its own copy.
 __device__ __forceinline__ void issue_tile(const TcArgs& a, long long tile, long long total,
                                            unsigned char* raw, uint64_t* bar, int lane) {
   const long long first = tile * kTileV;
@@ -217,7 +206,24 @@ __device__ __forceinline__ void issue_tile(const TcArgs& a, long long tile, long
   if (lane == 0) arrive_expect(bar, (unsigned)nvalid * kRawPitch);
   __syncwarp();
   const uint16_t* x = static_cast<const uint16_t*>(a.x);
-  if (a.st == TQ_D) {
+  if (a.st == TQ_D && a.tokens >= 32) {
+    if (lane == 0) {
+      int bh, t;
+      split_vec(a, first, bh, t);
+      int b = (int)((uint32_t)bh / (uint32_t)a.heads), h = bh - b * a.heads;
+      for (int v = 0; v < nvalid;) {
+        const int n = min(nvalid - v, a.tokens - t);
+        const long long off = (long long)b * a.sb + (long long)h * a.sh + (long long)t * TQ_D;
+        bulk_g2s(raw + v * kRawPitch, x + off, (unsigned)n * kRawPitch, bar);
+        v += n;
+        t = 0;
+        if (++h == a.heads) {
+          h = 0;
+          ++b;
+        }
+      }
+    }
+  } else if (a.st == TQ_D) {
     for (int v = lane; v < nvalid; v += 32) {
       int bh, t;
       split_vec(a, first + v, bh, t);
@@ -274,10 +280,11 @@ __device__ __forceinline__ void load_raw(const unsigned char* raw, int v, bool v
 // anywhere in the bf16 range.
 __device__ __forceinline__ void convert_chunks(const uint32_t (&w)[4][4], int dtype,
                                                uint32_t (&hw)[4][4], float& ns, int& s) {
+  // per chunk: its values, max |x| and Σ x² in chains of 8 (four chains run side by side)
   float f[4][8];
-  float mx = 0.f;
+  float mx[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < 4; ++j) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (dtype == TQ_BF16) {
@@ -288,27 +295,35 @@ __device__ __forceinline__ void convert_chunks(const uint32_t (&w)[4][4], int dt
         f[j][2 * e] = t.x;
         f[j][2 * e + 1] = t.y;
       }
-      mx = fmaxf(mx, fmaxf(fabsf(f[j][2 * e]), fabsf(f[j][2 * e + 1])));
     }
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  const int eb = (int)((__float_as_uint(mx) >> 23) & 0xffu);
+    float mh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mh[e] = fmaxf(fabsf(f[j][2 * e]), fabsf(f[j][2 * e + 1]));
+    mx[j] = fmaxf(fmaxf(mh[0], mh[1]), fmaxf(mh[2], mh[3]));
+  }
+  float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  const int eb = (int)((__float_as_uint(m) >> 23) & 0xffu);
   s = min(141 - eb, 126);
   const float sc = __uint_as_float((uint32_t)(s + 127) << 23);
-  float ss = 0.f;
+  float ss[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < 4; ++j) {
+    ss[j] = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float x0 = f[j][2 * e] * sc, x1 = f[j][2 * e + 1] * sc;
-      ss = fmaf(x0, x0, ss);
-      ss = fmaf(x1, x1, ss);
+      ss[j] = fmaf(x0, x0, ss[j]);
+      ss[j] = fmaf(x1, x1, ss[j]);
       const __half2 h2 = __floats2half2_rn(x0, x1);
       hw[j][e] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-  ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-  ns = sqrtf(ss);
+  }
+  float t = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+  t += __shfl_xor_sync(0xffffffffu, t, 8);
+  t += __shfl_xor_sync(0xffffffffu, t, 16);
+  ns = sqrtf(t);
 }
 __device__ __forceinline__ void store_canon(unsigned char* img, int v, int lane,
                                             const uint32_t (&hw)[4][4]) {
@@ -331,45 +346,54 @@ __device__ __forceinline__ float yscale_of(float ns) {
 template <int IB, bool kNib>
 __device__ __forceinline__ float cells_block(float (&dv)[32], float ysc, const tq_levels& lv,
                                              uint32_t (&code)[kNib ? 4 : IB]) {
-#pragma unroll
-  for (int k = 0; k < (kNib ? 4 : IB); ++k) code[k] = 0;
   float rr = 0.f;
+  if constexpr (IB == 2 && !kNib) {
+    // Two index bits, levels ±c0, ±c1, boundaries 0, ±b.  The decisions are taken on sign
+    // bits, which a funnel shift gathers into a word one coordinate per instruction: bit 1 of
+    // the cell is "y non-negative" (sign of y clear) and bit 0 is "bit 1 equals |y| > b" (sign
+    // of t = b − |y| set); the level is c0 or c1 by the sign of t, carrying the sign of y.
+    // Only a y of exactly ±0 or |y| of exactly b (inside the decision's exclusion band) can
+    // fall on the other side than the comparison y ≥ boundary would put it.  A zero vector
+    // (ysc = 0) takes the upper middle cell outright.
+    const float b = lv.b[2];
+    const uint32_t c0 = __float_as_uint(lv.c[2]), dc = c0 ^ __float_as_uint(lv.c[3]);
+    uint32_t sy = 0, sb = 0;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float y = dv[e] * ysc;
-    float level;
-    const int q = cell_of<IB>(y, lv, level);
-    if constexpr (kNib) {
-      code[e >> 3] |= (uint32_t)q << (4 * (e & 7));
-    } else {
-#pragma unroll
-      for (int p = 0; p < IB; ++p) code[p] |= (uint32_t)((q >> p) & 1) << e;
+    for (int e = 31; e >= 0; --e) {
+      const float y = dv[e] * ysc;
+      const float t = b - fabsf(y);
+      const uint32_t yb = __float_as_uint(y), tb = __float_as_uint(t);
+      sy = __funnelshift_l(yb, sy, 1);
+      sb = __funnelshift_l(tb, sb, 1);
+      const uint32_t big = (uint32_t)((int32_t)tb >> 31);
+      const float level = __uint_as_float((c0 ^ (dc & big)) ^ (yb & 0x80000000u));
+      const float rho = y - level;
+      rr = fmaf(rho, rho, rr);
+      dv[e] = rho * kRhoScale;
     }
-    const float rho = y - level;
-    rr = fmaf(rho, rho, rr);
-    dv[e] = rho * kRhoScale;
+    if (!(ysc > 0.f)) sy = sb = 0;
+    code[0] = sy ^ sb;
+    code[1] = ~sy;
+  } else {
+#pragma unroll
+    for (int k = 0; k < (kNib ? 4 : IB); ++k) code[k] = 0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float y = dv[e] * ysc;
+      float level;
+      const int q = cell_of<IB>(y, lv, level);
+      if constexpr (kNib) {
+        code[e >> 3] |= (uint32_t)q << (4 * (e & 7));
+      } else {
+#pragma unroll
+        for (int p = 0; p < IB; ++p) code[p] |= (uint32_t)((q >> p) & 1) << e;
+      }
+      const float rho = y - level;
+      rr = fmaf(rho, rho, rr);
+      dv[e] = rho * kRhoScale;
+    }
   }
   return rr;
-}
-// ρ̂ of one block as an fp16 pair into the canonical A images (row r, columns 32·blk + …)
-__device__ __forceinline__ void store_rho_pair(const float (&dv)[32], unsigned char* hi_img,
-                                               unsigned char* lo_img, int r, int blk) {
-#pragma unroll
-  for (int c8 = 0; c8 < 4; ++c8) {
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2) {
-      const float v0 = dv[8 * c8 + 2 * e2], v1 = dv[8 * c8 + 2 * e2 + 1];
-      const __half2 hh = __floats2half2_rn(v0, v1);
-      const float2 hf = __half22float2(hh);
-      const __half2 ll = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-      hi[e2] = *reinterpret_cast<const uint32_t*>(&hh);
-      lo[e2] = *reinterpret_cast<const uint32_t*>(&ll);
-    }
-    const int off = canon(r, 32 * blk + 8 * c8);
-    *reinterpret_cast<uint4*>(hi_img + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(lo_img + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-  }
 }
 // GEMM 1 of a tile: D1 = X̂ · (Π̂hi + Π̂lo)ᵀ (one thread)
 __device__ __forceinline__ void issue_gemm1(uint32_t d1, uint32_t sa, uint32_t sp) {
@@ -403,205 +427,124 @@ __device__ __forceinline__ int dest_pos(const TcArgs& a, const VecDest& d, int r
   return -1;
 }
 
-// The MSE quantiser.  One CTA per SM, persistent over tiles, made of two groups of 256 threads
-// (two per vector: warps q and q + 4 of a group share TMEM lane quadrant q, part p taking
-// coordinates 64p onwards) that take alternate tiles, each with its own operand and staging
-// buffers, accumulator columns and barriers, so that one group's conversion and epilogue
-// overlap the other's product and copies.  Per tile: conversion, GEMM 1, epilogue.
-template <int IB>
-__global__ void __launch_bounds__(128 * ML::kParts * ML::kGroups, 1)
-    quantize_mse_tc_kernel(TcArgs a) {
-  using L = ML;
-  constexpr int kGroups = L::kGroups;
-  constexpr int kGT = 128 * L::kParts;           // threads per group
-  constexpr bool kNib = IB == 4;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // this thread's group, and its warp inside the group
-  const int group = warp / (kGT / 32), gw = warp % (kGT / 32);
-  unsigned char* area = smem + L::area + group * L::gsize;
-  float* s_norm = reinterpret_cast<float*>(area + L::norm);
-  float* s_ysc = reinterpret_cast<float*>(area + L::ysc);
-  uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* bar_x = bar_const + 1 + 2 * group;
-  uint64_t* bar_mma = bar_x + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + 1 + 2 * kGroups);
-  unsigned char* raw = area + L::raw;
-  const long long total = (long long)a.batch * a.heads * a.tokens;
-  const long long ntiles = (total + kTileV - 1) / kTileV;
-  // the CTA's tiles blockIdx.x + k·gridDim.x go to its groups in turn
-  const long long tile0 = blockIdx.x + (long long)group * gridDim.x;
-  const long long tstep = (long long)kGroups * gridDim.x;
-
-  if (tid == 0) {
-    for (int b = 0; b < 1 + 2 * kGroups; ++b)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s32(bar_const + b)));
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     s32(s_tmem)),
-                 "r"(L::tmem_cols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_before();
-  __syncthreads();
-  tc_after();
-  const uint32_t tmem = *s_tmem;
-  const uint32_t d1 = tmem + 128 * group;
-  // TMEM lane quadrant (rows 32·quad..) and coordinate part (blocks 2·half..) of this warp
-  const int quad = gw & 3, half = gw >> 2;
-  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-
-  if (gw == 0) {
-    if (warp == 0 && lane == 0 && blockIdx.x < ntiles) {
-      arrive_expect(bar_const, 2 * kImg);
-      bulk_g2s(smem + L::pi, a.img, 2 * kImg, bar_const);
+// Converter warp cw: tile j's raw vectors, once in buffer j % NB, become X̂ in place, with
+// ‖x‖·2^s and s per vector; then the warp hands the buffer to the issuer.  An 8-vector group's
+// canonical image occupies exactly the bytes of its 8 raw rows, so a warp that holds a group's
+// raw chunks in registers may overwrite them.  False when the wait gave up.
+template <int NB, int kConvWarps>
+__device__ __forceinline__ bool convert_tile(const TcArgs& a, int j, long long first, int nvalid,
+                                             unsigned char* b, float* s_ns, signed char* s_exp,
+                                             uint64_t* bar_x, uint64_t* bar_a1, int cw,
+                                             int lane) {
+  const int k = j % NB;
+  if (!__all_sync(0xffffffffu, tq::mbar_wait(bar_x + k, (j / NB) & 1))) return false;
+  for (int g8 = cw; g8 < kTileV / 8; g8 += kConvWarps) {
+    const int v = 8 * g8 + (lane & 7);
+    uint32_t w[4][4], hw[4][4];
+    load_raw(b, v, v < nvalid, lane, w);
+    __syncwarp();   // the group's raw rows are in registers
+    float ns;
+    int s;
+    convert_chunks(w, a.dtype, hw, ns, s);
+    store_canon(b, v, lane, hw);
+    if (lane < 8) {
+      s_ns[k * kTileV + v] = ns;
+      s_exp[k * kTileV + v] = (signed char)s;
     }
-    if (tile0 < ntiles) issue_tile(a, tile0, total, raw, bar_x, lane);
   }
-  bool ok = blockIdx.x >= ntiles || bar_wait(bar_const, 0);
-  ok = __syncthreads_and(ok);
-  bool x_pending = tile0 < ntiles;        // a raw-tile copy is in flight
-  bool mma_pending = false;               // an MMA group is in flight
-  uint32_t px = 0, pm = 0;
-
-  for (long long tile = tile0; tile < ntiles && ok; tile += tstep) {
-    const long long first = tile * kTileV;
-    const int nvalid = (int)min((long long)kTileV, total - first);
-    const int r = 32 * quad + lane;   // this thread's vector in the epilogue
-    const VecDest vd = vec_dest(a, first, r, nvalid);   // requested now, used after the conversion
-    ok = group_sync_and(group, bar_wait(bar_x, px), kGT);
-    if (!ok) break;
-    px ^= 1;
-    x_pending = false;
-    // ---- raw → X̂ and ‖x‖: warp w of the group converts vectors 16w.., eight at a time
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int v = 16 * gw + 8 * pass + (lane & 7);
-      uint32_t w[4][4], hw[4][4];
-      load_raw(raw, v, v < nvalid, lane, w);
-      float ns;
-      int s;
-      convert_chunks(w, a.dtype, hw, ns, s);
-      store_canon(area + L::a, v, lane, hw);
-      if (lane < 8) {
-        s_norm[v] = norm_of(ns, s);
-        s_ysc[v] = yscale_of(ns);
-      }
-    }
-    const int dst = dest_pos(a, vd, r, nvalid);
-    const long long slot = (long long)vd.bh * a.capacity + dst;
-    async_proxy_fence();   // X̂ (generic writes) → tensor-core reads
-    tc_before();
-    group_sync(group, kGT);
-    tc_after();
-    if (gw == 0) {
-      if (lane == 0) {
-        issue_gemm1(d1, s32(area + L::a), s32(smem + L::pi));
-        mma_commit(bar_mma);
-      }
-      __syncwarp();
-    } else if (gw == 1) {
-      // the staging buffer is free: the group's next tile comes in while this one is computed
-      // (issued beside the MMAs: an MMA issue waits while the tensor core's queue is full)
-      const long long next = tile + tstep;
-      if (next < ntiles) {
-        async_proxy_fence();
-        issue_tile(a, next, total, raw, bar_x, lane);
-      }
-    }
-    x_pending = tile + tstep < ntiles;
-    mma_pending = true;
-    ok = group_sync_and(group, bar_wait(bar_mma, pm), kGT);
-    if (!ok) break;
-    pm ^= 1;
-    mma_pending = false;
-    tc_after();
-
-    // ---- epilogue (vector r, coordinate blocks 2·half, 2·half + 1): index codes
-    const float n = s_norm[r];
-    const float ysc = s_ysc[r];
-    uint32_t code[2][kNib ? 4 : IB];
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      float dv[32];
-      tmem_ld32(d1 + lane_base + 32 * (2 * half + hb), dv);
-      cells_block<IB, kNib>(dv, ysc, a.lv, code[hb]);
-    }
-    if (dst >= 0) {
-      if constexpr (kNib) {
-        uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 32 * half);
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-          dp[hb] = make_uint4(code[hb][0], code[hb][1], code[hb][2], code[hb][3]);
-      } else {
-#pragma unroll
-        for (int p = 0; p < IB; ++p) {
-          unsigned char* row =
-              a.idx + (((long long)vd.bh * IB + p) * a.capacity + dst) * 16 + 8 * half;
-          *reinterpret_cast<uint2*>(row) = make_uint2(code[0][p], code[1][p]);
-        }
-      }
-      if (half == 0) a.xnorm[slot] = n;
-    }
-    tc_before();
-    group_sync(group, kGT);   // D1 read and X̂ consumed before the next tile reuses them
-    tc_after();
-  }
-  if (!ok) {
-    // a bounded wait gave up: report it, let in-flight copies and MMAs land (bounded) and
-    // release the accumulator columns before leaving
-    if (tid == group * kGT) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-    if (x_pending) bar_wait(bar_x, px);
-    if (mma_pending) bar_wait(bar_mma, pm);
-  }
-  tc_before();
-  __syncthreads();
-  tc_after();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(L::tmem_cols));
+  async_proxy_fence();   // X̂ (generic writes) → tensor-core reads
+  __syncwarp();
+  if (lane == 0) tq::mbar_arrive(bar_a1 + k);
+  return true;
 }
 
-// The product quantiser.  One CTA per SM, persistent over the tiles blockIdx.x + j·gridDim.x,
-// two tiles in flight: 16 compute warps (four threads per vector: TMEM lane quadrant
-// q = warp & 3, part p = warp >> 2 taking coordinates 32p..32p+31) and one issuer warp, which
-// issues the MMAs and the tiles' bulk copies (an MMA issue waits while the tensor core's queue
-// is full, so an issuing compute warp would hold up every barrier of the tile).  Tile j's raw
-// vectors arrive in buffer j & 1 and are converted there in place to X̂; GEMM 1 reads them; the
-// first epilogue writes ρ̂ hi over X̂ and ρ̂ lo into the lo image; GEMM 2 reads both.  While
-// GEMM 2 of tile j runs, the compute warps convert tile j + 1 in the other buffer; while GEMM 1
-// of tile j + 1 runs, they take the sign epilogue of tile j, and tile j's buffer receives tile
-// j + 2.  The compute warps hand each operand to the issuer on an mbarrier (one arrival per
-// warp); the tensor core's commits hand the products back.
-template <int IB>
-__global__ void __launch_bounds__(PL::kThreads, 1) quantize_prod_tc_kernel(TcArgs a) {
-  using L = PL;
-  constexpr int kCompute = 128 * L::kParts;   // compute threads (warps 0..15)
+// Index codes of vector r's part (NBLK 32-column blocks of D1 from column d1c)
+template <int IB, bool kNib, int NBLK>
+__device__ __forceinline__ float epilogue_cells(uint32_t d1c, float ysc, const tq_levels& lv,
+                                                float (&dv)[NBLK][32],
+                                                uint32_t (&code)[NBLK][kNib ? 4 : IB]) {
+  float rr = 0.f;
+#pragma unroll
+  for (int hb = 0; hb < NBLK; ++hb) {
+    tmem_ld32(d1c + 32 * hb, dv[hb]);
+    rr += cells_block<IB, kNib>(dv[hb], ysc, lv, code[hb]);
+  }
+  return rr;
+}
+// stores of a part's index codes (planes: 4·NBLK bytes of each plane; nibbles: 16·NBLK bytes)
+template <int IB, bool kNib, int NBLK>
+__device__ __forceinline__ void store_codes(const TcArgs& a, int bh, int dst, long long slot,
+                                            int part, const uint32_t (&code)[NBLK][kNib ? 4 : IB]) {
+  if constexpr (kNib) {
+    uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 16 * NBLK * part);
+#pragma unroll
+    for (int hb = 0; hb < NBLK; ++hb)
+      dp[hb] = make_uint4(code[hb][0], code[hb][1], code[hb][2], code[hb][3]);
+  } else {
+#pragma unroll
+    for (int p = 0; p < IB; ++p) {
+      unsigned char* row =
+          a.idx + (((long long)bh * IB + p) * a.capacity + dst) * 16 + 4 * NBLK * part;
+      if constexpr (NBLK == 4)
+        *reinterpret_cast<uint4*>(row) = make_uint4(code[0][p], code[1][p], code[2][p], code[3][p]);
+      else
+        *reinterpret_cast<uint2*>(row) = make_uint2(code[0][p], code[1][p]);
+    }
+  }
+}
+
+// The quantisers.  One CTA per SM, persistent over the tiles blockIdx.x + j·gridDim.x, with
+// warp roles (an MMA issue waits while the tensor core's queue is full, so MMAs come from a warp
+// that does nothing else):
+//   converter warps  tile j's raw vectors → X̂ in buffer j % NB (in place);
+//   issuer warp      the tile copies, GEMM 1 (X̂ · Π̂ᵀ → D1) and for the product code GEMM 2
+//                    (ρ̂ · M̂ᵀ → D2, ρ̂ read from TMEM);
+//   epilogue warps   MSE code: the index codes and ‖x‖ from D1.  Product code: epilogue 1 (the
+//                    index planes, ‖x‖, ρ̂ hi | lo into TMEM, ‖ρ‖) and epilogue 2 (the signs of
+//                    D2), in the order epilogue 1 of tile j, epilogue 2 of tile j − 1.
+// D1 has two slots, so GEMM 1 of tile j + 2 runs while epilogue 1 of tile j + 1 reads the other
+// slot; GEMM 2 of tile j (once the signs of tile j − 1 are read from D2) runs under the cells of
+// tile j + 1, whose ρ̂ goes to TMEM once GEMM 2 of tile j has read the previous one.
+// Hand-overs are mbarriers: the converters' and epilogues' arrivals (one per warp) and the tensor
+// core's commits.  Every barrier's next phase can only complete after each of its waiters has
+// passed the previous one (the barriers that would otherwise run two phases ahead of a waiter
+// come one per buffer or accumulator slot), so waits on a phase's parity are exact.
+template <bool kProd, int IB>
+__global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_kernel(TcArgs a) {
+  using L = QL<kProd>;
+  using R = Roles<kProd, IB>;
+  constexpr int kEpiWarps = R::kEpiWarps, kConvWarps = R::kConvWarps;
+  constexpr int kEpiThreads = R::kEpiThreads, NBLK = R::kBlocks;
+  constexpr int NB = L::kBufs;
+  constexpr bool kNib = !kProd && IB == 4;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* s_ns = reinterpret_cast<float*>(smem + L::ns);
   float* s_rr = reinterpret_cast<float*>(smem + L::rr);
   signed char* s_exp = reinterpret_cast<signed char*>(smem + L::sexp);
   uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* bar_x = bar_const + 1;        // [2], one per tile buffer (bulk copies)
-  uint64_t* bar_g1 = bar_const + 3;       // GEMM 1 done (tensor-core commit)
-  uint64_t* bar_g2 = bar_const + 4;       // GEMM 2 done
-  uint64_t* bar_a1 = bar_const + 5;       // X̂ ready (one arrival per compute warp)
-  uint64_t* bar_a2 = bar_const + 6;       // ρ̂ ready
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + 7);
-  unsigned char* lo_img = smem + L::lo;
+  uint64_t* bar_x = bar_const + 1;          // [NB] raw tile in the buffer (bulk copies)
+  uint64_t* bar_a1 = bar_x + NB;            // [NB] X̂ in the buffer (converter warps)
+  uint64_t* bar_g1 = bar_a1 + NB;           // [2] GEMM 1 into D1[slot] done (tensor-core commit)
+  uint64_t* bar_a2 = bar_g1 + 2;            // epilogue (1) done: [2] per D1 slot (MSE), [1]
+  uint64_t* bar_a3 = bar_a2 + 1;            // epilogue 2 done (product code)
+  uint64_t* bar_g2 = bar_a3 + 1;            // GEMM 2 done (product code)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + L::nbars);
   const long long total = (long long)a.batch * a.heads * a.tokens;
   const long long ntiles = (total + kTileV - 1) / kTileV;
   const int nt = blockIdx.x < ntiles ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
   auto tile_first = [&](int j) { return (blockIdx.x + (long long)j * gridDim.x) * kTileV; };
-  auto buffer = [&](int j) { return smem + L::buf + (j & 1) * kImg; };
+  auto tile_valid = [&](int j) { return (int)min((long long)kTileV, total - tile_first(j)); };
+  auto buffer = [&](int j) { return smem + L::buf + (j % NB) * kImg; };
 
   if (tid == 0) {
-    for (int b = 0; b < 7; ++b)
+    for (int b = 0; b < L::nbars; ++b) {
+      int count = 1;                                                    // copies, commits
+      if (b >= 1 + NB && b < 1 + 2 * NB) count = kConvWarps;            // bar_a1
+      if (b >= 3 + 2 * NB && b < 5 + 2 * NB) count = kEpiWarps;         // bar_a2, bar_a2/a3
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s32(bar_const + b)),
-                   "r"(b >= 5 ? kCompute / 32 : 1));
+                   "r"(count));
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -614,194 +557,231 @@ __global__ void __launch_bounds__(PL::kThreads, 1) quantize_prod_tc_kernel(TcArg
   __syncthreads();
   tc_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t d1 = tmem, d2 = tmem + 128;
 
-  if (warp == kCompute / 32) {
-    // ---- issuer warp: the codec's images and the first two tiles, then per tile its GEMM 1,
-    // GEMM 2 and, once GEMM 2 has read the tile's buffer, the copy of the tile two ahead
+  if (warp == kEpiWarps + kConvWarps) {
+    // ================================================================ issuer warp
     bool ok = true;
-    uint32_t xbits = 0, xphase = 0;   // copies in flight per buffer; phases issued per buffer
-    int g1_issued = 0, g2_issued = 0, g2_seen = 0;
+    uint32_t cbits = 0, cpar = 0;   // buffers with a copy issued; per buffer, copies mod 2
+    uint64_t* last_bar = nullptr;   // barrier and phase of the last MMA commit
+    uint32_t last_par = 0;
     auto copy_tile = [&](int j) {
-      issue_tile(a, tile_first(j) / kTileV, total, buffer(j), bar_x + (j & 1), lane);
-      xbits |= 1u << (j & 1);
-      xphase ^= 1u << (j & 1);
+      issue_tile(a, tile_first(j) / kTileV, total, buffer(j), bar_x + j % NB, lane);
+      cbits |= 1u << (j % NB);
+      cpar ^= 1u << (j % NB);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+      ok = ok && __all_sync(0xffffffffu, tq::mbar_wait(bar, par));
+      return ok;
+    };
+    auto gemm1 = [&](int j) {   // X̂ of tile j · Π̂ᵀ → D1[j & 1]
+      if (lane == 0) {
+        issue_gemm1(tmem + 128 * (j & 1), s32(buffer(j)), s32(smem + L::pi));
+        mma_commit(bar_g1 + (j & 1));
+      }
+      __syncwarp();
+      last_bar = bar_g1 + (j & 1);
+      last_par = (j >> 1) & 1;
     };
     if (nt > 0) {
       if (lane == 0) {
-        arrive_expect(bar_const, 4 * kImg);
-        bulk_g2s(smem + L::pi, a.img, 4 * kImg, bar_const);
+        arrive_expect(bar_const, (kProd ? 4 : 2) * kImg);
+        bulk_g2s(smem + L::pi, a.img, (kProd ? 4 : 2) * kImg, bar_const);
       }
-      copy_tile(0);
-      if (nt > 1) copy_tile(1);
+      for (int j = 0; j < NB && j < nt; ++j) copy_tile(j);
+      wait(bar_const, 0);
     }
-    auto gemm1 = [&](int j) {
-      ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_a1, j & 1));   // uniform across the warp
-      if (!ok) return;
-      tc_after();
-      if (lane == 0) {
-        issue_gemm1(d1, s32(buffer(j)), s32(smem + L::pi));
-        mma_commit(bar_g1);
-      }
-      __syncwarp();
-      ++g1_issued;
-    };
-    auto gemm2 = [&](int j) {
-      ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_a2, j & 1));
-      if (!ok) return;
-      tc_after();
-      if (lane == 0) {
-        // D2 = ρ̂hi·M̂hiᵀ + ρ̂hi·M̂loᵀ + ρ̂lo·M̂hiᵀ
-        const uint32_t sh = s32(buffer(j)), sl = s32(lo_img);
-        const uint32_t smh = s32(smem + L::m), sml = smh + kImg;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t o = ks * 2 * kLBO;
-          mma_f16(d2, sdesc(sh + o), sdesc(smh + o), ks > 0 ? 1u : 0u);
-          mma_f16(d2, sdesc(sh + o), sdesc(sml + o), 1u);
-          mma_f16(d2, sdesc(sl + o), sdesc(smh + o), 1u);
+    if constexpr (kProd) {
+      for (int j = 0; j < 2 && j < nt && ok; ++j)
+        if (wait(bar_a1 + j, 0)) {
+          tc_after();
+          gemm1(j);
         }
-        mma_commit(bar_g2);
+      for (int j = 0; j < nt && ok; ++j) {
+        // epilogue 1 of tile j done: D1[j & 1] read, ρ̂ of tile j in TMEM; GEMM 1 of tile j had
+        // read the tile's buffer
+        if (!wait(bar_a2, j & 1)) break;
+        // the signs of tile j − 1 read from D2
+        if (j > 0 && !wait(bar_a3, (j - 1) & 1)) break;
+        tc_after();
+        if (lane == 0) {
+          // D2 = ρ̂hi·M̂hiᵀ + ρ̂hi·M̂loᵀ + ρ̂lo·M̂hiᵀ
+          const uint32_t d2 = tmem + kD2Col;
+          const uint32_t rh = tmem + kRhoCol, rl = rh + 64;
+          const uint32_t smh = s32(smem + L::pi + 2 * kImg), sml = smh + kImg;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = ks * 2 * kLBO;
+            tq::mma_ts(d2, rh + 8 * ks, sdesc(smh + o), kIdesc, ks > 0 ? 1u : 0u);
+            tq::mma_ts(d2, rh + 8 * ks, sdesc(sml + o), kIdesc, 1u);
+            tq::mma_ts(d2, rl + 8 * ks, sdesc(smh + o), kIdesc, 1u);
+          }
+          mma_commit(bar_g2);
+        }
+        __syncwarp();
+        last_bar = bar_g2;
+        last_par = j & 1;
+        // the tile's buffer is free (GEMM 1 of tile j has read it): the copy of tile j + NB,
+        // after GEMM 2 (on the critical path: ρ̂ of tile j + 1 waits for it)
+        if (j + NB < nt) {
+          async_proxy_fence();
+          copy_tile(j + NB);
+        }
+        if (j + 2 < nt) {
+          if (!wait(bar_a1 + (j + 2) % NB, ((j + 2) / NB) & 1)) break;
+          tc_after();
+          gemm1(j + 2);   // into D1[j & 1], read by epilogue 1 of tile j
+        }
       }
-      __syncwarp();
-      ++g2_issued;
-    };
-    if (nt > 0) gemm1(0);
-    if (nt > 0 && ok) gemm2(0);
-    for (int j = 0; j < nt && ok; ++j) {
-      if (j + 1 < nt) {
-        gemm1(j + 1);
-        if (!ok) break;
-      }
-      // GEMM 2 of tile j has read buffer j & 1 (and its raw copy was consumed before it)
-      ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_g2, j & 1));
-      if (!ok) break;
-      g2_seen = j + 1;
-      xbits &= ~(1u << (j & 1));
-      if (j + 2 < nt) {
-        async_proxy_fence();
-        copy_tile(j + 2);
-      }
-      if (j + 1 < nt) {
-        gemm2(j + 1);
-        if (!ok) break;
+    } else {
+      for (int j = 0; j < nt && ok; ++j) {
+        if (!wait(bar_a1 + j % NB, (j / NB) & 1)) break;
+        // the epilogue of tile j − 2 has read D1[j & 1] (and GEMM 1 had read its buffer)
+        if (j >= 2 && !wait(bar_a2 + (j & 1), ((j - 2) >> 1) & 1)) break;
+        tc_after();
+        gemm1(j);
+        if (j >= 2 && j + 2 < nt) {   // into the buffer of tile j − 2
+          async_proxy_fence();
+          copy_tile(j + 2);
+        }
       }
     }
     if (!ok) {
       // a bounded wait gave up: report it and let this warp's copies and MMAs land (bounded)
       if (lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-      for (int k = 0; k < 2; ++k)
-        if ((xbits >> k) & 1u) tq::mbar_wait(bar_x + k, ((xphase >> k) & 1u) ^ 1u);
-      if (g1_issued > 0) tq::mbar_wait(bar_g1, (g1_issued - 1) & 1);
-      if (g2_issued > g2_seen) tq::mbar_wait(bar_g2, (g2_issued - 1) & 1);
+      for (int b = 0; b < NB; ++b)
+        if ((cbits >> b) & 1u) tq::mbar_wait(bar_x + b, ((cpar >> b) & 1u) ^ 1u);
+      if (last_bar) tq::mbar_wait(last_bar, last_par);
     }
+  } else if (warp >= kEpiWarps) {
+    // ================================================================ converter warps
+    bool ok = true;
+    for (int j = 0; j < nt && ok; ++j)
+      ok = convert_tile<NB, kConvWarps>(a, j, tile_first(j), tile_valid(j), buffer(j), s_ns,
+                                        s_exp, bar_x, bar_a1, warp - kEpiWarps, lane);
+    if (!ok && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
   } else {
-    // ---- compute warps
+    // ================================================================ epilogue warps
     const int quad = warp & 3, part = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-    const int r = 32 * quad + lane;   // this thread's vector in the epilogues
-    bool ok = nt == 0 || bar_wait(bar_const, 0);
-    ok = group_sync_and(0, ok, kCompute);
-    uint32_t px = 0, pg1 = 0, pg2 = 0;   // parity of each barrier's next phase
-    // vector r of the tile whose sign epilogue comes next: its destination and ‖x‖
-    int dst = -1;
+    const int r = 32 * quad + lane;   // this thread's vector
+    bool ok = true;
+    // vector r of the tile whose signs come next: destination, ‖x‖ (product code)
+    int dst = -1, bh = 0;
     long long slot = 0;
     float n = 0.f;
-    VecDest vd;   // vector r of the tile whose first epilogue comes next
-    auto hand_over = [&](uint64_t* bar) {   // this warp's operand writes → the issuer
-      async_proxy_fence();
-      tc_before();
-      __syncwarp();
-      if (lane == 0) tq::mbar_arrive(bar);
-    };
-    // conversion of tile j in place
-    auto convert = [&](int j) {
-      const int k = j & 1;
-      unsigned char* b = buffer(j);
-      const long long first = tile_first(j);
-      const int nvalid = (int)min((long long)kTileV, total - first);
-      vd = vec_dest(a, first, r, nvalid);   // used by the first epilogue
-      ok = group_sync_and(0, bar_wait(bar_x + k, (px >> k) & 1u), kCompute);
+    auto begin = [&](int j, uint64_t* g1, uint32_t par) {
+      const int nvalid = tile_valid(j);
+      const VecDest vd = vec_dest(a, tile_first(j), r, nvalid);   // in flight during the wait
+      // GEMM 1 of tile j done; the converters' norms of tile j in place (an acquire of their
+      // arrival, which has completed before GEMM 1 was issued)
+      ok = group_sync_and(0, tq::mbar_wait(g1, par) &&
+                                 tq::mbar_wait(bar_a1 + j % NB, (j / NB) & 1),
+                          kEpiThreads);
       if (!ok) return;
-      px ^= 1u << k;
-      const int v = 8 * warp + (lane & 7);
-      uint32_t w[4][4], hw[4][4];
-      load_raw(b, v, v < nvalid, lane, w);
-      group_sync(0, kCompute);   // every raw chunk is in registers before the buffer is rewritten
-      float ns;
-      int s;
-      convert_chunks(w, a.dtype, hw, ns, s);
-      store_canon(b, v, lane, hw);
-      if (lane < 8) {
-        s_ns[k * kTileV + v] = ns;
-        s_exp[k * kTileV + v] = (signed char)s;
-      }
-      hand_over(bar_a1);
-      group_sync(0, kCompute);   // the norms are in place for the first epilogue
-    };
-    // first epilogue of tile j: index planes, ‖x‖, ρ̂, ‖ρ‖
-    auto epilogue1 = [&](int j) {
-      const int k = j & 1;
-      const long long first = tile_first(j);
-      const int nvalid = (int)min((long long)kTileV, total - first);
-      ok = group_sync_and(0, bar_wait(bar_g1, pg1), kCompute);
-      if (!ok) return;
-      pg1 ^= 1;
       tc_after();
       dst = dest_pos(a, vd, r, nvalid);
-      slot = (long long)vd.bh * a.capacity + dst;
-      const float ns = s_ns[k * kTileV + r];
-      n = norm_of(ns, s_exp[k * kTileV + r]);
-      float dv[32];
-      tmem_ld32(d1 + lane_base + 32 * part, dv);
-      uint32_t code[IB];
-      const float rr = cells_block<IB, false>(dv, yscale_of(ns), a.lv, code);
-      store_rho_pair(dv, buffer(j), lo_img, r, part);
-      if (part > 0) s_rr[(part - 1) * kTileV + r] = rr;
-      hand_over(bar_a2);
-      if (dst >= 0) {
-#pragma unroll
-        for (int p = 0; p < IB; ++p)
-          *reinterpret_cast<uint32_t*>(
-              a.idx + (((long long)vd.bh * IB + p) * a.capacity + dst) * 16 + 4 * part) = code[p];
-        if (part == 0) a.xnorm[slot] = n;
-      }
-      group_sync(0, kCompute);   // the parts of ‖ρ‖² are in place
-      if (part == 0 && dst >= 0) {
-        float rt = rr;
-#pragma unroll
-        for (int pp = 0; pp < L::kParts - 1; ++pp) rt += s_rr[pp * kTileV + r];
-        a.rnorm[slot] = n * sqrtf(rt);
-      }
+      bh = vd.bh;
+      slot = (long long)bh * a.capacity + dst;
     };
-    // sign epilogue of tile j
-    auto epilogue2 = [&](int j) {
-      ok = group_sync_and(0, bar_wait(bar_g2, pg2), kCompute);
-      if (!ok) return;
-      pg2 ^= 1;
-      tc_after();
-      float dv[32];
-      tmem_ld32(d2 + lane_base + 32 * part, dv);
-      uint32_t word = 0;
+    if constexpr (kProd) {
+      auto epilogue1 = [&](int j) {
+        begin(j, bar_g1 + (j & 1), (j >> 1) & 1);
+        if (!ok) return;
+        const int k = j % NB;
+        const float ns = s_ns[k * kTileV + r];
+        n = norm_of(ns, s_exp[k * kTileV + r]);
+        float dv[2][32];
+        uint32_t code[2][IB];
+        const float rr = epilogue_cells<IB, false, 2>(tmem + 128 * (j & 1) + lane_base + 64 * part,
+                                                      yscale_of(ns), a.lv, dv, code);
+        // ρ̂ (scaled residual) as fp16 pairs hi | lo into TMEM (K-major A operand of GEMM 2:
+        // column c of a row holds coordinates 2c, 2c + 1), once GEMM 2 of tile j − 1 has read it
+        if (j > 0) {
+          ok = group_sync_and(0, tq::mbar_wait(bar_g2, (j - 1) & 1), kEpiThreads);
+          if (!ok) return;
+          tc_after();
+        }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) word |= (dv[e] >= 0.f ? 1u : 0u) << e;
-      tc_before();   // D2 read before a later GEMM 2 is issued
-      if (dst >= 0)   // zero vector: zero residual, all signs +1
-        *reinterpret_cast<uint32_t*>(a.sgn + slot * 16 + 4 * part) = n > 0.f ? word : 0xffffffffu;
-    };
-
-    if (nt > 0 && ok) {
-      convert(0);
-      if (ok) epilogue1(0);
-    }
-    for (int j = 0; j < nt && ok; ++j) {
-      if (j + 1 < nt) {
-        convert(j + 1);
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const float v0 = dv[hb][2 * w], v1 = dv[hb][2 * w + 1];
+            const __half2 hh = __floats2half2_rn(v0, v1);
+            const float2 hf = __half22float2(hh);
+            const __half2 ll = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+            hi[w] = *reinterpret_cast<const uint32_t*>(&hh);
+            lo[w] = *reinterpret_cast<const uint32_t*>(&ll);
+          }
+          const uint32_t col = lane_base + 32 * part + 16 * hb;
+          tq::tmem_st_32x32b_x16(tmem + kRhoCol + col, hi);
+          tq::tmem_st_32x32b_x16(tmem + kRhoCol + 64 + col, lo);
+        }
+        tq::tmem_wait_st();
+        tc_before();
+        if (part == 1) s_rr[r] = rr;
+        __syncwarp();
+        if (lane == 0) tq::mbar_arrive(bar_a2);
+        if (dst >= 0) {
+          store_codes<IB, false, 2>(a, bh, dst, slot, part, code);
+          if (part == 0) a.xnorm[slot] = n;
+        }
+        group_sync(0, kEpiThreads);   // part 1's ‖ρ‖² is in place
+        if (part == 0 && dst >= 0) a.rnorm[slot] = n * sqrtf(rr + s_rr[r]);
+      };
+      // signs of tile j (GEMM 2 of tile j wrote D2 after the signs of tile j − 1 were read)
+      auto epilogue2 = [&](int j, int jdst, long long jslot, float jn) {
+        ok = group_sync_and(0, tq::mbar_wait(bar_g2, j & 1), kEpiThreads);
+        if (!ok) return;
+        tc_after();
+        uint32_t word[2];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          float dv[32];
+          tmem_ld32(tmem + kD2Col + lane_base + 64 * part + 32 * hb, dv);
+          // bit e = 1 where z_e is non-negative: the sign bits gathered by funnel shifts and
+          // inverted (a z of exactly −0 lies inside the sign decision's exclusion band)
+          uint32_t w = 0;
+#pragma unroll
+          for (int e = 31; e >= 0; --e) w = __funnelshift_l(__float_as_uint(dv[e]), w, 1);
+          word[hb] = jn > 0.f ? ~w : 0xffffffffu;   // zero vector: zero residual, all signs +1
+        }
+        tc_before();   // D2 read before GEMM 2 of tile j + 1
+        __syncwarp();
+        if (lane == 0) tq::mbar_arrive(bar_a3);
+        if (jdst >= 0)
+          *reinterpret_cast<uint2*>(a.sgn + jslot * 16 + 8 * part) = make_uint2(word[0], word[1]);
+      };
+      if (nt > 0) epilogue1(0);
+      for (int j = 1; j < nt && ok; ++j) {
+        const int pdst = dst;
+        const long long pslot = slot;
+        const float pn = n;
+        epilogue1(j);
         if (!ok) break;
+        epilogue2(j - 1, pdst, pslot, pn);
       }
-      epilogue2(j);
-      if (!ok) break;
-      if (j + 1 < nt) epilogue1(j + 1);
+      if (nt > 0 && ok) epilogue2(nt - 1, dst, slot, n);
+    } else {
+      for (int j = 0; j < nt && ok; ++j) {
+        begin(j, bar_g1 + (j & 1), (j >> 1) & 1);
+        if (!ok) break;
+        const int k = j % NB;
+        // the norms are read before the hand-over below frees the buffer slot for tile j + NB
+        const float ns = s_ns[k * kTileV + r];
+        const float xn = norm_of(ns, s_exp[k * kTileV + r]);
+        float dv[NBLK][32];
+        uint32_t code[NBLK][kNib ? 4 : IB];
+        epilogue_cells<IB, kNib, NBLK>(tmem + 128 * (j & 1) + lane_base + 32 * NBLK * part,
+                                       yscale_of(ns), a.lv, dv, code);
+        tc_before();   // D1 read before GEMM 1 of tile j + 2
+        __syncwarp();
+        if (lane == 0) tq::mbar_arrive(bar_a2 + (j & 1));
+        if (dst >= 0) {
+          store_codes<IB, kNib, NBLK>(a, bh, dst, slot, part, code);
+          if (part == 0) a.xnorm[slot] = xn;
+        }
+      }
     }
     if (!ok && tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
   }
@@ -813,29 +793,21 @@ __global__ void __launch_bounds__(PL::kThreads, 1) quantize_prod_tc_kernel(TcArg
                  "r"(L::tmem_cols));
 }
 
-template <typename Kernel>
-tq_status launch_tc(Kernel kernel, int threads, int smem_bytes, bool& configured,
-                    const TcArgs& a, int grid, cudaStream_t stream) {
-  if (!configured) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-        cudaSuccess)
-      return TQ_ERR_CUDA;
-    configured = true;
-  }
-  kernel<<<grid, threads, smem_bytes, stream>>>(a);
-  return tq_cuda_status(cudaGetLastError());
-}
-
 template <bool kProd, int IB>
 tq_status launch_tc(const TcArgs& a, int grid, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
-  if (kProd)
-    return launch_tc(quantize_prod_tc_kernel<IB>, PL::kThreads, PL::total, configured[dev], a,
-                     grid, stream);
-  return launch_tc(quantize_mse_tc_kernel<IB>, 128 * ML::kParts * ML::kGroups, ML::total,
-                   configured[dev], a, grid, stream);
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(quantize_tc_kernel<kProd, IB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QL<kProd>::total) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    configured[dev] = true;
+  }
+  constexpr int threads = Roles<kProd, IB>::kThreads;
+  quantize_tc_kernel<kProd, IB><<<grid, threads, QL<kProd>::total, stream>>>(a);
+  return tq_cuda_status(cudaGetLastError());
 }
 
 }  // namespace
