@@ -43,7 +43,7 @@ constexpr int kRawPitch = 256;                 // one raw bf16/fp16 vector
 constexpr float kPiScale = 64.f, kMScale = 8.f, kRhoScale = 256.f;
 
 // Roles of a quantiser CTA: epilogue warps (warp w reads TMEM lane quadrant w % 4, part w / 4 of
-// each vector's coordinates), converter warps and one issuer warp.  The product code's
+// each vector's coordinates), converter warps, an issuer warp (MMAs) and a copy warp.  The product code's
 // epilogues, and those of MSE codes of 3 or 4 bits (longer cell searches), carry most of the
 // work: two parts of 64 coordinates per vector; for 1- and 2-bit MSE codes the conversion does.
 template <bool kProd, int IB>
@@ -53,7 +53,8 @@ struct Roles {
   static constexpr int kParts = kEpiWarps / 4;              // threads per vector
   static constexpr int kBlocks = 4 / kParts;                // 32-coordinate blocks per thread
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kThreads = 32 * (kEpiWarps + kConvWarps + 1);
+  static constexpr int kIssuer = kEpiWarps + kConvWarps, kCopier = kIssuer + 1;   // warps
+  static constexpr int kThreads = 32 * (kEpiWarps + kConvWarps + 2);
 };
 
 // Shared-memory map (bytes from the dynamic base): the codec's images (Π̂ hi | lo, and for the
@@ -67,9 +68,10 @@ struct QL {
   static constexpr int ns = buf + kBufs * kImg;                  // float ‖x‖·2^s [kBufs][128]
   static constexpr int rr = ns + kBufs * 4 * kTileV;             // float ‖ρ‖² of part 1 [128]
   static constexpr int sexp = rr + 4 * kTileV;                   // int8 s [kBufs][128]
-  // codec images; per buffer: raw tile in, X̂ ready; per D1 slot: GEMM 1 done; then the
-  // epilogue done per D1 slot (MSE code), or epilogue 1 done, epilogue 2 done, GEMM 2 done
-  static constexpr int nbars = 1 + 2 * kBufs + 2 + (kProd ? 3 : 2);
+  // codec images; per buffer: raw tile in, X̂ ready, buffer free for the next copy; per D1
+  // slot: GEMM 1 done; then the epilogue done per D1 slot (MSE code), or epilogue 1 done,
+  // epilogue 2 done, GEMM 2 done
+  static constexpr int nbars = 1 + 3 * kBufs + 2 + (kProd ? 3 : 2);
   static constexpr int bars = (sexp + kBufs * kTileV + 7) / 8 * 8;
   static constexpr int total = bars + 8 * nbars + 8;
   static constexpr int tmem_cols = kProd ? 512 : 256;
@@ -525,7 +527,9 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* bar_x = bar_const + 1;          // [NB] raw tile in the buffer (bulk copies)
   uint64_t* bar_a1 = bar_x + NB;            // [NB] X̂ in the buffer (converter warps)
-  uint64_t* bar_g1 = bar_a1 + NB;           // [2] GEMM 1 into D1[slot] done (tensor-core commit)
+  uint64_t* bar_free = bar_a1 + NB;         // [NB] buffer free: GEMM 1 and the epilogue done
+                                            // with its tile (issuer warp)
+  uint64_t* bar_g1 = bar_free + NB;         // [2] GEMM 1 into D1[slot] done (tensor-core commit)
   uint64_t* bar_a2 = bar_g1 + 2;            // epilogue (1) done: [2] per D1 slot (MSE), [1]
   uint64_t* bar_a3 = bar_a2 + 1;            // epilogue 2 done (product code)
   uint64_t* bar_g2 = bar_a3 + 1;            // GEMM 2 done (product code)
@@ -541,7 +545,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     for (int b = 0; b < L::nbars; ++b) {
       int count = 1;                                                    // copies, commits
       if (b >= 1 + NB && b < 1 + 2 * NB) count = kConvWarps;            // bar_a1
-      if (b >= 3 + 2 * NB && b < 5 + 2 * NB) count = kEpiWarps;         // bar_a2, bar_a2/a3
+      if (b >= 3 + 3 * NB && b < 5 + 3 * NB) count = kEpiWarps;         // bar_a2, bar_a2/a3
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s32(bar_const + b)),
                    "r"(count));
     }
@@ -558,22 +562,47 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   tc_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == kEpiWarps + kConvWarps) {
-    // ================================================================ issuer warp
+  if (warp == R::kCopier) {
+    // ================================================================ copy warp
+    // the codec's images, the first NB tiles, then tile j + NB into buffer j % NB once the issuer
+    // has seen GEMM 1 and the epilogue done with tile j (the barrier's next phase needs the copy
+    // issued here)
     bool ok = true;
     uint32_t cbits = 0, cpar = 0;   // buffers with a copy issued; per buffer, copies mod 2
-    uint64_t* last_bar = nullptr;   // barrier and phase of the last MMA commit
-    uint32_t last_par = 0;
     auto copy_tile = [&](int j) {
       issue_tile(a, tile_first(j) / kTileV, total, buffer(j), bar_x + j % NB, lane);
       cbits |= 1u << (j % NB);
       cpar ^= 1u << (j % NB);
     };
+    if (nt > 0) {
+      if (lane == 0) {
+        arrive_expect(bar_const, (kProd ? 4 : 2) * kImg);
+        bulk_g2s(smem + L::pi, a.img, (kProd ? 4 : 2) * kImg, bar_const);
+      }
+      for (int j = 0; j < NB && j < nt; ++j) copy_tile(j);
+    }
+    for (int j = 0; j + NB < nt && ok; ++j) {
+      ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_free + j % NB, (j / NB) & 1));
+      if (!ok) break;
+      async_proxy_fence();
+      copy_tile(j + NB);
+    }
+    if (!ok) {
+      // a bounded wait gave up: report it and let this warp's copies land (bounded)
+      if (lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
+      for (int b = 0; b < NB; ++b)
+        if ((cbits >> b) & 1u) tq::mbar_wait(bar_x + b, ((cpar >> b) & 1u) ^ 1u);
+    }
+  } else if (warp == R::kIssuer) {
+    // ================================================================ issuer warp
+    bool ok = true;
+    uint64_t* last_bar = nullptr;   // barrier and phase of the last MMA commit
+    uint32_t last_par = 0;
     auto wait = [&](uint64_t* bar, uint32_t par) {
       ok = ok && __all_sync(0xffffffffu, tq::mbar_wait(bar, par));
       return ok;
     };
-    auto gemm1 = [&](int j) {   // X̂ of tile j · Π̂ᵀ → D1[j & 1]
+    auto gemm1 = [&](int j) {   // X̂ of tile j · Π̂ᵀ → D1[j & 1]; then its buffer is free
       if (lane == 0) {
         issue_gemm1(tmem + 128 * (j & 1), s32(buffer(j)), s32(smem + L::pi));
         mma_commit(bar_g1 + (j & 1));
@@ -582,14 +611,12 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
       last_bar = bar_g1 + (j & 1);
       last_par = (j >> 1) & 1;
     };
-    if (nt > 0) {
-      if (lane == 0) {
-        arrive_expect(bar_const, (kProd ? 4 : 2) * kImg);
-        bulk_g2s(smem + L::pi, a.img, (kProd ? 4 : 2) * kImg, bar_const);
-      }
-      for (int j = 0; j < NB && j < nt; ++j) copy_tile(j);
-      wait(bar_const, 0);
-    }
+    // tile j's buffer (and its norms) may take tile j + NB: its epilogue (1) has waited for its
+    // GEMM 1 and read the norms
+    auto release = [&](int j) {
+      if (lane == 0) tq::mbar_arrive(bar_free + j % NB);
+    };
+    if (nt > 0) wait(bar_const, 0);
     if constexpr (kProd) {
       for (int j = 0; j < 2 && j < nt && ok; ++j)
         if (wait(bar_a1 + j, 0)) {
@@ -597,9 +624,9 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
           gemm1(j);
         }
       for (int j = 0; j < nt && ok; ++j) {
-        // epilogue 1 of tile j done: D1[j & 1] read, ρ̂ of tile j in TMEM; GEMM 1 of tile j had
-        // read the tile's buffer
+        // epilogue 1 of tile j done: D1[j & 1] read, ρ̂ of tile j in TMEM
         if (!wait(bar_a2, j & 1)) break;
+        release(j);
         // the signs of tile j − 1 read from D2
         if (j > 0 && !wait(bar_a3, (j - 1) & 1)) break;
         tc_after();
@@ -620,12 +647,6 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         __syncwarp();
         last_bar = bar_g2;
         last_par = j & 1;
-        // the tile's buffer is free (GEMM 1 of tile j has read it): the copy of tile j + NB,
-        // after GEMM 2 (on the critical path: ρ̂ of tile j + 1 waits for it)
-        if (j + NB < nt) {
-          async_proxy_fence();
-          copy_tile(j + NB);
-        }
         if (j + 2 < nt) {
           if (!wait(bar_a1 + (j + 2) % NB, ((j + 2) / NB) & 1)) break;
           tc_after();
@@ -635,21 +656,18 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     } else {
       for (int j = 0; j < nt && ok; ++j) {
         if (!wait(bar_a1 + j % NB, (j / NB) & 1)) break;
-        // the epilogue of tile j − 2 has read D1[j & 1] (and GEMM 1 had read its buffer)
-        if (j >= 2 && !wait(bar_a2 + (j & 1), ((j - 2) >> 1) & 1)) break;
+        // the epilogue of tile j − 2 has read D1[j & 1]
+        if (j >= 2) {
+          if (!wait(bar_a2 + (j & 1), ((j - 2) >> 1) & 1)) break;
+          release(j - 2);
+        }
         tc_after();
         gemm1(j);
-        if (j >= 2 && j + 2 < nt) {   // into the buffer of tile j − 2
-          async_proxy_fence();
-          copy_tile(j + 2);
-        }
       }
     }
     if (!ok) {
-      // a bounded wait gave up: report it and let this warp's copies and MMAs land (bounded)
+      // a bounded wait gave up: report it and let this warp's MMAs land (bounded)
       if (lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
-      for (int b = 0; b < NB; ++b)
-        if ((cbits >> b) & 1u) tq::mbar_wait(bar_x + b, ((cpar >> b) & 1u) ^ 1u);
       if (last_bar) tq::mbar_wait(last_bar, last_par);
     }
   } else if (warp >= kEpiWarps) {
