@@ -68,11 +68,12 @@ struct QL {
   static constexpr int ns = buf + kBufs * kImg;                  // float ‖x‖·2^s [kBufs][128]
   static constexpr int rr = ns + kBufs * 4 * kTileV;             // float ‖ρ‖² of part 1 [128]
   static constexpr int sexp = rr + 4 * kTileV;                   // int8 s [kBufs][128]
+  static constexpr int tab = sexp + kBufs * kTileV;              // float boundaries, levels [16]
   // codec images; per buffer: raw tile in, X̂ ready, buffer free for the next copy; per D1
   // slot: GEMM 1 done; then the epilogue done per D1 slot (MSE code), or epilogue 1 done,
   // epilogue 2 done, GEMM 2 done
   static constexpr int nbars = 1 + 3 * kBufs + 2 + (kProd ? 3 : 2);
-  static constexpr int bars = (sexp + kBufs * kTileV + 7) / 8 * 8;
+  static constexpr int bars = tab + 16 * 4;
   static constexpr int total = bars + 8 * nbars + 8;
   static constexpr int tmem_cols = kProd ? 512 : 256;
 };
@@ -259,6 +260,22 @@ __device__ __forceinline__ int cell_of(float y, const tq_levels& lv, float& leve
   level = pos ? c : -c;
   return pos ? (h | cnt) : ((h - 1) ^ cnt);
 }
+// The same cell by binary search over the positive boundaries, with the positive boundaries
+// and levels in a shared-memory table (tab[0..7] boundaries, tab[8..15] levels): IB − 1
+// comparisons instead of 2^(IB−1) − 1 for 3- and 4-bit codes.  Ties go up, as above.
+template <int IB>
+__device__ __forceinline__ int cell_of_search(float y, const float* tab, float& level) {
+  constexpr int h = 1 << (IB - 1);
+  const float ay = fabsf(y);
+  int cnt = 0;
+#pragma unroll
+  for (int st = h / 2; st >= 1; st >>= 1)
+    if (tab[cnt + st - 1] <= ay) cnt += st;
+  const float c = tab[8 + cnt];
+  const bool pos = y >= 0.f;
+  level = pos ? c : -c;
+  return pos ? (h | cnt) : ((h - 1) ^ cnt);
+}
 
 // ---- conversion: raw bf16/fp16 vectors → X̂ (fp16, per-vector power-of-two scale) and ‖x‖.
 // A warp converts eight vectors: lane (i = lane & 7, g = lane >> 3) takes chunks
@@ -347,7 +364,7 @@ __device__ __forceinline__ float yscale_of(float ns) {
 // residual ρ = y − level, returned as Σ ρ² with kRhoScale·ρ left in dv.
 template <int IB, bool kNib>
 __device__ __forceinline__ float cells_block(float (&dv)[32], float ysc, const tq_levels& lv,
-                                             uint32_t (&code)[kNib ? 4 : IB]) {
+                                             const float* tab, uint32_t (&code)[kNib ? 4 : IB]) {
   float rr = 0.f;
   if constexpr (IB == 2 && !kNib) {
     // Two index bits, levels ±c0, ±c1, boundaries 0, ±b.  The decisions are taken on sign
@@ -383,7 +400,9 @@ __device__ __forceinline__ float cells_block(float (&dv)[32], float ysc, const t
     for (int e = 0; e < 32; ++e) {
       const float y = dv[e] * ysc;
       float level;
-      const int q = cell_of<IB>(y, lv, level);
+      int q;
+      if constexpr (IB >= 3) q = cell_of_search<IB>(y, tab, level);
+      else q = cell_of<IB>(y, lv, level);
       if constexpr (kNib) {
         code[e >> 3] |= (uint32_t)q << (4 * (e & 7));
       } else {
@@ -463,13 +482,13 @@ __device__ __forceinline__ bool convert_tile(const TcArgs& a, int j, long long f
 // Index codes of vector r's part (NBLK 32-column blocks of D1 from column d1c)
 template <int IB, bool kNib, int NBLK>
 __device__ __forceinline__ float epilogue_cells(uint32_t d1c, float ysc, const tq_levels& lv,
-                                                float (&dv)[NBLK][32],
+                                                const float* tab, float (&dv)[NBLK][32],
                                                 uint32_t (&code)[NBLK][kNib ? 4 : IB]) {
   float rr = 0.f;
 #pragma unroll
   for (int hb = 0; hb < NBLK; ++hb) {
     tmem_ld32(d1c + 32 * hb, dv[hb]);
-    rr += cells_block<IB, kNib>(dv[hb], ysc, lv, code[hb]);
+    rr += cells_block<IB, kNib>(dv[hb], ysc, lv, tab, code[hb]);
   }
   return rr;
 }
@@ -524,6 +543,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   float* s_ns = reinterpret_cast<float*>(smem + L::ns);
   float* s_rr = reinterpret_cast<float*>(smem + L::rr);
   signed char* s_exp = reinterpret_cast<signed char*>(smem + L::sexp);
+  float* s_tab = reinterpret_cast<float*>(smem + L::tab);
   uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* bar_x = bar_const + 1;          // [NB] raw tile in the buffer (bulk copies)
   uint64_t* bar_a1 = bar_x + NB;            // [NB] X̂ in the buffer (converter warps)
@@ -556,6 +576,12 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
                      s32(s_tmem)),
                  "r"(L::tmem_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid >= 32 && tid < 48) {   // the positive boundaries and levels (3- and 4-bit cells)
+    constexpr int h = 1 << (IB - 1);
+    const int k = tid - 32;
+    if (k < 8) s_tab[k] = k < h - 1 ? a.lv.b[h + k] : INFINITY;
+    else s_tab[k] = k - 8 < h ? a.lv.c[h + k - 8] : 0.f;
   }
   tc_before();
   __syncthreads();
@@ -711,7 +737,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         float dv[2][32];
         uint32_t code[2][IB];
         const float rr = epilogue_cells<IB, false, 2>(tmem + 128 * (j & 1) + lane_base + 64 * part,
-                                                      yscale_of(ns), a.lv, dv, code);
+                                                      yscale_of(ns), a.lv, s_tab, dv, code);
         // ρ̂ (scaled residual) as fp16 pairs hi | lo into TMEM (K-major A operand of GEMM 2:
         // column c of a row holds coordinates 2c, 2c + 1), once GEMM 2 of tile j − 1 has read it
         if (j > 0) {
@@ -791,7 +817,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         float dv[NBLK][32];
         uint32_t code[NBLK][kNib ? 4 : IB];
         epilogue_cells<IB, kNib, NBLK>(tmem + 128 * (j & 1) + lane_base + 32 * NBLK * part,
-                                       yscale_of(ns), a.lv, dv, code);
+                                       yscale_of(ns), a.lv, s_tab, dv, code);
         tc_before();   // D1 read before GEMM 1 of tile j + 2
         __syncwarp();
         if (lane == 0) tq::mbar_arrive(bar_a2 + (j & 1));
