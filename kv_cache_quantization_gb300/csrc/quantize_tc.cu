@@ -43,9 +43,10 @@ constexpr int kRawPitch = 256;                 // one raw bf16/fp16 vector
 constexpr float kPiScale = 64.f, kMScale = 8.f, kRhoScale = 256.f;
 
 // Roles of a quantiser CTA: epilogue warps (warp w reads TMEM lane quadrant w % 4, part w / 4 of
-// each vector's coordinates), converter warps, an issuer warp (MMAs) and a copy warp.  The product code's
-// epilogues, and those of MSE codes of 3 or 4 bits (longer cell searches), carry most of the
-// work: two parts of 64 coordinates per vector; for 1- and 2-bit MSE codes the conversion does.
+// each vector's coordinates), converter warps, an issuer warp (MMAs) and a copy warp.  The
+// product code's epilogues, and those of MSE codes of 3 or 4 bits (longer cell searches), carry
+// most of the work: two parts of 64 coordinates per vector; for 1- and 2-bit MSE codes the
+// conversion does.
 template <bool kProd, int IB>
 struct Roles {
   static constexpr bool kHeavyEpi = kProd || IB >= 3;
@@ -69,11 +70,12 @@ struct QL {
   static constexpr int rr = ns + kBufs * 4 * kTileV;             // float ‖ρ‖² of part 1 [128]
   static constexpr int sexp = rr + 4 * kTileV;                   // int8 s [kBufs][128]
   static constexpr int tab = sexp + kBufs * kTileV;              // float boundaries, levels [16]
+  static constexpr int tiles = tab + 16 * 4;                     // long long tile index [kBufs]
   // codec images; per buffer: raw tile in, X̂ ready, buffer free for the next copy; per D1
   // slot: GEMM 1 done; then the epilogue done per D1 slot (MSE code), or epilogue 1 done,
   // epilogue 2 done, GEMM 2 done
   static constexpr int nbars = 1 + 3 * kBufs + 2 + (kProd ? 3 : 2);
-  static constexpr int bars = tab + 16 * 4;
+  static constexpr int bars = tiles + 8 * 4;
   static constexpr int total = bars + 8 * nbars + 8;
   static constexpr int tmem_cols = kProd ? 512 : 256;
 };
@@ -196,6 +198,59 @@ __device__ __forceinline__ long long vec_offset(const TcArgs& a, long long gi) {
   const int b = (int)((uint32_t)bh / (uint32_t)a.heads);
   return (long long)b * a.sb + (long long)(bh - b * a.heads) * a.sh + (long long)t * a.st;
 }
+
+// Whether a tile holds a vector to store: with per-sequence counts, tiles past a sequence's
+// count (the padding of a ragged batch) are skipped; a tile that runs into the next sequence is
+// kept.
+__device__ __forceinline__ bool tile_live(const TcArgs& a, long long tile) {
+  if (!a.count) return true;
+  int bh, t;
+  split_vec(a, tile * kTileV, bh, t);
+  if (t + kTileV > a.tokens) return true;
+  return t < a.count[(uint32_t)bh / (uint32_t)a.heads];
+}
+// A cursor over the live tiles among tile0 + k·stride, in order: the position (batch, head,
+// token) of the candidate's first vector advances by additions, and a sequence's count is read
+// when the cursor enters its batch row.
+struct LiveCursor {
+  long long tile, ntiles;
+  int stride, b, h, t, cb, cnt;
+  __device__ __forceinline__ LiveCursor(const TcArgs& a, long long tile0, int stride_,
+                                        long long ntiles_)
+      : tile(tile0), ntiles(ntiles_), stride(stride_), cb(-1), cnt(0) {
+    int bh;
+    split_vec(a, tile0 * kTileV, bh, t);
+    b = (int)((uint32_t)bh / (uint32_t)a.heads);
+    h = bh - b * a.heads;
+  }
+  __device__ __forceinline__ bool live(const TcArgs& a) {
+    if (!a.count || t + kTileV > a.tokens) return true;
+    if (b != cb) {
+      cb = b;
+      cnt = a.count[b];
+    }
+    return t < cnt;
+  }
+  __device__ __forceinline__ void step(const TcArgs& a) {
+    tile += stride;
+    long long tt = (long long)t + (long long)stride * kTileV;
+    if (tt >= a.tokens) {
+      const long long q = tt / a.tokens;   // sequences passed (rarely more than one)
+      tt -= q * a.tokens;
+      const long long hh = h + q;
+      b += (int)(hh / a.heads);
+      h = (int)(hh % a.heads);
+    }
+    t = (int)tt;
+  }
+  // the next live tile (≥ ntiles when there is none)
+  __device__ __forceinline__ long long next(const TcArgs& a) {
+    while (tile < ntiles && !live(a)) step(a);
+    const long long r = tile;
+    if (tile < ntiles) step(a);
+    return r;
+  }
+};
 
 // Bring the raw vectors of `tile` into a tile buffer (one warp).  Where the token stride is one
 // vector, the tile's vectors of one (batch, head) are contiguous in memory and move as one bulk
@@ -453,12 +508,13 @@ __device__ __forceinline__ int dest_pos(const TcArgs& a, const VecDest& d, int r
 // canonical image occupies exactly the bytes of its 8 raw rows, so a warp that holds a group's
 // raw chunks in registers may overwrite them.  False when the wait gave up.
 template <int NB, int kConvWarps>
-__device__ __forceinline__ bool convert_tile(const TcArgs& a, int j, long long first, int nvalid,
-                                             unsigned char* b, float* s_ns, signed char* s_exp,
-                                             uint64_t* bar_x, uint64_t* bar_a1, int cw,
-                                             int lane) {
+__device__ __forceinline__ bool convert_tile(const TcArgs& a, int j, long long total,
+                                             const long long* s_tile, unsigned char* b,
+                                             float* s_ns, signed char* s_exp, uint64_t* bar_x,
+                                             uint64_t* bar_a1, int cw, int lane) {
   const int k = j % NB;
   if (!__all_sync(0xffffffffu, tq::mbar_wait(bar_x + k, (j / NB) & 1))) return false;
+  const int nvalid = (int)min((long long)kTileV, total - s_tile[k] * kTileV);
   for (int g8 = cw; g8 < kTileV / 8; g8 += kConvWarps) {
     const int v = 8 * g8 + (lane & 7);
     uint32_t w[4][4], hw[4][4];
@@ -544,6 +600,9 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   float* s_rr = reinterpret_cast<float*>(smem + L::rr);
   signed char* s_exp = reinterpret_cast<signed char*>(smem + L::sexp);
   float* s_tab = reinterpret_cast<float*>(smem + L::tab);
+  // the tile in each buffer, written by the copy warp before the copy's barrier arrival and
+  // read behind the barriers that follow it
+  long long* s_tile = reinterpret_cast<long long*>(smem + L::tiles);
   uint64_t* bar_const = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* bar_x = bar_const + 1;          // [NB] raw tile in the buffer (bulk copies)
   uint64_t* bar_a1 = bar_x + NB;            // [NB] X̂ in the buffer (converter warps)
@@ -556,9 +615,11 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + L::nbars);
   const long long total = (long long)a.batch * a.heads * a.tokens;
   const long long ntiles = (total + kTileV - 1) / kTileV;
-  const int nt = blockIdx.x < ntiles ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
-  auto tile_first = [&](int j) { return (blockIdx.x + (long long)j * gridDim.x) * kTileV; };
-  auto tile_valid = [&](int j) { return (int)min((long long)kTileV, total - tile_first(j)); };
+  // The CTA's tiles are the live ones among blockIdx.x + k·gridDim.x; the copy warp walks them in
+  // order and records the j-th in s_tile[j % NB] for the other roles.
+  auto tile_valid = [&](long long tile) {
+    return (int)min((long long)kTileV, total - tile * kTileV);
+  };
   auto buffer = [&](int j) { return smem + L::buf + (j % NB) * kImg; };
 
   if (tid == 0) {
@@ -587,6 +648,13 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   __syncthreads();
   tc_after();
   const uint32_t tmem = *s_tmem;
+  // the number of live tiles: every thread tests one tile per round
+  int nt = 0;
+  const long long mine = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  for (long long k0 = 0; k0 < mine; k0 += blockDim.x) {
+    const long long k = k0 + tid;
+    nt += __syncthreads_count(k < mine && tile_live(a, blockIdx.x + k * gridDim.x));
+  }
 
   if (warp == R::kCopier) {
     // ================================================================ copy warp
@@ -595,8 +663,12 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     // issued here)
     bool ok = true;
     uint32_t cbits = 0, cpar = 0;   // buffers with a copy issued; per buffer, copies mod 2
-    auto copy_tile = [&](int j) {
-      issue_tile(a, tile_first(j) / kTileV, total, buffer(j), bar_x + j % NB, lane);
+    LiveCursor cur(a, blockIdx.x, gridDim.x, ntiles);
+    auto copy_tile = [&](int j) {   // the j-th live tile: the next one on this warp's cursor
+      const long long tile = cur.next(a);
+      if (lane == 0) s_tile[j % NB] = tile;   // before issue_tile's barrier arrival
+      __syncwarp();
+      issue_tile(a, tile, total, buffer(j), bar_x + j % NB, lane);
       cbits |= 1u << (j % NB);
       cpar ^= 1u << (j % NB);
     };
@@ -700,8 +772,8 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     // ================================================================ converter warps
     bool ok = true;
     for (int j = 0; j < nt && ok; ++j)
-      ok = convert_tile<NB, kConvWarps>(a, j, tile_first(j), tile_valid(j), buffer(j), s_ns,
-                                        s_exp, bar_x, bar_a1, warp - kEpiWarps, lane);
+      ok = convert_tile<NB, kConvWarps>(a, j, total, s_tile, buffer(j), s_ns, s_exp, bar_x,
+                                        bar_a1, warp - kEpiWarps, lane);
     if (!ok && lane == 0) atomicOr(&g_tq_flags, TQ_FLAG_TIMEOUT);
   } else {
     // ================================================================ epilogue warps
@@ -714,13 +786,13 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     long long slot = 0;
     float n = 0.f;
     auto begin = [&](int j, uint64_t* g1, uint32_t par) {
-      const int nvalid = tile_valid(j);
-      const VecDest vd = vec_dest(a, tile_first(j), r, nvalid);   // in flight during the wait
-      // GEMM 1 of tile j done; the converters' norms of tile j in place (an acquire of their
-      // arrival, which has completed before GEMM 1 was issued)
-      ok = group_sync_and(0, tq::mbar_wait(g1, par) &&
-                                 tq::mbar_wait(bar_a1 + j % NB, (j / NB) & 1),
-                          kEpiThreads);
+      // the converters' norms and the tile index of tile j (an acquire of their arrival, which
+      // has completed before GEMM 1 was issued), then its destination, during GEMM 1
+      ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_a1 + j % NB, (j / NB) & 1));
+      const long long tile = s_tile[j % NB];
+      const int nvalid = tile_valid(tile);
+      const VecDest vd = vec_dest(a, tile * kTileV, r, nvalid);   // in flight during the wait
+      ok = group_sync_and(0, ok && tq::mbar_wait(g1, par), kEpiThreads);
       if (!ok) return;
       tc_after();
       dst = dest_pos(a, vd, r, nvalid);
