@@ -68,6 +68,60 @@ def test_tiled_positions_and_counts():
         match_prod_codes(x[1, hh, :17].double().cpu().numpy(), gi, gs, gx, gr, pi, s, c, stats)
 
 
+@pytest.mark.parametrize("layout", ["token-major", "short-rows"])
+def test_tiled_copy_paths_with_counts(layout):
+    """The tile copies take three paths: one copy per run of a long sequence, one per run
+    starting at each vector of sequences shorter than 32 tokens, and one per vector when the
+    token stride is not one vector ([batch, tokens, heads, 128] storage seen as [batch, heads,
+    tokens, 128]).  Each is run with per-sequence counts that leave whole tiles empty; every
+    stored slot's norm and a sample of its codes match the oracle, and untouched slots stay."""
+    if layout == "token-major":
+        bsz, h, t = 2, 4, 700
+        base = rand_x((bsz, t, h, D), 41, torch.bfloat16)
+        x = base.transpose(1, 2)                       # token stride = h vectors
+        assert x.stride(2) == h * D
+        counts = [700, 333]
+    else:
+        bsz, h, t = 8, 16, 20
+        x = rand_x((bsz, h, t, D), 42, torch.bfloat16)
+        counts = [20, 0, 7, 19, 1, 20, 13, 0]
+    cnt = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    cap = (t + 63) // 64 * 64
+    pi, s = oracle_constants()
+    for kind in ("prod", "mse"):
+        if kind == "prod":
+            codec = api.Codec.prod(3)
+            cache = api.ProdCache.empty(bsz, h, cap, 3)
+            cache.xnorm.fill_(-1)
+            api.quantize_prod(codec, x, cache, count=cnt)
+        else:
+            codec = api.Codec.mse(2)
+            cache = api.MSECache.empty(bsz, h, cap, 2)
+            cache.xnorm.fill_(-1)
+            api.quantize_mse(codec, x, cache, count=cnt)
+        flags_clear()
+        xn = cache.xnorm.cpu()
+        ref = x.float().norm(dim=-1).cpu()
+        stats = CodeStats()
+        c = oracle_codebook(2)
+        for b in range(bsz):
+            n = counts[b]
+            assert torch.allclose(xn[b, :, :n], ref[b, :, :n], rtol=2e-6), (kind, b)
+            assert (xn[b, :, n:] == -1).all(), (kind, b)
+            if n == 0:
+                continue
+            for hh in (0, h - 1):
+                toks = range(0, n, max(1, n // 12))
+                xs = x[b, hh, list(toks)].double().cpu().numpy()
+                if kind == "prod":
+                    gi, gs, gx, gr = unpack_prod_at(cache, b, hh, toks, 2)
+                    match_prod_codes(xs, gi, gs, gx, gr, pi, s, c, stats)
+                else:
+                    gi, gx = unpack_mse_at(cache, b, hh, toks, 2)
+                    match_mse_codes(xs, gi, gx, pi, c, stats)
+        assert stats.idx_excluded < 1e-4 * stats.coords + 3, stats
+
+
 def test_tiled_overflow_flag():
     """Tiled path: tokens past the capacity are skipped and raise TQ_FLAG_POS_OVERFLOW."""
     x = rand_x((1, 4, 400, D), 32, torch.bfloat16)
