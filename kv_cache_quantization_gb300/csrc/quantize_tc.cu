@@ -53,7 +53,6 @@ struct Roles {
   static constexpr int kEpiWarps = kHeavyEpi ? 8 : 4, kConvWarps = kHeavyEpi ? 4 : 8;
   static constexpr int kParts = kEpiWarps / 4;              // threads per vector
   static constexpr int kBlocks = 4 / kParts;                // 32-coordinate blocks per thread
-  static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kIssuer = kEpiWarps + kConvWarps, kCopier = kIssuer + 1;   // warps
   static constexpr int kThreads = 32 * (kEpiWarps + kConvWarps + 2);
 };
@@ -73,8 +72,8 @@ struct QL {
   static constexpr int tiles = tab + 16 * 4;                     // long long tile index [kBufs]
   // codec images; per buffer: raw tile in, X̂ ready, buffer free for the next copy; per D1
   // slot: GEMM 1 done; then the epilogue done per D1 slot (MSE code), or epilogue 1 done,
-  // epilogue 2 done, GEMM 2 done
-  static constexpr int nbars = 1 + 3 * kBufs + 2 + (kProd ? 3 : 2);
+  // epilogue 2 done, GEMM 2 done, part 1's ‖ρ‖² in place
+  static constexpr int nbars = 1 + 3 * kBufs + 2 + (kProd ? 4 : 2);
   static constexpr int bars = tiles + 8 * 4;
   static constexpr int total = bars + 8 * nbars + 8;
   static constexpr int tmem_cols = kProd ? 512 : 256;
@@ -134,20 +133,6 @@ __device__ __forceinline__ void tc_after() {
 }
 __device__ __forceinline__ void async_proxy_fence() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// barrier of one group of nt threads (named barrier 1 + group), and its AND-reduction
-__device__ __forceinline__ void group_sync(int group, int nt) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(nt) : "memory");
-}
-__device__ __forceinline__ bool group_sync_and(int group, bool v, int nt) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(1 + group), "r"(nt)
-      : "memory");
-  return r != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
                                          uint64_t* bar) {
@@ -591,7 +576,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   using L = QL<kProd>;
   using R = Roles<kProd, IB>;
   constexpr int kEpiWarps = R::kEpiWarps, kConvWarps = R::kConvWarps;
-  constexpr int kEpiThreads = R::kEpiThreads, NBLK = R::kBlocks;
+  constexpr int NBLK = R::kBlocks;
   constexpr int NB = L::kBufs;
   constexpr bool kNib = !kProd && IB == 4;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -612,6 +597,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
   uint64_t* bar_a2 = bar_g1 + 2;            // epilogue (1) done: [2] per D1 slot (MSE), [1]
   uint64_t* bar_a3 = bar_a2 + 1;            // epilogue 2 done (product code)
   uint64_t* bar_g2 = bar_a3 + 1;            // GEMM 2 done (product code)
+  uint64_t* bar_rr = bar_g2 + 1;            // part 1's ‖ρ‖² of the tile in place (product code)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_const + L::nbars);
   const long long total = (long long)a.batch * a.heads * a.tokens;
   const long long ntiles = (total + kTileV - 1) / kTileV;
@@ -627,6 +613,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
       int count = 1;                                                    // copies, commits
       if (b >= 1 + NB && b < 1 + 2 * NB) count = kConvWarps;            // bar_a1
       if (b >= 3 + 3 * NB && b < 5 + 3 * NB) count = kEpiWarps;         // bar_a2, bar_a2/a3
+      if (kProd && b == 6 + 3 * NB) count = kEpiWarps / 2;              // bar_rr
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s32(bar_const + b)),
                    "r"(count));
     }
@@ -792,7 +779,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
       const long long tile = s_tile[j % NB];
       const int nvalid = tile_valid(tile);
       const VecDest vd = vec_dest(a, tile * kTileV, r, nvalid);   // in flight during the wait
-      ok = group_sync_and(0, ok && tq::mbar_wait(g1, par), kEpiThreads);
+      ok = __all_sync(0xffffffffu, ok && tq::mbar_wait(g1, par));
       if (!ok) return;
       tc_after();
       dst = dest_pos(a, vd, r, nvalid);
@@ -813,7 +800,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         // ρ̂ (scaled residual) as fp16 pairs hi | lo into TMEM (K-major A operand of GEMM 2:
         // column c of a row holds coordinates 2c, 2c + 1), once GEMM 2 of tile j − 1 has read it
         if (j > 0) {
-          ok = group_sync_and(0, tq::mbar_wait(bar_g2, (j - 1) & 1), kEpiThreads);
+          ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_g2, (j - 1) & 1));
           if (!ok) return;
           tc_after();
         }
@@ -835,19 +822,32 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         }
         tq::tmem_wait_st();
         tc_before();
-        if (part == 1) s_rr[r] = rr;
+        // the two parts' ‖ρ‖² meet in shared memory; part 0 reads before its hand-over, so that
+        // part 1 (which writes the next tile's only after GEMM 2 of this tile, after that
+        // hand-over) cannot overwrite it early
+        float rt = rr;
+        if (part == 1) {
+          s_rr[r] = rr;
+          __syncwarp();
+          if (lane == 0) tq::mbar_arrive(bar_rr);
+        } else {
+          ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_rr, j & 1));
+          if (!ok) return;
+          rt += s_rr[r];
+        }
         __syncwarp();
         if (lane == 0) tq::mbar_arrive(bar_a2);
         if (dst >= 0) {
           store_codes<IB, false, 2>(a, bh, dst, slot, part, code);
-          if (part == 0) a.xnorm[slot] = n;
+          if (part == 0) {
+            a.xnorm[slot] = n;
+            a.rnorm[slot] = n * sqrtf(rt);
+          }
         }
-        group_sync(0, kEpiThreads);   // part 1's ‖ρ‖² is in place
-        if (part == 0 && dst >= 0) a.rnorm[slot] = n * sqrtf(rr + s_rr[r]);
       };
       // signs of tile j (GEMM 2 of tile j wrote D2 after the signs of tile j − 1 were read)
       auto epilogue2 = [&](int j, int jdst, long long jslot, float jn) {
-        ok = group_sync_and(0, tq::mbar_wait(bar_g2, j & 1), kEpiThreads);
+        ok = __all_sync(0xffffffffu, tq::mbar_wait(bar_g2, j & 1));
         if (!ok) return;
         tc_after();
         uint32_t word[2];
