@@ -59,7 +59,8 @@ struct Roles {
 
 // Shared-memory map (bytes from the dynamic base): the codec's images (Π̂ hi | lo, and for the
 // product code M̂ hi | lo), the tile buffers (each holds a tile's raw vectors, then X̂ in place),
-// per-buffer ‖x‖·2^s and s, part 1's ‖ρ‖², the mbarriers and the TMEM slot.
+// per-buffer ‖x‖·2^s and s, part 1's ‖ρ‖², the positive boundaries and levels (3- and 4-bit
+// cells), the tile index of each buffer, the mbarriers and the TMEM slot.
 template <bool kProd>
 struct QL {
   static constexpr int kBufs = kProd ? 3 : 4;
