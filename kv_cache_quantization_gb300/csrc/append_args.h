@@ -29,6 +29,7 @@ struct AppendKV {
   tq_levels klv, vlv;
   int kbits, vbits;            // index bits
   int v_nibbles;               // value codes nibble-packed (4 bits)
+  int shared_pi;               // the two codecs hold the same Π: kpiT serves the values too
 };
 
 }  // namespace tq

@@ -485,6 +485,7 @@ tq::AppendKV append_args(const StepIn& in, const tq_attn_desc* desc, const tq_co
   ap.kpiT = kc->d_piT; ap.kmT = kc->d_mT; ap.vpiT = vc->d_piT;
   ap.klv = a.kl; ap.vlv = a.vl;
   ap.kbits = kc->ibits; ap.vbits = vc->ibits; ap.v_nibbles = vc->ibits == 4;
+  ap.shared_pi = kc->pi_digest == vc->pi_digest;
   return ap;
 }
 
@@ -566,7 +567,7 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
     if (!step) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
     m.app = append_args(*step, desc, kc, vc, k, v, seq_lens, a);
     m.len_add = 1;
-    if (tq_step_prologue_fits(desc->batch, desc->kv_heads)) {
+    if (tq_step_prologue_fits(desc->batch, desc->kv_heads, m.app.shared_pi ? 1 : 2)) {
       // the appends and the query operand in one prologue launch, then the split decode; the
       // split grid reads the appended token only after the prologue has completed
       m.fresh = 1;

@@ -70,8 +70,9 @@ tq_status tq_launch_decode_tc(const tq_mma_launch& a, cudaStream_t stream);
 // The same after a prologue kernel that appends the step's new key and value and builds the
 // query operand in one launch.
 tq_status tq_launch_decode_step_tc(const tq_mma_launch& a, cudaStream_t stream);
-// Whether that prologue fits in one wave of CTAs (else the appends run as their own launch).
-bool tq_step_prologue_fits(int batch, int kv_heads);
+// Whether that prologue, with `appends` append CTAs per (batch, KV head), fits in one wave of
+// CTAs (else the appends run as their own launch).
+bool tq_step_prologue_fits(int batch, int kv_heads, int appends);
 // The appends of a decode step as one launch (quantize.cu), a programmatic-launch secondary.
 tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t stream);
 // Workspace bytes per (batch, KV head) for its query operand images.

@@ -369,15 +369,16 @@ __global__ void __launch_bounds__(kPrepThreads, SPC == 4 ? 4 : 1)
 }
 
 // Prologue of a decode step, the split kernel's programmatic-launch primary in place of the
-// operand kernel.  Grid (kSlices / SPC + 2, KV heads, batch): the first kSlices / SPC CTAs of a
-// (batch, KV head) build its query operand; the next one quantises the step's new key into the
-// key cache at position seq_lens[b] (product code), the last one the new value (MSE code).  One
-// launch does the work of the two appends and the operand kernel, which would otherwise run
-// one after the other.
+// operand kernel.  Grid (kSlices / SPC + appends, KV heads, batch): the first kSlices / SPC CTAs
+// of a (batch, KV head) build its query operand; the rest quantise the step's new key (product
+// code) and value (MSE code) into the caches at position seq_lens[b]: one CTA for both when
+// the two codecs share Π, else one CTA each.  One launch does the work of the appends and the
+// operand kernel, which would otherwise run one after the other.
 template <int KB, bool HILO, int SPC>
 __global__ void __launch_bounds__(kAppendThreads, 1) step_prologue_kernel(const tq_mma_launch a) {
   constexpr int nsl = kSlices / SPC;
   if ((int)blockIdx.x < nsl) query_prep_role<KB, HILO, SPC>(a, blockIdx.x);
+  else if (a.app.shared_pi) append_kv_pair_role(a.app, blockIdx.y, blockIdx.z);
   else append_kv_role(a.app, (int)blockIdx.x == nsl, blockIdx.y, blockIdx.z);
 }
 
@@ -1189,7 +1190,7 @@ tq_status launch_one(const tq_mma_launch& a0, bool step, cudaStream_t stream) {
     const int spc = units * kSlices <= 2LL * tq_num_sms() ? 1
                     : units * (kSlices / 2) <= 2LL * tq_num_sms() ? 2 : 4;
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(kSlices / spc + (step ? 2 : 0), a.Hkv, a.B);
+    pc.gridDim = dim3(kSlices / spc + (step ? (a.app.shared_pi ? 1 : 2) : 0), a.Hkv, a.B);
     pc.blockDim = dim3(step ? kAppendThreads : kPrepThreads);
     pc.stream = stream;
     cudaLaunchAttribute pa[1];
@@ -1299,11 +1300,11 @@ tq_status tq_launch_decode_step_tc(const tq_mma_launch& a, cudaStream_t stream) 
   return launch_kbits(a, true, stream);
 }
 
-bool tq_step_prologue_fits(int batch, int kv_heads) {
+bool tq_step_prologue_fits(int batch, int kv_heads, int appends) {
   // the prologue runs one CTA of 512 threads per SM (its append CTAs' registers): use it when
   // all its CTAs fit in one wave
   const long long units = (long long)batch * kv_heads;
   const int sms = tq_num_sms();
   const int spc = units * kSlices <= 2LL * sms ? 1 : units * (kSlices / 2) <= 2LL * sms ? 2 : 4;
-  return units * (kSlices / spc + 2) <= sms;
+  return units * (kSlices / spc + appends) <= sms;
 }

@@ -267,6 +267,12 @@ extern "C" tq_status tq_codec_create(int d, tq_kind kind, int bits, const double
         h_m[(size_t)i * d + j] = acc;
       }
   }
+  // the digest lets a decode step tell that its key and value codecs share Π (then one CTA
+  // appends both with one load of Πᵀ)
+  uint64_t dig = 1469598103934665603ull;
+  const unsigned char* pb = reinterpret_cast<const unsigned char*>(h_pi.data());
+  for (size_t i = 0; i < n * sizeof(float); ++i) dig = (dig ^ pb[i]) * 1099511628211ull;
+  c->pi_digest = dig;
   cudaError_t e = cudaSuccess;
   const size_t bytes = n * sizeof(float);
   e = cudaMalloc(&c->d_pi, bytes);

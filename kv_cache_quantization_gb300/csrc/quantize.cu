@@ -14,6 +14,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <climits>
+
 #include "tq_internal.h"
 
 TQ_DEFINE_FLAGS(tq_take_flags_quantize)
@@ -312,10 +315,11 @@ __global__ void __launch_bounds__(tq::kAppendThreads) quantize_small_kernel(Quan
   tq::append_quantize<kProd>(aa, tp, tm, sm, tid);
 }
 
-// The appends of a decode step in one launch: grid (2, KV heads, batch), CTA x = 0 the key,
-// x = 1 the value of (batch, KV head).
-__global__ void __launch_bounds__(tq::kAppendThreads) append_kv_kernel(const tq::AppendKV a) {
-  tq::append_kv_role(a, blockIdx.x == 0, blockIdx.y, blockIdx.z);
+// The appends of a decode step in one launch: at most one CTA per SM, each taking every
+// gridDim.x-th (batch, KV head) unit, key and value, with one load of the codecs' constants.
+__global__ void __launch_bounds__(tq::kAppendThreads, 1)
+    append_kv_kernel(const tq::AppendKV a, int units) {
+  tq::append_kv_units(a, units);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -463,8 +467,11 @@ tq_status tq_launch_quantize_tiles(const tq_codec* c, bool prod, const void* x, 
 }
 
 tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t stream) {
+  const long long units = (long long)batch * a.Hkv;
+  if (units <= 0) return TQ_OK;
+  if (units > INT_MAX) return TQ_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, a.Hkv, batch);
+  cfg.gridDim = dim3((unsigned)std::min<long long>(units, tq_num_sms()));
   cfg.blockDim = dim3(tq::kAppendThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -472,7 +479,8 @@ tq_status tq_launch_append_kv(const tq::AppendKV& a, int batch, cudaStream_t str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, append_kv_kernel, a) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, append_kv_kernel, a, (int)units) != cudaSuccess)
+    return TQ_ERR_CUDA;
   return tq_cuda_status(cudaGetLastError());
 }
 

@@ -31,6 +31,7 @@ struct tq_codec {
   double centroids_d[16];
   float lut_scale;   // fp16-friendly scale of the levels (decode pair table)
   void* d_img;       // tensor-core operand images: 64·Π as an fp16 pair, then (prod) 8·M
+  uint64_t pi_digest;  // FNV-1a of the float32 Π: equal for codecs that share the rotation
 };
 
 // Constants passed by value to kernels.

@@ -539,21 +539,26 @@ def test_decode_serving_loop():
     assert stats.sign_excluded < 1e-4 * stats.coords, stats
 
 
-@pytest.mark.parametrize("kbits,vbits,hq,hkv,batch", [
-    (3, 2, 32, 8, 1),     # the long-context shape (4-head groups, value planes)
-    (3, 4, 28, 4, 3),     # the 32K shape (7-head groups, value pair table)
-    (4, 4, 28, 4, 6),     # the serving shape (3-bit key indices)
-    (5, 3, 8, 2, 2),      # 4-bit key indices: the CUDA-core path
-    (3, 2, 16, 4, 40),    # 160 units: the appends as their own launch before the operand kernel
+@pytest.mark.parametrize("kbits,vbits,hq,hkv,batch,vlayer", [
+    (3, 2, 32, 8, 1, 0),     # the long-context shape (4-head groups, value planes)
+    (3, 4, 28, 4, 3, 0),     # the 32K shape (7-head groups, value pair table)
+    (4, 4, 28, 4, 6, 0),     # the serving shape (3-bit key indices)
+    (5, 3, 8, 2, 2, 0),      # 4-bit key indices: the CUDA-core path
+    (3, 2, 16, 4, 40, 0),    # 160 units: the appends as their own launch before the operand kernel
+    (3, 2, 32, 8, 1, 1),     # the value codec's Π from another layer: one append CTA per vector
+    (3, 4, 16, 4, 40, 1),    # the same in the appends' own launch (keys first, then values)
+    (5, 3, 8, 2, 2, 1),
 ])
-def test_decode_step_equals_separate_calls(kbits, vbits, hq, hkv, batch):
+def test_decode_step_equals_separate_calls(kbits, vbits, hq, hkv, batch, vlayer):
     """tq_decode_step gives bit for bit the caches and outputs of tq_quantize_prod +
     tq_quantize_mse (one token at pos) + tq_decode_attention over pos + 1 tokens, over three
-    chained steps (lens_out feeding the next step), with ragged lengths."""
+    chained steps (lens_out feeding the next step), with ragged lengths.  With the two codecs
+    sharing Π (vlayer 0) the step quantises each key and value together in one CTA; with
+    another Π for the values (vlayer 1) it appends them separately."""
     rng = np.random.default_rng(1700 + kbits * 10 + vbits)
     lens = [int(x) for x in rng.integers(1, 1500, size=batch)]
     cap = 1600
-    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits)
+    kc, vc = api.Codec.prod(kbits), api.Codec.mse(vbits, layer=vlayer)
     k = rand_x((batch, hkv, cap, D), 1701, torch.bfloat16)
     v = rand_x((batch, hkv, cap, D), 1702, torch.bfloat16)
     caches = []
