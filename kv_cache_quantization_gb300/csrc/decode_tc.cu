@@ -189,7 +189,10 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
   // they are gathered here and leave as 16-byte stores
   __shared__ __align__(16) unsigned char stage[SPC == 4 ? NP * kN * 32 : 16];
   __shared__ __align__(16) float qf[8][TQ_D];
-  __shared__ float red[SPC][2][16][8][8];   // [slice][Π|S][k chunk][j in slice][head]
+  // [slice][Π|S][head][k chunk · 8 + j in slice], rows padded to 136 floats: a warp's stores
+  // (8 j × 4 k chunks) and the sums' reads (8 j × 4 heads) fall in 32 distinct banks
+  constexpr int kRedPitch = 16 * 8 + 8;
+  __shared__ float red[SPC][2][8][kRedPitch];
   __shared__ float prod[SPC][2][8][8];      // [slice][Π|S][j in slice][head]
   __shared__ float s_nq[8], s_inq[8], s_uq[8], s_wq[8];
   __shared__ float s_off[SPC][2][8];        // [slice][index planes | sign plane][column]
@@ -272,14 +275,14 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
 #pragma unroll
         for (int k = 0; k < 8; ++k) x = fmaf(t[u][k], qf[h][8 * kq + k], x);
       }
-      if (act) red[u][which][kq][jl][h] = x;
+      if (act) red[u][which][h][kq * 8 + jl] = x;
     }
   __syncthreads();
   for (int it = tid; act && it < SPC * 2 * 8 * 8; it += kPrepThreads) {
-    const int u = it >> 7, wh = (it >> 6) & 1, jj = (it >> 3) & 7, h = it & 7;
+    const int u = it >> 7, wh = (it >> 6) & 1, h = (it >> 3) & 7, jj = it & 7;
     float x = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) x += red[u][wh][k][jj][h];
+    for (int k = 0; k < 16; ++k) x += red[u][wh][h][k * 8 + jj];
     prod[u][wh][jj][h] = x;
   }
   __syncthreads();
