@@ -43,6 +43,7 @@
  *                 uint8 [batch][heads][capacity][64]      (B = 4)
  *     mse xnorm : float [batch][heads][capacity]
  *   capacity must be a positive multiple of 64 and every array 16-byte aligned.
+ *   Paged caches (tq_pages below) keep the same layout with pages in place of sequences.
  */
 #ifndef TQ_H_
 #define TQ_H_
@@ -112,16 +113,43 @@ tq_status tq_codec_destroy(tq_codec* codec);
 
 /* ------------------------------------------------------------------ caches */
 
+/* A paged cache: the codes of a sequence live in fixed-size pages of a shared pool instead of
+ * one span of `capacity` slots per (sequence, head), so that sequences can grow by whole pages
+ * taken from a free list ([QJL] §六: the store appends in chunks; this block table is this
+ * library's form of it).  The pool has the flat layout above with `num_pages` in place of
+ * batch and `page_tokens` in place of capacity: page q holds, for each head h, the
+ * page_tokens slots of row q·heads + h.  Token t of sequence b is slot t % page_tokens of
+ * page block_table[b·max_pages + t / page_tokens]; the sequence's capacity is
+ * max_pages·page_tokens, which is what the calls' `capacity` argument must be.  A table entry
+ * read for a token that is written or attended and lies outside [0, num_pages) makes the
+ * kernel skip that token's page and raise TQ_FLAG_PAGE (the decode output of that row is then
+ * undefined).  Entries for pages past a sequence's tokens are never read.  Page sizes of 256
+ * tokens or more keep the decode's copies per 256-token stage at one or two per array. */
+typedef struct {
+  const int32_t* block_table;  /* device, int32 [batch][max_pages] */
+  int32_t max_pages;           /* entries per sequence, ≥ 1 */
+  int32_t page_tokens;         /* slots per page, a positive multiple of 64 */
+  int32_t num_pages;           /* pages in the pool, ≥ 1 */
+} tq_pages;
+
 typedef struct {
   uint8_t* idx;    /* device, [batch][heads][b−1][capacity][16] */
   uint8_t* sgn;    /* device, [batch][heads][capacity][16] */
   float* xnorm;    /* device, [batch][heads][capacity] */
   float* rnorm;    /* device, [batch][heads][capacity] */
+  /* host, NULL for the flat layout; else the pool's block table (read when a call is made:
+   * the struct may be reused or freed after the call returns, the table it points to may not
+   * change until the work has run).  Taken by tq_quantize_prod / tq_quantize_mse and by
+   * tq_decode_attention, its no-alloc form, tq_decode_step and tq_prefill_attention where
+   * they decode on the tensor cores (keys of 2 to 4 bits; 5-bit keys return
+   * TQ_ERR_UNSUPPORTED); the other calls take flat caches only (TQ_ERR_UNSUPPORTED). */
+  const tq_pages* pages;
 } tq_prod_cache;
 
 typedef struct {
   uint8_t* idx;    /* device, planes [batch][heads][B][capacity][16] or nibbles [..][capacity][64] */
   float* xnorm;    /* device, [batch][heads][capacity] */
+  const tq_pages* pages;   /* as in tq_prod_cache */
 } tq_mse_cache;
 
 /* Bytes of packed codes per token per head (norms included): prod b bits → (b−1)·16+16+8;
@@ -346,6 +374,7 @@ size_t tq_decode_noalloc_scratch_bytes(void);
 #define TQ_FLAG_POS_OVERFLOW 0x1u   /* a quantised token landed at or beyond capacity */
 #define TQ_FLAG_LEN_OVERFLOW 0x2u   /* a seq_len or tail_len exceeded its capacity */
 #define TQ_FLAG_TIMEOUT      0x4u   /* a bounded device-side wait gave up */
+#define TQ_FLAG_PAGE         0x8u   /* a block-table entry outside [0, num_pages) was skipped */
 
 /* Synchronises the current device, returns the status word in *flags (host) and clears
  * it.  Returns TQ_ERR_TIMEOUT if TQ_FLAG_TIMEOUT was set, else TQ_ERR_DEVICE_STATUS if any

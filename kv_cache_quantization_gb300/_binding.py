@@ -19,19 +19,25 @@ TQ_PROD, TQ_MSE = 0, 1
 TQ_HEAD_DIM = 128
 TQ_MAX_GROUP = 8
 TQ_CAPACITY_ALIGN = 64
-TQ_FLAG_POS_OVERFLOW, TQ_FLAG_LEN_OVERFLOW, TQ_FLAG_TIMEOUT = 1, 2, 4
+TQ_FLAG_POS_OVERFLOW, TQ_FLAG_LEN_OVERFLOW, TQ_FLAG_TIMEOUT, TQ_FLAG_PAGE = 1, 2, 4, 8
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
 
 
+class tq_pages(ctypes.Structure):
+    _fields_ = [("block_table", _vp), ("max_pages", _i32), ("page_tokens", _i32),
+                ("num_pages", _i32)]
+
+
 class tq_prod_cache(ctypes.Structure):
-    _fields_ = [("idx", _vp), ("sgn", _vp), ("xnorm", _vp), ("rnorm", _vp)]
+    _fields_ = [("idx", _vp), ("sgn", _vp), ("xnorm", _vp), ("rnorm", _vp),
+                ("pages", ctypes.POINTER(tq_pages))]
 
 
 class tq_mse_cache(ctypes.Structure):
-    _fields_ = [("idx", _vp), ("xnorm", _vp)]
+    _fields_ = [("idx", _vp), ("xnorm", _vp), ("pages", ctypes.POINTER(tq_pages))]
 
 
 class tq_attn_desc(ctypes.Structure):

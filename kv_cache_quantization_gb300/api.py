@@ -112,12 +112,46 @@ def _cap(capacity: int) -> int:
 
 
 @dataclasses.dataclass
+class Pages:
+    """A block table over a page pool (include/tq.h, tq_pages): token t of sequence b lives in
+    slot t % page_tokens of page block_table[b, t // page_tokens]."""
+    block_table: torch.Tensor   # int32 [batch, max_pages], on the device
+    page_tokens: int
+    num_pages: int
+
+    def __post_init__(self):
+        if self.block_table.dtype != torch.int32 or self.block_table.dim() != 2:
+            raise ValueError("block_table must be int32 [batch, max_pages]")
+        self.block_table = self.block_table.contiguous()
+        self._c = B.tq_pages(self.block_table.data_ptr(), self.block_table.shape[1],
+                             self.page_tokens, self.num_pages)
+
+    @property
+    def max_pages(self):
+        return self.block_table.shape[1]
+
+    @property
+    def capacity(self):
+        """Slots per sequence."""
+        return self.max_pages * self.page_tokens
+
+    def c(self):
+        return ctypes.pointer(self._c)
+
+
+def _pages_ptr(pages):
+    return None if pages is None else pages.c()
+
+
+@dataclasses.dataclass
 class ProdCache:
-    """Packed key cache [batch][heads][capacity] (layout of include/tq.h)."""
+    """Packed key cache [batch][heads][capacity] (layout of include/tq.h); with `pages` the
+    arrays are a page pool [num_pages][heads][page_tokens] addressed through a block table."""
     idx: torch.Tensor      # uint8 [B, H, b-1, cap, 16]
     sgn: torch.Tensor      # uint8 [B, H, cap, 16]
     xnorm: torch.Tensor    # float32 [B, H, cap]
     rnorm: torch.Tensor    # float32 [B, H, cap]
+    pages: Optional[Pages] = None
 
     @classmethod
     def empty(cls, batch, heads, capacity, bits, device="cuda"):
@@ -127,13 +161,22 @@ class ProdCache:
                    torch.zeros(batch, heads, cap, dtype=torch.float32, device=device),
                    torch.zeros(batch, heads, cap, dtype=torch.float32, device=device))
 
+    @classmethod
+    def empty_paged(cls, pages: Pages, heads, bits, device="cuda"):
+        """A zeroed page pool of pages.num_pages pages for the block table `pages`."""
+        c = cls.empty(pages.num_pages, heads, pages.page_tokens, bits, device)
+        if c.capacity != pages.page_tokens:
+            raise ValueError("page_tokens must be a multiple of TQ_CAPACITY_ALIGN")
+        c.pages = pages
+        return c
+
     @property
     def capacity(self):
-        return self.sgn.shape[2]
+        return self.pages.capacity if self.pages is not None else self.sgn.shape[2]
 
     def c(self):
         return B.tq_prod_cache(self.idx.data_ptr(), self.sgn.data_ptr(), self.xnorm.data_ptr(),
-                               self.rnorm.data_ptr())
+                               self.rnorm.data_ptr(), _pages_ptr(self.pages))
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in (self.idx, self.sgn, self.xnorm, self.rnorm))
@@ -141,10 +184,12 @@ class ProdCache:
 
 @dataclasses.dataclass
 class MSECache:
-    """Packed value cache [batch][heads][capacity]: bit planes, or nibbles for 4 bits."""
+    """Packed value cache [batch][heads][capacity]: bit planes, or nibbles for 4 bits; with
+    `pages` a page pool as for ProdCache."""
     idx: torch.Tensor      # uint8 [B, H, bits, cap, 16] or [B, H, cap, 64]
     xnorm: torch.Tensor    # float32 [B, H, cap]
     bits: int
+    pages: Optional[Pages] = None
 
     @classmethod
     def empty(cls, batch, heads, capacity, bits, device="cuda"):
@@ -155,12 +200,21 @@ class MSECache:
             idx = torch.zeros(batch, heads, bits, cap, 16, dtype=torch.uint8, device=device)
         return cls(idx, torch.zeros(batch, heads, cap, dtype=torch.float32, device=device), bits)
 
+    @classmethod
+    def empty_paged(cls, pages: Pages, heads, bits, device="cuda"):
+        """A zeroed page pool of pages.num_pages pages for the block table `pages`."""
+        c = cls.empty(pages.num_pages, heads, pages.page_tokens, bits, device)
+        if c.xnorm.shape[2] != pages.page_tokens:
+            raise ValueError("page_tokens must be a multiple of TQ_CAPACITY_ALIGN")
+        c.pages = pages
+        return c
+
     @property
     def capacity(self):
-        return self.xnorm.shape[2]
+        return self.pages.capacity if self.pages is not None else self.xnorm.shape[2]
 
     def c(self):
-        return B.tq_mse_cache(self.idx.data_ptr(), self.xnorm.data_ptr())
+        return B.tq_mse_cache(self.idx.data_ptr(), self.xnorm.data_ptr(), _pages_ptr(self.pages))
 
     def nbytes(self):
         return self.idx.numel() + self.xnorm.numel() * 4

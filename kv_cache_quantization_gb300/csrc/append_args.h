@@ -30,6 +30,7 @@ struct AppendKV {
   int kbits, vbits;            // index bits
   int v_nibbles;               // value codes nibble-packed (4 bits)
   int shared_pi;               // the two codecs hold the same Π: kpiT serves the values too
+  tq_rowmap kmap, vmap;        // the caches' row maps (flat, or block tables)
 };
 
 }  // namespace tq

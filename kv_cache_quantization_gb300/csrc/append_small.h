@@ -22,9 +22,9 @@ constexpr int kAppendThreads = 512;
 struct AppendArgs {
   const void* x;        // the vector's 128 coordinates (dtype), 16-byte aligned
   int dtype;
-  int dst;              // cache position
-  long long bh;         // (batch, head) row of the cache
-  int capacity;
+  int slot;             // slot in the cache row
+  long long row;        // cache row: batch·heads + head, or page·heads + head (paged)
+  int rowcap;           // slots per cache row
   uint8_t* idx;         // plane-major index codes, or nibbles (nibbles != 0)
   uint8_t* sgn;         // product code: sign plane (null for MSE codes)
   float* xnorm;
@@ -92,14 +92,14 @@ struct AppendSmem {
 };
 
 // Quantises the vector into the cache: every thread of the CTA calls it (it synchronises the
-// CTA); tp (and tm for a product code) were loaded by append_load_t.  The caller has checked
-// that a.dst lies inside the capacity.
+// CTA); tp (and tm for a product code) were loaded by append_load_t.  The caller has mapped
+// the position to a.row and a.slot, inside the cache.
 template <bool kProd>
 __device__ __forceinline__ void append_quantize(const AppendArgs& a, const float (&tp)[32],
                                                 const float (&tm)[32], AppendSmem& sm, int tid) {
   float vals[8];
   if (tid < 16) append_load8(a.x, a.dtype, tid * 8, vals);
-  const long long slot = a.bh * a.capacity + a.dst;
+  const long long slot = a.row * a.rowcap + a.slot;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < 16) {
 #pragma unroll
@@ -135,7 +135,7 @@ __device__ __forceinline__ void append_quantize(const AppendArgs& a, const float
         const unsigned word = __ballot_sync(0xffffffffu, (q >> p) & 1);
         if (lane == 0)
           reinterpret_cast<uint32_t*>(
-              a.idx + ((a.bh * a.ibits + p) * a.capacity + a.dst) * 16)[warp] = word;
+              a.idx + ((a.row * a.ibits + p) * a.rowcap + a.slot) * 16)[warp] = word;
       }
     }
     if (tid == 0) a.xnorm[slot] = n;
@@ -171,14 +171,17 @@ __device__ __forceinline__ void append_unit(const AppendKV& a, bool key, int kvh
     return;
   }
   AppendArgs aa;
+  const tq_rowmap& map = key ? a.kmap : a.vmap;
+  if (!tq_map_slot(map, a.Hkv, b, kvh, pos, aa.row, aa.slot)) {
+    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+    return;
+  }
+  aa.rowcap = tq_row_slots(map, a.cap);
   const long long off = bh * TQ_D;
   aa.x = a.dtype == TQ_F32
              ? static_cast<const void*>(static_cast<const float*>(key ? a.k_new : a.v_new) + off)
              : static_cast<const void*>(static_cast<const uint16_t*>(key ? a.k_new : a.v_new) + off);
   aa.dtype = a.dtype;
-  aa.dst = pos;
-  aa.bh = bh;
-  aa.capacity = a.cap;
   if (key) {
     aa.idx = a.kidx; aa.sgn = a.ksgn; aa.xnorm = a.kxn; aa.rnorm = a.krn;
     aa.lv = a.klv; aa.ibits = a.kbits; aa.nibbles = 0;
@@ -240,9 +243,19 @@ __device__ __forceinline__ void append_pair(const AppendKV& a, int kvh, int b,
     if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
     return;
   }
+  long long krow, vrow;
+  int kslot, vslot;
+  const bool kok = tq_map_slot(a.kmap, a.Hkv, b, kvh, pos, krow, kslot);
+  const bool vok = tq_map_slot(a.vmap, a.Hkv, b, kvh, pos, vrow, vslot);
+  if (!kok || !vok) {
+    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+    return;
+  }
+  const int krc = tq_row_slots(a.kmap, a.cap), vrc = tq_row_slots(a.vmap, a.cap);
   const int warp = tid >> 5, lane = tid & 31;
   const int side = warp >> 2;   // for tid < 256: 0 the key's coordinates, 1 the value's
-  const long long off = bh * TQ_D, slot = bh * a.cap + pos;
+  const long long off = bh * TQ_D;
+  const long long kslot_all = krow * krc + kslot, vslot_all = vrow * vrc + vslot;
   if (tid < 32) {
     const void* base = tid < 16 ? a.k_new : a.v_new;
     const void* x = a.dtype == TQ_F32
@@ -289,17 +302,19 @@ __device__ __forceinline__ void append_pair(const AppendKV& a, int kvh, int b,
     // index codes: warp w owns coordinates 32(w mod 4) .. 32(w mod 4) + 31 of its side
     if (side == 1 && a.v_nibbles) {
       const int other = __shfl_xor_sync(0xffffffffu, q, 1);
-      if ((lane & 1) == 0) a.vidx[slot * 64 + (j >> 1)] = (uint8_t)(q | (other << 4));
+      if ((lane & 1) == 0) a.vidx[vslot_all * 64 + (j >> 1)] = (uint8_t)(q | (other << 4));
     } else {
       const int ib = side ? a.vbits : a.kbits;
       uint8_t* idx = side ? a.vidx : a.kidx;
+      const long long row = side ? vrow : krow;
+      const int rc = side ? vrc : krc, sl = side ? vslot : kslot;
       for (int p = 0; p < ib; ++p) {
         const unsigned word = __ballot_sync(0xffffffffu, (q >> p) & 1);
         if (lane == 0)
-          reinterpret_cast<uint32_t*>(idx + ((bh * ib + p) * a.cap + pos) * 16)[warp & 3] = word;
+          reinterpret_cast<uint32_t*>(idx + ((row * ib + p) * rc + sl) * 16)[warp & 3] = word;
       }
     }
-    if (j == 0) (side ? a.vxn : a.kxn)[slot] = n;
+    if (j == 0) (side ? a.vxn : a.kxn)[side ? vslot_all : kslot_all] = n;
   }
   // the key's residual: ‖ρ‖² and the signs of M ρ
   float r2 = r * r;
@@ -312,8 +327,8 @@ __device__ __forceinline__ void append_pair(const AppendKV& a, int kvh, int b,
   const float z = append_matvec(tm, sm.rho, sm.part[0], tid);   // contains __syncthreads
   if (warp < 4) {
     const unsigned word = n > 0.f ? __ballot_sync(0xffffffffu, z >= 0.f) : 0xffffffffu;
-    if (lane == 0) reinterpret_cast<uint32_t*>(a.ksgn + slot * 16)[warp] = word;
-    if (tid == 0) a.krn[slot] = n * sqrtf((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3]));
+    if (lane == 0) reinterpret_cast<uint32_t*>(a.ksgn + kslot_all * 16)[warp] = word;
+    if (tid == 0) a.krn[kslot_all] = n * sqrtf((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3]));
   }
 }
 

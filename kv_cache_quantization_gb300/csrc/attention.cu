@@ -475,7 +475,8 @@ struct StepIn {
 // The appends of a decode step (the caches' pointers and the codecs' constants).
 tq::AppendKV append_args(const StepIn& in, const tq_attn_desc* desc, const tq_codec* kc,
                          const tq_codec* vc, const tq_prod_cache& k, const tq_mse_cache& v,
-                         const int32_t* pos, const DecodeArgs& a) {
+                         const tq_rowmap& kmap, const tq_rowmap& vmap, const int32_t* pos,
+                         const DecodeArgs& a) {
   tq::AppendKV ap{};
   ap.k_new = in.k_new; ap.v_new = in.v_new; ap.dtype = in.kv_dtype;
   ap.pos = pos; ap.lens_out = in.lens_out;
@@ -486,6 +487,7 @@ tq::AppendKV append_args(const StepIn& in, const tq_attn_desc* desc, const tq_co
   ap.klv = a.kl; ap.vlv = a.vl;
   ap.kbits = kc->ibits; ap.vbits = vc->ibits; ap.v_nibbles = vc->ibits == 4;
   ap.shared_pi = kc->pi_digest == vc->pi_digest;
+  ap.kmap = kmap; ap.vmap = vmap;
   return ap;
 }
 
@@ -511,6 +513,9 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
   if ((st = tq_check_codec(vc, TQ_MSE)) != TQ_OK) return st;
   if ((st = check_prod_cache(k)) != TQ_OK) return st;
   if ((st = check_mse_cache(v)) != TQ_OK) return st;
+  tq_rowmap kmap, vmap;
+  if ((st = tq_rowmap_of(k.pages, desc->capacity, &kmap)) != TQ_OK) return st;
+  if ((st = tq_rowmap_of(v.pages, desc->capacity, &vmap)) != TQ_OK) return st;
   if (!q || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < p.bytes)
     return TQ_ERR_INVALID_ARG;
@@ -539,6 +544,7 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
   const int rows = desc->batch * desc->q_heads;
   const bool tc = tq_tc_decode_supported(kc->ibits, vc->ibits, p.G, p.nsplit);
   if (!tc && qps > 1) return TQ_ERR_UNSUPPORTED;   // query rows sharing a cache row: tcgen05 path
+  if (!tc && (kmap.table || vmap.table)) return TQ_ERR_UNSUPPORTED;   // paged: tcgen05 path
   if (tc) {
     tq_mma_launch m{};
     m.qps = qps;
@@ -550,6 +556,7 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
     m.u = kc->d_u; m.w = kc->d_w; m.smax = kc->smax;
     m.qfrag = ws + p.q_off;
     m.kidx = k.idx; m.ksgn = k.sgn; m.kxn = k.xnorm; m.krn = k.rnorm;
+    m.kmap = kmap; m.vmap = vmap;
     m.kbits = kc->ibits; m.kd = tq_decompose_levels(kc);
     m.vidx = v.idx; m.vxn = v.xnorm; m.vbits = vc->ibits;
     if (vc->ibits < 4) m.vd = tq_decompose_levels(vc);
@@ -565,7 +572,7 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
     m.max_len = desc->max_seq_len;
     tq_tc_operand_scales(m.kd, &m.s_idx, &m.s_sgn);
     if (!step) return tq_launch_decode_tc(m, stream);   // query operand, split decode + merge
-    m.app = append_args(*step, desc, kc, vc, k, v, seq_lens, a);
+    m.app = append_args(*step, desc, kc, vc, k, v, kmap, vmap, seq_lens, a);
     m.len_add = 1;
     if (tq_step_prologue_fits(desc->batch, desc->kv_heads, m.app.shared_pi ? 1 : 2)) {
       // the appends and the query operand in one prologue launch, then the split decode; the
@@ -581,7 +588,7 @@ tq_status run_decode(const tq_attn_desc* desc, const tq_codec* kc, const tq_code
   }
   if (step) {
     // CUDA-core path: the appends, then attention over pos + 1 tokens
-    if ((st = tq_launch_append_kv(append_args(*step, desc, kc, vc, k, v, seq_lens, a),
+    if ((st = tq_launch_append_kv(append_args(*step, desc, kc, vc, k, v, kmap, vmap, seq_lens, a),
                                   desc->batch, stream)) != TQ_OK)
       return st;
     int32_t* lens = reinterpret_cast<int32_t*>(ws + p.lens_off);
@@ -650,6 +657,7 @@ extern "C" tq_status tq_decode_attention_asym(const tq_attn_desc* desc, const tq
   if (st != TQ_OK) return st;
   if ((st = tq_check_codec(vc, TQ_MSE)) != TQ_OK) return st;
   if ((st = check_mse_cache(v)) != TQ_OK) return st;
+  if (v.pages) return TQ_ERR_UNSUPPORTED;   // the asymmetric path takes flat value caches
   if (!q || !k_f16 || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
   if (desc->tail_capacity > 0 && (!k_tail || !v_tail || !tail_lens)) return TQ_ERR_INVALID_ARG;
   if (!aligned16(k_f16) || (k_tail && !aligned16(k_tail)) || (v_tail && !aligned16(v_tail)))

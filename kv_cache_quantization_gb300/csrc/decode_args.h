@@ -37,6 +37,8 @@ struct tq_mma_launch {
   tq_plane_decomp kd;
   const uint8_t* vidx;
   const float* vxn;
+  tq_rowmap kmap, vmap;        // the caches' row maps (flat, or block tables); cap = slots per
+                               // sequence
   int vbits;                   // value bits (1..4)
   tq_plane_decomp vd;          // value decomposition (vbits ≤ 3)
   const uint32_t* lut;         // vbits == 4: 256 × 32 pair table of the value codec (device)

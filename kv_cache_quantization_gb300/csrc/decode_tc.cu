@@ -448,8 +448,66 @@ struct TL {
   static_assert(d_col + NG * d_cols <= 512, "TMEM columns");
 };
 
+// ---------------------------------------------------------------- paged stage copies
+// One ring stage of a page pool's cache (include/tq.h, tq_pages): tokens [t0, t1) of sequence
+// `seq`, KV head kvh, as runs within one page each, up to the end of the page of the row's last
+// attended token (len; pages past it are not read).  A run whose table entry lies outside the
+// pool is left out and raises TQ_FLAG_PAGE (its rows keep stale data).  A cache without a
+// table (the other of the pair may have one) is read as one run of row ch.  Run bounds are
+// multiples of 64 tokens, so every copy is 16-byte aligned.  Called by the producer's lane.
+template <int KB, int VB>
+__device__ __noinline__ void paged_stage(const tq_mma_launch& a, int o_kplanes, int o_ksgn,
+                                         int o_kxn, int o_krn, int o_vcodes, int o_vxn,
+                                         unsigned char* base, uint64_t* bar, long long ch, int seq,
+                                         int kvh, int len, int t0, int t1) {
+  constexpr unsigned kTokK = KB * 16 + 16 + 4 + 4;              // key bytes per token
+  constexpr unsigned kTokV = (VB == 4 ? 64 : VB * 16) + 4;      // value bytes per token
+  // n tokens from slot `slot` of cache row `row` (rc slots a row) to stage token `off`
+  auto copy_k = [&](long long row, int rc, int slot, int n, int off) {
+    for (int p = 0; p < KB; ++p)
+      bulk_g2s(base + o_kplanes + (p * kStageTok + off) * 16,
+               a.kidx + ((row * KB + p) * rc + slot) * 16, n * 16, bar);
+    bulk_g2s(base + o_ksgn + off * 16, a.ksgn + (row * rc + slot) * 16, n * 16, bar);
+    bulk_g2s(base + o_kxn + off * 4, a.kxn + row * rc + slot, n * 4, bar);
+    bulk_g2s(base + o_krn + off * 4, a.krn + row * rc + slot, n * 4, bar);
+  };
+  auto copy_v = [&](long long row, int rc, int slot, int n, int off) {
+    if (VB == 4) {
+      bulk_g2s(base + o_vcodes + off * 64, a.vidx + (row * rc + slot) * 64, n * 64, bar);
+    } else {
+      for (int p = 0; p < VB; ++p)
+        bulk_g2s(base + o_vcodes + (p * kStageTok + off) * 16,
+                 a.vidx + ((row * VB + p) * rc + slot) * 16, n * 16, bar);
+    }
+    bulk_g2s(base + o_vxn + off * 4, a.vxn + row * rc + slot, n * 4, bar);
+  };
+  // f(row, slot, n, offset from t0) for each run of map m; bytes only (copy = false) or copies
+  auto runs = [&](const tq_rowmap& m, bool copy, auto&& f) {
+    if (!m.table) {
+      f(ch, a.cap, t0, t1 - t0, 0);
+      return;
+    }
+    const int P = m.page_tokens;
+    const int te_all = min(t1, ((len - 1) / P + 1) * P);
+    for (int t = t0; t < te_all;) {
+      const int q = t / P, te = min(te_all, (q + 1) * P);
+      const int pg = __ldg(m.table + (long long)seq * m.max_pages + q);
+      if (pg >= 0 && pg < m.num_pages) f((long long)pg * a.Hkv + kvh, P, t - q * P, te - t, t - t0);
+      else if (copy) atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+      t = te;
+    }
+  };
+  // the bytes of every run first: the barrier expects them before the copies land
+  unsigned bytes = 0;
+  runs(a.kmap, false, [&](long long, int, int, int n, int) { bytes += (unsigned)n * kTokK; });
+  runs(a.vmap, false, [&](long long, int, int, int n, int) { bytes += (unsigned)n * kTokV; });
+  mbar_expect_tx(bar, bytes);
+  runs(a.kmap, true, copy_k);
+  runs(a.vmap, true, copy_v);
+}
+
 // ---------------------------------------------------------------- the split kernel
-template <int KB, int VB, bool HILO, int NG>
+template <int KB, int VB, bool HILO, int NG, bool kPaged>
 __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const tq_mma_launch a) {
   using L = TL<KB, VB, HILO, NG>;
   using R = Roles<NG>;
@@ -567,28 +625,36 @@ __global__ void __launch_bounds__(Roles<NG>::threads, 1) decode_tc_kernel(const 
   // ============================================================ producer warp
   if (warp == R::issuer + 1) {
     if (lane == 0) {
+      // the stage's tokens [t0, t0 + 256) (not past the capacity); the flat layout's rows are
+      // contiguous, a page pool's are runs within pages (kPaged)
       auto issue = [&](int c) {
         const int st = c % kStages;
         const int t0 = t_begin + c * kStageTok;
-        const int n = min(kStageTok, a.cap - t0);   // a multiple of 64 (the capacity is)
-        unsigned char* base = smem + st * L::stage;
-        const unsigned bytes =
-            (unsigned)n * (KB * 16 + 16 + 4 + 4 + (VB == 4 ? 64 : VB * 16) + 4);
-        mbar_expect_tx(&full_bar[st], bytes);
-        for (int p = 0; p < KB; ++p)
-          bulk_g2s(base + L::kplanes + p * kStageTok * 16,
-                   a.kidx + ((ch * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::ksgn, a.ksgn + (ch * a.cap + t0) * 16, n * 16, &full_bar[st]);
-        bulk_g2s(base + L::kxn, a.kxn + ch * a.cap + t0, n * 4, &full_bar[st]);
-        bulk_g2s(base + L::krn, a.krn + ch * a.cap + t0, n * 4, &full_bar[st]);
-        if (VB == 4) {
-          bulk_g2s(base + L::vcodes, a.vidx + (ch * a.cap + t0) * 64, n * 64, &full_bar[st]);
+        if constexpr (!kPaged) {
+          const int n = min(kStageTok, a.cap - t0);   // a multiple of 64 (the capacity is)
+          unsigned char* base = smem + st * L::stage;
+          const unsigned bytes =
+              (unsigned)n * (KB * 16 + 16 + 4 + 4 + (VB == 4 ? 64 : VB * 16) + 4);
+          mbar_expect_tx(&full_bar[st], bytes);
+          for (int p = 0; p < KB; ++p)
+            bulk_g2s(base + L::kplanes + p * kStageTok * 16,
+                     a.kidx + ((ch * KB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+          bulk_g2s(base + L::ksgn, a.ksgn + (ch * a.cap + t0) * 16, n * 16, &full_bar[st]);
+          bulk_g2s(base + L::kxn, a.kxn + ch * a.cap + t0, n * 4, &full_bar[st]);
+          bulk_g2s(base + L::krn, a.krn + ch * a.cap + t0, n * 4, &full_bar[st]);
+          if (VB == 4) {
+            bulk_g2s(base + L::vcodes, a.vidx + (ch * a.cap + t0) * 64, n * 64, &full_bar[st]);
+          } else {
+            for (int p = 0; p < VB; ++p)
+              bulk_g2s(base + L::vcodes + p * kStageTok * 16,
+                       a.vidx + ((ch * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+          }
+          bulk_g2s(base + L::vxn, a.vxn + ch * a.cap + t0, n * 4, &full_bar[st]);
         } else {
-          for (int p = 0; p < VB; ++p)
-            bulk_g2s(base + L::vcodes + p * kStageTok * 16,
-                     a.vidx + ((ch * VB + p) * a.cap + t0) * 16, n * 16, &full_bar[st]);
+          paged_stage<KB, VB>(a, L::kplanes, L::ksgn, L::kxn, L::krn, L::vcodes, L::vxn,
+                              smem + st * L::stage, &full_bar[st], ch, b / a.qps, kvh, len, t0,
+                              min(t0 + kStageTok, a.cap));
         }
-        bulk_g2s(base + L::vxn, a.vxn + ch * a.cap + t0, n * 4, &full_bar[st]);
       };
       // Π is read again only by the split that merges: have it in L2 by then
       if (split == 0) bulk_prefetch_l2(a.pi, TQ_D * TQ_D * 4);
@@ -1159,22 +1225,26 @@ tq_status launch_one(const tq_mma_launch& a0, bool step, cudaStream_t stream) {
   constexpr int NG = 2;
   constexpr int kThreads = Roles<NG>::threads;
   constexpr int smem = TL<KB, VB, HILO, NG>::total;
-  auto kern = decode_tc_kernel<KB, VB, HILO, NG>;
-  static bool configured[64] = {};
-  static int max_ctas[64] = {};
+  // flat caches and page pools are separate instantiations: the flat kernel's producer has no
+  // block-table code
+  const int paged = a0.kmap.table || a0.vmap.table ? 1 : 0;
+  auto kern = paged ? decode_tc_kernel<KB, VB, HILO, NG, true>
+                    : decode_tc_kernel<KB, VB, HILO, NG, false>;
+  static bool configured[2][64] = {};
+  static int max_ctas[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
-  if (!configured[dev]) {
+  if (!configured[paged][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    max_ctas[dev] = per_sm * tq_num_sms();
-    configured[dev] = true;
+    max_ctas[paged][dev] = per_sm * tq_num_sms();
+    configured[paged][dev] = true;
   }
   const int units = a0.B * a0.Hkv;
-  int ns = max_ctas[dev] / units;
+  int ns = max_ctas[paged][dev] / units;
   if (ns > a0.nsplit || ns < 2) ns = a0.nsplit;
   if (ns < 1) ns = 1;
   tq_mma_launch a = a0;

@@ -182,6 +182,18 @@ tq_status tq_check_codec(const tq_codec* c, tq_kind kind) {
   return TQ_OK;
 }
 
+tq_status tq_rowmap_of(const tq_pages* pages, int capacity, tq_rowmap* out) {
+  if (!out) return TQ_ERR_INVALID_ARG;
+  *out = tq_rowmap{nullptr, 0, 0, 0};
+  if (!pages) return TQ_OK;
+  if (!pages->block_table || pages->max_pages < 1 || pages->num_pages < 1) return TQ_ERR_INVALID_ARG;
+  if (pages->page_tokens <= 0 || pages->page_tokens % TQ_CAPACITY_ALIGN) return TQ_ERR_INVALID_ARG;
+  if ((long long)pages->max_pages * pages->page_tokens != (long long)capacity) return TQ_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(pages->block_table) % 4) return TQ_ERR_INVALID_ARG;
+  *out = tq_rowmap{pages->block_table, pages->max_pages, pages->page_tokens, pages->num_pages};
+  return TQ_OK;
+}
+
 tq_levels tq_make_levels(const tq_codec* c) {
   tq_levels l;
   std::memset(&l, 0, sizeof(l));

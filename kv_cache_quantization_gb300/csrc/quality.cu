@@ -107,6 +107,7 @@ extern "C" tq_status tq_attention_quality(const tq_codec* kc, const float* q, in
   tq_status st = tq_check_codec(kc, TQ_PROD);
   if (st != TQ_OK) return st;
   if (!q || !k || !scratch || !kl || !top1_exact || !top1_comp) return TQ_ERR_INVALID_ARG;
+  if (codes.pages) return TQ_ERR_UNSUPPORTED;   // flat caches only
   if (k_dtype != TQ_F32 && k_dtype != TQ_F16 && k_dtype != TQ_BF16) return TQ_ERR_UNSUPPORTED;
   if (nq <= 0 || nq > 65535 || n <= 0 || n > capacity) return TQ_ERR_INVALID_ARG;
   if (scratch_bytes < tq_attention_quality_scratch_bytes(nq, n)) return TQ_ERR_INVALID_ARG;

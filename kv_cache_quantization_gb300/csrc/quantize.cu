@@ -40,7 +40,9 @@ struct QuantArgs {
   uint8_t* sgn;
   float* xnorm;
   float* rnorm;
-  int capacity;
+  int capacity;    // slots per sequence
+  tq_rowmap map;   // flat, or the pool's block table
+  int rowcap;      // slots per cache row: capacity (flat) or page_tokens (paged)
   const float* piT;
   const float* mT;
   tq_levels lv;
@@ -113,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   float* MT = PT + TQ_D * TQ_D;
   float* X = kProd ? MT + TQ_D * TQ_D : MT;
   __shared__ float s_norm[kTile];
-  __shared__ int s_dst[kTile];      // destination slot (bh * capacity + t), -1 = skip
-  __shared__ int s_bh[kTile];
+  __shared__ int s_dst[kTile];         // destination slot in its cache row, -1 = skip
+  __shared__ long long s_row[kTile];   // destination cache row
 
   const int tid = threadIdx.x;
   if (a.sparse) {
@@ -147,20 +149,24 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
     __syncthreads();  // previous tile fully consumed (and Πᵀ/Mᵀ loaded on the first pass)
     if (tid < kTile) {
       const long long i = tile * kTile + tid;
-      int dst = -1, bh = 0;
+      int dst = -1;
+      long long row = 0;
       if (i < total) {
         const int t = (int)(i % a.tokens);
-        bh = (int)(i / a.tokens);
+        const int bh = (int)(i / a.tokens);
         const int b = bh / a.heads;
         const int cnt = a.count ? a.count[b] : a.tokens;
         if (t < cnt) {
           const int p = (a.pos ? a.pos[b] : 0) + t;
-          if (p >= 0 && p < a.capacity) dst = p;
-          else atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
+          if (p < 0 || p >= a.capacity) atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
+          else if (!tq_map_slot(a.map, a.heads, b, bh - b * a.heads, p, row, dst)) {
+            atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+            dst = -1;
+          }
         }
       }
       s_dst[tid] = dst;
-      s_bh[tid] = bh;
+      s_row[tid] = row;
     }
     // activation tile: 64 vectors × 16 chunks of 8 elements
     for (int c = tid; c < kTile * 16; c += kThreads) {
@@ -219,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
       const int v = 4 * vg + i;
       const int dst = s_dst[v];
       if (dst < 0) continue;
-      const long long slot = (long long)s_bh[v] * a.capacity + dst;
+      const long long slot = s_row[v] * a.rowcap + dst;
       if (a.nibbles) {
         uint32_t word = 0;
 #pragma unroll
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
           uint32_t byte = 0;
 #pragma unroll
           for (int o = 0; o < 8; ++o) byte |= (uint32_t)((idx[i][o] >> p) & 1) << o;
-          a.idx[(((long long)s_bh[v] * a.ibits + p) * a.capacity + dst) * 16 + jg] = (uint8_t)byte;
+          a.idx[((s_row[v] * a.ibits + p) * a.rowcap + dst) * 16 + jg] = (uint8_t)byte;
         }
       }
       if (jg == 0) a.xnorm[slot] = s_norm[v];
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
 #pragma unroll
       for (int o = 0; o < 8; ++o) byte |= (uint32_t)(z[i][o] >= 0.f) << o;
       if (!(n > 0.f)) byte = 0xffu;   // zero vector: zero residual, all signs +1
-      const long long slot = (long long)s_bh[v] * a.capacity + dst;
+      const long long slot = s_row[v] * a.rowcap + dst;
       a.sgn[slot * 16 + jg] = (uint8_t)byte;
       if (jg == 0) a.rnorm[slot] = n * sqrtf(ss[i]);
     }
@@ -298,13 +304,15 @@ __global__ void __launch_bounds__(tq::kAppendThreads) quantize_small_kernel(Quan
     return;
   }
   tq::AppendArgs aa;
+  if (!tq_map_slot(a.map, a.heads, b, h, dst, aa.row, aa.slot)) {
+    if (tid == 0) atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+    return;
+  }
   aa.x = a.dtype == TQ_F32
              ? static_cast<const void*>(static_cast<const float*>(a.x) + b * a.sb + h * a.sh + t * a.st)
              : static_cast<const void*>(static_cast<const uint16_t*>(a.x) + b * a.sb + h * a.sh + t * a.st);
   aa.dtype = a.dtype;
-  aa.dst = dst;
-  aa.bh = bh;
-  aa.capacity = a.capacity;
+  aa.rowcap = a.rowcap;
   aa.idx = a.idx;
   aa.sgn = a.sgn;
   aa.xnorm = a.xnorm;
@@ -395,15 +403,19 @@ extern "C" tq_status tq_quantize_prod(const tq_codec* kc, const void* x, tq_dtyp
   if (!aligned16(cache.idx) || !aligned16(cache.sgn) || !aligned16(cache.xnorm) ||
       !aligned16(cache.rnorm))
     return TQ_ERR_INVALID_ARG;
+  tq_rowmap map;
+  if ((st = tq_rowmap_of(cache.pages, capacity, &map)) != TQ_OK) return st;
   if (use_tensor_cores(x_dtype, batch, heads, tokens))
     return tq_launch_quantize_tc(true, x, x_dtype, batch, heads, tokens, stride_b, stride_h,
                                  stride_t, pos, count, cache.idx, cache.sgn, cache.xnorm,
-                                 cache.rnorm, capacity, kc, reinterpret_cast<cudaStream_t>(stream));
+                                 cache.rnorm, capacity, map, kc,
+                                 reinterpret_cast<cudaStream_t>(stream));
   QuantArgs a{};
   a.x = x; a.dtype = x_dtype; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = stride_b; a.sh = stride_h; a.st = stride_t; a.pos = pos; a.count = count;
   a.idx = cache.idx; a.sgn = cache.sgn; a.xnorm = cache.xnorm; a.rnorm = cache.rnorm;
-  a.capacity = capacity; a.piT = kc->d_piT; a.mT = kc->d_mT; a.lv = tq_make_levels(kc);
+  a.capacity = capacity; a.map = map; a.rowcap = tq_row_slots(map, capacity);
+  a.piT = kc->d_piT; a.mT = kc->d_mT; a.lv = tq_make_levels(kc);
   a.ibits = kc->ibits; a.nibbles = 0;
   return launch<true>(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -419,15 +431,18 @@ extern "C" tq_status tq_quantize_mse(const tq_codec* vc, const void* x, tq_dtype
   if (st != TQ_OK) return st;
   if (!cache.idx || !cache.xnorm) return TQ_ERR_INVALID_ARG;
   if (!aligned16(cache.idx) || !aligned16(cache.xnorm)) return TQ_ERR_INVALID_ARG;
+  tq_rowmap map;
+  if ((st = tq_rowmap_of(cache.pages, capacity, &map)) != TQ_OK) return st;
   if (use_tensor_cores(x_dtype, batch, heads, tokens))
     return tq_launch_quantize_tc(false, x, x_dtype, batch, heads, tokens, stride_b, stride_h,
                                  stride_t, pos, count, cache.idx, nullptr, cache.xnorm, nullptr,
-                                 capacity, vc, reinterpret_cast<cudaStream_t>(stream));
+                                 capacity, map, vc, reinterpret_cast<cudaStream_t>(stream));
   QuantArgs a{};
   a.x = x; a.dtype = x_dtype; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = stride_b; a.sh = stride_h; a.st = stride_t; a.pos = pos; a.count = count;
   a.idx = cache.idx; a.sgn = nullptr; a.xnorm = cache.xnorm; a.rnorm = nullptr;
-  a.capacity = capacity; a.piT = vc->d_piT; a.mT = nullptr; a.lv = tq_make_levels(vc);
+  a.capacity = capacity; a.map = map; a.rowcap = tq_row_slots(map, capacity);
+  a.piT = vc->d_piT; a.mT = nullptr; a.lv = tq_make_levels(vc);
   a.ibits = vc->ibits; a.nibbles = vc->ibits == 4;
   return launch<false>(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -443,7 +458,8 @@ tq_status tq_launch_quantize_tiles(const tq_codec* c, bool prod, const void* x, 
   a.x = x; a.dtype = dt; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = sb; a.sh = sh; a.st = st; a.pos = pos; a.count = count;
   a.idx = idx; a.sgn = sgn; a.xnorm = xnorm; a.rnorm = rnorm;
-  a.capacity = capacity; a.piT = c->d_piT; a.mT = prod ? c->d_mT : nullptr;
+  a.capacity = capacity; a.map = tq_rowmap{nullptr, 0, 0, 0}; a.rowcap = capacity;
+  a.piT = c->d_piT; a.mT = prod ? c->d_mT : nullptr;
   a.lv = tq_make_levels(c); a.ibits = c->ibits; a.nibbles = !prod && c->ibits == 4;
   a.sparse = 1;
   const long long total = (long long)batch * heads * tokens;

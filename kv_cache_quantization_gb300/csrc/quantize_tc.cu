@@ -28,6 +28,8 @@
 // kernel.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "tc_ptx.h"
 #include "tq_internal.h"
 
@@ -159,7 +161,9 @@ struct TcArgs {
   uint8_t* sgn;
   float* xnorm;
   float* rnorm;
-  int capacity;
+  int capacity;              // slots per sequence
+  tq_rowmap map;             // flat, or the pool's block table
+  int rowcap;                // slots per cache row: capacity (flat) or page_tokens (paged)
   const void* img;           // Π̂ hi | lo (| M̂ hi | lo for prod), canonical images
   tq_levels lv;
   bool narrow;               // batch·heads·tokens < 2^32: vector indices split in 32 bits
@@ -480,13 +484,28 @@ __device__ __forceinline__ VecDest vec_dest(const TcArgs& a, long long first, in
   }
   return d;
 }
-// its cache position, or -1 (not stored; a position out of range is flagged)
-__device__ __forceinline__ int dest_pos(const TcArgs& a, const VecDest& d, int r, int nvalid) {
+// its cache row and slot in the row, or -1 (not stored; a position out of range, or a page
+// outside the pool, is flagged)
+template <bool kPaged>
+__device__ __forceinline__ int dest_slot(const TcArgs& a, const VecDest& d, int r, int nvalid,
+                                         long long& row) {
   if (r >= nvalid || d.t >= d.cnt) return -1;
   const int p = d.p0 + d.t;
-  if (p >= 0 && p < a.capacity) return p;
-  atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
-  return -1;
+  if (p < 0 || p >= a.capacity) {
+    atomicOr(&g_tq_flags, TQ_FLAG_POS_OVERFLOW);
+    return -1;
+  }
+  if constexpr (!kPaged) {
+    row = d.bh;
+    return p;
+  }
+  const int b = (int)((uint32_t)d.bh / (uint32_t)a.heads);
+  int slot;
+  if (!tq_map_slot(a.map, a.heads, b, d.bh - b * a.heads, p, row, slot)) {
+    atomicOr(&g_tq_flags, TQ_FLAG_PAGE);
+    return -1;
+  }
+  return slot;
 }
 
 // Converter warp cw: tile j's raw vectors, once in buffer j % NB, become X̂ in place, with
@@ -535,8 +554,8 @@ __device__ __forceinline__ float epilogue_cells(uint32_t d1c, float ysc, const t
   return rr;
 }
 // stores of a part's index codes (planes: 4·NBLK bytes of each plane; nibbles: 16·NBLK bytes)
-template <int IB, bool kNib, int NBLK>
-__device__ __forceinline__ void store_codes(const TcArgs& a, int bh, int dst, long long slot,
+template <int IB, bool kNib, int NBLK, typename RowT>
+__device__ __forceinline__ void store_codes(const TcArgs& a, RowT row, int dst, long long slot,
                                             int part, const uint32_t (&code)[NBLK][kNib ? 4 : IB]) {
   if constexpr (kNib) {
     uint4* dp = reinterpret_cast<uint4*>(a.idx + slot * 64 + 16 * NBLK * part);
@@ -546,12 +565,12 @@ __device__ __forceinline__ void store_codes(const TcArgs& a, int bh, int dst, lo
   } else {
 #pragma unroll
     for (int p = 0; p < IB; ++p) {
-      unsigned char* row =
-          a.idx + (((long long)bh * IB + p) * a.capacity + dst) * 16 + 4 * NBLK * part;
+      unsigned char* dp =
+          a.idx + (((long long)row * IB + p) * a.rowcap + dst) * 16 + 4 * NBLK * part;
       if constexpr (NBLK == 4)
-        *reinterpret_cast<uint4*>(row) = make_uint4(code[0][p], code[1][p], code[2][p], code[3][p]);
+        *reinterpret_cast<uint4*>(dp) = make_uint4(code[0][p], code[1][p], code[2][p], code[3][p]);
       else
-        *reinterpret_cast<uint2*>(row) = make_uint2(code[0][p], code[1][p]);
+        *reinterpret_cast<uint2*>(dp) = make_uint2(code[0][p], code[1][p]);
     }
   }
 }
@@ -571,8 +590,9 @@ __device__ __forceinline__ void store_codes(const TcArgs& a, int bh, int dst, lo
 // Hand-overs are mbarriers: the converters' and epilogues' arrivals (one per warp) and the tensor
 // core's commits.  Every barrier's next phase can only complete after each of its waiters has
 // passed the previous one (the barriers that would otherwise run two phases ahead of a waiter
-// come one per buffer or accumulator slot), so waits on a phase's parity are exact.
-template <bool kProd, int IB>
+// come one per buffer or accumulator slot), so waits on a phase's parity are exact.  kPaged:
+// the cache is a page pool, each vector's slot found through the block table.
+template <bool kProd, int IB, bool kPaged>
 __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_kernel(TcArgs a) {
   using L = QL<kProd>;
   using R = Roles<kProd, IB>;
@@ -769,8 +789,11 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const int r = 32 * quad + lane;   // this thread's vector
     bool ok = true;
-    // vector r of the tile whose signs come next: destination, ‖x‖ (product code)
-    int dst = -1, bh = 0;
+    // vector r of the tile whose signs come next: destination (cache row, slot in the row, and
+    // row·rowcap + slot), ‖x‖ (product code); a flat cache's rows (batch·heads + head) fit 32 bits
+    using RowT = typename std::conditional<kPaged, long long, int>::type;
+    int dst = -1;
+    RowT row = 0;
     long long slot = 0;
     float n = 0.f;
     auto begin = [&](int j, uint64_t* g1, uint32_t par) {
@@ -783,9 +806,10 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
       ok = __all_sync(0xffffffffu, ok && tq::mbar_wait(g1, par));
       if (!ok) return;
       tc_after();
-      dst = dest_pos(a, vd, r, nvalid);
-      bh = vd.bh;
-      slot = (long long)bh * a.capacity + dst;
+      long long rw = 0;
+      dst = dest_slot<kPaged>(a, vd, r, nvalid, rw);
+      row = (RowT)rw;
+      slot = (long long)row * a.rowcap + dst;
     };
     if constexpr (kProd) {
       auto epilogue1 = [&](int j) {
@@ -839,7 +863,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         __syncwarp();
         if (lane == 0) tq::mbar_arrive(bar_a2);
         if (dst >= 0) {
-          store_codes<IB, false, 2>(a, bh, dst, slot, part, code);
+          store_codes<IB, false, 2>(a, row, dst, slot, part, code);
           if (part == 0) {
             a.xnorm[slot] = n;
             a.rnorm[slot] = n * sqrtf(rt);
@@ -895,7 +919,7 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
         __syncwarp();
         if (lane == 0) tq::mbar_arrive(bar_a2 + (j & 1));
         if (dst >= 0) {
-          store_codes<IB, kNib, NBLK>(a, bh, dst, slot, part, code);
+          store_codes<IB, kNib, NBLK>(a, row, dst, slot, part, code);
           if (part == 0) a.xnorm[slot] = xn;
         }
       }
@@ -910,21 +934,29 @@ __global__ void __launch_bounds__(Roles<kProd, IB>::kThreads, 1) quantize_tc_ker
                  "r"(L::tmem_cols));
 }
 
-template <bool kProd, int IB>
-tq_status launch_tc(const TcArgs& a, int grid, cudaStream_t stream) {
+template <bool kProd, int IB, bool kPaged>
+tq_status launch_tc_layout(const TcArgs& a, int grid, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return TQ_ERR_CUDA;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(quantize_tc_kernel<kProd, IB>,
+    if (cudaFuncSetAttribute(quantize_tc_kernel<kProd, IB, kPaged>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              QL<kProd>::total) != cudaSuccess)
       return TQ_ERR_CUDA;
     configured[dev] = true;
   }
   constexpr int threads = Roles<kProd, IB>::kThreads;
-  quantize_tc_kernel<kProd, IB><<<grid, threads, QL<kProd>::total, stream>>>(a);
+  quantize_tc_kernel<kProd, IB, kPaged><<<grid, threads, QL<kProd>::total, stream>>>(a);
   return tq_cuda_status(cudaGetLastError());
+}
+
+// Flat caches and page pools are separate instantiations: the flat kernel carries no code of
+// the block-table lookup.
+template <bool kProd, int IB>
+tq_status launch_tc(const TcArgs& a, int grid, cudaStream_t stream) {
+  return a.map.table ? launch_tc_layout<kProd, IB, true>(a, grid, stream)
+                     : launch_tc_layout<kProd, IB, false>(a, grid, stream);
 }
 
 }  // namespace
@@ -934,12 +966,13 @@ bool tq_quantize_tc_supported(int dtype) { return dtype == TQ_BF16 || dtype == T
 tq_status tq_launch_quantize_tc(bool prod, const void* x, int dtype, int batch, int heads,
                                 int tokens, long long sb, long long sh, long long st,
                                 const int* pos, const int* count, uint8_t* idx, uint8_t* sgn,
-                                float* xnorm, float* rnorm, int capacity, const tq_codec* c,
-                                cudaStream_t stream) {
+                                float* xnorm, float* rnorm, int capacity, const tq_rowmap& map,
+                                const tq_codec* c, cudaStream_t stream) {
   TcArgs a{};
   a.x = x; a.dtype = dtype; a.batch = batch; a.heads = heads; a.tokens = tokens;
   a.sb = sb; a.sh = sh; a.st = st; a.pos = pos; a.count = count;
   a.idx = idx; a.sgn = sgn; a.xnorm = xnorm; a.rnorm = rnorm; a.capacity = capacity;
+  a.map = map; a.rowcap = tq_row_slots(map, capacity);
   a.img = c->d_img; a.lv = tq_make_levels(c);
   const long long total = (long long)batch * heads * tokens;
   a.narrow = total < (1ll << 32);

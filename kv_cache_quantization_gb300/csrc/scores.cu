@@ -65,6 +65,7 @@ extern "C" tq_status tq_prod_scores(const tq_codec* kc, const float* q, int32_t 
   if (st != TQ_OK) return st;
   if (!q || !scores || !keys.idx || !keys.sgn || !keys.xnorm || !keys.rnorm)
     return TQ_ERR_INVALID_ARG;
+  if (keys.pages) return TQ_ERR_UNSUPPORTED;   // flat caches only
   if (nq < 0 || nq > 65535 || n < 0 || capacity <= 0 || capacity % TQ_CAPACITY_ALIGN || n > capacity)
     return TQ_ERR_INVALID_ARG;
   if (q_stride < TQ_D || scores_stride < n) return TQ_ERR_INVALID_ARG;

@@ -110,6 +110,7 @@ extern "C" tq_status tq_store_append(const tq_codec* vc, int32_t batch, int32_t 
   tq_status st = tq_check_codec(vc, TQ_MSE);
   if (st != TQ_OK) return st;
   if (batch < 0 || kv_heads <= 0) return TQ_ERR_INVALID_ARG;
+  if (v.pages) return TQ_ERR_UNSUPPORTED;   // the store keeps a flat value cache
   if (capacity <= 0 || capacity % TQ_CAPACITY_ALIGN) return TQ_ERR_INVALID_ARG;
   if (tail_capacity <= 0 || tail_capacity % 8) return TQ_ERR_INVALID_ARG;
   if (dtype != TQ_F32 && dtype != TQ_F16 && dtype != TQ_BF16) return TQ_ERR_UNSUPPORTED;

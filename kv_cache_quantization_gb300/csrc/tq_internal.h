@@ -41,6 +41,41 @@ struct tq_levels {
   int levels;
 };
 
+// Where a cache keeps a (sequence, head, token): the flat layout (table null) holds row
+// b·heads + h of `capacity` slots; a paged pool holds row page·heads + h of page_tokens slots,
+// the page from the block table (include/tq.h, tq_pages).  Passed by value to kernels.
+struct tq_rowmap {
+  const int32_t* table;   // device [batch][max_pages], or null (flat)
+  int max_pages, page_tokens, num_pages;
+};
+
+// The row map of a cache argument: flat for pages == null, else the block table after the
+// checks the header states (capacity = max_pages·page_tokens); TQ_ERR_INVALID_ARG otherwise.
+tq_status tq_rowmap_of(const tq_pages* pages, int capacity, tq_rowmap* out);
+
+#ifdef __CUDACC__
+// Slots a row holds: capacity (flat) or page_tokens (paged).
+__host__ __device__ __forceinline__ int tq_row_slots(const tq_rowmap& m, int capacity) {
+  return m.table ? m.page_tokens : capacity;
+}
+// Row and slot of token t (0 ≤ t < capacity) of sequence b, head h.  False for a paged
+// cache whose table entry lies outside [0, num_pages): the caller skips the token and raises
+// TQ_FLAG_PAGE.
+__device__ __forceinline__ bool tq_map_slot(const tq_rowmap& m, int heads, int b, int h, int t,
+                                            long long& row, int& slot) {
+  if (!m.table) {
+    row = (long long)b * heads + h;
+    slot = t;
+    return true;
+  }
+  const int q = t / m.page_tokens;
+  const int pg = __ldg(m.table + (long long)b * m.max_pages + q);
+  row = (long long)pg * heads + h;
+  slot = t - q * m.page_tokens;
+  return pg >= 0 && pg < m.num_pages;
+}
+#endif
+
 // Device status words.  Kernels are compiled without relocatable device code, so every
 // translation unit that raises flags owns its word and a host function that reads and
 // clears it (on the current device); tq_device_status() ORs them together.
@@ -76,8 +111,8 @@ bool tq_quantize_tc_supported(int dtype);
 tq_status tq_launch_quantize_tc(bool prod, const void* x, int dtype, int batch, int heads,
                                 int tokens, long long sb, long long sh, long long st,
                                 const int* pos, const int* count, uint8_t* idx, uint8_t* sgn,
-                                float* xnorm, float* rnorm, int capacity, const tq_codec* c,
-                                cudaStream_t stream);
+                                float* xnorm, float* rnorm, int capacity, const tq_rowmap& map,
+                                const tq_codec* c, cudaStream_t stream);
 size_t tq_operand_image_bytes(bool prod);
 // FFMA tile quantiser, one CTA per tile of 64 vectors; tiles without a vector to write (count)
 // leave at once (quantize.cu).
