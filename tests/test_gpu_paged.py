@@ -269,3 +269,30 @@ def test_paged_argument_checks():
         plan.run(kc5, vc, rand_x((1, 2, D), 6, torch.bfloat16), k5, v2, lens, plan.new_out())
     assert e.value.status == B.TQ_ERR_UNSUPPORTED
     check_flags_clear()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_paged_prefill_equals_flat(causal):
+    """A chunk of queries per sequence (tq_prefill_attention): each query row reads its
+    sequence's pages through the block table."""
+    batch, nq, hq, hkv, P = 2, 5, 16, 4, 128
+    hist = [300, 1000]
+    used = [h + nq for h in hist]
+    max_pages = -(-1088 // P)
+    (kf, vf), (kp, vp), cap = caches(batch, hkv, 3, 4, used, P, max_pages, seed=880)
+    kc, vc = api.Codec.prod(3), api.Codec.mse(4)
+    k = rand_x((batch, hkv, max(used), D), 81, torch.bfloat16)
+    v = rand_x((batch, hkv, max(used), D), 82, torch.bfloat16)
+    q = rand_x((batch, nq, hq, D), 83, torch.bfloat16)
+    full = torch.tensor(used, dtype=torch.int32, device="cuda")
+    for kk, vv in ((kf, vf), (kp, vp)):
+        api.quantize_prod(kc, k, kk, count=full)
+        api.quantize_mse(vc, v, vv, count=full)
+    lens = torch.tensor(hist, dtype=torch.int32, device="cuda")
+    plan = api.PrefillPlan(batch, nq, hq, hkv, cap, max(used), causal=causal)
+    out_f = plan.run(kc, vc, q, kf, vf, lens, plan.new_out())
+    out_p = plan.run(kc, vc, q, kp, vp, lens, plan.new_out())
+    torch.cuda.synchronize()
+    check_flags_clear()
+    assert torch.isfinite(out_f).all()
+    assert torch.equal(out_f, out_p), f"max diff {(out_f - out_p).abs().max()}"
