@@ -267,16 +267,27 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
     }
   }
 #pragma unroll
-  for (int u = 0; u < SPC; ++u)
+  // head h's 8 query values of the lane's k chunk are read once for all SPC slices; heads past
+  // the group have q = 0, so their sums are exactly 0 without the products
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      float x = 0.f;
-      if (h < NCOL && act) {
+  for (int h = 0; h < 8; ++h) {
+    float x[SPC];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x = fmaf(t[u][k], qf[h][8 * kq + k], x);
-      }
-      if (act) red[u][which][h][kq * 8 + jl] = x;
+    for (int u = 0; u < SPC; ++u) x[u] = 0.f;
+    if (h < NCOL && h < a.G && act) {
+      const float4 qa = *reinterpret_cast<const float4*>(&qf[h][8 * kq]);
+      const float4 qb = *reinterpret_cast<const float4*>(&qf[h][8 * kq + 4]);
+      const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+      for (int u = 0; u < SPC; ++u)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[u] = fmaf(t[u][k], qv[k], x[u]);
     }
+    if (act) {
+#pragma unroll
+      for (int u = 0; u < SPC; ++u) red[u][which][h][kq * 8 + jl] = x[u];
+    }
+  }
   __syncthreads();
   for (int it = tid; act && it < SPC * 2 * 8 * 8; it += kPrepThreads) {
     const int u = it >> 7, wh = (it >> 6) & 1, h = (it >> 3) & 7, jj = it & 7;
