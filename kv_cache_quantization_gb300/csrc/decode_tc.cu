@@ -192,7 +192,7 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
   // [slice][Π|S][head][k chunk · 8 + j in slice], rows padded to 136 floats: a warp's stores
   // (8 j × 4 k chunks) and the sums' reads (8 j × 4 heads) fall in 32 distinct banks
   constexpr int kRedPitch = 16 * 8 + 8;
-  __shared__ float red[SPC][2][8][kRedPitch];
+  __shared__ __align__(16) float red[SPC][2][8][kRedPitch];
   __shared__ float prod[SPC][2][8][8];      // [slice][Π|S][j in slice][head]
   __shared__ float s_nq[8], s_inq[8], s_uq[8], s_wq[8];
   __shared__ float s_off[SPC][2][8];        // [slice][index planes | sign plane][column]
@@ -200,16 +200,26 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
   const long long bh = (long long)b * a.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool act = tid < kPrepThreads;
-  // thread (which, k chunk kq, j in slice jl): 8 entries of row j of M (M = Π or S, read from
-  // Mᵀ: the codec's constants) for each of its slices, requested at once
+  // thread (which, k chunk kq, jl): 8 entries of rows j of M (M = Π or S, read from Mᵀ: the
+  // codec's constants), requested at once.  SPC < 4: row j = 8(SPC·bx + u) + jl of each slice u
+  // (t[u]).  SPC = 4: the CTA's 32 rows are consecutive and the thread takes rows
+  // 32bx + 4jl + e (t[e]: slice jl / 2, j in slice 4(jl mod 2) + e) by 16-byte loads.
   const int which = (tid >> 7) & 1, kq = (tid >> 3) & 15, jl = tid & 7;
   const float* T = which ? a.sT : a.piT;
   float t[SPC][8];
+  if constexpr (SPC == 4) {
 #pragma unroll
-  for (int u = 0; u < SPC; ++u) {
-    const int j = 8 * (SPC * bx + u) + jl;
+    for (int k = 0; k < 8; ++k) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(&T[(8 * kq + k) * TQ_D + 32 * bx + 4 * jl]));
+      t[0][k] = v.x; t[1][k] = v.y; t[2][k] = v.z; t[3][k] = v.w;
+    }
+  } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[u][k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
+    for (int u = 0; u < SPC; ++u) {
+      const int j = 8 * (SPC * bx + u) + jl;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[u][k] = __ldg(&T[(8 * kq + k) * TQ_D + j]);
+    }
   }
   // the column sums Πᵀ1 and Sᵀ1 at the lane's coordinates (for the norm warps)
   float cu[4], cw[4];
@@ -284,8 +294,13 @@ __device__ __forceinline__ void query_prep_role(const tq_mma_launch& a, int bx) 
         for (int k = 0; k < 8; ++k) x[u] = fmaf(t[u][k], qv[k], x[u]);
     }
     if (act) {
+      if constexpr (SPC == 4) {
+        *reinterpret_cast<float4*>(&red[jl >> 1][which][h][kq * 8 + 4 * (jl & 1)]) =
+            make_float4(x[0], x[1], x[2], x[3]);
+      } else {
 #pragma unroll
-      for (int u = 0; u < SPC; ++u) red[u][which][h][kq * 8 + jl] = x[u];
+        for (int u = 0; u < SPC; ++u) red[u][which][h][kq * 8 + jl] = x[u];
+      }
     }
   }
   __syncthreads();
