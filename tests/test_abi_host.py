@@ -114,3 +114,45 @@ def test_invalid_arguments_rejected(lib):
                                  1 << 20, None) == B.TQ_ERR_INVALID_ARG
     assert B.tq_decode_attention_asym(d, None, 16, 16, B.tq_mse_cache(0, 0), 16, 16, 16, 16, 16,
                                       256, 1 << 20, None) == B.TQ_ERR_INVALID_ARG
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The binding's ctypes structs have the sizes and field offsets that the C header gives
+    (compiled here with the host C compiler)."""
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stddef.h>\n#include <stdio.h>\n#include \"tq.h\"\n"
+        "int main(void) {\n"
+        "  printf(\"%zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(tq_pages),\n"
+        "         offsetof(tq_pages, num_pages), sizeof(tq_prod_cache),\n"
+        "         offsetof(tq_prod_cache, pages), sizeof(tq_mse_cache),\n"
+        "         offsetof(tq_mse_cache, pages), sizeof(tq_attn_desc),\n"
+        "         offsetof(tq_attn_desc, out_dtype));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(B.tq_pages), B.tq_pages.num_pages.offset,
+            ctypes.sizeof(B.tq_prod_cache), B.tq_prod_cache.pages.offset,
+            ctypes.sizeof(B.tq_mse_cache), B.tq_mse_cache.pages.offset,
+            ctypes.sizeof(B.tq_attn_desc), B.tq_attn_desc.out_dtype.offset]
+    assert got == want
+
+
+def test_pages_host_object():
+    """api.Pages: the table's shape gives the pages per sequence and the capacity, the C struct
+    points at the table, and tables that are not int32 [batch, max_pages] are refused."""
+    import torch
+
+    from kv_cache_quantization_gb300 import api
+    t = torch.tensor([[3, 1, -1], [0, 2, -1]], dtype=torch.int32)
+    p = api.Pages(t, 64, 4)
+    assert p.max_pages == 3 and p.capacity == 192
+    c = p.c().contents
+    assert (c.block_table, c.max_pages, c.page_tokens, c.num_pages) == (t.data_ptr(), 3, 64, 4)
+    with pytest.raises(ValueError):
+        api.Pages(t.long(), 64, 4)
+    with pytest.raises(ValueError):
+        api.Pages(t[0], 64, 4)
